@@ -1,0 +1,483 @@
+#!/usr/bin/env python3
+"""Benchmark of the SwiAttn routed-attention hot path on GB300.
+
+Headline: routed prefill (swiattn_prefill: gate scheduling + tensor-core
+attention) on the long-context workload B=1, H=16, d=128, N=32768, W=1024,
+gates in runs at routed fraction 0.13, reported as useful TFLOP/s (4*d per
+visited query-key pair).  The same run also measures decode KV-read GB/s
+(16 sequences x 32768 cached tokens), the 'easy' 0.05 prefill, the router
+GEMV and the dual-branch training forward, each on its own workload.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One JSON line is printed by rank 0.  Under torchrun every rank runs its own
+independent sequence (weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import swiattn_inputs as inp  # noqa: E402
+
+METRIC = "prefill useful TFLOP/s at N=32K (% of bf16 peak); decode KV-read GB/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+# DRAM traffic per launch of the dominant kernels, from ncu captures
+# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the SHA-256 of the
+# kernel source it was taken on; a changed kernel reports null.
+MEASURED_TRAFFIC = {}
+
+
+def kernel_source_hash(name: str) -> str:
+    path = os.path.join(ROOT, "sliding_window_attention_router_gb300", "csrc", name)
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def useful_pairs(gate: np.ndarray, W: int) -> int:
+    """Visited (query, key) pairs per head: routed rows i+1, window rows min(i+1, W)."""
+    B, N = gate.shape
+    i = np.arange(N, dtype=np.int64)[None, :]
+    n = np.where(gate != 0, i + 1, np.minimum(i + 1, W))
+    return int(n.sum())
+
+
+# ------------------------------------------------------------------ dist --
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            if torch.cuda.is_available():
+                self.pg.barrier(device_ids=[self.local_rank])
+            else:
+                self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        return self._reduce(x, "max")
+
+    def sum(self, x: float) -> float:
+        return self._reduce(x, "sum")
+
+    def _reduce(self, x: float, op: str) -> float:
+        if not self.pg:
+            return float(x)
+        dev = torch.device("cuda", self.local_rank) if torch.cuda.is_available() else "cpu"
+        t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX if op == "max" else self.pg.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+def aggregate(units_per_rank: float, seconds_per_rank: float, dist: Dist):
+    """Whole-job throughput: units summed over ranks / slowest rank's time."""
+    total = dist.sum(units_per_rank)
+    slowest = dist.max(seconds_per_rank)
+    return total / slowest, slowest
+
+
+# ---------------------------------------------------------------- clocks --
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = None
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="swiattn_clocks_", suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu=timestamp,{self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) == 8:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        power = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[4 + k] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(rows[0][2]), "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(power) if power else None}
+
+
+# ----------------------------------------------------------------- timing --
+class Timer:
+    """Per-step CUDA-event timing with an L2 flush before every step."""
+
+    def __init__(self, device):
+        self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    def run(self, fn, steps: int, warmup: int, kernel_events: bool = False):
+        import sliding_window_attention_router_gb300 as swa
+        for _ in range(warmup):
+            self.flush.zero_()
+            fn()
+        torch.cuda.synchronize()
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        stops = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ks = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ke = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        for s in range(steps):
+            self.flush.zero_()
+            if kernel_events:
+                swa.set_profile_events(ks[s], ke[s])
+            starts[s].record()
+            fn()
+            stops[s].record()
+        if kernel_events:
+            swa.set_profile_events(None, None)
+        torch.cuda.synchronize()
+        step_ms = [a.elapsed_time(b) for a, b in zip(starts, stops)]
+        kern_ms = [a.elapsed_time(b) for a, b in zip(ks, ke)] if kernel_events else None
+        return step_ms, kern_ms
+
+
+# ------------------------------------------------------------ workloads --
+def prefill_section(swa, timer, dev, frac, steps, warmup, seed, with_e2e):
+    d = inp.prefill_32k(frac=frac, seed=seed)
+    B, N, H, D, W = d["B"], d["N"], d["Hq"], d["d"], d["W"]
+    pairs = useful_pairs(d["gate"].numpy(), W)
+    flops = 4.0 * D * H * pairs
+    host = {k: d[k].pin_memory() for k in ("q", "k", "v", "gate")}
+    q, k, v, gate = (host[n].to(dev, non_blocking=True) for n in ("q", "k", "v", "gate"))
+    o = torch.empty_like(q)
+    ws = torch.empty(swa.prefill_workspace(B, N, H, H, D, W, torch.bfloat16), dtype=torch.uint8,
+                     device=dev)
+    scale = 1.0 / math.sqrt(D)
+
+    def step():
+        swa.prefill(q, k, v, gate, W, scale, out=o, workspace=ws)
+
+    step_ms, kern_ms = timer.run(step, steps, warmup, kernel_events=True)
+    assert swa.get_device_error() == 0, "device-side wait timed out"
+    res = dict(d=d, flops=flops, pairs=pairs, step_ms=step_ms, kern_ms=kern_ms,
+               realised_frac=float(d["gate"].float().mean()))
+    if with_e2e:
+        o_host = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+
+        def e2e_step():
+            qd, kd, vd, gd = (t.to(dev, non_blocking=True) for t in
+                              (host["q"], host["k"], host["v"], host["gate"]))
+            swa.prefill(qd, kd, vd, gd, W, scale, out=o, workspace=ws)
+            o_host.copy_(o, non_blocking=True)
+
+        e2e_ms, _ = timer.run(e2e_step, max(3, steps // 2), 2)
+        h2d = sum(host[n].numel() * host[n].element_size() for n in host)
+        d2h = o_host.numel() * o_host.element_size()
+        res.update(e2e_ms=e2e_ms, h2d=h2d, d2h=d2h)
+    return res
+
+
+def decode_section(swa, timer, dev, steps, warmup, seed):
+    B, L, H, D, W = 16, 32768, 16, 128, 1024
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    kc = torch.randn(B, L, H, D, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    vc = torch.randn(B, L, H, D, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    q = torch.randn(B, H, D, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    gcpu = inp._gen(seed)
+    gate = inp.bernoulli_gates((B,), 0.13, gcpu).to(dev)
+    sl = torch.full((B,), L, dtype=torch.int32, device=dev)
+    o = torch.empty_like(q)
+    ws = torch.empty(swa.decode_workspace(B, L, H, H, D, W, torch.bfloat16), dtype=torch.uint8,
+                     device=dev)
+    n_routed = int(gate.sum())
+    entries = n_routed * L + (B - n_routed) * W
+    kv_bytes = entries * H * D * 2 * 2
+    qo_bytes = 2 * B * H * D * 2
+
+    def step():
+        swa.decode(q, kc, vc, sl, gate, W, out=o, workspace=ws)
+
+    step_ms, kern_ms = timer.run(step, steps, warmup, kernel_events=True)
+    assert swa.get_device_error() == 0
+    del kc, vc
+    return dict(step_ms=step_ms, kern_ms=kern_ms, bytes=kv_bytes + qo_bytes, n_routed=n_routed)
+
+
+def route_section(swa, timer, dev, steps, warmup, seed):
+    T, Dm = 32768, 2048
+    r = inp.router_inputs(T, Dm, torch.bfloat16, seed)
+    h, w = r["h"].to(dev), r["w"].to(dev)
+    logits = torch.empty(T, dtype=torch.float32, device=dev)
+    gate = torch.empty(T, dtype=torch.uint8, device=dev)
+
+    def step():
+        swa.route(h, w, r["bias"], logits=logits, gate=gate)
+
+    step_ms, _ = timer.run(step, steps, warmup)
+    nbytes = T * Dm * 2 + Dm * 2 + T * 5
+    return dict(step_ms=step_ms, bytes=nbytes)
+
+
+def dual_section(swa, timer, dev, steps, warmup, seed):
+    d = inp.dual_8k(seed=seed)
+    B, N, Hq, Hkv, D, W = d["B"], d["N"], d["Hq"], d["Hkv"], d["d"], d["W"]
+    q, k, v, lg, nll = (d[n].to(dev) for n in ("q", "k", "v", "logits", "nll"))
+    outs = dict(o_full=torch.empty_like(q), o_swa=torch.empty_like(q), o_gated=torch.empty_like(q),
+                mse=torch.empty(B, N, device=dev), gamma=torch.empty(B, N, device=dev),
+                reg_loss=torch.empty(B, N, device=dev))
+    ws = torch.empty(max(256, swa.dual_branch_workspace(B, N, Hq, Hkv, D, W, torch.bfloat16)),
+                     dtype=torch.uint8, device=dev)
+
+    def step():
+        swa.dual_branch(q, k, v, lg, nll, W, outs=outs, workspace=ws)
+
+    step_ms, kern_ms = timer.run(step, steps, warmup, kernel_events=True)
+    assert swa.get_device_error() == 0
+    pairs_full = N * (N + 1) // 2
+    flops = 4.0 * D * Hq * B * pairs_full
+    return dict(step_ms=step_ms, kern_ms=kern_ms, flops=flops)
+
+
+# ------------------------------------------------------------ CPU oracle --
+def oracle_sample(d, budget_s: float, seed: int = 0):
+    """Time the fp64 oracle on a random sample of (row, head) outputs of the
+    workload sized to about budget_s seconds; returns useful FLOP/s, cores,
+    description."""
+    import oracle
+    N, H, D, W = d["N"], d["Hq"], d["d"], d["W"]
+    gate = d["gate"].numpy()
+    q64, k64, v64 = (d[n].to(torch.float64).numpy() for n in ("q", "k", "v"))
+    rng = np.random.default_rng(seed)
+
+    def run(nrows):
+        sel = np.stack([np.zeros(nrows, np.int64), rng.integers(0, N, nrows),
+                        rng.integers(0, H, nrows)], 1)
+        i = sel[:, 1]
+        n = np.where(gate[0, i] != 0, i + 1, np.minimum(i + 1, W))
+        t0 = time.perf_counter()
+        oracle.prefill_rows(q64, k64, v64, gate, W, 1.0 / math.sqrt(D), sel)
+        return time.perf_counter() - t0, 4.0 * D * float(n.sum())
+
+    t, f = run(64)
+    per_row = max(t / 64, 1e-6)
+    nrows = int(min(max(budget_s / per_row, 64), 200000))
+    t, f = run(nrows)
+    return dict(flops_per_s=f / t, seconds=t, rows=nrows, cores=oracle.num_threads())
+
+
+# ------------------------------------------------------------------ arms --
+def run_reference(args, dist: Dist):
+    if dist.rank != 0:
+        return
+    d = inp.prefill_32k(frac=0.13, seed=0)
+    import oracle
+    oracle.build()
+    per_step = []
+    flops = []
+    cores = oracle.num_threads()
+    for s in range(args.warmup + args.steps):
+        r = oracle_sample(d, budget_s=3.0, seed=s)
+        if s >= args.warmup:
+            per_step.append(r["seconds"])
+            flops.append(r["flops_per_s"] * r["seconds"])
+    value = sum(flops) / sum(per_step) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * statistics.mean(per_step), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "long-context routed prefill, B=1 H=16 d=128 N=32768 W=1024, "
+                               "gate runs at routed fraction 0.13", "routed_fraction": 0.13},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": "each step: random (row, head) outputs of the workload, "
+                                   "about 3 s of fp64 oracle work"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, dist: Dist):
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU")
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    import sliding_window_attention_router_gb300 as swa
+    swa._load()   # fails loudly if the library is missing
+    peaks, peaks_src = load_peaks()
+    timer = Timer(dev)
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(dist.local_rank)).split(",")[0]) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else dist.local_rank
+
+    clocks = ClockSampler(gpu_index)
+    dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    main = prefill_section(swa, timer, dev, 0.13, args.steps, args.warmup, seed=dist.rank,
+                           with_e2e=True)
+    torch.cuda.synchronize()
+    dist.barrier()
+    wall = time.perf_counter() - t_wall0
+    clk = clocks.stop()
+
+    step_s = sum(main["step_ms"]) / 1e3
+    value, slowest = aggregate(main["flops"] * args.steps, step_s, dist)
+    e2e_s = sum(main["e2e_ms"]) / 1e3
+    e2e_value, _ = aggregate(main["flops"] * len(main["e2e_ms"]), e2e_s, dist)
+    kern_s = statistics.mean(main["kern_ms"]) / 1e3
+    achieved = main["flops"] / kern_s / 1e12
+    peak = float(peaks["bf16_tflops"])
+    src_hash = kernel_source_hash("attn_tc.cu")
+    traffic = MEASURED_TRAFFIC.get(("attn_tc.cu", src_hash, "prefill32k_f0.13"))
+
+    extra = {}
+    if not args.headline_only:
+        ks, kw = max(3, args.steps), max(3, args.warmup)
+        easy = prefill_section(swa, timer, dev, 0.05, ks, kw, seed=dist.rank, with_e2e=False)
+        extra["prefill_easy"] = {
+            "tflops": easy["flops"] / (sum(easy["step_ms"]) / 1e3 / ks) / 1e12,
+            "kernel_tflops": easy["flops"] / (statistics.mean(easy["kern_ms"]) / 1e3) / 1e12,
+            "ms_per_step": statistics.mean(easy["step_ms"]),
+            "realised_frac": easy["realised_frac"], "useful_tflop": easy["flops"] / 1e12}
+        dec = decode_section(swa, timer, dev, ks, kw, seed=dist.rank)
+        dk = statistics.mean(dec["kern_ms"]) / 1e3
+        ds = statistics.mean(dec["step_ms"]) / 1e3
+        hbm = float(peaks["hbm_gbs"])
+        extra["decode"] = {
+            "gbs": dec["bytes"] / ds / 1e9, "ms_per_step": ds * 1e3, "n_routed": dec["n_routed"],
+            "bytes_per_step": dec["bytes"],
+            "roofline": {"bound": "hbm", "achieved": dec["bytes"] / dk / 1e9, "peak": hbm,
+                         "unit": "GB/s", "frac": dec["bytes"] / dk / 1e9 / hbm,
+                         "kernel": "decode_split_kernel"},
+            "workload": "decode bf16: 16 sequences x 32768 cached tokens, H=16, d=128, W=1024, "
+                        "gate Bernoulli(0.13)"}
+        rt = route_section(swa, timer, dev, ks, kw, seed=dist.rank)
+        rs = statistics.mean(rt["step_ms"]) / 1e3
+        extra["route"] = {"gbs": rt["bytes"] / rs / 1e9, "ms_per_step": rs * 1e3,
+                          "workload": "router GEMV, 32768 tokens x d_model 2048, bf16"}
+        du = dual_section(swa, timer, dev, ks, kw, seed=dist.rank)
+        dm = statistics.mean(du["step_ms"]) / 1e3
+        extra["dual"] = {"tflops": du["flops"] / dm / 1e12, "ms_per_step": dm * 1e3,
+                         "kernel_tflops": du["flops"] / (statistics.mean(du["kern_ms"]) / 1e3) / 1e12,
+                         "workload": "dual-branch forward bf16, B=2 Hq=16 Hkv=4 d=128 N=8192 W=1024"}
+
+    cpu = None
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        r = oracle_sample(main["d"], budget_s=args.cpu_budget)
+        cpu = {"value": r["flops_per_s"] / 1e12, "unit": "TFLOP/s", "cores": r["cores"],
+               "kind": "oracle",
+               "sample": f"{r['rows']} random (row, head) outputs of the N=32768 workload, "
+                         f"{r['seconds']:.1f} s of fp64 oracle work on {r['cores']} threads"}
+
+    if dist.rank == 0:
+        d = main["d"]
+        line = {
+            "metric": METRIC, "value": value / 1e12, "unit": "TFLOP/s", "n_gpus": dist.world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * slowest / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "long-context routed prefill bf16: B=1 H=16 d=128 N=32768 "
+                                   "W=1024, gates in runs (mean routed run 64) at routed "
+                                   "fraction 0.13",
+                       "B": d["B"], "N": d["N"], "H": d["Hq"], "d": d["d"], "W": d["W"],
+                       "realised_routed_fraction": main["realised_frac"],
+                       "useful_tflop_per_step": main["flops"] / 1e12,
+                       "l2": "flushed (256 MiB write) before every timed step",
+                       "parallelism": f"replicas x{dist.world}, one sequence per GPU"},
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak,
+                         "traffic": traffic, "kernel": "tc_attention_kernel",
+                         "peak_source": f"{peaks_src} bf16 dense (burst)"},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value / 1e12, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": main["h2d"], "d2h_bytes_per_step": main["d2h"]},
+            "gpu_launches": 4 * args.steps,
+            "clocks": clk,
+            "wall_s_headline": wall,
+        }
+        line.update(extra)
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--headline-only", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    dist = Dist()
+    try:
+        if args.impl == "reference":
+            run_reference(args, dist)
+        else:
+            run_ours(args, dist)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,152 @@
+/*
+ * swiattn.h -- C ABI of libswiattn, the GB300 (sm_103a) hot path of SwiAttn,
+ * token-level routed hybrid attention.
+ *
+ * The method (SwiAttn report, paper-daily.com retrieval report of 2026-03-31,
+ * section 2 "方法详解"): at every layer a linear router R scores each token;
+ * the hard gate sigma = 1(sigmoid(R(h)) > 0.5) chooses, per query row, causal
+ * full attention over keys [0, i] (O_FULL) or sliding-window attention over
+ * keys [i-W+1, i] (O_SWA, the window definition of the weimeta.cn glossary
+ * "滑窗注意力 Sliding Window Attention 是什么", section "详细解释").  Both
+ * branches share one Q/K/V and, at decode time, one KV cache; the layer output
+ * is O = sigma*O_FULL + (1-sigma)*O_SWA.  Training adds the divergence
+ * ||o_FULL - o_SWA||^2, the adaptive weight
+ * gamma = gamma_base/(eps + NLL + alpha*||.||^2) and the regulariser
+ * gamma*softplus(R(h)).
+ *
+ * Conventions for every call
+ *  - Pointers are DEVICE pointers unless stated; the caller allocates and owns
+ *    every buffer, including workspaces.  The library keeps no pointer after a
+ *    call returns and allocates no device memory.
+ *  - All work is enqueued on `stream` (a cudaStream_t passed as void*; NULL is
+ *    the legacy default stream) and is asynchronous: a return of SWIATTN_OK
+ *    means "validated and launched".
+ *  - Arguments are validated before anything is launched; on any error
+ *    nothing is launched and outputs are untouched.
+ *  - Layouts are row-major and contiguous: q [B,N,Hq,d]; k, v [B,N,Hkv,d];
+ *    decode caches [B,Lmax,Hkv,d]; per-token arrays [B,N].  Every tensor
+ *    pointer must be 16-byte aligned.  Query head h reads KV head
+ *    h / (Hq/Hkv) (contiguous GQA groups; the glossary's FAQ on GQA).
+ *  - Rows are 0-based; the window is clipped at key 0.  The gate is
+ *    logit > 0 (strictly), which is sigmoid(logit) > 0.5.
+ *  - dtype selects the element type of the q/k/v/h/w/o tensors of the call:
+ *    SWIATTN_BF16 (compute in fp32 with bf16 operands on the tensor cores) or
+ *    SWIATTN_F32 (fp32 end to end on CUDA cores).  Statistics (logits, lse,
+ *    mse, gamma, reg_loss, nll) are always fp32.
+ *  - Device-side waits are bounded; if one ever expires the kernel returns
+ *    early and records the fact, which swiattn_get_device_error reports.
+ */
+#ifndef SWIATTN_H
+#define SWIATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SWIATTN_OK = 0,
+    SWIATTN_EINVAL = 1,        /* bad pointer, size, alignment or workspace too small */
+    SWIATTN_EUNSUPPORTED = 2,  /* valid request this build does not implement (e.g. d) */
+    SWIATTN_ECUDA = 3,         /* a CUDA runtime/driver call failed (launch, symbol, map) */
+    SWIATTN_ETIMEOUT = 4       /* a device-side bounded wait expired (from get_device_error) */
+} swiattn_status;
+
+typedef enum { SWIATTN_F32 = 0, SWIATTN_BF16 = 1 } swiattn_dtype;
+
+/* Router GEMV and hard gate (report section 2, router design; one scalar per
+ * token per layer, shared by every head):
+ *   logits[t] = sum_j h[t,j] * w[j] + bias   (fp32 accumulation)
+ *   gate[t]   = logits[t] > 0 ? 1 : 0
+ * h [tokens, d_model], w [d_model] of `dtype`; logits fp32 [tokens];
+ * gate uint8 [tokens].  d_model must be a multiple of 8 (bf16) or 4 (fp32).
+ * tokens == 0 is a valid no-op. */
+int swiattn_route(const void* h, const void* w, float bias, int64_t tokens, int d_model,
+                  int dtype, float* logits, uint8_t* gate, void* stream);
+
+/* Bytes of device workspace swiattn_prefill needs for these sizes. */
+size_t swiattn_prefill_workspace(int B, int N, int Hq, int Hkv, int d, int W, int dtype);
+
+/* Routed causal prefill (report section 2, dual-branch computation, inference
+ * form).  For each batch b, query head h and row i, with
+ *   [lo, hi] = gate[b,i] ? [0, i] : [max(0, i-W+1), i]
+ * o[b,i,h,:] = softmax_j(scale * q_i . k_j) v_j over j in [lo, hi], which equals
+ * sigma*O_FULL + (1-sigma)*O_SWA with a 0/1 gate.  Window rows cost about W
+ * keys, routed rows about i keys: masked and out-of-window key tiles are never
+ * visited.  gate uint8 [B,N]; o [B,N,Hq,d] of `dtype`; lse (nullable) fp32
+ * [B,N,Hq] receives ln sum_j exp(scale * q_i . k_j) over the visited keys.
+ * d in {64, 128} for SWIATTN_F32; d == 128 for SWIATTN_BF16.
+ * workspace: at least swiattn_prefill_workspace(...) bytes, 256-byte aligned;
+ * it is scratch only (its contents need not be preserved between calls).
+ * Calls that share one workspace must not overlap in time. */
+int swiattn_prefill(const void* q, const void* k, const void* v, const uint8_t* gate, void* o,
+                    float* lse, int B, int N, int Hq, int Hkv, int d, int W, float scale,
+                    int dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of device workspace swiattn_decode needs for these sizes. */
+size_t swiattn_decode_workspace(int B, int Lmax, int Hq, int Hkv, int d, int W, int dtype);
+
+/* One decode step over a shared KV cache (report section 2: both branches
+ * share the cache; section 6: decode reads the last W entries or all of them).
+ * Sequence b holds seq_lens[b] tokens (1 <= seq_lens[b] <= Lmax), the newest
+ * being the query's own, at position L = seq_lens[b]-1.  The query reads cache
+ * entries [max(0, L-W+1), L] if gate[b] == 0, else [0, L].
+ * q [B,Hq,d]; k_cache, v_cache [B,Lmax,Hkv,d]; seq_lens int32 [B];
+ * gate uint8 [B]; o [B,Hq,d]; lse (nullable) fp32 [B,Hq].
+ * d in {64, 128}; Hkv*d/8 (bf16) or Hkv*d/4 (fp32) <= 1024; Hq/Hkv <= 8.
+ * workspace: at least swiattn_decode_workspace(...) bytes, scratch only. */
+int swiattn_decode(const void* q, const void* k_cache, const void* v_cache,
+                   const int32_t* seq_lens, const uint8_t* gate, void* o, float* lse, int B,
+                   int Lmax, int Hq, int Hkv, int d, int W, float scale, int dtype,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of device workspace swiattn_dual_branch needs for these sizes. */
+size_t swiattn_dual_branch_workspace(int B, int N, int Hq, int Hkv, int d, int W, int dtype);
+
+/* Training-side dual-branch forward (report section 2, dual-branch computation
+ * and adaptive regularisation loss).  For every token both branches:
+ *   o_full[b,i,h,:] over keys [0, i];  o_swa[b,i,h,:] over [max(0,i-W+1), i]
+ *   mse[b,i]      = sum_{h,c} (o_full - o_swa)^2, from the fp32 values before
+ *                   any rounding to the output type
+ *   gamma[b,i]    = gamma_base / (eps + nll[b,i] + alpha * mse[b,i])
+ *   reg_loss[b,i] = gamma[b,i] * softplus(logits[b,i])
+ *   o_gated[b,i,h,:] (nullable) = logits[b,i] > 0 ? o_full : o_swa
+ * logits, nll fp32 [B,N] (nll is treated as a constant input); o_full, o_swa,
+ * o_gated [B,N,Hq,d] of `dtype`; mse, gamma, reg_loss fp32 [B,N].
+ * The report's values are gamma_base = 1e-3, eps = 0.1, alpha = 100.
+ * workspace: at least swiattn_dual_branch_workspace(...) bytes, scratch only. */
+int swiattn_dual_branch(const void* q, const void* k, const void* v, const float* logits,
+                        const float* nll, void* o_full, void* o_swa, void* o_gated, float* mse,
+                        float* gamma, float* reg_loss, int B, int N, int Hq, int Hkv, int d,
+                        int W, float scale, float gamma_base, float eps, float alpha, int dtype,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronises `stream`, then returns and clears the device error word of the
+ * current device: SWIATTN_OK, SWIATTN_ETIMEOUT if a bounded device wait
+ * expired since the last query, or SWIATTN_ECUDA if the synchronisation itself
+ * failed. */
+int swiattn_get_device_error(void* stream);
+
+/* Static, NUL-terminated name of a status code. */
+const char* swiattn_status_string(int status);
+
+/* Timing hook.  When both are non-NULL, every later swiattn_prefill,
+ * swiattn_decode and swiattn_dual_branch call records `start` (a cudaEvent_t
+ * passed as void*) on its stream immediately before launching its dominant
+ * kernel (the attention kernel, or the decode split kernel) and `stop`
+ * immediately after it, so cudaEventElapsedTime gives that kernel's device
+ * time alone.  Passing NULL, NULL turns the hook off.  Process-wide setting;
+ * the events stay owned by the caller and must outlive their use. */
+void swiattn_set_profile_events(void* start, void* stop);
+
+/* Number of SMs of the current device (the persistent kernels launch one CTA
+ * per SM), or -1 on a CUDA error. */
+int swiattn_num_sms(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SWIATTN_H */

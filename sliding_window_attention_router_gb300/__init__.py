@@ -1,0 +1,225 @@
+"""SwiAttn routed hybrid attention on GB300: thin Python binding of libswiattn.
+
+Every function here marshals arguments to the C ABI declared in
+``include/swiattn.h`` (same names, without the ``swiattn_`` prefix) and
+returns; all computation runs in the library's CUDA kernels.  PyTorch only
+provides device memory and the current stream.  There is no fallback: if the
+shared library is missing, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from typing import Optional
+
+import torch
+
+__all__ = [
+    "SwiAttnError", "F32", "BF16", "library_path", "route", "prefill", "decode", "dual_branch",
+    "prefill_workspace", "decode_workspace", "dual_branch_workspace", "get_device_error",
+    "status_string", "num_sms", "set_profile_events", "EXPORTS",
+]
+
+F32, BF16 = 0, 1
+_DT = {torch.float32: F32, torch.bfloat16: BF16}
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libswiattn.so")
+_lock = threading.Lock()
+_lib = None
+
+# Every symbol include/swiattn.h declares.
+EXPORTS = (
+    "swiattn_route", "swiattn_prefill_workspace", "swiattn_prefill", "swiattn_decode_workspace",
+    "swiattn_decode", "swiattn_dual_branch_workspace", "swiattn_dual_branch",
+    "swiattn_get_device_error", "swiattn_status_string", "swiattn_set_profile_events",
+    "swiattn_num_sms",
+)
+
+
+class SwiAttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def _load() -> ctypes.CDLL:
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(
+                    f"libswiattn.so not found at {_LIB_PATH}: build it first "
+                    "(python -c 'import __graft_entry__ as g; g.build()')")
+            lib = ctypes.CDLL(_LIB_PATH)
+            vp, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
+                                     ctypes.c_float, ctypes.c_size_t)
+            lib.swiattn_route.argtypes = [vp, vp, f32, i64, i32, i32, vp, vp, vp]
+            lib.swiattn_prefill_workspace.argtypes = [i32] * 7
+            lib.swiattn_prefill_workspace.restype = sz
+            lib.swiattn_prefill.argtypes = [vp] * 6 + [i32] * 6 + [f32, i32, vp, sz, vp]
+            lib.swiattn_decode_workspace.argtypes = [i32] * 7
+            lib.swiattn_decode_workspace.restype = sz
+            lib.swiattn_decode.argtypes = [vp] * 7 + [i32] * 6 + [f32, i32, vp, sz, vp]
+            lib.swiattn_dual_branch_workspace.argtypes = [i32] * 7
+            lib.swiattn_dual_branch_workspace.restype = sz
+            lib.swiattn_dual_branch.argtypes = ([vp] * 11 + [i32] * 6 + [f32] * 4
+                                                + [i32, vp, sz, vp])
+            lib.swiattn_get_device_error.argtypes = [vp]
+            lib.swiattn_status_string.argtypes = [i32]
+            lib.swiattn_status_string.restype = ctypes.c_char_p
+            lib.swiattn_num_sms.argtypes = []
+            lib.swiattn_set_profile_events.argtypes = [vp, vp]
+            lib.swiattn_set_profile_events.restype = None
+            for name in ("swiattn_route", "swiattn_prefill", "swiattn_decode",
+                         "swiattn_dual_branch", "swiattn_get_device_error", "swiattn_num_sms"):
+                getattr(lib, name).restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return _load().swiattn_status_string(int(status)).decode()
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise SwiAttnError(status, where)
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+def num_sms() -> int:
+    return int(_load().swiattn_num_sms())
+
+
+def set_profile_events(start: Optional[torch.cuda.Event], stop: Optional[torch.cuda.Event]):
+    """Record start/stop around the dominant kernel of later calls (None, None: off)."""
+    if start is None or stop is None:
+        _load().swiattn_set_profile_events(None, None)
+    else:
+        _load().swiattn_set_profile_events(ctypes.c_void_p(start.cuda_event),
+                                           ctypes.c_void_p(stop.cuda_event))
+
+
+def get_device_error() -> int:
+    """Synchronise the current stream; return and clear the device error word."""
+    return int(_load().swiattn_get_device_error(_stream()))
+
+
+def route(h: torch.Tensor, w: torch.Tensor, bias: float, logits=None, gate=None):
+    """logits = h @ w + bias (fp32), gate = logits > 0 (uint8).  h [T, D]."""
+    _dev(h, "h")
+    _dev(w, "w", h.dtype)
+    T, D = h.shape
+    logits = logits if logits is not None else torch.empty(T, device=h.device, dtype=torch.float32)
+    gate = gate if gate is not None else torch.empty(T, device=h.device, dtype=torch.uint8)
+    _check(_load().swiattn_route(_ptr(h), _ptr(w), float(bias), T, D, _DT[h.dtype], _ptr(logits),
+                                 _ptr(gate), _stream()), "swiattn_route")
+    return logits, gate
+
+
+def prefill_workspace(B, N, Hq, Hkv, d, W, dtype) -> int:
+    return int(_load().swiattn_prefill_workspace(B, N, Hq, Hkv, d, W, _DT.get(dtype, dtype)))
+
+
+def decode_workspace(B, Lmax, Hq, Hkv, d, W, dtype) -> int:
+    return int(_load().swiattn_decode_workspace(B, Lmax, Hq, Hkv, d, W, _DT.get(dtype, dtype)))
+
+
+def dual_branch_workspace(B, N, Hq, Hkv, d, W, dtype) -> int:
+    return int(_load().swiattn_dual_branch_workspace(B, N, Hq, Hkv, d, W, _DT.get(dtype, dtype)))
+
+
+def _workspace(nbytes: int, device, ws: Optional[torch.Tensor]):
+    if ws is None:
+        ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+    return ws
+
+
+def prefill(q, k, v, gate, W: int, scale: Optional[float] = None, out=None, want_lse=False,
+            workspace=None):
+    """Routed prefill.  q [B,N,Hq,d], k/v [B,N,Hkv,d], gate uint8 [B,N] -> o [B,N,Hq,d]."""
+    _dev(q, "q")
+    _dev(k, "k", q.dtype)
+    _dev(v, "v", q.dtype)
+    _dev(gate, "gate", torch.uint8)
+    B, N, Hq, d = q.shape
+    Hkv = k.shape[2]
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o = out if out is not None else torch.empty_like(q)
+    lse = torch.empty((B, N, Hq), device=q.device, dtype=torch.float32) if want_lse else None
+    nbytes = prefill_workspace(B, N, Hq, Hkv, d, W, q.dtype)
+    ws = _workspace(nbytes, q.device, workspace)
+    _check(_load().swiattn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(o), _ptr(lse), B, N,
+                                   Hq, Hkv, d, W, float(scale), _DT[q.dtype], _ptr(ws),
+                                   ws.numel(), _stream()), "swiattn_prefill")
+    return (o, lse) if want_lse else o
+
+
+def decode(q, k_cache, v_cache, seq_lens, gate, W: int, scale: Optional[float] = None, out=None,
+           want_lse=False, workspace=None):
+    """One decode step.  q [B,Hq,d], caches [B,Lmax,Hkv,d], seq_lens int32 [B], gate uint8 [B]."""
+    _dev(q, "q")
+    _dev(k_cache, "k_cache", q.dtype)
+    _dev(v_cache, "v_cache", q.dtype)
+    _dev(seq_lens, "seq_lens", torch.int32)
+    _dev(gate, "gate", torch.uint8)
+    B, Hq, d = q.shape
+    Lmax, Hkv = k_cache.shape[1], k_cache.shape[2]
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o = out if out is not None else torch.empty_like(q)
+    lse = torch.empty((B, Hq), device=q.device, dtype=torch.float32) if want_lse else None
+    ws = _workspace(decode_workspace(B, Lmax, Hq, Hkv, d, W, q.dtype), q.device, workspace)
+    _check(_load().swiattn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens),
+                                  _ptr(gate), _ptr(o), _ptr(lse), B, Lmax, Hq, Hkv, d, W,
+                                  float(scale), _DT[q.dtype], _ptr(ws), ws.numel(), _stream()),
+           "swiattn_decode")
+    return (o, lse) if want_lse else o
+
+
+def dual_branch(q, k, v, logits, nll, W: int, scale: Optional[float] = None, gamma_base=1e-3,
+                eps=0.1, alpha=100.0, want_gated=True, outs=None, workspace=None):
+    """Dual-branch forward: dict(o_full, o_swa, o_gated, mse, gamma, reg_loss)."""
+    _dev(q, "q")
+    _dev(k, "k", q.dtype)
+    _dev(v, "v", q.dtype)
+    _dev(logits, "logits", torch.float32)
+    _dev(nll, "nll", torch.float32)
+    B, N, Hq, d = q.shape
+    Hkv = k.shape[2]
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    if outs is None:
+        outs = dict(o_full=torch.empty_like(q), o_swa=torch.empty_like(q),
+                    o_gated=torch.empty_like(q) if want_gated else None,
+                    mse=torch.empty((B, N), device=q.device, dtype=torch.float32),
+                    gamma=torch.empty((B, N), device=q.device, dtype=torch.float32),
+                    reg_loss=torch.empty((B, N), device=q.device, dtype=torch.float32))
+    ws = _workspace(dual_branch_workspace(B, N, Hq, Hkv, d, W, q.dtype), q.device, workspace)
+    _check(_load().swiattn_dual_branch(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(logits), _ptr(nll), _ptr(outs["o_full"]),
+        _ptr(outs["o_swa"]), _ptr(outs.get("o_gated")), _ptr(outs["mse"]), _ptr(outs["gamma"]),
+        _ptr(outs["reg_loss"]), B, N, Hq, Hkv, d, W, float(scale), float(gamma_base), float(eps),
+        float(alpha), _DT[q.dtype], _ptr(ws), ws.numel(), _stream()), "swiattn_dual_branch")
+    return outs

@@ -1,0 +1,264 @@
+// Decode over a KV cache shared by both branches (SwiAttn report, section 2:
+// the two branches share the KV cache; section 6: decode reads either the
+// window or the whole history).  A window token reads the last W cache
+// entries, a routed one all L: the bytes moved are the whole cost.
+//
+// Split-KV: CTA (chunk c, sequence b) streams `chunk` consecutive tokens of the
+// visited range.  A token's K (or V) row for every KV head is one contiguous
+// Hkv*d run, so each thread issues one 16-byte load per token and tensor, and
+// the whole CTA reads it fully coalesced.  Threads of one KV head (d/VEC
+// consecutive lanes) reduce q.k with xor-shuffles; each holds VEC output
+// columns of the G = Hq/Hkv query heads of its group.  Partial (m, l, o) per
+// chunk go to the workspace; a second kernel merges them by log-sum-exp.
+
+#include "swiattn_internal.h"
+
+#include <cuda_bf16.h>
+#include <math.h>
+
+namespace swi {
+namespace {
+
+constexpr int kChunk = 128;   // tokens per split
+constexpr int kUnroll = 8;    // tokens in flight per thread
+
+template <typename T>
+struct Vec;
+template <>
+struct Vec<__nv_bfloat16> {
+    static constexpr int N = 8;
+    __device__ static void load(const uint4& u, float* f) {
+        const __nv_bfloat162* x = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const float2 a = __bfloat1622float2(x[t]);
+            f[2 * t] = a.x;
+            f[2 * t + 1] = a.y;
+        }
+    }
+};
+template <>
+struct Vec<float> {
+    static constexpr int N = 4;
+    __device__ static void load(const uint4& u, float* f) {
+        f[0] = __uint_as_float(u.x);
+        f[1] = __uint_as_float(u.y);
+        f[2] = __uint_as_float(u.z);
+        f[3] = __uint_as_float(u.w);
+    }
+};
+
+__device__ __forceinline__ float ex2f(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ void visited(const int32_t* seq_lens, const uint8_t* gate, int b, int W,
+                                        int& lo, int& n) {
+    const int L = seq_lens[b];
+    const int pos = L - 1;
+    lo = gate[b] ? 0 : max(0, pos - W + 1);
+    n = L - lo;
+}
+
+template <typename T, int D, int G>
+__global__ void decode_split_kernel(const T* __restrict__ q, const T* __restrict__ kc,
+                                    const T* __restrict__ vc, const int32_t* __restrict__ seq_lens,
+                                    const uint8_t* __restrict__ gate, float* __restrict__ part,
+                                    int Lmax, int Hq, int Hkv, int W, float scale_log2,
+                                    int max_chunks) {
+    constexpr int VEC = Vec<T>::N;
+    constexpr int LPH = D / VEC;   // lanes per KV head
+    const int b = blockIdx.y, c = blockIdx.x;
+    int lo, n;
+    visited(seq_lens, gate, b, W, lo, n);
+    const int t0 = lo + c * kChunk;
+    if (c * kChunk >= n) return;
+    const int t1 = min(lo + n, t0 + kChunk);
+
+    // Threads past Hkv*LPH (block rounded up to whole warps) mirror the last
+    // KV head so shuffles stay full-warp; they write nothing.
+    const int active = threadIdx.x < Hkv * LPH;
+    const int tid = active ? threadIdx.x : (Hkv - 1) * LPH + (threadIdx.x % LPH);
+    const int kvh = tid / LPH, sub = tid % LPH;
+    const size_t row_vecs = (size_t)Hkv * LPH;   // uint4 per token row (all KV heads)
+
+    float qf[G][VEC], acc[G][VEC], m[G], l[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        const int hq = kvh * G + g;
+        uint4 u = *reinterpret_cast<const uint4*>(q + ((size_t)b * Hq + hq) * D + sub * VEC);
+        Vec<T>::load(u, qf[g]);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+            qf[g][e] *= scale_log2;
+            acc[g][e] = 0.f;
+        }
+        m[g] = -INFINITY;
+        l[g] = 0.f;
+    }
+
+    const uint4* kb = reinterpret_cast<const uint4*>(kc) + (size_t)b * Lmax * row_vecs + tid;
+    const uint4* vb = reinterpret_cast<const uint4*>(vc) + (size_t)b * Lmax * row_vecs + tid;
+    for (int t = t0; t < t1; t += kUnroll) {
+        uint4 ku[kUnroll], vu[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int tt = min(t + u, t1 - 1);   // clamp: duplicates are masked below
+            ku[u] = ld_stream(kb + (size_t)tt * row_vecs);
+            vu[u] = ld_stream(vb + (size_t)tt * row_vecs);
+        }
+        float s[kUnroll][G];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            float kf[VEC];
+            Vec<T>::load(ku[u], kf);
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                float d0 = 0.f;
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) d0 = fmaf(qf[g][e], kf[e], d0);
+#pragma unroll
+                for (int off = LPH / 2; off > 0; off >>= 1)
+                    d0 += __shfl_xor_sync(0xffffffffu, d0, off);
+                s[u][g] = (t + u < t1) ? d0 : -INFINITY;
+            }
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            float mx = m[g];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) mx = fmaxf(mx, s[u][g]);
+            const float corr = ex2f(m[g] - mx);
+            float ps = 0.f;
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) acc[g][e] *= corr;
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const float p = ex2f(s[u][g] - mx);
+                ps += p;
+                float vf[VEC];
+                Vec<T>::load(vu[u], vf);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) acc[g][e] = fmaf(p, vf[e], acc[g][e]);
+            }
+            l[g] = l[g] * corr + ps;
+            m[g] = mx;
+        }
+    }
+
+    if (!active) return;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        const int hq = kvh * G + g;
+        float* dst = part + (((size_t)b * max_chunks + c) * Hq + hq) * (D + 2);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) dst[sub * VEC + e] = acc[g][e];
+        if (sub == 0) {
+            dst[D] = m[g];
+            dst[D + 1] = l[g];
+        }
+    }
+}
+
+template <typename T, int D>
+__global__ void decode_combine_kernel(const float* __restrict__ part,
+                                      const int32_t* __restrict__ seq_lens,
+                                      const uint8_t* __restrict__ gate, T* __restrict__ o,
+                                      float* __restrict__ lse, int Hq, int W, int max_chunks) {
+    const int hq = blockIdx.x, b = blockIdx.y, cidx = threadIdx.x;
+    int lo, n;
+    visited(seq_lens, gate, b, W, lo, n);
+    const int nc = (n + kChunk - 1) / kChunk;
+    const float* base = part + ((size_t)b * max_chunks * Hq + hq) * (D + 2);
+    const size_t cstride = (size_t)Hq * (D + 2);
+    float M = -INFINITY;
+    for (int c = 0; c < nc; ++c) M = fmaxf(M, base[c * cstride + D]);
+    float L = 0.f, acc = 0.f;
+    for (int c = 0; c < nc; ++c) {
+        const float* pc = base + c * cstride;
+        const float w = ex2f(pc[D] - M);
+        L = fmaf(pc[D + 1], w, L);
+        acc = fmaf(pc[cidx], w, acc);
+    }
+    const float val = acc / L;
+    T* dst = o + ((size_t)b * Hq + hq) * D + cidx;
+    if constexpr (sizeof(T) == 2) {
+        *dst = __float2bfloat16_rn(val);
+    } else {
+        *dst = val;
+    }
+    if (lse && cidx == 0) lse[(size_t)b * Hq + hq] = (M + __log2f(L)) * 0.69314718055994531f;
+}
+
+template <typename T, int D, int G>
+cudaError_t launch_split(const void* q, const void* kc, const void* vc, const int32_t* sl,
+                         const uint8_t* gate, float* part, int B, int Lmax, int Hq, int Hkv, int W,
+                         float scale_log2, int max_chunks, cudaStream_t s) {
+    const int threads = (Hkv * (D / Vec<T>::N) + 31) / 32 * 32;
+    dim3 grid(max_chunks, B);
+    decode_split_kernel<T, D, G><<<grid, threads, 0, s>>>(
+        static_cast<const T*>(q), static_cast<const T*>(kc), static_cast<const T*>(vc), sl, gate,
+        part, Lmax, Hq, Hkv, W, scale_log2, max_chunks);
+    return cudaGetLastError();
+}
+
+template <typename T, int D>
+cudaError_t launch_typed(const void* q, const void* kc, const void* vc, const int32_t* sl,
+                         const uint8_t* gate, void* o, float* lse, int B, int Lmax, int Hq,
+                         int Hkv, int W, float scale, float* part, int max_chunks, cudaStream_t s) {
+    const float sl2 = scale * 1.4426950408889634f;
+    const int G = Hq / Hkv;
+    cudaError_t e;
+    prof_start(s);
+    switch (G) {
+        case 1: e = launch_split<T, D, 1>(q, kc, vc, sl, gate, part, B, Lmax, Hq, Hkv, W, sl2, max_chunks, s); break;
+        case 2: e = launch_split<T, D, 2>(q, kc, vc, sl, gate, part, B, Lmax, Hq, Hkv, W, sl2, max_chunks, s); break;
+        case 4: e = launch_split<T, D, 4>(q, kc, vc, sl, gate, part, B, Lmax, Hq, Hkv, W, sl2, max_chunks, s); break;
+        case 8: e = launch_split<T, D, 8>(q, kc, vc, sl, gate, part, B, Lmax, Hq, Hkv, W, sl2, max_chunks, s); break;
+        default: return cudaErrorInvalidValue;
+    }
+    prof_stop(s);
+    if (e != cudaSuccess) return e;
+    decode_combine_kernel<T, D><<<dim3(Hq, B), D, 0, s>>>(part, sl, gate, static_cast<T*>(o), lse,
+                                                          Hq, W, max_chunks);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+DecodeWs decode_ws_layout(int B, int Lmax, int Hq, int d) {
+    DecodeWs L;
+    L.chunk = kChunk;
+    L.max_chunks = (Lmax + kChunk - 1) / kChunk;
+    L.part = 0;
+    L.total = sizeof(float) * (size_t)B * L.max_chunks * Hq * (d + 2);
+    L.total = (L.total + 255) & ~static_cast<size_t>(255);
+    return L;
+}
+
+cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const int32_t* seq_lens,
+                          const uint8_t* gate, void* o, float* lse, int B, int Lmax, int Hq,
+                          int Hkv, int d, int W, float scale, int dtype, const DecodeWs& L,
+                          char* ws, cudaStream_t s) {
+    float* part = reinterpret_cast<float*>(ws + L.part);
+    if (dtype == 1) {
+        if (d == 128) return launch_typed<__nv_bfloat16, 128>(q, kc, vc, seq_lens, gate, o, lse, B, Lmax, Hq, Hkv, W, scale, part, L.max_chunks, s);
+        if (d == 64) return launch_typed<__nv_bfloat16, 64>(q, kc, vc, seq_lens, gate, o, lse, B, Lmax, Hq, Hkv, W, scale, part, L.max_chunks, s);
+    } else {
+        if (d == 128) return launch_typed<float, 128>(q, kc, vc, seq_lens, gate, o, lse, B, Lmax, Hq, Hkv, W, scale, part, L.max_chunks, s);
+        if (d == 64) return launch_typed<float, 64>(q, kc, vc, seq_lens, gate, o, lse, B, Lmax, Hq, Hkv, W, scale, part, L.max_chunks, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace swi

@@ -1,0 +1,190 @@
+// Gate-driven scheduling for the routed prefill.
+//
+// A row i of batch b is a "far" row when its gate routes it to full attention
+// and i >= W (for i < W its full range [0, i] equals its window).  Far rows
+// are compacted (ascending i) so that 128 of them share one query tile that
+// walks keys [0, max i]; every other row is served by the 128-row band tile
+// that holds it, which walks only the window keys.  The work list is sorted by
+// cost (key blocks), longest first, for the persistent attention kernel.
+
+#include "swiattn_internal.h"
+
+#include <cuda_bf16.h>
+
+namespace swi {
+namespace {
+
+constexpr int kScanThreads = 1024;
+constexpr int kCostBuckets = 4096;
+
+__device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+// One CTA per batch: exclusive scan of the far-row flags.
+__global__ void __launch_bounds__(kScanThreads) scan_far_rows_kernel(
+    const uint8_t* __restrict__ gate, int N, int W, int* __restrict__ routed_list,
+    int* __restrict__ routed_count, int* __restrict__ tile_prefix) {
+    __shared__ int warp_tot[32];
+    __shared__ int carry;
+    const int b = blockIdx.x;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int NT = cdiv(N, kBM);
+    if (threadIdx.x == 0) carry = 0;
+    __syncthreads();
+    for (int base = 0; base < N; base += kScanThreads) {
+        const int i = base + threadIdx.x;
+        const int f = (i < N && i >= W && gate[(size_t)b * N + i] != 0) ? 1 : 0;
+        int x = f;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) warp_tot[w] = x;
+        __syncthreads();
+        if (w == 0) {
+            int t = warp_tot[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, t, o);
+                if (lane >= o) t += y;
+            }
+            warp_tot[lane] = t;   // inclusive totals per warp
+        }
+        __syncthreads();
+        const int excl = carry + (w > 0 ? warp_tot[w - 1] : 0) + x - f;
+        if (f) routed_list[(size_t)b * N + excl] = i;
+        if (i < N && (i % kBM) == 0) tile_prefix[(size_t)b * (NT + 1) + i / kBM] = excl;
+        __syncthreads();
+        if (threadIdx.x == kScanThreads - 1) carry = excl + f;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        routed_count[b] = carry;
+        tile_prefix[(size_t)b * (NT + 1) + NT] = carry;
+    }
+}
+
+// Cost (key blocks) of tile u of the enumeration [far tiles | band tiles] per
+// batch, or -1 when the tile does not exist or has nothing to write.
+__device__ __forceinline__ int tile_cost(int u, const int* routed_list, const int* routed_count,
+                                         const int* tile_prefix, int N, int W, int NT, int& b,
+                                         int& kind, int& tile) {
+    b = u / (2 * NT);
+    const int rem = u % (2 * NT);
+    if (rem < NT) {
+        kind = kItemFar;
+        tile = rem;
+        const int R = routed_count[b];
+        if (tile * kBM >= R) return -1;
+        const int last = min(R, (tile + 1) * kBM) - 1;
+        return cdiv(routed_list[(size_t)b * N + last] + 1, kBN);
+    }
+    kind = kItemBand;
+    tile = rem - NT;
+    const int q0 = tile * kBM;
+    const int nrows = min(kBM, N - q0);
+    const int far_rows = tile_prefix[(size_t)b * (NT + 1) + tile + 1] -
+                         tile_prefix[(size_t)b * (NT + 1) + tile];
+    if (far_rows >= nrows) return -1;
+    const int kv0 = max(0, q0 - W + 1);
+    return cdiv(q0 + nrows - kv0, kBN);
+}
+
+// Single CTA: counting sort of tiles by descending cost, Hq items per tile.
+__global__ void __launch_bounds__(1024) build_items_kernel(
+    const int* __restrict__ routed_list, const int* __restrict__ routed_count,
+    const int* __restrict__ tile_prefix, int B, int N, int Hq, int W, WorkItem* __restrict__ items,
+    int* __restrict__ n_items) {
+    __shared__ int hist[kCostBuckets];
+    __shared__ int total;
+    const int NT = cdiv(N, kBM);
+    const int U = B * 2 * NT;
+    for (int c = threadIdx.x; c < kCostBuckets; c += blockDim.x) hist[c] = 0;
+    __syncthreads();
+    for (int u = threadIdx.x; u < U; u += blockDim.x) {
+        int b, kind, tile;
+        const int cost = tile_cost(u, routed_list, routed_count, tile_prefix, N, W, NT, b, kind, tile);
+        if (cost >= 0) atomicAdd(&hist[min(cost, kCostBuckets - 1)], 1);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // exclusive offsets in descending cost order
+        int run = 0;
+        for (int c = kCostBuckets - 1; c >= 0; --c) {
+            const int h = hist[c];
+            hist[c] = run;
+            run += h;
+        }
+        total = run;
+    }
+    __syncthreads();
+    for (int u = threadIdx.x; u < U; u += blockDim.x) {
+        int b, kind, tile;
+        const int cost = tile_cost(u, routed_list, routed_count, tile_prefix, N, W, NT, b, kind, tile);
+        if (cost < 0) continue;
+        const int pos = atomicAdd(&hist[min(cost, kCostBuckets - 1)], 1);
+        for (int h = 0; h < Hq; ++h) items[(size_t)pos * Hq + h] = WorkItem{kind, b, h, tile};
+    }
+    if (threadIdx.x == 0) n_items[0] = total * Hq;
+}
+
+// Compacted queries of far rows: qc[b, r] = q[b, routed_list[b, r]] for
+// r < R_b, zero up to the end of the last 128-row tile.
+__global__ void gather_far_q_kernel(const uint4* __restrict__ q, const int* __restrict__ routed_list,
+                                    const int* __restrict__ routed_count, uint4* __restrict__ qc,
+                                    int B, int N, int Hq) {
+    const int per_row = Hq * (kHD * 2 / 16);
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    for (int b = 0; b < B; ++b) {
+        const int R = routed_count[b];
+        const int Rp = min(N, cdiv(R, kBM) * kBM);
+        const size_t total = (size_t)Rp * per_row;
+        for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += stride) {
+            const int r = (int)(idx / per_row);
+            const int c = (int)(idx % per_row);
+            uint4 val = make_uint4(0u, 0u, 0u, 0u);
+            if (r < R) val = q[((size_t)b * N + routed_list[(size_t)b * N + r]) * per_row + c];
+            qc[((size_t)b * N + r) * per_row + c] = val;
+        }
+    }
+}
+
+}  // namespace
+
+PrefillWs prefill_ws_layout(int B, int N, int Hq, int d) {
+    auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+    const size_t NT = (static_cast<size_t>(N) + kBM - 1) / kBM;
+    PrefillWs L;
+    size_t off = 0;
+    L.routed_list = off;
+    off = up(off + sizeof(int) * (size_t)B * N);
+    L.routed_count = off;
+    off = up(off + sizeof(int) * (size_t)B);
+    L.tile_prefix = off;
+    off = up(off + sizeof(int) * (size_t)B * (NT + 1));
+    L.n_items = off;
+    off = up(off + sizeof(int) * 4);
+    L.max_items = static_cast<int>((size_t)B * 2 * NT * Hq);
+    L.items = off;
+    off = up(off + sizeof(WorkItem) * (size_t)L.max_items);
+    L.qc = off;
+    off = up(off + 2 * (size_t)B * N * Hq * d);
+    L.total = off;
+    return L;
+}
+
+cudaError_t launch_schedule(const uint8_t* gate, const void* q, int B, int N, int Hq, int W,
+                            const PrefillWs& L, char* ws, int num_sms, cudaStream_t s) {
+    int* list = reinterpret_cast<int*>(ws + L.routed_list);
+    int* count = reinterpret_cast<int*>(ws + L.routed_count);
+    int* prefix = reinterpret_cast<int*>(ws + L.tile_prefix);
+    scan_far_rows_kernel<<<B, kScanThreads, 0, s>>>(gate, N, W, list, count, prefix);
+    build_items_kernel<<<1, 1024, 0, s>>>(list, count, prefix, B, N, Hq, W,
+                                          reinterpret_cast<WorkItem*>(ws + L.items),
+                                          reinterpret_cast<int*>(ws + L.n_items));
+    gather_far_q_kernel<<<num_sms * 4, 256, 0, s>>>(static_cast<const uint4*>(q), list, count,
+                                                   reinterpret_cast<uint4*>(ws + L.qc), B, N, Hq);
+    return cudaGetLastError();
+}
+
+}  // namespace swi

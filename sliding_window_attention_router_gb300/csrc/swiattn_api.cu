@@ -1,0 +1,307 @@
+// C ABI of libswiattn: argument validation, workspace carving and launches.
+// Declarations and the contract of every entry point are in include/swiattn.h.
+
+#include "swiattn.h"
+#include "swiattn_internal.h"
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstring>
+#include <mutex>
+
+namespace swi {
+namespace {
+
+// Device error word: kernels OR kDevErrTimeout into it when a bounded wait
+// expires.  Host code reaches it through cudaGetSymbolAddress, once per device.
+__device__ unsigned int g_device_error;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned int* g_err_ptr[kMaxDevices];
+int g_num_sms[kMaxDevices];
+
+struct DeviceInfo {
+    unsigned int* err;
+    int sms;
+};
+
+bool device_info(DeviceInfo& out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_err_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return false;
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return false;
+        g_err_ptr[dev] = static_cast<unsigned int*>(p);
+        g_num_sms[dev] = sms;
+    }
+    out.err = g_err_ptr[dev];
+    out.sms = g_num_sms[dev];
+    return true;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+cudaEvent_t g_prof_start = nullptr, g_prof_stop = nullptr;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+
+int launched(cudaError_t e) { return e == cudaSuccess ? SWIATTN_OK : SWIATTN_ECUDA; }
+
+bool attn_shape_ok(int B, int N, int Hq, int Hkv, int d, int W) {
+    return B > 0 && N > 0 && Hq > 0 && Hkv > 0 && W > 0 && Hq % Hkv == 0 && (d == 64 || d == 128) &&
+           (int64_t)B * N * Hq * d < (int64_t(1) << 40);
+}
+
+}  // namespace
+
+void prof_start(cudaStream_t s) {
+    if (g_prof_start && g_prof_stop) cudaEventRecord(g_prof_start, s);
+}
+void prof_stop(cudaStream_t s) {
+    if (g_prof_start && g_prof_stop) cudaEventRecord(g_prof_stop, s);
+}
+
+bool make_tmap_4d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                       uint64_t d3, uint32_t box0, uint32_t box2) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[4] = {d0, d1, d2, d3};
+    const cuuint64_t strides[3] = {d0 * 2, d0 * d1 * 2, d0 * d1 * d2 * 2};
+    const cuuint32_t box[4] = {box0, 1, box2, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+DualWs dual_ws_layout(int B, int N, int Hq, int d, int dtype) {
+    DualWs L;
+    L.mse_part = 0;
+    L.total = dtype == SWIATTN_BF16 ? sizeof(float) * (size_t)B * N * Hq : 0;
+    L.total = (L.total + 255) & ~static_cast<size_t>(255);
+    (void)d;
+    return L;
+}
+
+}  // namespace swi
+
+using namespace swi;
+
+extern "C" {
+
+const char* swiattn_status_string(int status) {
+    switch (status) {
+        case SWIATTN_OK: return "SWIATTN_OK";
+        case SWIATTN_EINVAL: return "SWIATTN_EINVAL";
+        case SWIATTN_EUNSUPPORTED: return "SWIATTN_EUNSUPPORTED";
+        case SWIATTN_ECUDA: return "SWIATTN_ECUDA";
+        case SWIATTN_ETIMEOUT: return "SWIATTN_ETIMEOUT";
+        default: return "SWIATTN_UNKNOWN";
+    }
+}
+
+void swiattn_set_profile_events(void* start, void* stop) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_prof_start = static_cast<cudaEvent_t>(start);
+    g_prof_stop = static_cast<cudaEvent_t>(stop);
+}
+
+int swiattn_num_sms(void) {
+    DeviceInfo di;
+    return device_info(di) ? di.sms : -1;
+}
+
+int swiattn_get_device_error(void* stream) {
+    DeviceInfo di;
+    if (!device_info(di)) return SWIATTN_ECUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned int host = 0;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SWIATTN_ECUDA;
+    if (cudaMemcpy(&host, di.err, sizeof(host), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return SWIATTN_ECUDA;
+    if (host) {
+        const unsigned int zero = 0;
+        if (cudaMemcpy(di.err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+            return SWIATTN_ECUDA;
+    }
+    return (host & kDevErrTimeout) ? SWIATTN_ETIMEOUT : SWIATTN_OK;
+}
+
+int swiattn_route(const void* h, const void* w, float bias, int64_t tokens, int d_model, int dtype,
+                  float* logits, uint8_t* gate, void* stream) {
+    if (tokens < 0 || d_model <= 0) return SWIATTN_EINVAL;
+    if (dtype != SWIATTN_BF16 && dtype != SWIATTN_F32) return SWIATTN_EINVAL;
+    if (d_model % (dtype == SWIATTN_BF16 ? 8 : 4) != 0) return SWIATTN_EINVAL;
+    if (tokens == 0) return SWIATTN_OK;
+    if (!h || !w || !logits || !gate || !aligned16(h) || !aligned16(w)) return SWIATTN_EINVAL;
+    return launched(launch_route(h, w, bias, tokens, d_model, dtype, logits, gate,
+                                 static_cast<cudaStream_t>(stream)));
+}
+
+size_t swiattn_prefill_workspace(int B, int N, int Hq, int Hkv, int d, int W, int dtype) {
+    if (!attn_shape_ok(B, N, Hq, Hkv, d, W)) return 0;
+    if (dtype != SWIATTN_BF16) return 256;   // the fp32 path needs none
+    return prefill_ws_layout(B, N, Hq, d).total;
+}
+
+int swiattn_prefill(const void* q, const void* k, const void* v, const uint8_t* gate, void* o,
+                    float* lse, int B, int N, int Hq, int Hkv, int d, int W, float scale,
+                    int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+    if (!attn_shape_ok(B, N, Hq, Hkv, d, W)) return SWIATTN_EINVAL;
+    if (!q || !k || !v || !gate || !o) return SWIATTN_EINVAL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return SWIATTN_EINVAL;
+    if (!(scale > 0.f)) return SWIATTN_EINVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == SWIATTN_F32) {
+        return launched(launch_simt_attention(q, k, v, gate, -1, o, lse, B, N, Hq, Hkv, d, W,
+                                              scale, dtype, s));
+    }
+    if (dtype != SWIATTN_BF16) return SWIATTN_EINVAL;
+    if (d != kHD) return SWIATTN_EUNSUPPORTED;
+    const PrefillWs L = prefill_ws_layout(B, N, Hq, d);
+    if (!workspace || !aligned256(workspace) || workspace_bytes < L.total) return SWIATTN_EINVAL;
+    DeviceInfo di;
+    if (!device_info(di)) return SWIATTN_ECUDA;
+    char* ws = static_cast<char*>(workspace);
+    cudaError_t e = launch_schedule(gate, q, B, N, Hq, W, L, ws, di.sms, s);
+    if (e != cudaSuccess) return SWIATTN_ECUDA;
+    TcAttnArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.mode = 0;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.qc = ws + L.qc;
+    a.routed_list = reinterpret_cast<const int*>(ws + L.routed_list);
+    a.routed_count = reinterpret_cast<const int*>(ws + L.routed_count);
+    a.n_items = reinterpret_cast<const int*>(ws + L.n_items);
+    a.items = reinterpret_cast<const WorkItem*>(ws + L.items);
+    a.gate = gate;
+    a.o = o;
+    a.lse = lse;
+    a.B = B;
+    a.N = N;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.W = W;
+    a.scale = scale;
+    prof_start(s);
+    e = launch_tc_attention(a, di.err, di.sms, s);
+    prof_stop(s);
+    return launched(e);
+}
+
+size_t swiattn_decode_workspace(int B, int Lmax, int Hq, int Hkv, int d, int W, int dtype) {
+    (void)dtype;
+    if (!attn_shape_ok(B, Lmax, Hq, Hkv, d, W)) return 0;
+    return decode_ws_layout(B, Lmax, Hq, d).total;
+}
+
+int swiattn_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* seq_lens,
+                   const uint8_t* gate, void* o, float* lse, int B, int Lmax, int Hq, int Hkv,
+                   int d, int W, float scale, int dtype, void* workspace, size_t workspace_bytes,
+                   void* stream) {
+    if (!attn_shape_ok(B, Lmax, Hq, Hkv, d, W)) return SWIATTN_EINVAL;
+    if (dtype != SWIATTN_BF16 && dtype != SWIATTN_F32) return SWIATTN_EINVAL;
+    if (!q || !k_cache || !v_cache || !seq_lens || !gate || !o) return SWIATTN_EINVAL;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return SWIATTN_EINVAL;
+    if (!(scale > 0.f)) return SWIATTN_EINVAL;
+    const int G = Hq / Hkv;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return SWIATTN_EUNSUPPORTED;
+    if ((int64_t)Hkv * d / (dtype == SWIATTN_BF16 ? 8 : 4) > 1024) return SWIATTN_EUNSUPPORTED;
+    if (B > 65535) return SWIATTN_EUNSUPPORTED;
+    const DecodeWs L = decode_ws_layout(B, Lmax, Hq, d);
+    if (!workspace || !aligned256(workspace) || workspace_bytes < L.total) return SWIATTN_EINVAL;
+    return launched(launch_decode(q, k_cache, v_cache, seq_lens, gate, o, lse, B, Lmax, Hq, Hkv,
+                                  d, W, scale, dtype, L, static_cast<char*>(workspace),
+                                  static_cast<cudaStream_t>(stream)));
+}
+
+size_t swiattn_dual_branch_workspace(int B, int N, int Hq, int Hkv, int d, int W, int dtype) {
+    if (!attn_shape_ok(B, N, Hq, Hkv, d, W)) return 0;
+    return dual_ws_layout(B, N, Hq, d, dtype).total;
+}
+
+int swiattn_dual_branch(const void* q, const void* k, const void* v, const float* logits,
+                        const float* nll, void* o_full, void* o_swa, void* o_gated, float* mse,
+                        float* gamma, float* reg_loss, int B, int N, int Hq, int Hkv, int d, int W,
+                        float scale, float gamma_base, float eps, float alpha, int dtype,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+    if (!attn_shape_ok(B, N, Hq, Hkv, d, W)) return SWIATTN_EINVAL;
+    if (!q || !k || !v || !logits || !nll || !o_full || !o_swa || !mse || !gamma || !reg_loss)
+        return SWIATTN_EINVAL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o_full) ||
+        !aligned16(o_swa) || (o_gated && !aligned16(o_gated)))
+        return SWIATTN_EINVAL;
+    if (!(scale > 0.f)) return SWIATTN_EINVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == SWIATTN_F32) {
+        cudaError_t e = launch_simt_attention(q, k, v, nullptr, 1, o_full, nullptr, B, N, Hq, Hkv,
+                                              d, W, scale, dtype, s);
+        if (e == cudaSuccess)
+            e = launch_simt_attention(q, k, v, nullptr, 0, o_swa, nullptr, B, N, Hq, Hkv, d, W,
+                                      scale, dtype, s);
+        if (e == cudaSuccess)
+            e = launch_dual_epilogue_f32(static_cast<const float*>(o_full),
+                                         static_cast<const float*>(o_swa), logits, nll,
+                                         static_cast<float*>(o_gated), mse, gamma, reg_loss, B, N,
+                                         Hq, d, gamma_base, eps, alpha, s);
+        return launched(e);
+    }
+    if (dtype != SWIATTN_BF16) return SWIATTN_EINVAL;
+    if (d != kHD) return SWIATTN_EUNSUPPORTED;
+    const DualWs L = dual_ws_layout(B, N, Hq, d, dtype);
+    if (!workspace || !aligned256(workspace) || workspace_bytes < L.total) return SWIATTN_EINVAL;
+    DeviceInfo di;
+    if (!device_info(di)) return SWIATTN_ECUDA;
+    float* part = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.mse_part);
+    TcAttnArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.mode = 1;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.logits = logits;
+    a.o = o_full;
+    a.o_swa = o_swa;
+    a.o_gated = o_gated;
+    a.mse_part = part;
+    a.B = B;
+    a.N = N;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.W = W;
+    a.scale = scale;
+    prof_start(s);
+    cudaError_t e = launch_tc_attention(a, di.err, di.sms, s);
+    prof_stop(s);
+    if (e == cudaSuccess)
+        e = launch_dual_epilogue_parts(part, logits, nll, mse, gamma, reg_loss, B, N, Hq,
+                                       gamma_base, eps, alpha, s);
+    return launched(e);
+}
+
+}  // extern "C"

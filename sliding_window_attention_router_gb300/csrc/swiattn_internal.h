@@ -1,0 +1,119 @@
+// Internal declarations shared by the translation units of libswiattn.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace swi {
+
+// Device error word bits (OR-ed by kernels, read by swiattn_get_device_error).
+constexpr unsigned int kDevErrTimeout = 1u;
+
+// A healthy wait in these kernels lasts microseconds; after this long a
+// kernel gives up, flags a timeout and returns.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
+constexpr uint64_t kDrainLimitNs = 100000000ull;   // 0.1 s, waits while aborting
+
+// ------------------------------------------------------------ tiling --------
+constexpr int kBM = 128;   // query rows per tile (TMEM lanes)
+constexpr int kBN = 128;   // keys per tile
+constexpr int kHD = 128;   // head dim of the tensor-core path
+
+// Work item kinds of the routed-prefill schedule.
+constexpr int kItemBand = 0;   // 128 consecutive rows, window keys, writes non-far rows
+constexpr int kItemFar = 1;    // 128 compacted routed rows, causal keys [0, i]
+
+struct WorkItem {
+    int kind, b, h, tile;
+};
+
+// Workspace layout of swiattn_prefill (byte offsets from a 256-aligned base).
+struct PrefillWs {
+    size_t routed_list;   // int32 [B*N]   far rows of each batch, ascending
+    size_t routed_count;  // int32 [B]
+    size_t tile_prefix;   // int32 [B*(NT+1)] far rows before each 128-row tile
+    size_t n_items;       // int32 [4]
+    size_t items;         // WorkItem [max_items]
+    size_t qc;            // bf16 [B*N*Hq*d]  compacted queries of far rows
+    size_t total;
+    int max_items;
+};
+PrefillWs prefill_ws_layout(int B, int N, int Hq, int d);
+
+struct DecodeWs {
+    size_t part;   // float [B * max_chunks * Hq * (d+2)]
+    size_t total;
+    int max_chunks;
+    int chunk;
+};
+DecodeWs decode_ws_layout(int B, int Lmax, int Hq, int d);
+
+struct DualWs {
+    size_t mse_part;  // float [B*N*Hq]
+    size_t total;
+};
+DualWs dual_ws_layout(int B, int N, int Hq, int d, int dtype);
+
+// ------------------------------------------------------------ launchers -----
+// Each returns cudaSuccess or the launch error.
+cudaError_t launch_route(const void* h, const void* w, float bias, int64_t tokens, int d_model,
+                         int dtype, float* logits, uint8_t* gate, cudaStream_t s);
+
+cudaError_t launch_schedule(const uint8_t* gate, const void* q, int B, int N, int Hq, int W,
+                            const PrefillWs& L, char* ws, int num_sms, cudaStream_t s);
+
+struct TcAttnArgs {
+    int mode;          // 0 routed prefill, 1 dual branch
+    const void* q;     // [B,N,Hq,128] bf16
+    const void* k;     // [B,N,Hkv,128]
+    const void* v;
+    const void* qc;    // compacted far queries (prefill)
+    const int* routed_list;
+    const int* routed_count;
+    const int* n_items;
+    const WorkItem* items;
+    const uint8_t* gate;
+    const float* logits;   // dual: for o_gated
+    void* o;               // prefill output / dual o_full
+    void* o_swa;           // dual
+    void* o_gated;         // dual, nullable
+    float* lse;            // prefill, nullable
+    float* mse_part;       // dual
+    int B, N, Hq, Hkv, W;
+    float scale;
+};
+cudaError_t launch_tc_attention(const TcAttnArgs& a, unsigned int* err, int num_sms,
+                                cudaStream_t s);
+
+cudaError_t launch_simt_attention(const void* q, const void* k, const void* v,
+                                  const uint8_t* gate, int force, void* o, float* lse, int B,
+                                  int N, int Hq, int Hkv, int d, int W, float scale, int dtype,
+                                  cudaStream_t s);
+
+cudaError_t launch_dual_epilogue_f32(const float* o_full, const float* o_swa,
+                                     const float* logits, const float* nll, float* o_gated,
+                                     float* mse, float* gamma, float* reg, int B, int N, int Hq,
+                                     int d, float gamma_base, float eps, float alpha,
+                                     cudaStream_t s);
+
+cudaError_t launch_dual_epilogue_parts(const float* mse_part, const float* logits,
+                                       const float* nll, float* mse, float* gamma, float* reg,
+                                       int B, int N, int Hq, float gamma_base, float eps,
+                                       float alpha, cudaStream_t s);
+
+cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const int32_t* seq_lens,
+                          const uint8_t* gate, void* o, float* lse, int B, int Lmax, int Hq,
+                          int Hkv, int d, int W, float scale, int dtype, const DecodeWs& L,
+                          char* ws, cudaStream_t s);
+
+// Timing hook around the dominant kernel of a call (no-ops unless set).
+void prof_start(cudaStream_t s);
+void prof_stop(cudaStream_t s);
+
+// TMA descriptor creation through the driver entry point (no libcuda link).
+bool make_tmap_4d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                       uint64_t d3, uint32_t box0, uint32_t box2);
+
+}  // namespace swi

@@ -1,0 +1,98 @@
+"""The C-ABI library loads without a GPU and exports every declared symbol;
+host-side validation rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "swiattn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    from sliding_window_attention_router_gb300 import build
+    build.build()
+    import sliding_window_attention_router_gb300 as swa
+    return swa._load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(swiattn_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_four_calls():
+    names = declared_functions()
+    for call in ("swiattn_route", "swiattn_prefill", "swiattn_decode", "swiattn_dual_branch"):
+        assert call in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    import sliding_window_attention_router_gb300 as swa
+    names = declared_functions()
+    assert sorted(swa.EXPORTS) == names
+    for name in names:
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    import sliding_window_attention_router_gb300 as swa
+    assert swa.status_string(0) == "SWIATTN_OK"
+    assert swa.status_string(1) == "SWIATTN_EINVAL"
+    assert swa.status_string(4) == "SWIATTN_ETIMEOUT"
+    assert swa.status_string(99) == "SWIATTN_UNKNOWN"
+
+
+def test_workspace_sizes(lib):
+    import sliding_window_attention_router_gb300 as swa
+    bf16, f32 = swa.BF16, swa.F32
+    n = swa.prefill_workspace(1, 32768, 16, 16, 128, 1024, bf16)
+    # compacted queries alone are the size of Q
+    assert n >= 32768 * 16 * 128 * 2 and n % 256 == 0
+    assert swa.prefill_workspace(1, 0, 16, 16, 128, 1024, bf16) == 0
+    assert swa.prefill_workspace(1, 64, 6, 4, 128, 8, bf16) == 0   # Hq % Hkv != 0
+    dw = swa.decode_workspace(16, 32768, 16, 16, 128, 1024, bf16)
+    assert dw >= 16 * (32768 // 128) * 16 * 130 * 4
+    assert swa.dual_branch_workspace(2, 8192, 16, 4, 128, 1024, bf16) >= 2 * 8192 * 16 * 4
+    assert swa.dual_branch_workspace(1, 256, 2, 2, 64, 32, f32) == 0
+
+
+def test_invalid_arguments_rejected_before_launch(lib):
+    vp = ctypes.c_void_p
+    fake = vp(1 << 20)          # never dereferenced: validation fails first
+    odd = vp((1 << 20) + 8)     # not 16-byte aligned
+    # route: bad dtype, misaligned h, d_model not a multiple of 8
+    assert lib.swiattn_route(fake, fake, 0.0, 4, 64, 7, fake, fake, None) == 1
+    assert lib.swiattn_route(odd, fake, 0.0, 4, 64, 1, fake, fake, None) == 1
+    assert lib.swiattn_route(fake, fake, 0.0, 4, 60, 1, fake, fake, None) == 1
+    assert lib.swiattn_route(None, None, 0.0, 0, 64, 1, None, None, None) == 0   # no-op
+    args = [fake, fake, fake, fake, fake, None]
+    # prefill: W < 1, Hq % Hkv, d = 96, misaligned q, workspace too small, bad scale
+    assert lib.swiattn_prefill(*args, 1, 64, 4, 4, 128, 0, 0.1, 1, fake, 1 << 30, None) == 1
+    assert lib.swiattn_prefill(*args, 1, 64, 6, 4, 128, 8, 0.1, 1, fake, 1 << 30, None) == 1
+    assert lib.swiattn_prefill(*args, 1, 64, 4, 4, 96, 8, 0.1, 1, fake, 1 << 30, None) == 1
+    assert lib.swiattn_prefill(odd, *args[1:], 1, 64, 4, 4, 128, 8, 0.1, 1, fake, 1 << 30, None) == 1
+    assert lib.swiattn_prefill(*args, 1, 64, 4, 4, 128, 8, 0.1, 1, fake, 16, None) == 1
+    assert lib.swiattn_prefill(*args, 1, 64, 4, 4, 128, 8, 0.0, 1, fake, 1 << 30, None) == 1
+    # bf16 head dim 64 is valid but not implemented on the tensor-core path
+    assert lib.swiattn_prefill(*args, 1, 64, 4, 4, 64, 8, 0.1, 1, fake, 1 << 30, None) == 2
+    # decode: Hq/Hkv = 3 unsupported; workspace too small
+    dargs = [fake] * 7
+    assert lib.swiattn_decode(*dargs, 2, 64, 6, 2, 128, 8, 0.1, 1, fake, 1 << 30, None) == 2
+    assert lib.swiattn_decode(*dargs, 2, 64, 4, 4, 128, 8, 0.1, 1, fake, 8, None) == 1
+    # dual: missing output
+    xargs = [fake] * 5 + [None] + [fake] * 5
+    assert lib.swiattn_dual_branch(*xargs, 1, 64, 4, 4, 128, 8, 0.1, 1e-3, 0.1, 100.0, 1, fake,
+                                   1 << 30, None) == 1
+
+
+def test_no_gpu_reports_cuda_error_or_runs(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("GPU present")
+    assert lib.swiattn_num_sms() == -1
