@@ -183,6 +183,12 @@ class Timer:
         stops = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
         ks = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
         ke = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        if kernel_events:
+            # torch creates events lazily: record once so the handles exist
+            # before the library records them around its kernel.
+            for e in ks + ke:
+                e.record()
+            torch.cuda.synchronize()
         for s in range(steps):
             self.flush.zero_()
             if kernel_events:
