@@ -365,17 +365,22 @@ __device__ bool softmax_role(const TcParams& p, uint8_t* smem, uint64_t* bar, ui
             ++s_iter;
 
             float* s = reinterpret_cast<float*>(sr);
-            float mx = -INFINITY;
+            // Eight independent partial maxima keep the dependency chains short.
+            float m8[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) m8[t] = -INFINITY;
             if (a <= 0 && e >= kBN - 1) {
 #pragma unroll
-                for (int cc = 0; cc < kBN; ++cc) mx = fmaxf(mx, s[cc]);
+                for (int cc = 0; cc < kBN; ++cc) m8[cc & 7] = fmaxf(m8[cc & 7], s[cc]);
             } else {
 #pragma unroll
                 for (int cc = 0; cc < kBN; ++cc) {
                     s[cc] = (cc >= a && cc <= e) ? s[cc] : -INFINITY;
-                    mx = fmaxf(mx, s[cc]);
+                    m8[cc & 7] = fmaxf(m8[cc & 7], s[cc]);
                 }
             }
+            const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
             // Running max in scaled log2 units; O and l are only rescaled when
             // the max grows by more than 2^8, otherwise p stays <= 256.
             const float mnew = fmaxf(m2, mx * sl);
@@ -386,15 +391,18 @@ __device__ bool softmax_role(const TcParams& p, uint8_t* smem, uint64_t* bar, ui
                 m2 = mnew;
             }
             const float mb = (m2 == -INFINITY) ? 0.f : m2;
-            float rs = 0.f;
+            float r8[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) r8[t] = 0.f;
             uint32_t pk[64];
 #pragma unroll
             for (int cc = 0; cc < kBN; cc += 2) {
                 const float p0 = ex2_approx(fmaf(s[cc], sl, -mb));
                 const float p1 = ex2_approx(fmaf(s[cc + 1], sl, -mb));
-                rs += p0 + p1;
+                r8[(cc >> 1) & 7] += p0 + p1;
                 pk[cc >> 1] = pack_bf16x2(p0, p1);
             }
+            const float rs = ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
 
             if (j >= 1) {
                 // P buffer free and O stable once the previous PV completed.

@@ -37,10 +37,20 @@ def bernoulli_gates(shape, frac: float, gen: torch.Generator) -> torch.Tensor:
     return (torch.rand(*shape, generator=gen) < frac).to(torch.uint8)
 
 
-def run_gates(N: int, frac: float, gen: torch.Generator, mean_run: float = 64.0) -> torch.Tensor:
+def run_gates(N: int, frac: float, gen: torch.Generator, mean_run: float = 64.0,
+              tol: float = None) -> torch.Tensor:
     """Two-state run process: routed runs ~ Geometric(mean mean_run), window runs
     ~ Geometric(mean mean_run*(1-frac)/frac), first state ~ Bernoulli(frac).
+    With tol, whole sequences are redrawn until the realised routed fraction is
+    within tol of frac (the same generator continues, so it stays seeded).
     Returns uint8 [N]."""
+    while True:
+        out = _run_gates_once(N, frac, gen, mean_run)
+        if tol is None or abs(float(out.float().mean()) - frac) <= tol:
+            return out
+
+
+def _run_gates_once(N: int, frac: float, gen: torch.Generator, mean_run: float) -> torch.Tensor:
     out = torch.zeros(N, dtype=torch.uint8)
     state = 1 if float(torch.rand(1, generator=gen)) < frac else 0
     means = {1: mean_run, 0: mean_run * (1.0 - frac) / frac}
@@ -109,11 +119,11 @@ def prefill_4k(seed: int = 0) -> dict:
 def prefill_32k(frac: float = 0.13, seed: int = 0, N: int = 32768) -> dict:
     """Long-context prefill: B=1, H=16, d=128, N=32768, W=1024, bf16; gates in
     runs (mean routed run 64) at routed fraction frac (0.13 'standard',
-    0.05 'easy')."""
+    0.05 'easy'), realised fraction within 0.005 of frac."""
     g = _gen(seed)
     B, H, d, W = 1, 16, 128, 1024
     q, k, v = attention_qkv(B, N, H, H, d, torch.bfloat16, g)
-    gate = run_gates(N, frac, g).reshape(1, N)
+    gate = run_gates(N, frac, g, tol=0.005).reshape(1, N)
     return dict(q=q, k=k, v=v, gate=gate, W=W, B=B, N=N, Hq=H, Hkv=H, d=d, frac=frac)
 
 
