@@ -1,0 +1,548 @@
+// Routed prefill on the 5th-generation tensor cores (sm_103a): two query
+// tiles per CTA sharing every K/V block.
+//
+// A work item holds 256 query rows of one (batch, head): two 128-row tiles A
+// and B.  Band items take 256 consecutive rows and walk their window keys; far
+// items take 256 compacted routed rows and walk keys [0, max i].  The CTA
+// streams one sequence of 128-key blocks; each tile uses the contiguous run of
+// blocks its rows can see, so every K/V block is loaded once for both tiles.
+//
+// Per tile the chain is S = Q K^T (TMEM) -> softmax (P, bf16, written back
+// over S in TMEM) -> O += P V (P read from TMEM) -> next S.  The two tiles'
+// chains interleave on the tensor core: while warpgroup A turns S_A into P_A,
+// the tensor core runs tile B's PV and next S, and the reverse.
+//   warps 0-3   softmax + epilogue of tile A (thread r owns row r = TMEM lane r)
+//   warps 4-7   softmax + epilogue of tile B
+//   warp 8      TMA producer: Q tiles, K and V blocks
+//   warp 9      TMEM allocator, single-thread MMA issuer
+//   warps 10-11 idle (complete the third warpgroup for register reconfiguration)
+// TMEM: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
+// Key sets per row (SwiAttn report, section 2; window per the weimeta.cn SWA
+// glossary): window rows [max(0, i-W+1), i], routed rows [0, i].
+
+#include "ptx.cuh"
+#include "swiattn_internal.h"
+
+#include <cuda_bf16.h>
+#include <math.h>
+
+namespace swi {
+namespace {
+
+constexpr int kStages = 2;
+constexpr int kThreads = 384;   // 3 warpgroups
+// Launched at 168 registers per thread (12 warps x 32 x 168 = 64512); the
+// producer/MMA warpgroup gives up registers to the two softmax warpgroups:
+// 2 x 128 x 224 + 128 x 56 = 64512.
+constexpr uint32_t kRegsSoftmax = 224;
+constexpr uint32_t kRegsOther = 56;
+constexpr int kTileBytes = kBM * kHD * 2;    // 32 KiB
+constexpr int kHalfBytes = kTileBytes / 2;   // 16 KiB
+
+constexpr int kOffQ = 0;                                  // Q_A, Q_B
+constexpr int kOffK = kOffQ + 2 * kTileBytes;
+constexpr int kOffV = kOffK + kStages * kTileBytes;
+constexpr int kOffBar = kOffV + kStages * kTileBytes;
+
+enum {
+    BAR_Q_FULL = 0,                    // [2]
+    BAR_Q_EMPTY = BAR_Q_FULL + 2,      // [2]
+    BAR_K_FULL = BAR_Q_EMPTY + 2,      // [kStages]
+    BAR_K_EMPTY = BAR_K_FULL + kStages,
+    BAR_V_FULL = BAR_K_EMPTY + kStages,
+    BAR_V_EMPTY = BAR_V_FULL + kStages,
+    BAR_S_FULL = BAR_V_EMPTY + kStages,   // [2] per tile
+    BAR_P_FULL = BAR_S_FULL + 2,          // [2]
+    BAR_O_FULL = BAR_P_FULL + 2,          // [2]
+    BAR_O_FREE = BAR_O_FULL + 2,          // [2]
+    BAR_DRAIN = BAR_O_FREE + 2,
+    BAR_COUNT
+};
+
+constexpr int kOffMisc = kOffBar + BAR_COUNT * 8;
+constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+
+constexpr uint32_t kTmemCols = 512;
+__device__ __forceinline__ uint32_t col_s(int x) { return x ? 128u : 0u; }
+__device__ __forceinline__ uint32_t col_o(int x) { return x ? 384u : 256u; }
+
+constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, false, false);
+constexpr uint32_t kIdescO = idesc_bf16_f32(kBM, kHD, false, true);
+
+struct PfParams {
+    CUtensorMap tm_q, tm_qc, tm_k, tm_v;
+    const int* routed_list;
+    const int* routed_count;
+    const int* tile_prefix;
+    const int* n_items;
+    const WorkItem* items;
+    const uint8_t* gate;
+    __nv_bfloat16* o;
+    float* lse;
+    unsigned int* err;
+    int B, N, Hq, Hkv, W, NT;
+    float scale_log2;
+};
+
+struct Plan {
+    int b, h, kvh, kind;
+    int row0;          // band: first query row of tile A; far: first compacted index of tile A
+    int kv0, nblk;     // first key of the block sequence and its length
+    int j0[2], j1[2];  // active block range per tile (j0 > j1: tile empty)
+    int nrows[2];      // valid rows per tile
+};
+
+__device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+__device__ __forceinline__ int snake_index(int k, int c, int G) {
+    return k * G + ((k & 1) ? (G - 1 - c) : c);
+}
+
+__device__ __forceinline__ Plan make_plan(const PfParams& p, int idx) {
+    const WorkItem it = p.items[idx];
+    Plan pl;
+    pl.b = it.b;
+    pl.h = it.h;
+    pl.kvh = it.h / (p.Hq / p.Hkv);
+    pl.kind = it.kind;
+    pl.row0 = it.tile * 2 * kBM;
+    if (it.kind == kItemFar) {
+        const int cnt = p.routed_count[it.b];
+        const int* list = p.routed_list + (size_t)it.b * p.N;
+        pl.kv0 = 0;
+        int maxb = 0;
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+            const int r0 = pl.row0 + x * kBM;
+            pl.nrows[x] = max(0, min(kBM, cnt - r0));
+            pl.j0[x] = 0;
+            pl.j1[x] = pl.nrows[x] > 0 ? list[r0 + pl.nrows[x] - 1] / kBN : -1;
+            maxb = max(maxb, pl.j1[x] + 1);
+        }
+        pl.nblk = maxb;
+    } else {
+        const int q0 = pl.row0;
+        pl.kv0 = max(0, q0 - p.W + 1);
+        const int* pre = p.tile_prefix + (size_t)it.b * (p.NT + 1);
+        int last = -1;
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+            const int r0 = q0 + x * kBM;
+            pl.nrows[x] = max(0, min(kBM, p.N - r0));
+            const int t = r0 / kBM;
+            const bool has_rows = pl.nrows[x] > 0 && (pre[t + 1] - pre[t]) < pl.nrows[x];
+            if (has_rows) {
+                const int lo_key = max(0, r0 - p.W + 1);
+                const int hi_key = r0 + pl.nrows[x] - 1;
+                pl.j0[x] = (lo_key - pl.kv0) / kBN;
+                pl.j1[x] = (hi_key - pl.kv0) / kBN;
+                last = max(last, pl.j1[x]);
+            } else {
+                pl.j0[x] = 1;
+                pl.j1[x] = 0;
+            }
+        }
+        pl.nblk = last + 1;
+    }
+    return pl;
+}
+
+__device__ __forceinline__ bool tile_active(const Plan& pl, int x) { return pl.j0[x] <= pl.j1[x]; }
+
+// ----------------------------------------------------------------- roles --
+
+// One producer thread: Q tiles, then K one block ahead of V (a K slot frees
+// when S of the block two back completes, a V slot when PV three back does,
+// which the MMA order completes first).
+__device__ bool producer(const PfParams& p, uint8_t* smem, uint64_t* bar, volatile int* abort_flag,
+                         uint32_t& k_issued, uint32_t& v_issued, uint32_t* q_issued) {
+    const int G = gridDim.x, c = blockIdx.x;
+    const int n = *p.n_items;
+    for (int k = 0;; ++k) {
+        const int idx = snake_index(k, c, G);
+        if (idx >= n) break;
+        const Plan pl = make_plan(p, idx);
+        const CUtensorMap* qm = (pl.kind == kItemFar) ? &p.tm_qc : &p.tm_q;
+        auto load_q = [&](int x) -> bool {
+            if (!mbar_wait(&bar[BAR_Q_EMPTY + x], (q_issued[x] & 1u) ^ 1u, abort_flag, p.err)) return false;
+            mbar_arrive_expect_tx(&bar[BAR_Q_FULL + x], kTileBytes);
+            uint8_t* dst = smem + kOffQ + x * kTileBytes;
+            const int row = pl.row0 + x * kBM;
+            tma_load_4d(dst, qm, &bar[BAR_Q_FULL + x], 0, pl.h, row, pl.b);
+            tma_load_4d(dst + kHalfBytes, qm, &bar[BAR_Q_FULL + x], 64, pl.h, row, pl.b);
+            ++q_issued[x];
+            return true;
+        };
+        auto load_kv = [&](int base_bar, int off, const CUtensorMap* map, uint32_t& issued,
+                           int j) -> bool {
+            const uint32_t st = issued % kStages, ph = (issued / kStages) & 1u;
+            if (!mbar_wait(&bar[base_bar + kStages + st], ph ^ 1u, abort_flag, p.err)) return false;
+            mbar_arrive_expect_tx(&bar[base_bar + st], kTileBytes);
+            uint8_t* dst = smem + off + st * kTileBytes;
+            const int key0 = pl.kv0 + j * kBN;
+            tma_load_4d(dst, map, &bar[base_bar + st], 0, pl.kvh, key0, pl.b);
+            tma_load_4d(dst + kHalfBytes, map, &bar[base_bar + st], 64, pl.kvh, key0, pl.b);
+            ++issued;
+            return true;
+        };
+        if (tile_active(pl, 0) && !load_q(0)) return false;
+        for (int j = 0; j <= pl.nblk; ++j) {
+            if (j < pl.nblk) {
+                if (tile_active(pl, 1) && j == pl.j0[1] && !load_q(1)) return false;
+                if (!load_kv(BAR_K_FULL, kOffK, &p.tm_k, k_issued, j)) return false;
+            }
+            if (j >= 1 && !load_kv(BAR_V_FULL, kOffV, &p.tm_v, v_issued, j - 1)) return false;
+        }
+    }
+    return true;
+}
+
+__device__ void drain_loads(uint64_t* full_bars, uint32_t issued) {
+    for (uint32_t back = 1; back <= kStages && back <= issued; ++back) {
+        const uint32_t it = issued - back;
+        mbar_drain(&full_bars[it % kStages], (it / kStages) & 1u);
+    }
+}
+
+__device__ bool mma_issuer(const PfParams& p, uint8_t* smem, uint64_t* bar, uint32_t tmem,
+                           volatile int* abort_flag) {
+    const int G = gridDim.x, c = blockIdx.x;
+    const int n = *p.n_items;
+    uint32_t kv_base = 0;
+    uint32_t q_cnt[2] = {0, 0}, p_cnt[2] = {0, 0}, o_cnt[2] = {0, 0};
+
+    for (int k = 0;; ++k) {
+        const int idx = snake_index(k, c, G);
+        if (idx >= n) break;
+        const Plan pl = make_plan(p, idx);
+        int pend[2] = {-1, -1};
+        bool first_pv[2] = {true, true};
+
+        auto issue_pv = [&](int x, int jj) -> bool {
+            const uint32_t kvi = kv_base + jj;
+            const uint32_t st = kvi % kStages, ph = (kvi / kStages) & 1u;
+            if (!mbar_wait(&bar[BAR_P_FULL + x], p_cnt[x] & 1u, abort_flag, p.err)) return false;
+            ++p_cnt[x];
+            if (!mbar_wait(&bar[BAR_V_FULL + st], ph, abort_flag, p.err)) return false;
+            if (first_pv[x]) {
+                if (!mbar_wait(&bar[BAR_O_FREE + x], (o_cnt[x] & 1u) ^ 1u, abort_flag, p.err))
+                    return false;
+                ++o_cnt[x];
+            }
+            tc_fence_after();
+            const uint32_t sV = smem_u32(smem + kOffV + st * kTileBytes);
+#pragma unroll
+            for (int kk = 0; kk < kBN / 16; ++kk) {
+                const uint64_t bdesc = sdesc_sw128(sV + kk * 16 * 128, kHalfBytes, 1024);
+                umma_bf16_ts(tmem + col_o(x), tmem + col_s(x) + kk * 8, bdesc, kIdescO,
+                             (first_pv[x] && kk == 0) ? 0u : 1u);
+            }
+            first_pv[x] = false;
+            if (jj == pl.j1[x]) umma_commit(&bar[BAR_O_FULL + x]);
+            return true;
+        };
+
+        for (int j = 0; j < pl.nblk; ++j) {
+            const uint32_t kvi = kv_base + j;
+            const uint32_t st = kvi % kStages, ph = (kvi / kStages) & 1u;
+            if (!mbar_wait(&bar[BAR_K_FULL + st], ph, abort_flag, p.err)) return false;
+            tc_fence_after();
+            const uint32_t sK = smem_u32(smem + kOffK + st * kTileBytes);
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+                if (pend[x] >= 0) {
+                    if (!issue_pv(x, pend[x])) return false;
+                    pend[x] = -1;
+                }
+                if (j >= pl.j0[x] && j <= pl.j1[x]) {
+                    if (j == pl.j0[x]) {
+                        if (!mbar_wait(&bar[BAR_Q_FULL + x], q_cnt[x] & 1u, abort_flag, p.err))
+                            return false;
+                        ++q_cnt[x];
+                        tc_fence_after();
+                    }
+                    const uint32_t sQ = smem_u32(smem + kOffQ + x * kTileBytes);
+#pragma unroll
+                    for (int kk = 0; kk < kHD / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+                        umma_bf16(tmem + col_s(x), sdesc_sw128(sQ + off, 16, 1024),
+                                  sdesc_sw128(sK + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
+                    }
+                    umma_commit(&bar[BAR_S_FULL + x]);
+                    if (j == pl.j1[x]) umma_commit(&bar[BAR_Q_EMPTY + x]);
+                    pend[x] = j;
+                }
+            }
+            umma_commit(&bar[BAR_K_EMPTY + st]);
+            if (j >= 1) umma_commit(&bar[BAR_V_EMPTY + (kvi - 1) % kStages]);
+        }
+#pragma unroll
+        for (int x = 0; x < 2; ++x)
+            if (pend[x] >= 0 && !issue_pv(x, pend[x])) return false;
+        if (pl.nblk > 0) umma_commit(&bar[BAR_V_EMPTY + (kv_base + pl.nblk - 1) % kStages]);
+        kv_base += pl.nblk;
+    }
+    return true;
+}
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned int* err) {
+    const bool ok = mbar_wait(bar, parity, abort_flag, err);
+    return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float* v) {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        uint4 w;
+        w.x = pack_bf16x2(v[8 * g + 0], v[8 * g + 1]);
+        w.y = pack_bf16x2(v[8 * g + 2], v[8 * g + 3]);
+        w.z = pack_bf16x2(v[8 * g + 4], v[8 * g + 5]);
+        w.w = pack_bf16x2(v[8 * g + 6], v[8 * g + 7]);
+        d4[g] = w;
+    }
+}
+
+__device__ bool softmax_role(const PfParams& p, uint64_t* bar, uint32_t tmem, volatile int* abort_flag,
+                             int x, int wq, int lane) {
+    const int G = gridDim.x, c = blockIdx.x;
+    const int n = *p.n_items;
+    const int r = wq * 32 + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    const uint32_t tS = lane_base + col_s(x);
+    const uint32_t tO = lane_base + col_o(x);
+    const float sl = p.scale_log2;
+    uint32_t s_cnt = 0, o_cnt = 0;
+
+    for (int k = 0;; ++k) {
+        const int idx = snake_index(k, c, G);
+        if (idx >= n) break;
+        const Plan pl = make_plan(p, idx);
+        if (!tile_active(pl, x)) continue;
+        const bool far = pl.kind == kItemFar;
+        int i = -1;
+        if (r < pl.nrows[x]) {
+            const int rr = pl.row0 + x * kBM + r;
+            i = far ? p.routed_list[(size_t)pl.b * p.N + rr] : rr;
+        }
+        bool write_row = i >= 0;
+        if (!far && i >= 0) write_row = !(p.gate[(size_t)pl.b * p.N + i] != 0 && i >= p.W);
+        const int lo = (i < 0) ? 1 : (far ? 0 : max(0, i - p.W + 1));
+        const int hi = (i < 0) ? 0 : i;
+
+        float m2 = -INFINITY, l = 0.f;
+        for (int j = pl.j0[x]; j <= pl.j1[x]; ++j) {
+            const int key0 = pl.kv0 + j * kBN;
+            const int a = lo - key0, e = hi - key0;
+            if (!warp_wait(&bar[BAR_S_FULL + x], s_cnt & 1u, abort_flag, p.err)) return false;
+            ++s_cnt;
+            tc_fence_after();
+            uint32_t sr[128];
+            tmem_ld32(tS + 0, sr);
+            tmem_ld32(tS + 32, sr + 32);
+            tmem_ld32(tS + 64, sr + 64);
+            tmem_ld32(tS + 96, sr + 96);
+            tmem_ld_wait();
+            float* s = reinterpret_cast<float*>(sr);
+            float m8[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) m8[t] = -INFINITY;
+            if (a <= 0 && e >= kBN - 1) {
+#pragma unroll
+                for (int cc = 0; cc < kBN; ++cc) m8[cc & 7] = fmaxf(m8[cc & 7], s[cc]);
+            } else {
+                const uint32_t span = static_cast<uint32_t>(e - a);
+#pragma unroll
+                for (int cc = 0; cc < kBN; ++cc) {
+                    const bool ok = static_cast<uint32_t>(cc - a) <= span && e >= a;
+                    s[cc] = ok ? s[cc] : -INFINITY;
+                    m8[cc & 7] = fmaxf(m8[cc & 7], s[cc]);
+                }
+            }
+            const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            // Running max in scaled log2 units; O and l are rescaled only when
+            // the max grows by more than 2^8 (p stays <= 256 otherwise).
+            const float mnew = fmaxf(m2, mx * sl);
+            const bool resc = mnew > m2 + 8.0f;
+            float alpha = 1.f;
+            if (resc) {
+                alpha = ex2_approx(m2 - mnew);
+                m2 = mnew;
+            }
+            // O_X is stable here: S_X(j) completing implies the earlier PV_X did.
+            const bool need = resc && l > 0.f;
+            if (__any_sync(0xffffffffu, need)) {
+                const float f = need ? alpha : 1.f;
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint32_t orr[32];
+                    tmem_ld32(tO + q4 * 32, orr);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) orr[t] = __float_as_uint(__uint_as_float(orr[t]) * f);
+                    tmem_st32(tO + q4 * 32, orr);
+                }
+            }
+            const float mb = (m2 == -INFINITY) ? 0.f : m2;
+            float r8[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) r8[t] = 0.f;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int cc = 0; cc < 64; cc += 2) {
+                    const float p0 = ex2_approx(fmaf(s[hh * 64 + cc], sl, -mb));
+                    const float p1 = ex2_approx(fmaf(s[hh * 64 + cc + 1], sl, -mb));
+                    r8[(cc >> 1) & 7] += p0 + p1;
+                    pk[cc >> 1] = pack_bf16x2(p0, p1);
+                }
+                // P over the S columns this half has already consumed.
+                tmem_st32(tS + hh * 32, pk);
+            }
+            tmem_st_wait();
+            l = l * alpha + (((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7])));
+            tc_fence_before();
+            mbar_arrive(&bar[BAR_P_FULL + x]);
+        }
+
+        if (!warp_wait(&bar[BAR_O_FULL + x], o_cnt & 1u, abort_flag, p.err)) return false;
+        ++o_cnt;
+        tc_fence_after();
+        const float inv = (l > 0.f) ? 1.f / l : 0.f;
+        const size_t out_row = (i >= 0) ? (((size_t)pl.b * p.N + i) * p.Hq + pl.h) : 0;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t orr[32];
+            tmem_ld32(tO + q4 * 32, orr);
+            tmem_ld_wait();
+            float* ov = reinterpret_cast<float*>(orr);
+#pragma unroll
+            for (int t = 0; t < 32; ++t) ov[t] *= inv;
+            if (write_row) store_row_bf16(p.o + out_row * kHD + q4 * 32, ov);
+        }
+        if (write_row && p.lse) p.lse[out_row] = (m2 + __log2f(l)) * 0.69314718055994531f;
+        tc_fence_before();
+        mbar_arrive(&bar[BAR_O_FREE + x]);
+    }
+    return true;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PfParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kOffBar);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(&bar[BAR_Q_FULL + x], 1);
+            mbar_init(&bar[BAR_Q_EMPTY + x], 1);
+            mbar_init(&bar[BAR_S_FULL + x], 1);
+            mbar_init(&bar[BAR_P_FULL + x], kBM);
+            mbar_init(&bar[BAR_O_FULL + x], 1);
+            mbar_init(&bar[BAR_O_FREE + x], kBM);
+        }
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&bar[BAR_K_FULL + s], 1);
+            mbar_init(&bar[BAR_K_EMPTY + s], 1);
+            mbar_init(&bar[BAR_V_FULL + s], 1);
+            mbar_init(&bar[BAR_V_EMPTY + s], 1);
+        }
+        mbar_init(&bar[BAR_DRAIN], 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 9) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp < 8) {
+        warpgroup_reg_inc<kRegsSoftmax>();
+        softmax_role(p, bar, tmem, abort_flag, warp >> 2, warp & 3, lane);
+    } else {
+        warpgroup_reg_dec<kRegsOther>();
+    }
+    if (warp < 8) {
+    } else if (warp == 8) {
+        if (lane == 0) {
+            prefetch_tensormap(&p.tm_q);
+            prefetch_tensormap(&p.tm_qc);
+            prefetch_tensormap(&p.tm_k);
+            prefetch_tensormap(&p.tm_v);
+            uint32_t k_issued = 0, v_issued = 0, q_issued[2] = {0, 0};
+            if (!producer(p, smem, bar, abort_flag, k_issued, v_issued, q_issued)) {
+                drain_loads(&bar[BAR_K_FULL], k_issued);
+                drain_loads(&bar[BAR_V_FULL], v_issued);
+                for (int x = 0; x < 2; ++x)
+                    if (q_issued[x]) mbar_drain(&bar[BAR_Q_FULL + x], (q_issued[x] - 1) & 1u);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 9) {
+        if (lane == 0) {
+            mma_issuer(p, smem, bar, tmem, abort_flag);
+            umma_commit(&bar[BAR_DRAIN]);
+            mbar_drain(&bar[BAR_DRAIN], 0);
+        }
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 9) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_tc(const TcAttnArgs& a, const int* tile_prefix, unsigned int* err,
+                              int num_sms, cudaStream_t s) {
+    PfParams p;
+    memset(&p, 0, sizeof(p));
+    const uint64_t N = a.N, B = a.B;
+    bool ok = make_tmap_4d_bf16(&p.tm_q, a.q, kHD, a.Hq, N, B, 64, kBM) &&
+              make_tmap_4d_bf16(&p.tm_qc, a.qc, kHD, a.Hq, N, B, 64, kBM) &&
+              make_tmap_4d_bf16(&p.tm_k, a.k, kHD, a.Hkv, N, B, 64, kBN) &&
+              make_tmap_4d_bf16(&p.tm_v, a.v, kHD, a.Hkv, N, B, 64, kBN);
+    if (!ok) return cudaErrorInvalidValue;
+    p.routed_list = a.routed_list;
+    p.routed_count = a.routed_count;
+    p.tile_prefix = tile_prefix;
+    p.n_items = a.n_items;
+    p.items = a.items;
+    p.gate = a.gate;
+    p.o = static_cast<__nv_bfloat16*>(a.o);
+    p.lse = a.lse;
+    p.err = err;
+    p.B = a.B;
+    p.N = a.N;
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.W = a.W;
+    p.NT = (a.N + kBM - 1) / kBM;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    prefill_kernel<<<num_sms, kThreads, kSmemBytes, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace swi

@@ -226,6 +226,18 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, b
            | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
+// Register reconfiguration for a whole warpgroup (every warp of it executes
+// the same instruction).  The counts of all warpgroups must add up to at most
+// the registers the CTA was launched with.
+template <uint32_t kRegs>
+__device__ __forceinline__ void warpgroup_reg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void warpgroup_reg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
 // ------------------------------------------------------------------- misc --
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;

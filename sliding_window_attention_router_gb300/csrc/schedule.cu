@@ -4,8 +4,9 @@
 // and i >= W (for i < W its full range [0, i] equals its window).  Far rows
 // are compacted (ascending i) so that 128 of them share one query tile that
 // walks keys [0, max i]; every other row is served by the 128-row band tile
-// that holds it, which walks only the window keys.  The work list is sorted by
-// cost (key blocks), longest first, for the persistent attention kernel.
+// that holds it, which walks only the window keys.  Work items are pairs of
+// such tiles (256 rows, one head); the list is sorted by cost (key blocks),
+// longest first, for the persistent attention kernel.
 
 #include "swiattn_internal.h"
 
@@ -64,33 +65,50 @@ __global__ void __launch_bounds__(kScanThreads) scan_far_rows_kernel(
     }
 }
 
-// Cost (key blocks) of tile u of the enumeration [far tiles | band tiles] per
-// batch, or -1 when the tile does not exist or has nothing to write.
-__device__ __forceinline__ int tile_cost(int u, const int* routed_list, const int* routed_count,
-                                         const int* tile_prefix, int N, int W, int NT, int& b,
-                                         int& kind, int& tile) {
-    b = u / (2 * NT);
-    const int rem = u % (2 * NT);
-    if (rem < NT) {
-        kind = kItemFar;
-        tile = rem;
-        const int R = routed_count[b];
-        if (tile * kBM >= R) return -1;
-        const int last = min(R, (tile + 1) * kBM) - 1;
-        return cdiv(routed_list[(size_t)b * N + last] + 1, kBN);
-    }
-    kind = kItemBand;
-    tile = rem - NT;
-    const int q0 = tile * kBM;
-    const int nrows = min(kBM, N - q0);
-    const int far_rows = tile_prefix[(size_t)b * (NT + 1) + tile + 1] -
-                         tile_prefix[(size_t)b * (NT + 1) + tile];
-    if (far_rows >= nrows) return -1;
-    const int kv0 = max(0, q0 - W + 1);
-    return cdiv(q0 + nrows - kv0, kBN);
+// Key blocks a 128-row band tile starting at row r0 walks, or 0 when it has
+// no row to write (out of range, or every row is a far row).
+__device__ __forceinline__ int band_tile_blocks(int b, int r0, int kv0, const int* tile_prefix,
+                                                int N, int W, int NT) {
+    const int nrows = min(kBM, N - r0);
+    if (nrows <= 0) return 0;
+    const int t = r0 / kBM;
+    const int far_rows = tile_prefix[(size_t)b * (NT + 1) + t + 1] -
+                         tile_prefix[(size_t)b * (NT + 1) + t];
+    if (far_rows >= nrows) return 0;
+    const int lo_key = max(0, r0 - W + 1);
+    return (r0 + nrows - 1 - kv0) / kBN - (lo_key - kv0) / kBN + 1;
 }
 
-// Single CTA: counting sort of tiles by descending cost, Hq items per tile.
+// Cost (key blocks over both tiles) of pair u of the enumeration
+// [far pairs | band pairs] per batch; 0 when the pair has nothing to do.
+__device__ __forceinline__ int pair_cost(int u, const int* routed_list, const int* routed_count,
+                                         const int* tile_prefix, int N, int W, int NT, int NP,
+                                         int& b, int& kind, int& pair) {
+    b = u / (2 * NP);
+    const int rem = u % (2 * NP);
+    if (rem < NP) {
+        kind = kItemFar;
+        pair = rem;
+        const int R = routed_count[b];
+        int cost = 0;
+        for (int x = 0; x < 2; ++x) {
+            const int r0 = pair * 2 * kBM + x * kBM;
+            if (r0 >= R) break;
+            const int last = min(R, r0 + kBM) - 1;
+            cost += routed_list[(size_t)b * N + last] / kBN + 1;
+        }
+        return cost;
+    }
+    kind = kItemBand;
+    pair = rem - NP;
+    const int q0 = pair * 2 * kBM;
+    const int kv0 = max(0, q0 - W + 1);
+    return band_tile_blocks(b, q0, kv0, tile_prefix, N, W, NT) +
+           band_tile_blocks(b, q0 + kBM, kv0, tile_prefix, N, W, NT);
+}
+
+// Single CTA: counting sort of 256-row pairs by descending cost, Hq items per
+// pair (one per query head).
 __global__ void __launch_bounds__(1024) build_items_kernel(
     const int* __restrict__ routed_list, const int* __restrict__ routed_count,
     const int* __restrict__ tile_prefix, int B, int N, int Hq, int W, WorkItem* __restrict__ items,
@@ -98,13 +116,14 @@ __global__ void __launch_bounds__(1024) build_items_kernel(
     __shared__ int hist[kCostBuckets];
     __shared__ int total;
     const int NT = cdiv(N, kBM);
-    const int U = B * 2 * NT;
+    const int NP = cdiv(N, 2 * kBM);
+    const int U = B * 2 * NP;
     for (int c = threadIdx.x; c < kCostBuckets; c += blockDim.x) hist[c] = 0;
     __syncthreads();
     for (int u = threadIdx.x; u < U; u += blockDim.x) {
-        int b, kind, tile;
-        const int cost = tile_cost(u, routed_list, routed_count, tile_prefix, N, W, NT, b, kind, tile);
-        if (cost >= 0) atomicAdd(&hist[min(cost, kCostBuckets - 1)], 1);
+        int b, kind, pair;
+        const int cost = pair_cost(u, routed_list, routed_count, tile_prefix, N, W, NT, NP, b, kind, pair);
+        if (cost > 0) atomicAdd(&hist[min(cost, kCostBuckets - 1)], 1);
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -119,11 +138,11 @@ __global__ void __launch_bounds__(1024) build_items_kernel(
     }
     __syncthreads();
     for (int u = threadIdx.x; u < U; u += blockDim.x) {
-        int b, kind, tile;
-        const int cost = tile_cost(u, routed_list, routed_count, tile_prefix, N, W, NT, b, kind, tile);
-        if (cost < 0) continue;
+        int b, kind, pair;
+        const int cost = pair_cost(u, routed_list, routed_count, tile_prefix, N, W, NT, NP, b, kind, pair);
+        if (cost <= 0) continue;
         const int pos = atomicAdd(&hist[min(cost, kCostBuckets - 1)], 1);
-        for (int h = 0; h < Hq; ++h) items[(size_t)pos * Hq + h] = WorkItem{kind, b, h, tile};
+        for (int h = 0; h < Hq; ++h) items[(size_t)pos * Hq + h] = WorkItem{kind, b, h, pair};
     }
     if (threadIdx.x == 0) n_items[0] = total * Hq;
 }
@@ -164,7 +183,7 @@ PrefillWs prefill_ws_layout(int B, int N, int Hq, int d) {
     off = up(off + sizeof(int) * (size_t)B * (NT + 1));
     L.n_items = off;
     off = up(off + sizeof(int) * 4);
-    L.max_items = static_cast<int>((size_t)B * 2 * NT * Hq);
+    L.max_items = static_cast<int>((size_t)B * 2 * ((N + 2 * kBM - 1) / (2 * kBM)) * Hq);
     L.items = off;
     off = up(off + sizeof(WorkItem) * (size_t)L.max_items);
     L.qc = off;

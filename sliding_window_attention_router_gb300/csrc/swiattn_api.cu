@@ -209,7 +209,7 @@ int swiattn_prefill(const void* q, const void* k, const void* v, const uint8_t* 
     a.W = W;
     a.scale = scale;
     prof_start(s);
-    e = launch_tc_attention(a, di.err, di.sms, s);
+    e = launch_prefill_tc(a, reinterpret_cast<const int*>(ws + L.tile_prefix), di.err, di.sms, s);
     prof_stop(s);
     return launched(e);
 }

@@ -22,8 +22,8 @@ constexpr int kBN = 128;   // keys per tile
 constexpr int kHD = 128;   // head dim of the tensor-core path
 
 // Work item kinds of the routed-prefill schedule.
-constexpr int kItemBand = 0;   // 128 consecutive rows, window keys, writes non-far rows
-constexpr int kItemFar = 1;    // 128 compacted routed rows, causal keys [0, i]
+constexpr int kItemBand = 0;   // 256 consecutive rows, window keys, writes non-far rows
+constexpr int kItemFar = 1;    // 256 compacted routed rows, causal keys [0, i]
 
 struct WorkItem {
     int kind, b, h, tile;
@@ -86,6 +86,10 @@ struct TcAttnArgs {
 };
 cudaError_t launch_tc_attention(const TcAttnArgs& a, unsigned int* err, int num_sms,
                                 cudaStream_t s);
+
+// Routed prefill, two query tiles per CTA (work items from launch_schedule).
+cudaError_t launch_prefill_tc(const TcAttnArgs& a, const int* tile_prefix, unsigned int* err,
+                              int num_sms, cudaStream_t s);
 
 cudaError_t launch_simt_attention(const void* q, const void* k, const void* v,
                                   const uint8_t* gate, int force, void* o, float* lse, int B,
