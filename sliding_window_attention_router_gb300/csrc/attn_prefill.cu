@@ -13,8 +13,8 @@
 // the tensor core runs tile B's PV and next S, and the reverse.
 //   warps 0-3   softmax + epilogue of tile A (thread r owns row r = TMEM lane r)
 //   warps 4-7   softmax + epilogue of tile B
-//   warp 8      TMA producer: Q tiles, K and V blocks
-//   warp 9      TMEM allocator, single-thread MMA issuer
+//   warp 8      TMA producer: Q tiles, K and V blocks (converged, elected issue)
+//   warp 9      TMEM allocator and MMA issuer (converged, elected issue)
 //   warps 10-11 idle (complete the third warpgroup for register reconfiguration)
 // TMEM: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
 // Key sets per row (SwiAttn report, section 2; window per the weimeta.cn SWA
@@ -33,9 +33,9 @@ constexpr int kStages = 2;
 constexpr int kThreads = 384;   // 3 warpgroups
 // Launched at 168 registers per thread (12 warps x 32 x 168 = 64512); the
 // producer/MMA warpgroup gives up registers to the two softmax warpgroups:
-// 2 x 128 x 224 + 128 x 56 = 64512.
-constexpr uint32_t kRegsSoftmax = 224;
-constexpr uint32_t kRegsOther = 56;
+// 2 x 128 x 216 + 128 x 72 = 64512.
+constexpr uint32_t kRegsSoftmax = 216;
+constexpr uint32_t kRegsOther = 72;
 constexpr int kTileBytes = kBM * kHD * 2;    // 32 KiB
 constexpr int kHalfBytes = kTileBytes / 2;   // 16 KiB
 
@@ -164,24 +164,24 @@ __device__ bool producer(const PfParams& p, uint8_t* smem, uint64_t* bar, volati
         const Plan pl = make_plan(p, idx);
         const CUtensorMap* qm = (pl.kind == kItemFar) ? &p.tm_qc : &p.tm_q;
         auto load_q = [&](int x) -> bool {
-            if (!mbar_wait(&bar[BAR_Q_EMPTY + x], (q_issued[x] & 1u) ^ 1u, abort_flag, p.err)) return false;
-            mbar_arrive_expect_tx(&bar[BAR_Q_FULL + x], kTileBytes);
+            if (!mbar_wait_w(&bar[BAR_Q_EMPTY + x], (q_issued[x] & 1u) ^ 1u, abort_flag, p.err)) return false;
+            mbar_arrive_expect_tx_w(&bar[BAR_Q_FULL + x], kTileBytes);
             uint8_t* dst = smem + kOffQ + x * kTileBytes;
             const int row = pl.row0 + x * kBM;
-            tma_load_4d(dst, qm, &bar[BAR_Q_FULL + x], 0, pl.h, row, pl.b);
-            tma_load_4d(dst + kHalfBytes, qm, &bar[BAR_Q_FULL + x], 64, pl.h, row, pl.b);
+            tma_load_4d_w(dst, qm, &bar[BAR_Q_FULL + x], 0, pl.h, row, pl.b);
+            tma_load_4d_w(dst + kHalfBytes, qm, &bar[BAR_Q_FULL + x], 64, pl.h, row, pl.b);
             ++q_issued[x];
             return true;
         };
         auto load_kv = [&](int base_bar, int off, const CUtensorMap* map, uint32_t& issued,
                            int j) -> bool {
             const uint32_t st = issued % kStages, ph = (issued / kStages) & 1u;
-            if (!mbar_wait(&bar[base_bar + kStages + st], ph ^ 1u, abort_flag, p.err)) return false;
-            mbar_arrive_expect_tx(&bar[base_bar + st], kTileBytes);
+            if (!mbar_wait_w(&bar[base_bar + kStages + st], ph ^ 1u, abort_flag, p.err)) return false;
+            mbar_arrive_expect_tx_w(&bar[base_bar + st], kTileBytes);
             uint8_t* dst = smem + off + st * kTileBytes;
             const int key0 = pl.kv0 + j * kBN;
-            tma_load_4d(dst, map, &bar[base_bar + st], 0, pl.kvh, key0, pl.b);
-            tma_load_4d(dst + kHalfBytes, map, &bar[base_bar + st], 64, pl.kvh, key0, pl.b);
+            tma_load_4d_w(dst, map, &bar[base_bar + st], 0, pl.kvh, key0, pl.b);
+            tma_load_4d_w(dst + kHalfBytes, map, &bar[base_bar + st], 64, pl.kvh, key0, pl.b);
             ++issued;
             return true;
         };
@@ -221,11 +221,11 @@ __device__ bool mma_issuer(const PfParams& p, uint8_t* smem, uint64_t* bar, uint
         auto issue_pv = [&](int x, int jj) -> bool {
             const uint32_t kvi = kv_base + jj;
             const uint32_t st = kvi % kStages, ph = (kvi / kStages) & 1u;
-            if (!mbar_wait(&bar[BAR_P_FULL + x], p_cnt[x] & 1u, abort_flag, p.err)) return false;
+            if (!mbar_wait_w(&bar[BAR_P_FULL + x], p_cnt[x] & 1u, abort_flag, p.err)) return false;
             ++p_cnt[x];
-            if (!mbar_wait(&bar[BAR_V_FULL + st], ph, abort_flag, p.err)) return false;
+            if (!mbar_wait_w(&bar[BAR_V_FULL + st], ph, abort_flag, p.err)) return false;
             if (first_pv[x]) {
-                if (!mbar_wait(&bar[BAR_O_FREE + x], (o_cnt[x] & 1u) ^ 1u, abort_flag, p.err))
+                if (!mbar_wait_w(&bar[BAR_O_FREE + x], (o_cnt[x] & 1u) ^ 1u, abort_flag, p.err))
                     return false;
                 ++o_cnt[x];
             }
@@ -234,18 +234,18 @@ __device__ bool mma_issuer(const PfParams& p, uint8_t* smem, uint64_t* bar, uint
 #pragma unroll
             for (int kk = 0; kk < kBN / 16; ++kk) {
                 const uint64_t bdesc = sdesc_sw128(sV + kk * 16 * 128, kHalfBytes, 1024);
-                umma_bf16_ts(tmem + col_o(x), tmem + col_s(x) + kk * 8, bdesc, kIdescO,
+                umma_bf16_ts_w(tmem + col_o(x), tmem + col_s(x) + kk * 8, bdesc, kIdescO,
                              (first_pv[x] && kk == 0) ? 0u : 1u);
             }
             first_pv[x] = false;
-            if (jj == pl.j1[x]) umma_commit(&bar[BAR_O_FULL + x]);
+            if (jj == pl.j1[x]) umma_commit_w(&bar[BAR_O_FULL + x]);
             return true;
         };
 
         for (int j = 0; j < pl.nblk; ++j) {
             const uint32_t kvi = kv_base + j;
             const uint32_t st = kvi % kStages, ph = (kvi / kStages) & 1u;
-            if (!mbar_wait(&bar[BAR_K_FULL + st], ph, abort_flag, p.err)) return false;
+            if (!mbar_wait_w(&bar[BAR_K_FULL + st], ph, abort_flag, p.err)) return false;
             tc_fence_after();
             const uint32_t sK = smem_u32(smem + kOffK + st * kTileBytes);
 #pragma unroll
@@ -256,7 +256,7 @@ __device__ bool mma_issuer(const PfParams& p, uint8_t* smem, uint64_t* bar, uint
                 }
                 if (j >= pl.j0[x] && j <= pl.j1[x]) {
                     if (j == pl.j0[x]) {
-                        if (!mbar_wait(&bar[BAR_Q_FULL + x], q_cnt[x] & 1u, abort_flag, p.err))
+                        if (!mbar_wait_w(&bar[BAR_Q_FULL + x], q_cnt[x] & 1u, abort_flag, p.err))
                             return false;
                         ++q_cnt[x];
                         tc_fence_after();
@@ -265,21 +265,21 @@ __device__ bool mma_issuer(const PfParams& p, uint8_t* smem, uint64_t* bar, uint
 #pragma unroll
                     for (int kk = 0; kk < kHD / 16; ++kk) {
                         const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                        umma_bf16(tmem + col_s(x), sdesc_sw128(sQ + off, 16, 1024),
+                        umma_bf16_w(tmem + col_s(x), sdesc_sw128(sQ + off, 16, 1024),
                                   sdesc_sw128(sK + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
                     }
-                    umma_commit(&bar[BAR_S_FULL + x]);
-                    if (j == pl.j1[x]) umma_commit(&bar[BAR_Q_EMPTY + x]);
+                    umma_commit_w(&bar[BAR_S_FULL + x]);
+                    if (j == pl.j1[x]) umma_commit_w(&bar[BAR_Q_EMPTY + x]);
                     pend[x] = j;
                 }
             }
-            umma_commit(&bar[BAR_K_EMPTY + st]);
-            if (j >= 1) umma_commit(&bar[BAR_V_EMPTY + (kvi - 1) % kStages]);
+            umma_commit_w(&bar[BAR_K_EMPTY + st]);
+            if (j >= 1) umma_commit_w(&bar[BAR_V_EMPTY + (kvi - 1) % kStages]);
         }
 #pragma unroll
         for (int x = 0; x < 2; ++x)
             if (pend[x] >= 0 && !issue_pv(x, pend[x])) return false;
-        if (pl.nblk > 0) umma_commit(&bar[BAR_V_EMPTY + (kv_base + pl.nblk - 1) % kStages]);
+        if (pl.nblk > 0) umma_commit_w(&bar[BAR_V_EMPTY + (kv_base + pl.nblk - 1) % kStages]);
         kv_base += pl.nblk;
     }
     return true;
@@ -473,28 +473,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     } else {
         warpgroup_reg_dec<kRegsOther>();
     }
-    if (warp < 8) {
-    } else if (warp == 8) {
+    if (warp == 8) {
         if (lane == 0) {
             prefetch_tensormap(&p.tm_q);
             prefetch_tensormap(&p.tm_qc);
             prefetch_tensormap(&p.tm_k);
             prefetch_tensormap(&p.tm_v);
-            uint32_t k_issued = 0, v_issued = 0, q_issued[2] = {0, 0};
-            if (!producer(p, smem, bar, abort_flag, k_issued, v_issued, q_issued)) {
-                drain_loads(&bar[BAR_K_FULL], k_issued);
-                drain_loads(&bar[BAR_V_FULL], v_issued);
-                for (int x = 0; x < 2; ++x)
-                    if (q_issued[x]) mbar_drain(&bar[BAR_Q_FULL + x], (q_issued[x] - 1) & 1u);
-            }
+        }
+        __syncwarp();
+        uint32_t k_issued = 0, v_issued = 0, q_issued[2] = {0, 0};
+        if (!producer(p, smem, bar, abort_flag, k_issued, v_issued, q_issued)) {
+            drain_loads(&bar[BAR_K_FULL], k_issued);
+            drain_loads(&bar[BAR_V_FULL], v_issued);
+            for (int x = 0; x < 2; ++x)
+                if (q_issued[x]) mbar_drain(&bar[BAR_Q_FULL + x], (q_issued[x] - 1) & 1u);
         }
         __syncwarp();
     } else if (warp == 9) {
-        if (lane == 0) {
-            mma_issuer(p, smem, bar, tmem, abort_flag);
-            umma_commit(&bar[BAR_DRAIN]);
-            mbar_drain(&bar[BAR_DRAIN], 0);
-        }
+        mma_issuer(p, smem, bar, tmem, abort_flag);
+        // Every MMA this warp issued has completed once this arrives.
+        umma_commit_w(&bar[BAR_DRAIN]);
+        mbar_drain(&bar[BAR_DRAIN], 0);
         __syncwarp();
     }
 
