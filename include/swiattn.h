@@ -102,6 +102,28 @@ int swiattn_decode(const void* q, const void* k_cache, const void* v_cache,
                    int Lmax, int Hq, int Hkv, int d, int W, float scale, int dtype,
                    void* workspace, size_t workspace_bytes, void* stream);
 
+/* swiattn_decode without a workspace argument, for callers that cannot
+ * allocate device memory (for example code that runs inside an allocator-free
+ * runtime or a host framework that owns every device allocation and exposes
+ * none to plug-ins).  The paper has no counterpart: this is a deployment
+ * convenience.  Arguments, layouts and results are those of swiattn_decode.
+ *  - The split-KV partials go to one fixed 16 MiB device array inside the
+ *    library, which every GPU that loads the library holds until the process
+ *    exits.  A call whose partials, B * ceil(Lmax/128) * Hq * (d+2) * 4 bytes
+ *    rounded up to 256, exceed 16 MiB returns SWIATTN_EINVAL and launches
+ *    nothing (e.g. B=16, Hq=16, d=128 allows Lmax up to 16 128).
+ *  - The call allocates nothing.  Its first call on a device looks up that
+ *    array's device address (once per device, with the device current); make
+ *    that first call before any stream capture.
+ *  - All calls share the one array: calls that overlap on the GPU (different
+ *    streams, or different host threads without ordering) race and corrupt
+ *    each other's results.  No state carries over between calls that do not
+ *    overlap. */
+int swiattn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* seq_lens, const uint8_t* gate, void* o, float* lse,
+                           int B, int Lmax, int Hq, int Hkv, int d, int W, float scale, int dtype,
+                           void* stream);
+
 /* Bytes of device workspace swiattn_dual_branch needs for these sizes. */
 size_t swiattn_dual_branch_workspace(int B, int N, int Hq, int Hkv, int d, int W, int dtype);
 

@@ -32,7 +32,8 @@ _lib = None
 # Every symbol include/swiattn.h declares.
 EXPORTS = (
     "swiattn_route", "swiattn_prefill_workspace", "swiattn_prefill", "swiattn_decode_workspace",
-    "swiattn_decode", "swiattn_dual_branch_workspace", "swiattn_dual_branch",
+    "swiattn_decode", "swiattn_decode_noalloc", "swiattn_dual_branch_workspace",
+    "swiattn_dual_branch",
     "swiattn_get_device_error", "swiattn_status_string", "swiattn_set_profile_events",
     "swiattn_num_sms",
 )
@@ -66,6 +67,7 @@ def _load() -> ctypes.CDLL:
             lib.swiattn_decode_workspace.argtypes = [i32] * 7
             lib.swiattn_decode_workspace.restype = sz
             lib.swiattn_decode.argtypes = [vp] * 7 + [i32] * 6 + [f32, i32, vp, sz, vp]
+            lib.swiattn_decode_noalloc.argtypes = [vp] * 7 + [i32] * 6 + [f32, i32, vp]
             lib.swiattn_dual_branch_workspace.argtypes = [i32] * 7
             lib.swiattn_dual_branch_workspace.restype = sz
             lib.swiattn_dual_branch.argtypes = ([vp] * 11 + [i32] * 6 + [f32] * 4
@@ -76,7 +78,7 @@ def _load() -> ctypes.CDLL:
             lib.swiattn_num_sms.argtypes = []
             lib.swiattn_set_profile_events.argtypes = [vp, vp]
             lib.swiattn_set_profile_events.restype = None
-            for name in ("swiattn_route", "swiattn_prefill", "swiattn_decode",
+            for name in ("swiattn_route", "swiattn_prefill", "swiattn_decode", "swiattn_decode_noalloc",
                          "swiattn_dual_branch", "swiattn_get_device_error", "swiattn_num_sms"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib

@@ -1,0 +1,82 @@
+"""swiattn_decode_noalloc: the decode entry point for callers that cannot
+allocate device memory (a host runtime that owns every allocation, or code
+that must not allocate while it runs).  It keeps its split-KV partials in a
+fixed array inside the library instead of a caller workspace, so it must give
+the same results as swiattn_decode.  Collected last on purpose: a run that
+stops at the first failure has run every other test by then.
+"""
+import ctypes
+import math
+
+import pytest
+import torch
+
+import swiattn_inputs as inp
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def swa():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    import __graft_entry__
+    __graft_entry__.build()
+    import sliding_window_attention_router_gb300 as m
+    return m
+
+
+def _call_noalloc(lib, q, kc, vc, sl, gate, o, lse, W, scale, dtype):
+    B, Hq, d = q.shape
+    Lmax, Hkv = kc.shape[1], kc.shape[2]
+    vp = ctypes.c_void_p
+    return lib.swiattn_decode_noalloc(
+        vp(q.data_ptr()), vp(kc.data_ptr()), vp(vc.data_ptr()), vp(sl.data_ptr()),
+        vp(gate.data_ptr()), vp(o.data_ptr()), vp(lse.data_ptr()), B, Lmax, Hq, Hkv, d, W,
+        float(scale), dtype, vp(torch.cuda.current_stream().cuda_stream))
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_noalloc_decode_matches_workspace_decode_twice(swa, dtype):
+    lib = swa._load()
+    g = inp._gen(2024)
+    B, Lmax, Hq, Hkv, d, W = 6, 3000, 8, 4, 128, 500
+    scale = 1 / math.sqrt(d)
+    code = swa._DT[dtype]
+    for call in range(2):   # two calls in a row share the library's scratch array
+        kc = inp.randn((B, Lmax, Hkv, d), dtype, g).cuda()
+        vc = inp.randn((B, Lmax, Hkv, d), dtype, g).cuda()
+        q = inp.randn((B, Hq, d), dtype, g).cuda()
+        sl = torch.tensor([1, 499, 500, 501, 2999, 3000], dtype=torch.int32).roll(call).cuda()
+        gate = torch.tensor([0, 1, 0, 1, 0, 1], dtype=torch.uint8).roll(call).cuda()
+        ref, ref_lse = swa.decode(q, kc, vc, sl, gate, W, scale, want_lse=True)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, Hq), dtype=torch.float32, device="cuda")
+        assert _call_noalloc(lib, q, kc, vc, sl, gate, o, lse, W, scale, code) == 0
+        torch.cuda.synchronize()
+        tol = 1e-4 if dtype == torch.float32 else 2e-2
+        assert (o.float() - ref.float()).abs().max().item() <= tol
+        assert (lse - ref_lse).abs().max().item() <= 1e-4
+    assert swa.get_device_error() == 0
+
+
+def test_noalloc_decode_rejects_partials_beyond_scratch(swa):
+    lib = swa._load()
+    B, Hq, Hkv, d, W = 16, 16, 16, 128, 1024
+    q = torch.zeros(B, Hq, d, dtype=torch.bfloat16, device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty(B, Hq, dtype=torch.float32, device="cuda")
+    sl = torch.full((B,), 8, dtype=torch.int32, device="cuda")
+    gate = torch.zeros(B, dtype=torch.uint8, device="cuda")
+    small = torch.zeros(B, 8, Hkv, d, dtype=torch.bfloat16, device="cuda")
+    # Lmax = 16 256 needs 127 chunks of partials: 16.9 MB > 16 MiB.  The caches
+    # are never read because validation rejects the call first.
+    rc = _call_noalloc(lib, q, small, small, sl, gate, o, lse, W, 0.1, swa.BF16)
+    assert rc == 0
+    vp = ctypes.c_void_p
+    rc = lib.swiattn_decode_noalloc(vp(q.data_ptr()), vp(small.data_ptr()), vp(small.data_ptr()),
+                                    vp(sl.data_ptr()), vp(gate.data_ptr()), vp(o.data_ptr()),
+                                    vp(lse.data_ptr()), B, 16256, Hq, Hkv, d, W, 0.1, swa.BF16,
+                                    vp(torch.cuda.current_stream().cuda_stream))
+    assert rc == 1   # SWIATTN_EINVAL, nothing launched
+    torch.cuda.synchronize()
