@@ -7,13 +7,17 @@
 // streams one sequence of 128-key blocks; each tile uses the contiguous run of
 // blocks its rows can see, so every K/V block is loaded once for both tiles.
 //
+// Items are claimed dynamically from the cost-sorted list (longest first).
+//
 // Per tile the chain is S = Q K^T (TMEM) -> softmax (P, bf16, written back
 // over S in TMEM) -> O += P V (P read from TMEM) -> next S.  The two tiles'
 // chains interleave on the tensor core: while warpgroup A turns S_A into P_A,
 // the tensor core runs tile B's PV and next S, and the reverse.
 //   warps 0-3   softmax + epilogue of tile A (thread r owns row r = TMEM lane r)
+//               (the epilogue stages rows in shared memory for coalesced stores)
 //   warps 4-7   softmax + epilogue of tile B
-//   warp 8      TMA producer: Q tiles, K and V blocks (converged, elected issue)
+//   warp 8      item claimer and TMA producer: Q tiles, K and V blocks
+//               (converged, elected issue)
 //   warp 9      TMEM allocator and MMA issuer (converged, elected issue)
 //   warps 10-11 idle (complete the third warpgroup for register reconfiguration)
 // TMEM: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
@@ -39,28 +43,36 @@ constexpr uint32_t kRegsOther = 72;
 constexpr int kTileBytes = kBM * kHD * 2;    // 32 KiB
 constexpr int kHalfBytes = kTileBytes / 2;   // 16 KiB
 
+constexpr int kSched = 4;                                 // item broadcast ring
+constexpr int kStageBytesPerWarp = 32 * 64 * 2;           // 32 rows x 64 bf16 output columns
+
 constexpr int kOffQ = 0;                                  // Q_A, Q_B
-constexpr int kOffK = kOffQ + 2 * kTileBytes;
-constexpr int kOffV = kOffK + kStages * kTileBytes;
-constexpr int kOffBar = kOffV + kStages * kTileBytes;
+constexpr int kOffK = kOffQ + 2 * kTileBytes;             // K slots
+constexpr int kOffV = kOffK + kStages * kTileBytes;       // V slots
+constexpr int kOffStage = kOffV + kStages * kTileBytes;   // epilogue staging, 8 warps
+constexpr int kOffBar = kOffStage + 8 * kStageBytesPerWarp;
 
 enum {
-    BAR_Q_FULL = 0,                    // [2]
-    BAR_Q_EMPTY = BAR_Q_FULL + 2,      // [2]
-    BAR_K_FULL = BAR_Q_EMPTY + 2,      // [kStages]
-    BAR_K_EMPTY = BAR_K_FULL + kStages,
-    BAR_V_FULL = BAR_K_EMPTY + kStages,
-    BAR_V_EMPTY = BAR_V_FULL + kStages,
-    BAR_S_FULL = BAR_V_EMPTY + kStages,   // [2] per tile
-    BAR_P_FULL = BAR_S_FULL + 2,          // [2]
-    BAR_O_FULL = BAR_P_FULL + 2,          // [2]
-    BAR_O_FREE = BAR_O_FULL + 2,          // [2]
-    BAR_DRAIN = BAR_O_FREE + 2,
+    BAR_Q_FULL = 0,                        // [2] per tile
+    BAR_Q_EMPTY = BAR_Q_FULL + 2,          // [2]
+    BAR_KV_FULL = BAR_Q_EMPTY + 2,         // [kStages]: slot of step g holds K_j and V_{j-1}
+    BAR_KV_EMPTY = BAR_KV_FULL + kStages,  // [kStages]
+    BAR_S_FULL = BAR_KV_EMPTY + kStages,   // [2]
+    BAR_P_FULL = BAR_S_FULL + 2,           // [2]
+    BAR_O_FULL = BAR_P_FULL + 2,           // [2]
+    BAR_O_FREE = BAR_O_FULL + 2,           // [2]
+    BAR_SCHED_FULL = BAR_O_FREE + 2,       // [kSched]
+    BAR_SCHED_EMPTY = BAR_SCHED_FULL + kSched,
+    BAR_DRAIN = BAR_SCHED_EMPTY + kSched,
     BAR_COUNT
 };
+// Consumers of a broadcast item: the MMA warp and the eight softmax warps.
+constexpr uint32_t kSchedConsumers = 1 + 8;
 
-constexpr int kOffMisc = kOffBar + BAR_COUNT * 8;
+constexpr int kOffSched = kOffBar + BAR_COUNT * 8;
+constexpr int kOffMisc = kOffSched + kSched * 4;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 constexpr uint32_t kTmemCols = 512;
 __device__ __forceinline__ uint32_t col_s(int x) { return x ? 128u : 0u; }
@@ -75,6 +87,7 @@ struct PfParams {
     const int* routed_count;
     const int* tile_prefix;
     const int* n_items;
+    int* next_item;          // work counter, zeroed by the schedule
     const WorkItem* items;
     const uint8_t* gate;
     __nv_bfloat16* o;
@@ -93,10 +106,6 @@ struct Plan {
 };
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
-
-__device__ __forceinline__ int snake_index(int k, int c, int G) {
-    return k * G + ((k & 1) ? (G - 1 - c) : c);
-}
 
 __device__ __forceinline__ Plan make_plan(const PfParams& p, int idx) {
     const WorkItem it = p.items[idx];
@@ -150,17 +159,51 @@ __device__ __forceinline__ Plan make_plan(const PfParams& p, int idx) {
 __device__ __forceinline__ bool tile_active(const Plan& pl, int x) { return pl.j0[x] <= pl.j1[x]; }
 
 // ----------------------------------------------------------------- roles --
+//
+// Items are taken dynamically, longest first (the list is cost-sorted): the
+// producer warp claims the next index with an atomic and broadcasts it through
+// a kSched-slot ring in shared memory; a negative index ends the stream.
 
-// One producer thread: Q tiles, then K one block ahead of V (a K slot frees
-// when S of the block two back completes, a V slot when PV three back does,
-// which the MMA order completes first).
-__device__ bool producer(const PfParams& p, uint8_t* smem, uint64_t* bar, volatile int* abort_flag,
-                         uint32_t& k_issued, uint32_t& v_issued, uint32_t* q_issued) {
-    const int G = gridDim.x, c = blockIdx.x;
+// Producer side: claim item k's index and publish it (or -1 past the end).
+__device__ bool publish_item(const PfParams& p, uint64_t* bar, volatile int* sched, int k, int n,
+                             volatile int* abort_flag, int& idx) {
+    const int slot = k % kSched;
+    const uint32_t par = (static_cast<uint32_t>(k) / kSched) & 1u;
+    if (!mbar_wait_w(&bar[BAR_SCHED_EMPTY + slot], par ^ 1u, abort_flag, p.err)) return false;
+    int v = 0;
+    if ((threadIdx.x & 31) == 0) v = atomicAdd(p.next_item, 1);
+    v = __shfl_sync(0xffffffffu, v, 0);
+    idx = v < n ? v : -1;
+    if ((threadIdx.x & 31) == 0) {
+        sched[slot] = idx;
+        mbar_arrive(&bar[BAR_SCHED_FULL + slot]);   // release: the write above is visible
+    }
+    __syncwarp();
+    return true;
+}
+
+// Consumer side (a whole warp): read item k's index and free its slot.
+__device__ bool consume_item(const PfParams& p, uint64_t* bar, volatile int* sched, int k,
+                             volatile int* abort_flag, int& idx) {
+    const int slot = k % kSched;
+    const uint32_t par = (static_cast<uint32_t>(k) / kSched) & 1u;
+    if (!mbar_wait_w(&bar[BAR_SCHED_FULL + slot], par, abort_flag, p.err)) return false;
+    idx = sched[slot];
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&bar[BAR_SCHED_EMPTY + slot]);
+    return true;
+}
+
+// Producer warp (converged, one elected lane issues): per item, the Q tiles,
+// then one K/V slot per step g: step j of an item carries K_j (j < nblk) and
+// V_{j-1} (j >= 1), so a slot is freed by one commit after S(j) and PV(j-1).
+__device__ bool producer(const PfParams& p, uint8_t* smem, uint64_t* bar, volatile int* sched,
+                         volatile int* abort_flag, uint32_t& g, uint32_t* q_issued) {
     const int n = *p.n_items;
     for (int k = 0;; ++k) {
-        const int idx = snake_index(k, c, G);
-        if (idx >= n) break;
+        int idx;
+        if (!publish_item(p, bar, sched, k, n, abort_flag, idx)) return false;
+        if (idx < 0) break;
         const Plan pl = make_plan(p, idx);
         const CUtensorMap* qm = (pl.kind == kItemFar) ? &p.tm_qc : &p.tm_q;
         auto load_q = [&](int x) -> bool {
@@ -173,25 +216,26 @@ __device__ bool producer(const PfParams& p, uint8_t* smem, uint64_t* bar, volati
             ++q_issued[x];
             return true;
         };
-        auto load_kv = [&](int base_bar, int off, const CUtensorMap* map, uint32_t& issued,
-                           int j) -> bool {
-            const uint32_t st = issued % kStages, ph = (issued / kStages) & 1u;
-            if (!mbar_wait_w(&bar[base_bar + kStages + st], ph ^ 1u, abort_flag, p.err)) return false;
-            mbar_arrive_expect_tx_w(&bar[base_bar + st], kTileBytes);
-            uint8_t* dst = smem + off + st * kTileBytes;
-            const int key0 = pl.kv0 + j * kBN;
-            tma_load_4d_w(dst, map, &bar[base_bar + st], 0, pl.kvh, key0, pl.b);
-            tma_load_4d_w(dst + kHalfBytes, map, &bar[base_bar + st], 64, pl.kvh, key0, pl.b);
-            ++issued;
-            return true;
-        };
         if (tile_active(pl, 0) && !load_q(0)) return false;
         for (int j = 0; j <= pl.nblk; ++j) {
+            if (j < pl.nblk && tile_active(pl, 1) && j == pl.j0[1] && !load_q(1)) return false;
+            const uint32_t st = g % kStages, ph = (g / kStages) & 1u;
+            if (!mbar_wait_w(&bar[BAR_KV_EMPTY + st], ph ^ 1u, abort_flag, p.err)) return false;
+            const uint32_t bytes = (j < pl.nblk ? kTileBytes : 0) + (j >= 1 ? kTileBytes : 0);
+            mbar_arrive_expect_tx_w(&bar[BAR_KV_FULL + st], bytes);
             if (j < pl.nblk) {
-                if (tile_active(pl, 1) && j == pl.j0[1] && !load_q(1)) return false;
-                if (!load_kv(BAR_K_FULL, kOffK, &p.tm_k, k_issued, j)) return false;
+                uint8_t* dst = smem + kOffK + st * kTileBytes;
+                const int key0 = pl.kv0 + j * kBN;
+                tma_load_4d_w(dst, &p.tm_k, &bar[BAR_KV_FULL + st], 0, pl.kvh, key0, pl.b);
+                tma_load_4d_w(dst + kHalfBytes, &p.tm_k, &bar[BAR_KV_FULL + st], 64, pl.kvh, key0, pl.b);
             }
-            if (j >= 1 && !load_kv(BAR_V_FULL, kOffV, &p.tm_v, v_issued, j - 1)) return false;
+            if (j >= 1) {
+                uint8_t* dst = smem + kOffV + st * kTileBytes;
+                const int key0 = pl.kv0 + (j - 1) * kBN;
+                tma_load_4d_w(dst, &p.tm_v, &bar[BAR_KV_FULL + st], 0, pl.kvh, key0, pl.b);
+                tma_load_4d_w(dst + kHalfBytes, &p.tm_v, &bar[BAR_KV_FULL + st], 64, pl.kvh, key0, pl.b);
+            }
+            ++g;
         }
     }
     return true;
@@ -204,57 +248,53 @@ __device__ void drain_loads(uint64_t* full_bars, uint32_t issued) {
     }
 }
 
-__device__ bool mma_issuer(const PfParams& p, uint8_t* smem, uint64_t* bar, uint32_t tmem,
-                           volatile int* abort_flag) {
-    const int G = gridDim.x, c = blockIdx.x;
-    const int n = *p.n_items;
-    uint32_t kv_base = 0;
+__device__ bool mma_issuer(const PfParams& p, uint8_t* smem, uint64_t* bar, volatile int* sched,
+                           uint32_t tmem, volatile int* abort_flag) {
+    uint32_t g = 0;
     uint32_t q_cnt[2] = {0, 0}, p_cnt[2] = {0, 0}, o_cnt[2] = {0, 0};
 
     for (int k = 0;; ++k) {
-        const int idx = snake_index(k, c, G);
-        if (idx >= n) break;
+        int idx;
+        if (!consume_item(p, bar, sched, k, abort_flag, idx)) return false;
+        if (idx < 0) break;
         const Plan pl = make_plan(p, idx);
         int pend[2] = {-1, -1};
         bool first_pv[2] = {true, true};
 
-        auto issue_pv = [&](int x, int jj) -> bool {
-            const uint32_t kvi = kv_base + jj;
-            const uint32_t st = kvi % kStages, ph = (kvi / kStages) & 1u;
+        auto issue_pv = [&](int x, int jj, uint32_t sV) -> bool {
             if (!mbar_wait_w(&bar[BAR_P_FULL + x], p_cnt[x] & 1u, abort_flag, p.err)) return false;
             ++p_cnt[x];
-            if (!mbar_wait_w(&bar[BAR_V_FULL + st], ph, abort_flag, p.err)) return false;
             if (first_pv[x]) {
                 if (!mbar_wait_w(&bar[BAR_O_FREE + x], (o_cnt[x] & 1u) ^ 1u, abort_flag, p.err))
                     return false;
                 ++o_cnt[x];
             }
             tc_fence_after();
-            const uint32_t sV = smem_u32(smem + kOffV + st * kTileBytes);
 #pragma unroll
             for (int kk = 0; kk < kBN / 16; ++kk) {
                 const uint64_t bdesc = sdesc_sw128(sV + kk * 16 * 128, kHalfBytes, 1024);
                 umma_bf16_ts_w(tmem + col_o(x), tmem + col_s(x) + kk * 8, bdesc, kIdescO,
-                             (first_pv[x] && kk == 0) ? 0u : 1u);
+                               (first_pv[x] && kk == 0) ? 0u : 1u);
             }
             first_pv[x] = false;
             if (jj == pl.j1[x]) umma_commit_w(&bar[BAR_O_FULL + x]);
             return true;
         };
 
-        for (int j = 0; j < pl.nblk; ++j) {
-            const uint32_t kvi = kv_base + j;
-            const uint32_t st = kvi % kStages, ph = (kvi / kStages) & 1u;
-            if (!mbar_wait_w(&bar[BAR_K_FULL + st], ph, abort_flag, p.err)) return false;
+        for (int j = 0; j <= pl.nblk; ++j) {
+            const uint32_t st = g % kStages, ph = (g / kStages) & 1u;
+            if (!mbar_wait_w(&bar[BAR_KV_FULL + st], ph, abort_flag, p.err)) return false;
             tc_fence_after();
             const uint32_t sK = smem_u32(smem + kOffK + st * kTileBytes);
+            const uint32_t sV = smem_u32(smem + kOffV + st * kTileBytes);
 #pragma unroll
             for (int x = 0; x < 2; ++x) {
+                // PV of the previous block first: P_x lives in S_x's columns.
                 if (pend[x] >= 0) {
-                    if (!issue_pv(x, pend[x])) return false;
+                    if (!issue_pv(x, pend[x], sV)) return false;
                     pend[x] = -1;
                 }
-                if (j >= pl.j0[x] && j <= pl.j1[x]) {
+                if (j < pl.nblk && j >= pl.j0[x] && j <= pl.j1[x]) {
                     if (j == pl.j0[x]) {
                         if (!mbar_wait_w(&bar[BAR_Q_FULL + x], q_cnt[x] & 1u, abort_flag, p.err))
                             return false;
@@ -266,21 +306,16 @@ __device__ bool mma_issuer(const PfParams& p, uint8_t* smem, uint64_t* bar, uint
                     for (int kk = 0; kk < kHD / 16; ++kk) {
                         const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
                         umma_bf16_w(tmem + col_s(x), sdesc_sw128(sQ + off, 16, 1024),
-                                  sdesc_sw128(sK + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
+                                    sdesc_sw128(sK + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
                     }
                     umma_commit_w(&bar[BAR_S_FULL + x]);
                     if (j == pl.j1[x]) umma_commit_w(&bar[BAR_Q_EMPTY + x]);
                     pend[x] = j;
                 }
             }
-            umma_commit_w(&bar[BAR_K_EMPTY + st]);
-            if (j >= 1) umma_commit_w(&bar[BAR_V_EMPTY + (kvi - 1) % kStages]);
+            umma_commit_w(&bar[BAR_KV_EMPTY + st]);
+            ++g;
         }
-#pragma unroll
-        for (int x = 0; x < 2; ++x)
-            if (pend[x] >= 0 && !issue_pv(x, pend[x])) return false;
-        if (pl.nblk > 0) umma_commit_w(&bar[BAR_V_EMPTY + (kv_base + pl.nblk - 1) % kStages]);
-        kv_base += pl.nblk;
     }
     return true;
 }
@@ -291,33 +326,21 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
     return __all_sync(0xffffffffu, ok);
 }
 
-__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float* v) {
-    uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {
-        uint4 w;
-        w.x = pack_bf16x2(v[8 * g + 0], v[8 * g + 1]);
-        w.y = pack_bf16x2(v[8 * g + 2], v[8 * g + 3]);
-        w.z = pack_bf16x2(v[8 * g + 4], v[8 * g + 5]);
-        w.w = pack_bf16x2(v[8 * g + 6], v[8 * g + 7]);
-        d4[g] = w;
-    }
-}
-
-__device__ bool softmax_role(const PfParams& p, uint64_t* bar, uint32_t tmem, volatile int* abort_flag,
-                             int x, int wq, int lane) {
-    const int G = gridDim.x, c = blockIdx.x;
-    const int n = *p.n_items;
+__device__ bool softmax_role(const PfParams& p, uint8_t* smem, uint64_t* bar, volatile int* sched,
+                             uint32_t tmem, volatile int* abort_flag, int x, int wq, int lane) {
     const int r = wq * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const uint32_t tS = lane_base + col_s(x);
     const uint32_t tO = lane_base + col_o(x);
     const float sl = p.scale_log2;
+    // This warp's 4 KiB staging area for coalesced output stores.
+    const uint32_t stg = smem_u32(smem + kOffStage + (x * 4 + wq) * kStageBytesPerWarp);
     uint32_t s_cnt = 0, o_cnt = 0;
 
     for (int k = 0;; ++k) {
-        const int idx = snake_index(k, c, G);
-        if (idx >= n) break;
+        int idx;
+        if (!consume_item(p, bar, sched, k, abort_flag, idx)) return false;
+        if (idx < 0) break;
         const Plan pl = make_plan(p, idx);
         if (!tile_active(pl, x)) continue;
         const bool far = pl.kind == kItemFar;
@@ -408,20 +431,42 @@ __device__ bool softmax_role(const PfParams& p, uint64_t* bar, uint32_t tmem, vo
             mbar_arrive(&bar[BAR_P_FULL + x]);
         }
 
+        // Epilogue: O/l as bf16.  Each thread stages its row (64 columns at a
+        // time) in shared memory; the warp then stores 4 whole rows per
+        // instruction (8 lanes x 16 bytes per 128-byte row segment).
         if (!warp_wait(&bar[BAR_O_FULL + x], o_cnt & 1u, abort_flag, p.err)) return false;
         ++o_cnt;
         tc_fence_after();
         const float inv = (l > 0.f) ? 1.f / l : 0.f;
-        const size_t out_row = (i >= 0) ? (((size_t)pl.b * p.N + i) * p.Hq + pl.h) : 0;
+        const unsigned long long out_row =
+            (i >= 0) ? (((unsigned long long)pl.b * p.N + i) * p.Hq + pl.h) : 0ull;
+        const int wflag = write_row ? 1 : 0;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-            uint32_t orr[32];
-            tmem_ld32(tO + q4 * 32, orr);
+        for (int hh = 0; hh < 2; ++hh) {
+            uint32_t orr[64];
+            tmem_ld32(tO + hh * 64, orr);
+            tmem_ld32(tO + hh * 64 + 32, orr + 32);
             tmem_ld_wait();
-            float* ov = reinterpret_cast<float*>(orr);
 #pragma unroll
-            for (int t = 0; t < 32; ++t) ov[t] *= inv;
-            if (write_row) store_row_bf16(p.o + out_row * kHD + q4 * 32, ov);
+            for (int u = 0; u < 8; ++u) {
+                const uint32_t addr = stg + lane * 128 + ((((uint32_t)u) ^ ((uint32_t)lane & 7u)) << 4);
+                st_shared_v4(addr,
+                             pack_bf16x2(__uint_as_float(orr[8 * u + 0]) * inv, __uint_as_float(orr[8 * u + 1]) * inv),
+                             pack_bf16x2(__uint_as_float(orr[8 * u + 2]) * inv, __uint_as_float(orr[8 * u + 3]) * inv),
+                             pack_bf16x2(__uint_as_float(orr[8 * u + 4]) * inv, __uint_as_float(orr[8 * u + 5]) * inv),
+                             pack_bf16x2(__uint_as_float(orr[8 * u + 6]) * inv, __uint_as_float(orr[8 * u + 7]) * inv));
+            }
+            __syncwarp();
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+                const int row = it * 4 + (lane >> 3);
+                const uint32_t u = lane & 7;
+                const unsigned long long orow = __shfl_sync(0xffffffffu, out_row, row);
+                const int wf = __shfl_sync(0xffffffffu, wflag, row);
+                const uint4 val = ld_shared_v4(stg + row * 128 + ((u ^ ((uint32_t)row & 7u)) << 4));
+                if (wf) *reinterpret_cast<uint4*>(p.o + orow * kHD + hh * 64 + u * 8) = val;
+            }
+            __syncwarp();
         }
         if (write_row && p.lse) p.lse[out_row] = (m2 + __log2f(l)) * 0.69314718055994531f;
         tc_fence_before();
@@ -435,6 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kOffBar);
+    volatile int* sched = reinterpret_cast<volatile int*>(smem + kOffSched);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -448,11 +494,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             mbar_init(&bar[BAR_O_FULL + x], 1);
             mbar_init(&bar[BAR_O_FREE + x], kBM);
         }
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&bar[BAR_K_FULL + s], 1);
-            mbar_init(&bar[BAR_K_EMPTY + s], 1);
-            mbar_init(&bar[BAR_V_FULL + s], 1);
-            mbar_init(&bar[BAR_V_EMPTY + s], 1);
+        for (int st = 0; st < kStages; ++st) {
+            mbar_init(&bar[BAR_KV_FULL + st], 1);
+            mbar_init(&bar[BAR_KV_EMPTY + st], 1);
+        }
+        for (int st = 0; st < kSched; ++st) {
+            mbar_init(&bar[BAR_SCHED_FULL + st], 1);
+            mbar_init(&bar[BAR_SCHED_EMPTY + st], kSchedConsumers);
         }
         mbar_init(&bar[BAR_DRAIN], 1);
         *abort_flag = 0;
@@ -469,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 
     if (warp < 8) {
         warpgroup_reg_inc<kRegsSoftmax>();
-        softmax_role(p, bar, tmem, abort_flag, warp >> 2, warp & 3, lane);
+        softmax_role(p, smem, bar, sched, tmem, abort_flag, warp >> 2, warp & 3, lane);
     } else {
         warpgroup_reg_dec<kRegsOther>();
     }
@@ -481,16 +529,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             prefetch_tensormap(&p.tm_v);
         }
         __syncwarp();
-        uint32_t k_issued = 0, v_issued = 0, q_issued[2] = {0, 0};
-        if (!producer(p, smem, bar, abort_flag, k_issued, v_issued, q_issued)) {
-            drain_loads(&bar[BAR_K_FULL], k_issued);
-            drain_loads(&bar[BAR_V_FULL], v_issued);
+        uint32_t g = 0, q_issued[2] = {0, 0};
+        if (!producer(p, smem, bar, sched, abort_flag, g, q_issued)) {
+            drain_loads(&bar[BAR_KV_FULL], g);
             for (int x = 0; x < 2; ++x)
                 if (q_issued[x]) mbar_drain(&bar[BAR_Q_FULL + x], (q_issued[x] - 1) & 1u);
         }
         __syncwarp();
     } else if (warp == 9) {
-        mma_issuer(p, smem, bar, tmem, abort_flag);
+        mma_issuer(p, smem, bar, sched, tmem, abort_flag);
         // Every MMA this warp issued has completed once this arrives.
         umma_commit_w(&bar[BAR_DRAIN]);
         mbar_drain(&bar[BAR_DRAIN], 0);
@@ -521,6 +568,7 @@ cudaError_t launch_prefill_tc(const TcAttnArgs& a, const int* tile_prefix, unsig
     p.routed_count = a.routed_count;
     p.tile_prefix = tile_prefix;
     p.n_items = a.n_items;
+    p.next_item = const_cast<int*>(a.n_items) + 1;
     p.items = a.items;
     p.gate = a.gate;
     p.o = static_cast<__nv_bfloat16*>(a.o);

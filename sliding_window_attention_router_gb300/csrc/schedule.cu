@@ -144,7 +144,10 @@ __global__ void __launch_bounds__(1024) build_items_kernel(
         const int pos = atomicAdd(&hist[min(cost, kCostBuckets - 1)], 1);
         for (int h = 0; h < Hq; ++h) items[(size_t)pos * Hq + h] = WorkItem{kind, b, h, pair};
     }
-    if (threadIdx.x == 0) n_items[0] = total * Hq;
+    if (threadIdx.x == 0) {
+        n_items[0] = total * Hq;
+        n_items[1] = 0;   // work counter the attention kernel claims items from
+    }
 }
 
 // Compacted queries of far rows: qc[b, r] = q[b, routed_list[b, r]] for
