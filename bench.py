@@ -458,7 +458,7 @@ def run_ours(args, dist: Dist):
                          "peak_source": f"{peaks_src} bf16 dense (burst)"},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": 4 * args.steps,
+            "gpu_launches": 3 * args.steps,
             "clocks": clk,
             "wall_s_headline": wall,
         }

@@ -20,48 +20,61 @@ constexpr int kCostBuckets = 4096;
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 
-// One CTA per batch: exclusive scan of the far-row flags.
+// Block-wide exclusive scan of one value per thread; *total receives the sum.
+// Every thread of the block must call it.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_tot[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        int t = lane < nwarps ? warp_tot[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += y;
+        }
+        warp_tot[lane] = t;   // inclusive totals per warp
+    }
+    __syncthreads();
+    const int excl = (w > 0 ? warp_tot[w - 1] : 0) + x - v;
+    *total = warp_tot[nwarps - 1];
+    __syncthreads();
+    return excl;
+}
+
+// One CTA per batch, one pass: each thread counts the far-row flags of a
+// contiguous chunk (all its gate loads in flight), one block scan, then each
+// thread writes its far rows and the per-tile prefix counts of its chunk.
 __global__ void __launch_bounds__(kScanThreads) scan_far_rows_kernel(
     const uint8_t* __restrict__ gate, int N, int W, int* __restrict__ routed_list,
     int* __restrict__ routed_count, int* __restrict__ tile_prefix) {
     __shared__ int warp_tot[32];
-    __shared__ int carry;
     const int b = blockIdx.x;
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int NT = cdiv(N, kBM);
-    if (threadIdx.x == 0) carry = 0;
-    __syncthreads();
-    for (int base = 0; base < N; base += kScanThreads) {
-        const int i = base + threadIdx.x;
-        const int f = (i < N && i >= W && gate[(size_t)b * N + i] != 0) ? 1 : 0;
-        int x = f;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o) x += y;
-        }
-        if (lane == 31) warp_tot[w] = x;
-        __syncthreads();
-        if (w == 0) {
-            int t = warp_tot[lane];
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, t, o);
-                if (lane >= o) t += y;
-            }
-            warp_tot[lane] = t;   // inclusive totals per warp
-        }
-        __syncthreads();
-        const int excl = carry + (w > 0 ? warp_tot[w - 1] : 0) + x - f;
-        if (f) routed_list[(size_t)b * N + excl] = i;
-        if (i < N && (i % kBM) == 0) tile_prefix[(size_t)b * (NT + 1) + i / kBM] = excl;
-        __syncthreads();
-        if (threadIdx.x == kScanThreads - 1) carry = excl + f;
-        __syncthreads();
+    const int C = cdiv(N, kScanThreads);
+    const int i0 = min(N, threadIdx.x * C), i1 = min(N, i0 + C);
+    const uint8_t* g = gate + (size_t)b * N;
+    int cnt = 0;
+#pragma unroll 8
+    for (int i = i0; i < i1; ++i) cnt += (i >= W && g[i] != 0) ? 1 : 0;
+    int total;
+    int run = block_exclusive_scan(cnt, warp_tot, &total);
+    int* list = routed_list + (size_t)b * N;
+    int* pre = tile_prefix + (size_t)b * (NT + 1);
+    for (int i = i0; i < i1; ++i) {
+        if ((i % kBM) == 0) pre[i / kBM] = run;
+        if (i >= W && g[i] != 0) list[run++] = i;
     }
     if (threadIdx.x == 0) {
-        routed_count[b] = carry;
-        tile_prefix[(size_t)b * (NT + 1) + NT] = carry;
+        routed_count[b] = total;
+        pre[NT] = total;
     }
 }
 
@@ -107,61 +120,68 @@ __device__ __forceinline__ int pair_cost(int u, const int* routed_list, const in
            band_tile_blocks(b, q0 + kBM, kv0, tile_prefix, N, W, NT);
 }
 
-// Single CTA: counting sort of 256-row pairs by descending cost, Hq items per
-// pair (one per query head).
-__global__ void __launch_bounds__(1024) build_items_kernel(
+// Block 0: counting sort of 256-row pairs by descending cost, Hq items per
+// pair (one per query head), and reset of the attention kernel's work
+// counter.  Other blocks: compacted queries of far rows,
+// qc[b, r] = q[b, routed_list[b, r]] for r < R_b, zero up to the end of the
+// last 128-row tile.
+constexpr int kBuildThreads = 512;
+constexpr int kBucketsPerThread = kCostBuckets / kBuildThreads;
+
+__global__ void __launch_bounds__(kBuildThreads) build_and_gather_kernel(
     const int* __restrict__ routed_list, const int* __restrict__ routed_count,
     const int* __restrict__ tile_prefix, int B, int N, int Hq, int W, WorkItem* __restrict__ items,
-    int* __restrict__ n_items) {
-    __shared__ int hist[kCostBuckets];
-    __shared__ int total;
-    const int NT = cdiv(N, kBM);
-    const int NP = cdiv(N, 2 * kBM);
-    const int U = B * 2 * NP;
-    for (int c = threadIdx.x; c < kCostBuckets; c += blockDim.x) hist[c] = 0;
-    __syncthreads();
-    for (int u = threadIdx.x; u < U; u += blockDim.x) {
-        int b, kind, pair;
-        const int cost = pair_cost(u, routed_list, routed_count, tile_prefix, N, W, NT, NP, b, kind, pair);
-        if (cost > 0) atomicAdd(&hist[min(cost, kCostBuckets - 1)], 1);
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        // exclusive offsets in descending cost order
-        int run = 0;
-        for (int c = kCostBuckets - 1; c >= 0; --c) {
+    int* __restrict__ n_items, const uint4* __restrict__ q, uint4* __restrict__ qc) {
+    if (blockIdx.x == 0) {
+        __shared__ int hist[kCostBuckets];
+        __shared__ int warp_tot[32];
+        const int NT = cdiv(N, kBM);
+        const int NP = cdiv(N, 2 * kBM);
+        const int U = B * 2 * NP;
+        for (int c = threadIdx.x; c < kCostBuckets; c += blockDim.x) hist[c] = 0;
+        __syncthreads();
+        for (int u = threadIdx.x; u < U; u += blockDim.x) {
+            int b, kind, pair;
+            const int cost = pair_cost(u, routed_list, routed_count, tile_prefix, N, W, NT, NP, b, kind, pair);
+            if (cost > 0) atomicAdd(&hist[min(cost, kCostBuckets - 1)], 1);
+        }
+        __syncthreads();
+        // Exclusive offsets in descending cost order: thread t owns buckets
+        // 4095-8t ... 4095-8t-7.
+        int own = 0;
+#pragma unroll
+        for (int k = 0; k < kBucketsPerThread; ++k)
+            own += hist[kCostBuckets - 1 - (threadIdx.x * kBucketsPerThread + k)];
+        int total;
+        int run = block_exclusive_scan(own, warp_tot, &total);
+#pragma unroll
+        for (int k = 0; k < kBucketsPerThread; ++k) {
+            const int c = kCostBuckets - 1 - (threadIdx.x * kBucketsPerThread + k);
             const int h = hist[c];
             hist[c] = run;
             run += h;
         }
-        total = run;
+        __syncthreads();
+        for (int u = threadIdx.x; u < U; u += blockDim.x) {
+            int b, kind, pair;
+            const int cost = pair_cost(u, routed_list, routed_count, tile_prefix, N, W, NT, NP, b, kind, pair);
+            if (cost <= 0) continue;
+            const int pos = atomicAdd(&hist[min(cost, kCostBuckets - 1)], 1);
+            for (int h = 0; h < Hq; ++h) items[(size_t)pos * Hq + h] = WorkItem{kind, b, h, pair};
+        }
+        if (threadIdx.x == 0) {
+            n_items[0] = total * Hq;
+            n_items[1] = 0;   // work counter the attention kernel claims items from
+        }
+        return;
     }
-    __syncthreads();
-    for (int u = threadIdx.x; u < U; u += blockDim.x) {
-        int b, kind, pair;
-        const int cost = pair_cost(u, routed_list, routed_count, tile_prefix, N, W, NT, NP, b, kind, pair);
-        if (cost <= 0) continue;
-        const int pos = atomicAdd(&hist[min(cost, kCostBuckets - 1)], 1);
-        for (int h = 0; h < Hq; ++h) items[(size_t)pos * Hq + h] = WorkItem{kind, b, h, pair};
-    }
-    if (threadIdx.x == 0) {
-        n_items[0] = total * Hq;
-        n_items[1] = 0;   // work counter the attention kernel claims items from
-    }
-}
-
-// Compacted queries of far rows: qc[b, r] = q[b, routed_list[b, r]] for
-// r < R_b, zero up to the end of the last 128-row tile.
-__global__ void gather_far_q_kernel(const uint4* __restrict__ q, const int* __restrict__ routed_list,
-                                    const int* __restrict__ routed_count, uint4* __restrict__ qc,
-                                    int B, int N, int Hq) {
     const int per_row = Hq * (kHD * 2 / 16);
-    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    const size_t stride = (size_t)(gridDim.x - 1) * blockDim.x;
     for (int b = 0; b < B; ++b) {
         const int R = routed_count[b];
         const int Rp = min(N, cdiv(R, kBM) * kBM);
         const size_t total = (size_t)Rp * per_row;
-        for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += stride) {
+        for (size_t idx = (size_t)(blockIdx.x - 1) * blockDim.x + threadIdx.x; idx < total; idx += stride) {
             const int r = (int)(idx / per_row);
             const int c = (int)(idx % per_row);
             uint4 val = make_uint4(0u, 0u, 0u, 0u);
@@ -201,11 +221,10 @@ cudaError_t launch_schedule(const uint8_t* gate, const void* q, int B, int N, in
     int* count = reinterpret_cast<int*>(ws + L.routed_count);
     int* prefix = reinterpret_cast<int*>(ws + L.tile_prefix);
     scan_far_rows_kernel<<<B, kScanThreads, 0, s>>>(gate, N, W, list, count, prefix);
-    build_items_kernel<<<1, 1024, 0, s>>>(list, count, prefix, B, N, Hq, W,
-                                          reinterpret_cast<WorkItem*>(ws + L.items),
-                                          reinterpret_cast<int*>(ws + L.n_items));
-    gather_far_q_kernel<<<num_sms * 4, 256, 0, s>>>(static_cast<const uint4*>(q), list, count,
-                                                   reinterpret_cast<uint4*>(ws + L.qc), B, N, Hq);
+    build_and_gather_kernel<<<1 + num_sms * 2, kBuildThreads, 0, s>>>(
+        list, count, prefix, B, N, Hq, W, reinterpret_cast<WorkItem*>(ws + L.items),
+        reinterpret_cast<int*>(ws + L.n_items), static_cast<const uint4*>(q),
+        reinterpret_cast<uint4*>(ws + L.qc));
     return cudaGetLastError();
 }
 
