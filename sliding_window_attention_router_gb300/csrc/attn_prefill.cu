@@ -368,12 +368,15 @@ __device__ bool softmax_role(const PfParams& p, uint8_t* smem, uint64_t* bar, vo
             tmem_ld32(tS + 96, sr + 96);
             tmem_ld_wait();
             float* s = reinterpret_cast<float*>(sr);
+            const bool full = a <= 0 && e >= kBN - 1;   // every key of the block visible
             float m8[8];
 #pragma unroll
             for (int t = 0; t < 8; ++t) m8[t] = -INFINITY;
-            if (a <= 0 && e >= kBN - 1) {
+            if (full) {
 #pragma unroll
-                for (int cc = 0; cc < kBN; ++cc) m8[cc & 7] = fmaxf(m8[cc & 7], s[cc]);
+                for (int cc = 0; cc < kBN; cc += 16)
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) m8[t] = fmax3(m8[t], s[cc + 2 * t], s[cc + 2 * t + 1]);
             } else {
                 const uint32_t span = static_cast<uint32_t>(e - a);
 #pragma unroll
@@ -383,8 +386,8 @@ __device__ bool softmax_role(const PfParams& p, uint8_t* smem, uint64_t* bar, vo
                     m8[cc & 7] = fmaxf(m8[cc & 7], s[cc]);
                 }
             }
-            const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            const float mx = fmaxf(fmax3(m8[0], m8[1], m8[2]),
+                                   fmax3(fmax3(m8[3], m8[4], m8[5]), m8[6], m8[7]));
             // Running max in scaled log2 units; O and l are rescaled only when
             // the max grows by more than 2^8 (p stays <= 256 otherwise).
             const float mnew = fmaxf(m2, mx * sl);
@@ -409,24 +412,38 @@ __device__ bool softmax_role(const PfParams& p, uint8_t* smem, uint64_t* bar, vo
                 }
             }
             const float mb = (m2 == -INFINITY) ? 0.f : m2;
-            float r8[8];
+            const float2 sl2 = make_float2(sl, sl), nmb = make_float2(-mb, -mb);
+            float2 r4[4];
 #pragma unroll
-            for (int t = 0; t < 8; ++t) r8[t] = 0.f;
+            for (int t = 0; t < 4; ++t) r4[t] = make_float2(0.f, 0.f);
+            // p = 2^(s * scale * log2 e - m).  In blocks with every key visible
+            // one pair in four is evaluated on the FMA pipe (exp2_poly2) to
+            // offload the MUFU; blocks with masked keys use the MUFU only, so a
+            // masked key's weight is exactly 0.
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 uint32_t pk[32];
 #pragma unroll
-                for (int cc = 0; cc < 64; cc += 2) {
-                    const float p0 = ex2_approx(fmaf(s[hh * 64 + cc], sl, -mb));
-                    const float p1 = ex2_approx(fmaf(s[hh * 64 + cc + 1], sl, -mb));
-                    r8[(cc >> 1) & 7] += p0 + p1;
-                    pk[cc >> 1] = pack_bf16x2(p0, p1);
+                for (int pp = 0; pp < 32; ++pp) {
+                    const int cc = hh * 64 + 2 * pp;
+                    const float2 xv = ffma2(make_float2(s[cc], s[cc + 1]), sl2, nmb);
+                    float2 pv;
+                    if (full && (pp & 3) == 3) {
+                        pv = exp2_poly2(xv);
+                    } else {
+                        pv.x = ex2_approx(xv.x);
+                        pv.y = ex2_approx(xv.y);
+                    }
+                    r4[pp & 3] = fadd2(r4[pp & 3], pv);
+                    pk[pp] = pack_bf16x2(pv.x, pv.y);
                 }
                 // P over the S columns this half has already consumed.
                 tmem_st32(tS + hh * 32, pk);
             }
+            const float2 rs2 = fadd2(fadd2(r4[0], r4[1]), fadd2(r4[2], r4[3]));
+            const float rs = rs2.x + rs2.y;
             tmem_st_wait();
-            l = l * alpha + (((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7])));
+            l = l * alpha + rs;
             tc_fence_before();
             mbar_arrive(&bar[BAR_P_FULL + x]);
         }
