@@ -416,10 +416,9 @@ __device__ bool softmax_role(const PfParams& p, uint8_t* smem, uint64_t* bar, vo
             float2 r4[4];
 #pragma unroll
             for (int t = 0; t < 4; ++t) r4[t] = make_float2(0.f, 0.f);
-            // p = 2^(s * scale * log2 e - m).  In blocks with every key visible
-            // one pair in four is evaluated on the FMA pipe (exp2_poly2) to
-            // offload the MUFU; blocks with masked keys use the MUFU only, so a
-            // masked key's weight is exactly 0.
+            // p = 2^(s * scale * log2 e - m) on the MUFU (a masked key's
+            // weight is exactly 0); scale-and-subtract and the row sums use
+            // packed fp32 pairs.
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 uint32_t pk[32];
@@ -428,12 +427,8 @@ __device__ bool softmax_role(const PfParams& p, uint8_t* smem, uint64_t* bar, vo
                     const int cc = hh * 64 + 2 * pp;
                     const float2 xv = ffma2(make_float2(s[cc], s[cc + 1]), sl2, nmb);
                     float2 pv;
-                    if (full && (pp & 3) == 3) {
-                        pv = exp2_poly2(xv);
-                    } else {
-                        pv.x = ex2_approx(xv.x);
-                        pv.y = ex2_approx(xv.y);
-                    }
+                    pv.x = ex2_approx(xv.x);
+                    pv.y = ex2_approx(xv.y);
                     r4[pp & 3] = fadd2(r4[pp & 3], pv);
                     pk[pp] = pack_bf16x2(pv.x, pv.y);
                 }

@@ -320,30 +320,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return d;
 }
 
-// 2^x for a pair, on the FMA pipe instead of the MUFU.  Range reduction
-// x = j + f with j = round-to-nearest(x) (adding 1.5 * 2^23 leaves j in the
-// low mantissa bits), f in [-1/2, 1/2]; 2^f by the degree-3 polynomial that
-// minimises the maximum relative error on [-1/2, 1/2] (Remez exchange;
-// relative error 7.5e-5 in fp32); 2^j enters through the exponent field.
-// Valid for x in [-125, 127]; x is clamped below at -125 (2^-125 ~ 2e-38).
-constexpr float kExp2C0 = 0.9999280571937561f;
-constexpr float kExp2C1 = 0.6932609677314758f;
-constexpr float kExp2C2 = 0.2426111251115799f;
-constexpr float kExp2C3 = 0.0551716685295105f;
-__device__ __forceinline__ float2 exp2_poly2(float2 x) {
-    constexpr float kShift = 12582912.0f;   // 1.5 * 2^23
-    x.x = fmaxf(x.x, -125.0f);
-    x.y = fmaxf(x.y, -125.0f);
-    const float2 t = fadd2(x, make_float2(kShift, kShift));
-    const float2 r = fadd2(t, make_float2(-kShift, -kShift));
-    const float2 f = ffma2(r, make_float2(-1.0f, -1.0f), x);
-    float2 q = ffma2(make_float2(kExp2C3, kExp2C3), f, make_float2(kExp2C2, kExp2C2));
-    q = ffma2(q, f, make_float2(kExp2C1, kExp2C1));
-    q = ffma2(q, f, make_float2(kExp2C0, kExp2C0));
-    // j occupies the low bits of t's pattern; (t_bits << 23) is j << 23 mod 2^32.
-    return make_float2(__int_as_float(__float_as_int(q.x) + (__float_as_int(t.x) << 23)),
-                       __int_as_float(__float_as_int(q.y) + (__float_as_int(t.y) << 23)));
-}
 
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t saddr) {
     uint4 v;
