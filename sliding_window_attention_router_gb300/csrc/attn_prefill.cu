@@ -322,8 +322,7 @@ __device__ bool mma_issuer(const PfParams& p, uint8_t* smem, uint64_t* bar, vola
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           unsigned int* err) {
-    const bool ok = mbar_wait(bar, parity, abort_flag, err);
-    return __all_sync(0xffffffffu, ok);
+    return mbar_wait_w(bar, parity, abort_flag, err);
 }
 
 __device__ bool softmax_role(const PfParams& p, uint8_t* smem, uint64_t* bar, volatile int* sched,

@@ -275,9 +275,18 @@ __device__ __forceinline__ void tma_load_4d_w(void* smem_dst, const CUtensorMap*
         : "memory");
 }
 
-// Warp-wide bounded wait: passes only when it passed for every lane.
+// Warp-wide bounded wait: passes only when it passed for every lane.  The
+// common case (phase already complete) is one try_wait and one warp vote.
 __device__ __forceinline__ bool mbar_wait_w(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                             unsigned int* err) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "vote.sync.all.pred q, p, 0xffffffff;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (done) return true;
     const bool ok = mbar_wait(bar, parity, abort_flag, err);
     return __all_sync(0xffffffffu, ok);
 }
