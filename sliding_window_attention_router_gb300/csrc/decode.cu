@@ -172,22 +172,53 @@ __global__ void decode_split_kernel(const T* __restrict__ q, const T* __restrict
     }
 }
 
+// Log-sum-exp merge of the chunk partials of one (sequence, query head):
+// block (hq, b), D threads, thread c owns output column c.  The maximum over
+// chunks is a block reduction; the weighted sums run 8 chunks per iteration
+// so their loads are in flight together.
 template <typename T, int D>
-__global__ void decode_combine_kernel(const float* __restrict__ part,
-                                      const int32_t* __restrict__ seq_lens,
-                                      const uint8_t* __restrict__ gate, T* __restrict__ o,
-                                      float* __restrict__ lse, int Hq, int W, int max_chunks) {
+__global__ void __launch_bounds__(D) decode_combine_kernel(const float* __restrict__ part,
+                                                           const int32_t* __restrict__ seq_lens,
+                                                           const uint8_t* __restrict__ gate,
+                                                           T* __restrict__ o, float* __restrict__ lse,
+                                                           int Hq, int W, int max_chunks) {
+    __shared__ float red[D / 32];
     const int hq = blockIdx.x, b = blockIdx.y, cidx = threadIdx.x;
+    const int lane = cidx & 31, wid = cidx >> 5;
     int lo, n;
     visited(seq_lens, gate, b, W, lo, n);
     const int nc = (n + kChunk - 1) / kChunk;
     const float* base = part + ((size_t)b * max_chunks * Hq + hq) * (D + 2);
     const size_t cstride = (size_t)Hq * (D + 2);
     float M = -INFINITY;
-    for (int c = 0; c < nc; ++c) M = fmaxf(M, base[c * cstride + D]);
+    for (int c = cidx; c < nc; c += D) M = fmaxf(M, base[c * cstride + D]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    if (lane == 0) red[wid] = M;
+    __syncthreads();
+    M = red[0];
+#pragma unroll
+    for (int w = 1; w < D / 32; ++w) M = fmaxf(M, red[w]);
     float L = 0.f, acc = 0.f;
-    for (int c = 0; c < nc; ++c) {
-        const float* pc = base + c * cstride;
+    int c = 0;
+    for (; c + 8 <= nc; c += 8) {
+        float mv[8], lv[8], ov[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const float* pc = base + (size_t)(c + u) * cstride;
+            mv[u] = pc[D];
+            lv[u] = pc[D + 1];
+            ov[u] = pc[cidx];
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const float w = ex2f(mv[u] - M);
+            L = fmaf(lv[u], w, L);
+            acc = fmaf(ov[u], w, acc);
+        }
+    }
+    for (; c < nc; ++c) {
+        const float* pc = base + (size_t)c * cstride;
         const float w = ex2f(pc[D] - M);
         L = fmaf(pc[D + 1], w, L);
         acc = fmaf(pc[cidx], w, acc);
