@@ -38,16 +38,30 @@ METRIC = "prefill useful TFLOP/s at N=32K (% of bf16 peak); decode KV-read GB/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
 
-# DRAM traffic per launch of the dominant kernels, from ncu captures
-# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the SHA-256 of the
-# kernel source it was taken on; a changed kernel reports null.
-MEASURED_TRAFFIC = {}
+# DRAM traffic per launch of the dominant kernels (dram__bytes_read.sum +
+# dram__bytes_write.sum from ncu on the default workloads), keyed by the
+# SHA-256 of the kernel's source files at capture time; a kernel whose source
+# has changed since reports null.
+MEASURED_TRAFFIC = {
+    # prefill_kernel, long-context prefill N=32768 f=0.13: 1 082 483 456 read + 132 495 104 written
+    ("prefill", "2376c004e3f9ab56"): 1082483456 + 132495104,
+    # decode_split_kernel, 16 x 32768 decode: 654 404 608 read + 4 849 664 written
+    ("decode", "9af2601a1a731ff1"): 654404608 + 4849664,
+}
+KERNEL_SOURCES = {"prefill": ("attn_prefill.cu", "ptx.cuh"), "decode": ("decode.cu",)}
 
 
-def kernel_source_hash(name: str) -> str:
-    path = os.path.join(ROOT, "sliding_window_attention_router_gb300", "csrc", name)
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def kernel_source_hash(kernel: str) -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        path = os.path.join(ROOT, "sliding_window_attention_router_gb300", "csrc", name)
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel: str):
+    return MEASURED_TRAFFIC.get((kernel, kernel_source_hash(kernel)))
 
 
 def load_peaks():
@@ -395,8 +409,7 @@ def run_ours(args, dist: Dist):
     kern_s = statistics.mean(main["kern_ms"]) / 1e3
     achieved = main["flops"] / kern_s / 1e12
     peak = float(peaks["bf16_tflops"])
-    src_hash = kernel_source_hash("attn_tc.cu")
-    traffic = MEASURED_TRAFFIC.get(("attn_tc.cu", src_hash, "prefill32k_f0.13"))
+    traffic = measured_traffic("prefill") if args.n == 32768 else None
 
     extra = {}
     if not args.headline_only:
@@ -416,6 +429,7 @@ def run_ours(args, dist: Dist):
             "bytes_per_step": dec["bytes"],
             "roofline": {"bound": "hbm", "achieved": dec["bytes"] / dk / 1e9, "peak": hbm,
                          "unit": "GB/s", "frac": dec["bytes"] / dk / 1e9 / hbm,
+                         "traffic": measured_traffic("decode"),
                          "kernel": "decode_split_kernel"},
             "workload": "decode bf16: 16 sequences x 32768 cached tokens, H=16, d=128, W=1024, "
                         "gate Bernoulli(0.13)"}
@@ -454,7 +468,7 @@ def run_ours(args, dist: Dist):
                        "parallelism": f"replicas x{dist.world}, one sequence per GPU"},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak,
-                         "traffic": traffic, "kernel": "tc_attention_kernel",
+                         "traffic": traffic, "kernel": "prefill_kernel",
                          "peak_source": f"{peaks_src} bf16 dense (burst)"},
             "cpu_baseline": cpu,
             "e2e": e2e,
