@@ -354,7 +354,7 @@ def run_reference(args, dist: Dist):
     flops = []
     cores = oracle.num_threads()
     for s in range(args.warmup + args.steps):
-        r = oracle_sample(d, budget_s=3.0, seed=s)
+        r = oracle_sample(d, budget_s=args.ref_step_budget, seed=s)
         if s >= args.warmup:
             per_step.append(r["seconds"])
             flops.append(r["flops_per_s"] * r["seconds"])
@@ -368,7 +368,7 @@ def run_reference(args, dist: Dist):
                                "gate runs at routed fraction 0.13", "routed_fraction": 0.13},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": "each step: random (row, head) outputs of the workload, "
-                                   "about 3 s of fp64 oracle work"},
+                                   f"about {args.ref_step_budget:g} s of fp64 oracle work"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -492,6 +492,8 @@ def main():
     ap.add_argument("--n", type=int, default=32768,
                     help="sequence length of the headline workload (profiling runs only)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ref-step-budget", type=float, default=3.0,
+                    help="seconds of oracle work per step of the reference arm")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -1,6 +1,7 @@
-// Routed causal attention on the 5th-generation tensor cores (sm_103a).
+// Dual-branch training forward on the 5th-generation tensor cores (sm_103a).
 //
-// One persistent CTA per SM walks a list of 128-row query tiles.  Per tile it
+// One persistent CTA per SM walks the 128-row query tiles of every
+// (batch, head), latest (longest) tiles first.  Per tile it
 // streams 128-key K/V blocks with TMA into 128-byte-swizzled shared memory,
 // computes S = Q K^T with tcgen05.mma into TMEM, runs an fp32 online softmax
 // (one thread per query row, exp2 on the MUFU), writes P as bf16 back to
@@ -11,12 +12,12 @@
 //   warp 6     TMA producer for V
 // All hand-offs are shared-memory mbarriers with bounded waits.
 //
-// Visited keys per row follow the SwiAttn report (section 2, dual-branch
-// computation) with the window of the weimeta.cn SWA glossary ("详细解释"):
-//   band tile  (window rows):  [max(0, i-W+1), i]
-//   far tile   (routed rows):  [0, i]
-//   dual tile: band keys first (snapshot -> O_SWA), then [0, i-W] (-> O_FULL)
-// Key blocks outside a tile's union of row ranges are never loaded.
+// Per tile (SwiAttn report, section 2, dual-branch computation; window per the
+// weimeta.cn SWA glossary, "详细解释"): the window keys [max(0, i-W+1), i]
+// first, then O/l is snapshotted as O_SWA (kept in TMEM, written as bf16),
+// then the remaining keys [0, i-W] complete O_FULL.  The epilogue writes
+// O_FULL, the gated output and each row's squared distance ||o_FULL - o_SWA||^2
+// for its head, from the fp32 values.
 
 #include "ptx.cuh"
 #include "swiattn_internal.h"
@@ -64,87 +65,53 @@ constexpr uint32_t kIdescO = idesc_bf16_f32(kBM, kHD, false, true);    // P: K-m
 
 struct TcParams {
     CUtensorMap tm_q;    // Q  [B,N,Hq,128], box 64 x 1 x 128 x 1
-    CUtensorMap tm_qc;   // compacted far queries, same shape as Q
     CUtensorMap tm_k;    // K  [B,N,Hkv,128]
     CUtensorMap tm_v;    // V
-    const int* routed_list;
-    const int* routed_count;
-    const int* n_items;
-    const WorkItem* items;
-    const uint8_t* gate;
     const float* logits;
-    __nv_bfloat16* o;
+    __nv_bfloat16* o;        // O_FULL
     __nv_bfloat16* o_swa;
-    __nv_bfloat16* o_gated;
-    float* lse;
-    float* mse_part;
+    __nv_bfloat16* o_gated;  // nullable
+    float* mse_part;         // [B,N,Hq] squared distance per (token, head)
     unsigned int* err;
-    int mode, B, N, Hq, Hkv, W;
+    int B, N, Hq, Hkv, W;
     float scale_log2;
 };
 
 // What one work item asks for.
 struct Plan {
-    int b, h, kvh, kind;   // kind: kItemBand, kItemFar or 2 (dual)
-    int row0, nrows;       // band/dual: first query row; far: first index into the routed list
-    int kv1, nblk1;        // first key and block count of segment 1
-    int kv2, nblk2;        // segment 2 (dual: keys [0, i-W])
+    int b, h, kvh;
+    int row0, nrows;   // first query row, valid rows
+    int kv1, nblk1;    // window keys: first key and block count
+    int kv2, nblk2;    // remaining keys [0, i-W]
 };
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 
-__device__ __forceinline__ int item_count(const TcParams& p) {
-    if (p.mode == 1) return p.B * p.Hq * cdiv(p.N, kBM);
-    return *p.n_items;
-}
+__device__ __forceinline__ int item_count(const TcParams& p) { return p.B * p.Hq * cdiv(p.N, kBM); }
 
-// Snake order over the (cost-sorted) item list: CTA c takes items
-// c, 2G-1-c, 2G+c, 4G-1-c, ... so every CTA gets one item of every rank band.
+// Snake order over the cost-ordered items: CTA c takes items c, 2G-1-c,
+// 2G+c, 4G-1-c, ... so every CTA gets one item of every rank band.
 __device__ __forceinline__ int snake_index(int k, int c, int G) {
     return k * G + ((k & 1) ? (G - 1 - c) : c);
 }
 
 __device__ __forceinline__ Plan make_plan(const TcParams& p, int idx) {
     Plan pl;
-    int kind, b, h, tile;
-    if (p.mode == 1) {
-        const int nqt = cdiv(p.N, kBM);
-        const int per = p.B * p.Hq;
-        tile = nqt - 1 - idx / per;   // longest (latest) tiles first
-        const int rem = idx % per;
-        b = rem / p.Hq;
-        h = rem % p.Hq;
-        kind = 2;
-    } else {
-        const WorkItem it = p.items[idx];
-        kind = it.kind;
-        b = it.b;
-        h = it.h;
-        tile = it.tile;
-    }
-    pl.b = b;
-    pl.h = h;
-    pl.kvh = h / (p.Hq / p.Hkv);
-    pl.kind = kind;
+    const int nqt = cdiv(p.N, kBM);
+    const int per = p.B * p.Hq;
+    const int tile = nqt - 1 - idx / per;   // longest (latest) tiles first
+    const int rem = idx % per;
+    pl.b = rem / p.Hq;
+    pl.h = rem % p.Hq;
+    pl.kvh = pl.h / (p.Hq / p.Hkv);
     pl.row0 = tile * kBM;
+    pl.nrows = min(kBM, p.N - pl.row0);
+    const int hi_row = pl.row0 + pl.nrows - 1;
+    pl.kv1 = max(0, pl.row0 - p.W + 1);
+    pl.nblk1 = cdiv(hi_row - pl.kv1 + 1, kBN);
     pl.kv2 = 0;
-    pl.nblk2 = 0;
-    if (kind == kItemFar) {
-        const int cnt = p.routed_count[b];
-        pl.nrows = min(kBM, cnt - pl.row0);
-        const int max_i = p.routed_list[(size_t)b * p.N + pl.row0 + pl.nrows - 1];
-        pl.kv1 = 0;
-        pl.nblk1 = cdiv(max_i + 1, kBN);
-    } else {
-        pl.nrows = min(kBM, p.N - pl.row0);
-        const int hi_row = pl.row0 + pl.nrows - 1;
-        pl.kv1 = max(0, pl.row0 - p.W + 1);
-        pl.nblk1 = cdiv(hi_row - pl.kv1 + 1, kBN);
-        if (kind == 2) {
-            const int far_hi = hi_row - p.W;
-            if (far_hi >= 0) pl.nblk2 = cdiv(far_hi + 1, kBN);
-        }
-    }
+    const int far_hi = hi_row - p.W;
+    pl.nblk2 = far_hi >= 0 ? cdiv(far_hi + 1, kBN) : 0;
     return pl;
 }
 
@@ -164,9 +131,8 @@ __device__ bool producer_qk(const TcParams& p, uint8_t* smem, uint64_t* bar, vol
         const Plan pl = make_plan(p, idx);
         if (!mbar_wait(&bar[BAR_Q_EMPTY], (q_issued & 1u) ^ 1u, abort_flag, p.err)) return false;
         mbar_arrive_expect_tx(&bar[BAR_Q_FULL], kTileBytes);
-        const CUtensorMap* qm = (pl.kind == kItemFar) ? &p.tm_qc : &p.tm_q;
-        tma_load_4d(smem + kOffQ, qm, &bar[BAR_Q_FULL], 0, pl.h, pl.row0, pl.b);
-        tma_load_4d(smem + kOffQ + kHalfBytes, qm, &bar[BAR_Q_FULL], 64, pl.h, pl.row0, pl.b);
+        tma_load_4d(smem + kOffQ, &p.tm_q, &bar[BAR_Q_FULL], 0, pl.h, pl.row0, pl.b);
+        tma_load_4d(smem + kOffQ + kHalfBytes, &p.tm_q, &bar[BAR_Q_FULL], 64, pl.h, pl.row0, pl.b);
         ++q_issued;
         const int nblk = pl.nblk1 + pl.nblk2;
         for (int j = 0; j < nblk; ++j) {
@@ -286,12 +252,9 @@ __device__ __forceinline__ void row_range(const Plan& pl, int j, int i, int W, i
     if (i < 0) {
         lo = 1;
         hi = 0;
-    } else if (j >= pl.nblk1) {   // dual, far part
+    } else if (j >= pl.nblk1) {   // keys beyond the window
         lo = 0;
         hi = i - W;
-    } else if (pl.kind == kItemFar) {
-        lo = 0;
-        hi = i;
     } else {
         lo = max(0, i - W + 1);
         hi = i;
@@ -334,12 +297,7 @@ __device__ bool softmax_role(const TcParams& p, uint8_t* smem, uint64_t* bar, ui
         const int idx = snake_index(k, c, G);
         if (idx >= n) break;
         const Plan pl = make_plan(p, idx);
-        int i = -1;
-        if (r < pl.nrows)
-            i = (pl.kind == kItemFar) ? p.routed_list[(size_t)pl.b * p.N + pl.row0 + r] : pl.row0 + r;
-        bool write_row = i >= 0;
-        if (pl.kind == kItemBand && i >= 0)   // far rows are written by their far tile
-            write_row = !(p.gate[(size_t)pl.b * p.N + i] != 0 && i >= p.W);
+        const int i = (r < pl.nrows) ? pl.row0 + r : -1;
         const size_t out_row = (i >= 0) ? (((size_t)pl.b * p.N + i) * p.Hq + pl.h) : 0;
 
         float m2 = -INFINITY, l = 0.f;
@@ -409,7 +367,7 @@ __device__ bool softmax_role(const TcParams& p, uint8_t* smem, uint64_t* bar, ui
                 if (!warp_wait(&bar[BAR_PV_DONE], pv_iter & 1u, abort_flag, p.err)) return false;
                 ++pv_iter;
                 tc_fence_after();
-                if (p.mode == 1 && j == pl.nblk1) {
+                if (j == pl.nblk1) {
                     // End of the window keys: O/l is this row's O_SWA.
                     const float inv = (l > 0.f) ? 1.f / l : 0.f;
 #pragma unroll
@@ -462,8 +420,7 @@ __device__ bool softmax_role(const TcParams& p, uint8_t* smem, uint64_t* bar, ui
         tc_fence_after();
         const float inv = (l > 0.f) ? 1.f / l : 0.f;
         float mse = 0.f;
-        const bool gated_full = (p.mode == 1 && i >= 0 && p.logits) ?
-                                    (p.logits[(size_t)pl.b * p.N + i] > 0.f) : false;
+        const bool gated_full = (i >= 0) ? (p.logits[(size_t)pl.b * p.N + i] > 0.f) : false;
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
             uint32_t orr[32];
@@ -472,7 +429,7 @@ __device__ bool softmax_role(const TcParams& p, uint8_t* smem, uint64_t* bar, ui
             float* ov = reinterpret_cast<float*>(orr);
 #pragma unroll
             for (int t = 0; t < 32; ++t) ov[t] *= inv;
-            if (p.mode == 1) {
+            {
                 uint32_t srr[32];
                 float* sv = reinterpret_cast<float*>(srr);
                 if (snapped) {
@@ -497,17 +454,9 @@ __device__ bool softmax_role(const TcParams& p, uint8_t* smem, uint64_t* bar, ui
                         store_row_bf16(p.o_gated + out_row * kHD + q4 * 32, gv, 4);
                     }
                 }
-            } else if (write_row) {
-                store_row_bf16(p.o + out_row * kHD + q4 * 32, ov, 4);
             }
         }
-        if (i >= 0) {
-            if (p.mode == 1) {
-                p.mse_part[out_row] = mse;
-            } else if (write_row && p.lse) {
-                p.lse[out_row] = (m2 + __log2f(l)) * 0.69314718055994531f;
-            }
-        }
+        if (i >= 0) p.mse_part[out_row] = mse;
         tc_fence_before();
         mbar_arrive(&bar[BAR_O_FREE]);
     }
@@ -557,7 +506,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_attention_kernel(const __grid_
     } else if (warp == 4) {
         if (lane == 0) {
             prefetch_tensormap(&p.tm_q);
-            prefetch_tensormap(&p.tm_qc);
             prefetch_tensormap(&p.tm_k);
             uint32_t kv_issued = 0, q_issued = 0;
             if (!producer_qk(p, smem, bar, abort_flag, kv_issued, q_issued)) {
@@ -599,23 +547,15 @@ cudaError_t launch_tc_attention(const TcAttnArgs& a, unsigned int* err, int num_
     memset(&p, 0, sizeof(p));
     const uint64_t N = a.N, B = a.B;
     bool ok = make_tmap_4d_bf16(&p.tm_q, a.q, kHD, a.Hq, N, B, 64, kBM) &&
-              make_tmap_4d_bf16(&p.tm_qc, a.qc ? a.qc : a.q, kHD, a.Hq, N, B, 64, kBM) &&
               make_tmap_4d_bf16(&p.tm_k, a.k, kHD, a.Hkv, N, B, 64, kBN) &&
               make_tmap_4d_bf16(&p.tm_v, a.v, kHD, a.Hkv, N, B, 64, kBN);
     if (!ok) return cudaErrorInvalidValue;
-    p.routed_list = a.routed_list;
-    p.routed_count = a.routed_count;
-    p.n_items = a.n_items;
-    p.items = a.items;
-    p.gate = a.gate;
     p.logits = a.logits;
     p.o = static_cast<__nv_bfloat16*>(a.o);
     p.o_swa = static_cast<__nv_bfloat16*>(a.o_swa);
     p.o_gated = static_cast<__nv_bfloat16*>(a.o_gated);
-    p.lse = a.lse;
     p.mse_part = a.mse_part;
     p.err = err;
-    p.mode = a.mode;
     p.B = a.B;
     p.N = a.N;
     p.Hq = a.Hq;

@@ -190,7 +190,6 @@ int swiattn_prefill(const void* q, const void* k, const void* v, const uint8_t* 
     if (e != cudaSuccess) return SWIATTN_ECUDA;
     TcAttnArgs a;
     std::memset(&a, 0, sizeof(a));
-    a.mode = 0;
     a.q = q;
     a.k = k;
     a.v = v;
@@ -280,7 +279,6 @@ int swiattn_dual_branch(const void* q, const void* k, const void* v, const float
     float* part = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.mse_part);
     TcAttnArgs a;
     std::memset(&a, 0, sizeof(a));
-    a.mode = 1;
     a.q = q;
     a.k = k;
     a.v = v;

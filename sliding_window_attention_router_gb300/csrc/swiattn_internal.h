@@ -65,7 +65,6 @@ cudaError_t launch_schedule(const uint8_t* gate, const void* q, int B, int N, in
                             const PrefillWs& L, char* ws, int num_sms, cudaStream_t s);
 
 struct TcAttnArgs {
-    int mode;          // 0 routed prefill, 1 dual branch
     const void* q;     // [B,N,Hq,128] bf16
     const void* k;     // [B,N,Hkv,128]
     const void* v;
@@ -84,6 +83,7 @@ struct TcAttnArgs {
     int B, N, Hq, Hkv, W;
     float scale;
 };
+// Dual-branch forward (q, k, v, logits, o = O_FULL, o_swa, o_gated, mse_part).
 cudaError_t launch_tc_attention(const TcAttnArgs& a, unsigned int* err, int num_sms,
                                 cudaStream_t s);
 
