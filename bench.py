@@ -25,6 +25,7 @@ import subprocess
 import sys
 import tempfile
 import time
+import datetime
 
 import numpy as np
 import torch
@@ -146,7 +147,9 @@ class ClockSampler:
         except (OSError, FileNotFoundError):
             self.proc = None
 
-    def stop(self):
+    def stop(self, t_from=None, t_to=None):
+        """Stop sampling; summarise the samples taken between the host times
+        t_from and t_to (datetime, local clock) when given."""
         if not self.proc:
             return None
         self.proc.terminate()
@@ -159,8 +162,16 @@ class ClockSampler:
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) == 8:
-                    rows.append(parts)
+                if len(parts) != 8:
+                    continue
+                if t_from is not None:
+                    try:
+                        ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+                    except ValueError:
+                        continue
+                    if ts < t_from or ts > t_to:
+                        continue
+                rows.append(parts)
         os.unlink(self.path)
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
@@ -186,6 +197,15 @@ class Timer:
 
     def __init__(self, device):
         self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    def hold(self, fn, seconds: float):
+        """Keep running fn (untimed) for about `seconds`, so clock sampling sees
+        the kernel under sustained load."""
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < seconds:
+            for _ in range(8):
+                fn()
+            torch.cuda.synchronize()
 
     def run(self, fn, steps: int, warmup: int, kernel_events: bool = False):
         import sliding_window_attention_router_gb300 as swa
@@ -219,7 +239,7 @@ class Timer:
 
 
 # ------------------------------------------------------------ workloads --
-def prefill_section(swa, timer, dev, frac, steps, warmup, seed, with_e2e, N=32768):
+def prefill_section(swa, timer, dev, frac, steps, warmup, seed, with_e2e, N=32768, hold_s=0.0):
     d = inp.prefill_32k(frac=frac, seed=seed, N=N)
     B, N, H, D, W = d["B"], d["N"], d["Hq"], d["d"], d["W"]
     pairs = useful_pairs(d["gate"].numpy(), W)
@@ -234,10 +254,14 @@ def prefill_section(swa, timer, dev, frac, steps, warmup, seed, with_e2e, N=3276
     def step():
         swa.prefill(q, k, v, gate, W, scale, out=o, workspace=ws)
 
+    t_from = datetime.datetime.now()
     step_ms, kern_ms = timer.run(step, steps, warmup, kernel_events=True)
+    if hold_s > 0:
+        timer.hold(step, hold_s)
+    t_to = datetime.datetime.now()
     assert swa.get_device_error() == 0, "device-side wait timed out"
     res = dict(d=d, flops=flops, pairs=pairs, step_ms=step_ms, kern_ms=kern_ms,
-               realised_frac=float(d["gate"].float().mean()))
+               realised_frac=float(d["gate"].float().mean()), t_from=t_from, t_to=t_to)
     if with_e2e:
         o_host = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
 
@@ -294,6 +318,29 @@ def route_section(swa, timer, dev, steps, warmup, seed):
     step_ms, _ = timer.run(step, steps, warmup)
     nbytes = T * Dm * 2 + Dm * 2 + T * 5
     return dict(step_ms=step_ms, bytes=nbytes)
+
+
+def layer_4k_section(swa, timer, dev, steps, warmup, seed):
+    """Single-layer prefill: router GEMV + gate, then routed prefill on its gates."""
+    d = inp.prefill_4k(seed=seed)
+    B, N, H, D, W = d["B"], d["N"], d["Hq"], d["d"], d["W"]
+    h, w = d["h"].to(dev), d["w"].to(dev)
+    q, k, v = (d[n].to(dev) for n in ("q", "k", "v"))
+    logits = torch.empty(B * N, dtype=torch.float32, device=dev)
+    gate = torch.empty(B * N, dtype=torch.uint8, device=dev)
+    o = torch.empty_like(q)
+    ws = torch.empty(swa.prefill_workspace(B, N, H, H, D, W, torch.bfloat16), dtype=torch.uint8,
+                     device=dev)
+
+    def step():
+        swa.route(h, w, d["bias"], logits=logits, gate=gate)
+        swa.prefill(q, k, v, gate.view(B, N), W, out=o, workspace=ws)
+
+    step_ms, _ = timer.run(step, steps, warmup)
+    assert swa.get_device_error() == 0
+    pairs = useful_pairs(gate.view(B, N).cpu().numpy(), W)
+    return dict(step_ms=step_ms, flops=4.0 * D * H * pairs,
+                routed_frac=float(gate.float().mean()))
 
 
 def dual_section(swa, timer, dev, steps, warmup, seed):
@@ -392,11 +439,13 @@ def run_ours(args, dist: Dist):
     torch.cuda.synchronize()
     t_wall0 = time.perf_counter()
     main = prefill_section(swa, timer, dev, 0.13, args.steps, args.warmup, seed=dist.rank,
-                           with_e2e=not args.no_e2e, N=args.n)
+                           with_e2e=not args.no_e2e, N=args.n, hold_s=0.6)
     torch.cuda.synchronize()
     dist.barrier()
     wall = time.perf_counter() - t_wall0
-    clk = clocks.stop()
+    clk = clocks.stop(main["t_from"], main["t_to"])
+    if clk is not None:
+        clk["window"] = "timed headline steps plus 0.6 s of the same step under load"
 
     step_s = sum(main["step_ms"]) / 1e3
     value, slowest = aggregate(main["flops"] * args.steps, step_s, dist)
@@ -437,6 +486,12 @@ def run_ours(args, dist: Dist):
         rs = statistics.mean(rt["step_ms"]) / 1e3
         extra["route"] = {"gbs": rt["bytes"] / rs / 1e9, "ms_per_step": rs * 1e3,
                           "workload": "router GEMV, 32768 tokens x d_model 2048, bf16"}
+        l4 = layer_4k_section(swa, timer, dev, ks, kw, seed=dist.rank)
+        l4s = statistics.mean(l4["step_ms"]) / 1e3
+        extra["layer_4k"] = {"tflops": l4["flops"] / l4s / 1e12, "ms_per_step": l4s * 1e3,
+                             "routed_frac": l4["routed_frac"],
+                             "workload": "single-layer prefill bf16: router GEMV over h [4096, 2048] "
+                                         "then routed prefill B=1 H=16 d=128 N=4096 W=1024 on its gates"}
         du = dual_section(swa, timer, dev, ks, kw, seed=dist.rank)
         dm = statistics.mean(du["step_ms"]) / 1e3
         extra["dual"] = {"tflops": du["flops"] / dm / 1e12, "ms_per_step": dm * 1e3,
