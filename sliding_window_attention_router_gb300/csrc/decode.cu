@@ -21,7 +21,7 @@
 namespace swi {
 namespace {
 
-constexpr int kChunk = 128;   // tokens per split
+constexpr int kChunk = 256;   // tokens per split
 constexpr int kUnroll = 8;    // tokens in flight per thread
 
 template <typename T>

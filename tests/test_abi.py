@@ -57,7 +57,7 @@ def test_workspace_sizes(lib):
     assert swa.prefill_workspace(1, 0, 16, 16, 128, 1024, bf16) == 0
     assert swa.prefill_workspace(1, 64, 6, 4, 128, 8, bf16) == 0   # Hq % Hkv != 0
     dw = swa.decode_workspace(16, 32768, 16, 16, 128, 1024, bf16)
-    assert dw >= 16 * (32768 // 128) * 16 * 130 * 4
+    assert dw >= 16 * (32768 // 256) * 16 * 130 * 4
     assert swa.dual_branch_workspace(2, 8192, 16, 4, 128, 1024, bf16) >= 2 * 8192 * 16 * 4
     assert swa.dual_branch_workspace(1, 256, 2, 2, 64, 32, f32) == 0
 

@@ -69,14 +69,14 @@ def test_noalloc_decode_rejects_partials_beyond_scratch(swa):
     sl = torch.full((B,), 8, dtype=torch.int32, device="cuda")
     gate = torch.zeros(B, dtype=torch.uint8, device="cuda")
     small = torch.zeros(B, 8, Hkv, d, dtype=torch.bfloat16, device="cuda")
-    # Lmax = 16 256 needs 127 chunks of partials: 16.9 MB > 16 MiB.  The caches
+    # Lmax = 32 512 needs 127 chunks of partials: 16.9 MB > 16 MiB.  The caches
     # are never read because validation rejects the call first.
     rc = _call_noalloc(lib, q, small, small, sl, gate, o, lse, W, 0.1, swa.BF16)
     assert rc == 0
     vp = ctypes.c_void_p
     rc = lib.swiattn_decode_noalloc(vp(q.data_ptr()), vp(small.data_ptr()), vp(small.data_ptr()),
                                     vp(sl.data_ptr()), vp(gate.data_ptr()), vp(o.data_ptr()),
-                                    vp(lse.data_ptr()), B, 16256, Hq, Hkv, d, W, 0.1, swa.BF16,
+                                    vp(lse.data_ptr()), B, 32512, Hq, Hkv, d, W, 0.1, swa.BF16,
                                     vp(torch.cuda.current_stream().cuda_stream))
     assert rc == 1   # SWIATTN_EINVAL, nothing launched
     torch.cuda.synchronize()
