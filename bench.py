@@ -46,8 +46,8 @@ L2_FLUSH_BYTES = 256 << 20
 MEASURED_TRAFFIC = {
     # prefill_kernel, long-context prefill N=32768 f=0.13: 1 082 483 456 read + 132 495 104 written
     ("prefill", "2376c004e3f9ab56"): 1082483456 + 132495104,
-    # decode_split_kernel, 16 x 32768 decode: 654 404 608 read + 4 849 664 written
-    ("decode", "9af2601a1a731ff1"): 654404608 + 4849664,
+    # decode_split_kernel, 16 x 32768 decode: 654 404 352 read + 2 732 800 written
+    ("decode", "ef5ddd11247ce63e"): 654404352 + 2732800,
 }
 KERNEL_SOURCES = {"prefill": ("attn_prefill.cu", "ptx.cuh"), "decode": ("decode.cu",)}
 
