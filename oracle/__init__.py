@@ -62,9 +62,18 @@ def _load():
                                         + [ctypes.c_double] * 4 + [dp] * 5)
             lib.oracle_dual_rows.argtypes = ([dp, dp, dp, dp, dp] + [i64] * 6
                                              + [ctypes.c_double] * 4 + [i64p, i64] + [dp] * 5)
+            lib.oracle_prefill_backward.argtypes = ([dp, dp, dp, u8p, dp] + [i64] * 6
+                                                    + [ctypes.c_double, dp, dp, dp])
+            lib.oracle_prefill_backward_rows.argtypes = ([dp, dp, dp, u8p, dp] + [i64] * 6
+                                                         + [ctypes.c_double, i64p, i64, dp])
+            lib.oracle_prefill_backward_keys.argtypes = ([dp, dp, dp, u8p, dp] + [i64] * 6
+                                                         + [ctypes.c_double, i64p, i64, dp, dp])
+            lib.oracle_route_backward.argtypes = [dp] * 8 + [i64] * 3 + [dp] * 4
             for name in ("oracle_row_ranges", "oracle_route", "oracle_prefill",
                          "oracle_prefill_rows", "oracle_decode", "oracle_regulariser",
-                         "oracle_dual", "oracle_dual_rows", "oracle_num_threads"):
+                         "oracle_dual", "oracle_dual_rows", "oracle_num_threads",
+                         "oracle_prefill_backward", "oracle_prefill_backward_rows",
+                         "oracle_prefill_backward_keys", "oracle_route_backward"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -203,3 +212,77 @@ def dual_rows(q, k, v, logits, nll, W: int, scale: float, sel, gamma_base=1e-3, 
                                     float(alpha), _ptr(sel), n, _ptr(of), _ptr(os_), _ptr(mse),
                                     _ptr(gamma), _ptr(reg)), "dual_rows")
     return dict(o_full=of, o_swa=os_, mse=mse, gamma=gamma, reg=reg)
+
+
+def prefill_backward(q, k, v, gate, d_o, W: int, scale: float):
+    """Gradient of the routed prefill for the output gradient d_o [B,N,Hq,d]:
+    returns dq [B,N,Hq,d], dk, dv [B,N,Hkv,d].  Each row's gradient flows
+    through the branch its (hard) gate selected."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(d_o)
+    g = np.ascontiguousarray(np.asarray(gate, dtype=np.uint8))
+    B, N, Hq, d = q.shape
+    Hkv = k.shape[2]
+    dq, dk, dv = np.empty_like(q), np.empty_like(k), np.empty_like(v)
+    _check(_load().oracle_prefill_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(do), B, N,
+                                           Hq, Hkv, d, W, float(scale), _ptr(dq), _ptr(dk),
+                                           _ptr(dv)), "prefill_backward")
+    return dq, dk, dv
+
+
+def prefill_backward_rows(q, k, v, gate, d_o, W: int, scale: float, sel):
+    """dq of selected (b, i, h) rows -> [nsel, d]."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(d_o)
+    g = np.ascontiguousarray(np.asarray(gate, dtype=np.uint8))
+    sel = np.ascontiguousarray(np.asarray(sel, dtype=np.int64).reshape(-1, 3))
+    B, N, Hq, d = q.shape
+    Hkv = k.shape[2]
+    dq = np.empty((sel.shape[0], d), np.float64)
+    _check(_load().oracle_prefill_backward_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(do), B,
+                                                N, Hq, Hkv, d, W, float(scale), _ptr(sel),
+                                                sel.shape[0], _ptr(dq)), "prefill_backward_rows")
+    return dq
+
+
+def prefill_backward_keys(q, k, v, gate, d_o, W: int, scale: float, sel):
+    """dk, dv of selected (b, j, kv head) keys -> two [nsel, d] arrays."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(d_o)
+    g = np.ascontiguousarray(np.asarray(gate, dtype=np.uint8))
+    sel = np.ascontiguousarray(np.asarray(sel, dtype=np.int64).reshape(-1, 3))
+    B, N, Hq, d = q.shape
+    Hkv = k.shape[2]
+    n = sel.shape[0]
+    dk, dv = np.empty((n, d), np.float64), np.empty((n, d), np.float64)
+    _check(_load().oracle_prefill_backward_keys(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(do), B,
+                                                N, Hq, Hkv, d, W, float(scale), _ptr(sel), n,
+                                                _ptr(dk), _ptr(dv)), "prefill_backward_keys")
+    return dk, dv
+
+
+def route_backward(logits, o_full, o_swa, d_o, gamma, d_reg=None, h=None, w=None):
+    """Router backward through the straight-through gate and the regulariser.
+    logits/gamma/d_reg [T]; o_full/o_swa/d_o [T, HD]; h [T, D], w [D] optional.
+    Returns dict d_logits [T] and, when h and w are given, dh [T, D], dw [D], db."""
+    lg, of, os_, do, gm = (_f64(x) for x in (logits, o_full, o_swa, d_o, gamma))
+    T = lg.size
+    of, os_, do = of.reshape(T, -1), os_.reshape(T, -1), do.reshape(T, -1)
+    HD = of.shape[1]
+    dr = None if d_reg is None else _f64(d_reg).ravel()
+    dl = np.empty(T, np.float64)
+    out = dict(d_logits=dl)
+    hh = ww = dh = dw = None
+    db = np.zeros(1, np.float64)
+    D = 0
+    if h is not None:
+        hh, ww = _f64(h).reshape(T, -1), _f64(w).ravel()
+        D = ww.size
+        dh, dw = np.empty((T, D), np.float64), np.empty(D, np.float64)
+    _check(_load().oracle_route_backward(_ptr(lg), _ptr(of), _ptr(os_), _ptr(do), _ptr(gm),
+                                         None if dr is None else _ptr(dr),
+                                         None if hh is None else _ptr(hh),
+                                         None if ww is None else _ptr(ww), T, HD, D, _ptr(dl),
+                                         None if dh is None else _ptr(dh),
+                                         None if dw is None else _ptr(dw),
+                                         _ptr(db) if h is not None else None), "route_backward")
+    if h is not None:
+        out.update(dh=dh, dw=dw, db=float(db[0]))
+    return out

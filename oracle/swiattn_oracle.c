@@ -30,7 +30,10 @@
  *  - the softmax scale is a parameter (callers pass 1/sqrt(d));
  *  - GQA: query head h reads KV head h / (Hq/Hkv) (contiguous groups);
  *  - ||o_FULL - o_SWA||^2 sums over all Hq*d output elements of the token;
- *  - decode: the cache already holds the new token, whose position is L-1.
+ *  - decode: the cache already holds the new token, whose position is L-1;
+ *  - training backward: the straight-through gate's forward value is the hard
+ *    0/1, so dO reaches the selected branch only; the adaptive weight gamma
+ *    is a coefficient of the regulariser and carries no gradient.
  *
  * Layouts (row-major, contiguous): q [B,N,Hq,d], k/v [B,N,Hkv,d],
  * decode caches [B,Lmax,Hkv,d], per-token arrays [B,N].
@@ -301,6 +304,222 @@ int oracle_dual_rows(const double *q, const double *k, const double *v, const do
                        scale, gamma_base, eps, alpha, s, of_sel + r * Hq * d,
                        os_sel + r * Hq * d, mse + r, gamma + r, reg + r);
         free(s);
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * Training backward.
+ *
+ * Report section 2 (router design): the hard gate is formed with the
+ * straight-through estimator, sigma = 1(sigmoid(R) > 0.5) + sigmoid(R)
+ * - sg(sigmoid(R)).  Its forward value is exactly 0 or 1, so in
+ * O = sigma*O_FULL + (1-sigma)*O_SWA the output gradient dO reaches only the
+ * branch the gate selected; the gate itself receives dO.(O_FULL - O_SWA)
+ * times the derivative of the soft sigmoid.  The adaptive weight gamma is a
+ * coefficient of the regulariser (like NLL, it carries no gradient), so
+ * dL_t/dR_t = gamma_t * sigmoid(R_t).
+ * ------------------------------------------------------------------------- */
+
+/* Gradient of one row's softmax attention over keys [lo, hi] (chain rule):
+ *   p_j = softmax_j(scale <q, k_j>),  o = sum_j p_j v_j,  D = <dO, o>,
+ *   dS_j = p_j (<dO, v_j> - D),
+ *   dq  += scale sum_j dS_j k_j,  dk_j += scale dS_j q,  dv_j += p_j dO.
+ * dq is (d) for this row, or NULL; dk/dv point at key 0 of this (b, kv head)
+ * with stride kstride, or are NULL.  s, o are scratch (n and d doubles). */
+static void attend_backward(const double *q, const double *k, const double *v, const double *dout,
+                            int64_t kstride, int64_t lo, int64_t hi, int64_t d, double scale,
+                            double *s, double *o, double *dq, double *dk, double *dv)
+{
+    int64_t n = hi - lo + 1;
+    double lse;
+    attend(q, k, v, kstride, kstride, lo, hi, d, scale, s, o, &lse);
+    double D = 0.0;
+    for (int64_t c = 0; c < d; ++c) D += dout[c] * o[c];
+    for (int64_t t = 0; t < n; ++t) {
+        int64_t j = lo + t;
+        const double *kj = k + j * kstride, *vj = v + j * kstride;
+        double p = exp(s[t] - lse);
+        double dp = 0.0;
+        for (int64_t c = 0; c < d; ++c) dp += dout[c] * vj[c];
+        double ds = p * (dp - D);
+        if (dq)
+            for (int64_t c = 0; c < d; ++c) dq[c] += scale * ds * kj[c];
+        if (dk)
+            for (int64_t c = 0; c < d; ++c) dk[j * kstride + c] += scale * ds * q[c];
+        if (dv)
+            for (int64_t c = 0; c < d; ++c) dv[j * kstride + c] += p * dout[c];
+    }
+}
+
+/* Backward of the routed prefill: dq [B,N,Hq,d], dk/dv [B,N,Hkv,d] (zeroed
+ * here, then accumulated).  One thread per (b, kv head) owns every dk/dv row
+ * it writes and the dq rows of that head group. */
+int oracle_prefill_backward(const double *q, const double *k, const double *v,
+                            const uint8_t *gate, const double *dout, int64_t B, int64_t N,
+                            int64_t Hq, int64_t Hkv, int64_t d, int64_t W, double scale,
+                            double *dq, double *dk, double *dv)
+{
+    if (!shapes_ok(B, N, Hq, Hkv, d, W)) return -1;
+    memset(dq, 0, sizeof(double) * (size_t)(B * N * Hq * d));
+    memset(dk, 0, sizeof(double) * (size_t)(B * N * Hkv * d));
+    memset(dv, 0, sizeof(double) * (size_t)(B * N * Hkv * d));
+    int64_t G = Hq / Hkv;
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)N);
+        double *o = (double *)malloc(sizeof(double) * (size_t)d);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t u = 0; u < B * Hkv; ++u) {
+            int64_t b = u / Hkv, kvh = u % Hkv;
+            const double *kb = k + (b * N * Hkv + kvh) * d;
+            const double *vb = v + (b * N * Hkv + kvh) * d;
+            double *dkb = dk + (b * N * Hkv + kvh) * d;
+            double *dvb = dv + (b * N * Hkv + kvh) * d;
+            for (int64_t h = kvh * G; h < (kvh + 1) * G; ++h)
+                for (int64_t i = 0; i < N; ++i) {
+                    int64_t lo, hi, r = (b * N + i) * Hq + h;
+                    key_range(gate[b * N + i] != 0, i, W, &lo, &hi);
+                    attend_backward(q + r * d, kb, vb, dout + r * d, Hkv * d, lo, hi, d, scale,
+                                    s, o, dq + r * d, dkb, dvb);
+                }
+        }
+        free(s);
+        free(o);
+    }
+    return 0;
+}
+
+/* dq of selected rows: sel holds nsel triples (b, i, h); dq_sel [nsel, d]. */
+int oracle_prefill_backward_rows(const double *q, const double *k, const double *v,
+                                 const uint8_t *gate, const double *dout, int64_t B, int64_t N,
+                                 int64_t Hq, int64_t Hkv, int64_t d, int64_t W, double scale,
+                                 const int64_t *sel, int64_t nsel, double *dq_sel)
+{
+    if (!shapes_ok(B, N, Hq, Hkv, d, W) || nsel < 0) return -1;
+    for (int64_t r = 0; r < nsel; ++r) {
+        int64_t b = sel[3 * r], i = sel[3 * r + 1], h = sel[3 * r + 2];
+        if (b < 0 || b >= B || i < 0 || i >= N || h < 0 || h >= Hq) return -1;
+    }
+    memset(dq_sel, 0, sizeof(double) * (size_t)(nsel * d));
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)N);
+        double *o = (double *)malloc(sizeof(double) * (size_t)d);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < nsel; ++r) {
+            int64_t b = sel[3 * r], i = sel[3 * r + 1], h = sel[3 * r + 2];
+            int64_t kvh = h / (Hq / Hkv), lo, hi, row = (b * N + i) * Hq + h;
+            key_range(gate[b * N + i] != 0, i, W, &lo, &hi);
+            attend_backward(q + row * d, k + (b * N * Hkv + kvh) * d, v + (b * N * Hkv + kvh) * d,
+                            dout + row * d, Hkv * d, lo, hi, d, scale, s, o, dq_sel + r * d, NULL,
+                            NULL);
+        }
+        free(s);
+        free(o);
+    }
+    return 0;
+}
+
+/* dk and dv of selected keys: sel holds nsel triples (b, j, kv head);
+ * dk_sel/dv_sel [nsel, d].  Every row i >= j of the head group whose visited
+ * range holds key j contributes scale*dS_ij*q_i and p_ij*dO_i; each such row's
+ * softmax is recomputed in full. */
+int oracle_prefill_backward_keys(const double *q, const double *k, const double *v,
+                                 const uint8_t *gate, const double *dout, int64_t B, int64_t N,
+                                 int64_t Hq, int64_t Hkv, int64_t d, int64_t W, double scale,
+                                 const int64_t *sel, int64_t nsel, double *dk_sel,
+                                 double *dv_sel)
+{
+    if (!shapes_ok(B, N, Hq, Hkv, d, W) || nsel < 0) return -1;
+    for (int64_t r = 0; r < nsel; ++r) {
+        int64_t b = sel[3 * r], j = sel[3 * r + 1], kvh = sel[3 * r + 2];
+        if (b < 0 || b >= B || j < 0 || j >= N || kvh < 0 || kvh >= Hkv) return -1;
+    }
+    int64_t G = Hq / Hkv;
+    for (int64_t r = 0; r < nsel; ++r) {
+        int64_t b = sel[3 * r], j = sel[3 * r + 1], kvh = sel[3 * r + 2];
+        const double *kb = k + (b * N * Hkv + kvh) * d;
+        const double *vb = v + (b * N * Hkv + kvh) * d;
+        const double *vj = vb + j * Hkv * d;
+        double *dk_r = dk_sel + r * d, *dv_r = dv_sel + r * d;
+        for (int64_t c = 0; c < d; ++c) dk_r[c] = dv_r[c] = 0.0;
+#pragma omp parallel
+        {
+            double *s = (double *)malloc(sizeof(double) * (size_t)N);
+            double *o = (double *)malloc(sizeof(double) * (size_t)d);
+            double *pk = (double *)calloc((size_t)d, sizeof(double));
+            double *pv = (double *)calloc((size_t)d, sizeof(double));
+#pragma omp for schedule(dynamic, 4)
+            for (int64_t u = 0; u < G * (N - j); ++u) {
+                int64_t h = kvh * G + u % G, i = j + u / G, lo, hi, row = (b * N + i) * Hq + h;
+                key_range(gate[b * N + i] != 0, i, W, &lo, &hi);
+                if (j < lo) continue;
+                double lse, D = 0.0, dp = 0.0;
+                attend(q + row * d, kb, vb, Hkv * d, Hkv * d, lo, hi, d, scale, s, o, &lse);
+                for (int64_t c = 0; c < d; ++c) D += dout[row * d + c] * o[c];
+                for (int64_t c = 0; c < d; ++c) dp += dout[row * d + c] * vj[c];
+                double p = exp(s[j - lo] - lse), ds = p * (dp - D);
+                for (int64_t c = 0; c < d; ++c) {
+                    pk[c] += scale * ds * q[row * d + c];
+                    pv[c] += p * dout[row * d + c];
+                }
+            }
+#pragma omp critical
+            for (int64_t c = 0; c < d; ++c) {
+                dk_r[c] += pk[c];
+                dv_r[c] += pv[c];
+            }
+            free(s);
+            free(o);
+            free(pk);
+            free(pv);
+        }
+    }
+    return 0;
+}
+
+static double sigmoid(double x)
+{
+    return 1.0 / (1.0 + exp(-x));
+}
+
+/* Router backward through the straight-through gate and the regulariser.
+ * Per token t (T tokens; per-token rows of HD = Hq*d attention outputs):
+ *   d_logit_t = s_t (1 - s_t) * <dO_t, O_FULL,t - O_SWA,t>
+ *             + d_reg_t * gamma_t * sigmoid(logit_t),     s_t = sigmoid(logit_t)
+ * (d_reg may be NULL: no regulariser gradient).  Then through the linear
+ * router logit_t = <h_t, w> + b:
+ *   dh_t = d_logit_t w,   dw = sum_t d_logit_t h_t,   db = sum_t d_logit_t.
+ * dh [T, D], dw [D], db [1] may each be NULL (h and w then unused). */
+int oracle_route_backward(const double *logits, const double *o_full, const double *o_swa,
+                          const double *dout, const double *gamma, const double *d_reg,
+                          const double *h, const double *w, int64_t T, int64_t HD, int64_t D,
+                          double *d_logits, double *dh, double *dw, double *db)
+{
+    if (T < 0 || HD <= 0 || ((dh || dw) && D <= 0)) return -1;
+    for (int64_t t = 0; t < T; ++t) {
+        double acc = 0.0;
+        for (int64_t c = 0; c < HD; ++c)
+            acc += dout[t * HD + c] * (o_full[t * HD + c] - o_swa[t * HD + c]);
+        double sg = sigmoid(logits[t]);
+        double g = sg * (1.0 - sg) * acc;
+        if (d_reg) g += d_reg[t] * gamma[t] * sg;
+        d_logits[t] = g;
+    }
+    if (dh)
+        for (int64_t t = 0; t < T; ++t)
+            for (int64_t j = 0; j < D; ++j) dh[t * D + j] = d_logits[t] * w[j];
+    if (dw)
+        for (int64_t j = 0; j < D; ++j) {
+            double acc = 0.0;
+            for (int64_t t = 0; t < T; ++t) acc += d_logits[t] * h[t * D + j];
+            dw[j] = acc;
+        }
+    if (db) {
+        double acc = 0.0;
+        for (int64_t t = 0; t < T; ++t) acc += d_logits[t];
+        *db = acc;
     }
     return 0;
 }
