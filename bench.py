@@ -363,6 +363,60 @@ def dual_section(swa, timer, dev, steps, warmup, seed):
     return dict(step_ms=step_ms, kern_ms=kern_ms, flops=flops)
 
 
+def backward_section(swa, timer, dev, steps, warmup, seed, workload):
+    """Training backward (swiattn_prefill_backward): forward output and lse are
+    computed once, untimed; a step is one backward call (schedule, dK/dV and dQ
+    kernels).  Useful work: 10*d FLOP per visited (query, key) pair and query
+    head, the five d-long products of the attention backward (recomputed
+    scores, dP, dV, dK, dQ)."""
+    if workload == "dual_8k":
+        d = inp.dual_8k(seed=seed)
+        gate_cpu = (d["logits"] > 0).to(torch.uint8)
+    else:
+        d = inp.prefill_32k(frac=0.13, seed=seed)
+        gate_cpu = d["gate"]
+    B, N, Hq, Hkv, D, W = d["B"], d["N"], d["Hq"], d["Hkv"], d["d"], d["W"]
+    q, k, v = (d[n].to(dev) for n in ("q", "k", "v"))
+    gate = gate_cpu.to(dev)
+    do = inp.output_grad(d["q"].shape, torch.bfloat16, seed + 1).to(dev)
+    o, lse = swa.prefill(q, k, v, gate, W, want_lse=True)
+    outs = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+    ws = torch.empty(swa.prefill_backward_workspace(B, N, Hq, Hkv, D, W, torch.bfloat16),
+                     dtype=torch.uint8, device=dev)
+
+    def step():
+        swa.prefill_backward(q, k, v, gate, o, lse, do, W, outs=outs, workspace=ws)
+
+    step_ms, kern_ms = timer.run(step, steps, warmup, kernel_events=True)
+    assert swa.get_device_error() == 0
+    pairs = useful_pairs(gate_cpu.numpy(), W)
+    return dict(step_ms=step_ms, kern_ms=kern_ms, flops=10.0 * D * Hq * pairs,
+                routed_frac=float(gate_cpu.float().mean()))
+
+
+def route_backward_section(swa, timer, dev, steps, warmup, seed):
+    """Router backward on the dual-branch workload's shapes: 16384 tokens,
+    hd = 16*128 attention outputs per token, d_model 2048 (HBM-bound: reads
+    o_full, o_swa, dO and h, writes dh)."""
+    T, HD, Dm = 2 * 8192, 16 * 128, 2048
+    g = inp._gen(seed)
+    of, os_, do = (inp.randn((T, HD), torch.bfloat16, g).to(dev) for _ in range(3))
+    r = inp.router_inputs(T, Dm, torch.bfloat16, seed)
+    h, w = r["h"].to(dev), r["w"].to(dev)
+    logits = inp.logits_with_margin((T,), g).to(dev)
+    gamma = torch.full((T,), 1e-3, device=dev)
+    d_reg = torch.ones(T, device=dev)
+    ws = torch.empty(swa.route_backward_workspace(T, Dm, torch.bfloat16), dtype=torch.uint8,
+                     device=dev)
+
+    def step():
+        swa.route_backward(logits, of, os_, do, gamma, d_reg, h, w, workspace=ws)
+
+    step_ms, _ = timer.run(step, steps, warmup)
+    nbytes = 3 * T * HD * 2 + 2 * T * Dm * 2 + T * 16 + Dm * 4
+    return dict(step_ms=step_ms, bytes=nbytes)
+
+
 # ------------------------------------------------------------ CPU oracle --
 def oracle_sample(d, budget_s: float, seed: int = 0):
     """Time the fp64 oracle on a random sample of (row, head) outputs of the
@@ -497,6 +551,26 @@ def run_ours(args, dist: Dist):
         extra["dual"] = {"tflops": du["flops"] / dm / 1e12, "ms_per_step": dm * 1e3,
                          "kernel_tflops": du["flops"] / (statistics.mean(du["kern_ms"]) / 1e3) / 1e12,
                          "workload": "dual-branch forward bf16, B=2 Hq=16 Hkv=4 d=128 N=8192 W=1024"}
+        for wl, desc in (("dual_8k", "training backward bf16 on the dual-branch workload: B=2 "
+                                     "Hq=16 Hkv=4 d=128 N=8192 W=1024, gates = logits > 0"),
+                         ("prefill_32k", "training backward bf16 on the long-context prefill "
+                                         "workload: B=1 H=16 d=128 N=32768 W=1024, f=0.13")):
+            bw = backward_section(swa, timer, dev, ks, kw, dist.rank, wl)
+            bms = statistics.mean(bw["step_ms"]) / 1e3
+            bk = statistics.mean(bw["kern_ms"]) / 1e3
+            extra["backward_" + wl] = {
+                "tflops": bw["flops"] / bms / 1e12, "ms_per_step": bms * 1e3,
+                "routed_frac": bw["routed_frac"], "useful_tflop": bw["flops"] / 1e12,
+                "roofline": {"bound": "tensor", "achieved": bw["flops"] / bk / 1e12,
+                             "peak": peak, "unit": "TFLOP/s",
+                             "frac": bw["flops"] / bk / 1e12 / peak, "traffic": None,
+                             "kernel": "dkdv_kernel + dq_kernel"},
+                "workload": desc}
+        rb = route_backward_section(swa, timer, dev, ks, kw, dist.rank)
+        rbs = statistics.mean(rb["step_ms"]) / 1e3
+        extra["route_backward"] = {
+            "gbs": rb["bytes"] / rbs / 1e9, "ms_per_step": rbs * 1e3,
+            "workload": "router backward bf16: 16384 tokens, 2048 outputs per token, d_model 2048"}
 
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:

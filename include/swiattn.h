@@ -145,6 +145,61 @@ int swiattn_dual_branch(const void* q, const void* k, const void* v, const float
                         int W, float scale, float gamma_base, float eps, float alpha, int dtype,
                         void* workspace, size_t workspace_bytes, void* stream);
 
+/* Bytes of device workspace swiattn_prefill_backward needs for these sizes. */
+size_t swiattn_prefill_backward_workspace(int B, int N, int Hq, int Hkv, int d, int W, int dtype);
+
+/* Gradient of swiattn_prefill for training (report section 2, router design:
+ * the straight-through gate's forward value is the hard 0/1, so the output
+ * gradient of row i reaches only the branch its gate selected).  Inputs: the
+ * forward's q, k, v, gate, its output o and lse (swiattn_prefill with
+ * lse != NULL; the same values the dual branch's gated output has), and
+ * d_o = dLoss/do [B,N,Hq,d].  Outputs dq [B,N,Hq,d] and dk, dv [B,N,Hkv,d] of
+ * `dtype`, by the chain rule through each row's softmax over its visited keys
+ * [lo, hi] (as in swiattn_prefill):
+ *   D_i = <d_o_i, o_i>,   p_ij = exp(scale q_i.k_j - lse_i),
+ *   dS_ij = p_ij (<d_o_i, v_j> - D_i),
+ *   dq_i = scale sum_j dS_ij k_j,  dk_j = scale sum_i dS_ij q_i,
+ *   dv_j = sum_i p_ij d_o_i,
+ * the sums running over the (i, j) pairs the forward visits; dk and dv sum
+ * over the query heads of each GQA group.  Every element of dq, dk, dv is
+ * written.  No atomics: results are bitwise repeatable.  Support as for
+ * swiattn_prefill (bf16: d == 128, tensor cores; fp32: d in {64, 128}).
+ * workspace: at least swiattn_prefill_backward_workspace(...) bytes, 256-byte
+ * aligned, scratch only. */
+int swiattn_prefill_backward(const void* q, const void* k, const void* v, const uint8_t* gate,
+                             const void* o, const float* lse, const void* d_o, void* dq, void* dk,
+                             void* dv, int B, int N, int Hq, int Hkv, int d, int W, float scale,
+                             int dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of device workspace swiattn_route_backward needs (only when dw is
+ * requested). */
+size_t swiattn_route_backward_workspace(int64_t tokens, int d_model, int dtype);
+
+/* Router backward through the straight-through gate and the adaptive
+ * regulariser (report section 2).  The gate sigma = 1(s > 0.5) + s - sg(s),
+ * s = sigmoid(logit), passes d sigma / d logit = s (1 - s); the output
+ * O = sigma O_FULL + (1 - sigma) O_SWA gives dO / d sigma = O_FULL - O_SWA;
+ * gamma is a coefficient of the regulariser (no gradient flows through it,
+ * as through NLL).  Per token t:
+ *   d_logits[t] = s_t (1 - s_t) * sum_c d_o[t,c] (o_full[t,c] - o_swa[t,c])
+ *               + d_reg[t] * gamma[t] * s_t
+ * with d_reg = dLoss/dreg_loss (nullable: no regulariser term).  Then through
+ * the linear router logits = h.w + bias:
+ *   dh[t,:] = d_logits[t] w,   dw = sum_t d_logits[t] h[t,:],   db = sum_t d_logits[t].
+ * o_full, o_swa, d_o [tokens, hd] of `dtype` (hd = Hq*d: one token's attention
+ * outputs); logits, gamma, d_reg fp32 [tokens]; h [tokens, d_model] and
+ * w [d_model] of `dtype`; outputs d_logits fp32 [tokens], dh [tokens, d_model]
+ * of `dtype`, dw fp32 [d_model], db fp32 [1].  dh, dw and db are each
+ * nullable; h and w may be NULL when dh and dw both are.  hd and d_model are
+ * multiples of 8.  dw and db are reduced in a fixed order (repeatable).
+ * workspace: swiattn_route_backward_workspace(...) bytes when dw != NULL,
+ * otherwise unused (may be NULL).  tokens == 0 is a valid no-op. */
+int swiattn_route_backward(const void* h, const void* w, const float* logits, const void* o_full,
+                           const void* o_swa, const void* d_o, const float* gamma,
+                           const float* d_reg, int64_t tokens, int hd, int d_model, int dtype,
+                           float* d_logits, void* dh, float* dw, float* db, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
 /* Synchronises `stream`, then returns and clears the device error word of the
  * current device: SWIATTN_OK, SWIATTN_ETIMEOUT if a bounded device wait
  * expired since the last query, or SWIATTN_ECUDA if the synchronisation itself
@@ -155,11 +210,12 @@ int swiattn_get_device_error(void* stream);
 const char* swiattn_status_string(int status);
 
 /* Timing hook.  When both are non-NULL, every later swiattn_prefill,
- * swiattn_decode and swiattn_dual_branch call records `start` (a cudaEvent_t
- * passed as void*) on its stream immediately before launching its dominant
- * kernel (the attention kernel, or the decode split kernel) and `stop`
- * immediately after it, so cudaEventElapsedTime gives that kernel's device
- * time alone.  Passing NULL, NULL turns the hook off.  Process-wide setting;
+ * swiattn_decode, swiattn_dual_branch and swiattn_prefill_backward call
+ * records `start` (a cudaEvent_t passed as void*) on its stream immediately
+ * before launching its dominant kernel (the attention kernel, the decode
+ * split kernel, or the backward's two attention kernels, dK/dV then dQ) and
+ * `stop` immediately after it, so cudaEventElapsedTime gives that kernel's
+ * device time alone.  Passing NULL, NULL turns the hook off.  Process-wide setting;
  * the events stay owned by the caller and must outlive their use. */
 void swiattn_set_profile_events(void* start, void* stop);
 

@@ -19,7 +19,8 @@ import torch
 __all__ = [
     "SwiAttnError", "F32", "BF16", "library_path", "route", "prefill", "decode", "dual_branch",
     "prefill_workspace", "decode_workspace", "dual_branch_workspace", "get_device_error",
-    "status_string", "num_sms", "set_profile_events", "EXPORTS",
+    "status_string", "num_sms", "set_profile_events", "EXPORTS", "prefill_backward",
+    "prefill_backward_workspace", "route_backward", "route_backward_workspace",
 ]
 
 F32, BF16 = 0, 1
@@ -33,7 +34,8 @@ _lib = None
 EXPORTS = (
     "swiattn_route", "swiattn_prefill_workspace", "swiattn_prefill", "swiattn_decode_workspace",
     "swiattn_decode", "swiattn_decode_noalloc", "swiattn_dual_branch_workspace",
-    "swiattn_dual_branch",
+    "swiattn_dual_branch", "swiattn_prefill_backward_workspace", "swiattn_prefill_backward",
+    "swiattn_route_backward_workspace", "swiattn_route_backward",
     "swiattn_get_device_error", "swiattn_status_string", "swiattn_set_profile_events",
     "swiattn_num_sms",
 )
@@ -72,6 +74,12 @@ def _load() -> ctypes.CDLL:
             lib.swiattn_dual_branch_workspace.restype = sz
             lib.swiattn_dual_branch.argtypes = ([vp] * 11 + [i32] * 6 + [f32] * 4
                                                 + [i32, vp, sz, vp])
+            lib.swiattn_prefill_backward_workspace.argtypes = [i32] * 7
+            lib.swiattn_prefill_backward_workspace.restype = sz
+            lib.swiattn_prefill_backward.argtypes = [vp] * 10 + [i32] * 6 + [f32, i32, vp, sz, vp]
+            lib.swiattn_route_backward_workspace.argtypes = [i64, i32, i32]
+            lib.swiattn_route_backward_workspace.restype = sz
+            lib.swiattn_route_backward.argtypes = [vp] * 8 + [i64, i32, i32, i32] + [vp] * 5 + [sz, vp]
             lib.swiattn_get_device_error.argtypes = [vp]
             lib.swiattn_status_string.argtypes = [i32]
             lib.swiattn_status_string.restype = ctypes.c_char_p
@@ -79,7 +87,8 @@ def _load() -> ctypes.CDLL:
             lib.swiattn_set_profile_events.argtypes = [vp, vp]
             lib.swiattn_set_profile_events.restype = None
             for name in ("swiattn_route", "swiattn_prefill", "swiattn_decode", "swiattn_decode_noalloc",
-                         "swiattn_dual_branch", "swiattn_get_device_error", "swiattn_num_sms"):
+                         "swiattn_dual_branch", "swiattn_get_device_error", "swiattn_num_sms",
+                         "swiattn_prefill_backward", "swiattn_route_backward"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -225,3 +234,73 @@ def dual_branch(q, k, v, logits, nll, W: int, scale: Optional[float] = None, gam
         _ptr(outs["reg_loss"]), B, N, Hq, Hkv, d, W, float(scale), float(gamma_base), float(eps),
         float(alpha), _DT[q.dtype], _ptr(ws), ws.numel(), _stream()), "swiattn_dual_branch")
     return outs
+
+
+def prefill_backward_workspace(B, N, Hq, Hkv, d, W, dtype) -> int:
+    return int(_load().swiattn_prefill_backward_workspace(B, N, Hq, Hkv, d, W,
+                                                          _DT.get(dtype, dtype)))
+
+
+def prefill_backward(q, k, v, gate, o, lse, d_o, W: int, scale: Optional[float] = None,
+                     outs=None, workspace=None):
+    """Gradient of prefill: (dq, dk, dv) for output gradient d_o [B,N,Hq,d], given the
+    forward's o and lse (prefill(..., want_lse=True))."""
+    _dev(q, "q")
+    _dev(k, "k", q.dtype)
+    _dev(v, "v", q.dtype)
+    _dev(gate, "gate", torch.uint8)
+    _dev(o, "o", q.dtype)
+    _dev(lse, "lse", torch.float32)
+    _dev(d_o, "d_o", q.dtype)
+    B, N, Hq, d = q.shape
+    Hkv = k.shape[2]
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    dq, dk, dv = outs if outs is not None else (torch.empty_like(q), torch.empty_like(k),
+                                                torch.empty_like(v))
+    ws = _workspace(prefill_backward_workspace(B, N, Hq, Hkv, d, W, q.dtype), q.device, workspace)
+    _check(_load().swiattn_prefill_backward(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(o), _ptr(lse), _ptr(d_o), _ptr(dq), _ptr(dk),
+        _ptr(dv), B, N, Hq, Hkv, d, W, float(scale), _DT[q.dtype], _ptr(ws), ws.numel(),
+        _stream()), "swiattn_prefill_backward")
+    return dq, dk, dv
+
+
+def route_backward_workspace(tokens, d_model, dtype) -> int:
+    return int(_load().swiattn_route_backward_workspace(tokens, d_model, _DT.get(dtype, dtype)))
+
+
+def route_backward(logits, o_full, o_swa, d_o, gamma=None, d_reg=None, h=None, w=None,
+                   want_dh=True, want_dw=True, want_db=True, workspace=None):
+    """Router backward through the straight-through gate and the regulariser.
+    o_full/o_swa/d_o [T, hd] (any shape with T leading rows), logits/gamma/d_reg fp32 [T],
+    h [T, D], w [D].  Returns dict(d_logits[, dh, dw, db])."""
+    _dev(logits, "logits", torch.float32)
+    _dev(o_full, "o_full")
+    _dev(o_swa, "o_swa", o_full.dtype)
+    _dev(d_o, "d_o", o_full.dtype)
+    T = logits.numel()
+    hd = o_full.numel() // max(T, 1)
+    if d_reg is not None:
+        _dev(d_reg, "d_reg", torch.float32)
+        _dev(gamma, "gamma", torch.float32)
+    out = dict(d_logits=torch.empty(T, device=logits.device, dtype=torch.float32))
+    D = 0
+    if h is not None:
+        _dev(h, "h", o_full.dtype)
+        _dev(w, "w", o_full.dtype)
+        D = w.numel()
+        if want_dh:
+            out["dh"] = torch.empty_like(h)
+        if want_dw:
+            out["dw"] = torch.empty(D, device=h.device, dtype=torch.float32)
+        if want_db:
+            out["db"] = torch.empty(1, device=h.device, dtype=torch.float32)
+    ws = None
+    if "dw" in out:
+        ws = _workspace(route_backward_workspace(T, D, o_full.dtype), logits.device, workspace)
+    _check(_load().swiattn_route_backward(
+        _ptr(h), _ptr(w), _ptr(logits), _ptr(o_full), _ptr(o_swa), _ptr(d_o), _ptr(gamma),
+        _ptr(d_reg), T, hd, D, _DT[o_full.dtype], _ptr(out["d_logits"]), _ptr(out.get("dh")),
+        _ptr(out.get("dw")), _ptr(out.get("db")), _ptr(ws), 0 if ws is None else ws.numel(),
+        _stream()), "swiattn_route_backward")
+    return out

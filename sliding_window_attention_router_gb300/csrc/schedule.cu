@@ -228,4 +228,11 @@ cudaError_t launch_schedule(const uint8_t* gate, const void* q, int B, int N, in
     return cudaGetLastError();
 }
 
+cudaError_t launch_far_scan(const uint8_t* gate, int B, int N, int W, int* routed_list,
+                            int* routed_count, int* tile_prefix, cudaStream_t s) {
+    scan_far_rows_kernel<<<B, kScanThreads, 0, s>>>(gate, N, W, routed_list, routed_count,
+                                                    tile_prefix);
+    return cudaGetLastError();
+}
+
 }  // namespace swi

@@ -302,4 +302,101 @@ int swiattn_dual_branch(const void* q, const void* k, const void* v, const float
     return launched(e);
 }
 
+size_t swiattn_prefill_backward_workspace(int B, int N, int Hq, int Hkv, int d, int W, int dtype) {
+    if (!attn_shape_ok(B, N, Hq, Hkv, d, W)) return 0;
+    if (dtype != SWIATTN_BF16) {   // fp32 path: D per row
+        const size_t n = sizeof(float) * (size_t)B * N * Hq;
+        return (n + 255) & ~static_cast<size_t>(255);
+    }
+    return bwd_ws_layout(B, N, Hq, Hkv).total;
+}
+
+int swiattn_prefill_backward(const void* q, const void* k, const void* v, const uint8_t* gate,
+                             const void* o, const float* lse, const void* d_o, void* dq, void* dk,
+                             void* dv, int B, int N, int Hq, int Hkv, int d, int W, float scale,
+                             int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+    if (!attn_shape_ok(B, N, Hq, Hkv, d, W)) return SWIATTN_EINVAL;
+    if (!q || !k || !v || !gate || !o || !lse || !d_o || !dq || !dk || !dv) return SWIATTN_EINVAL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(d_o) ||
+        !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+        return SWIATTN_EINVAL;
+    if (!(scale > 0.f)) return SWIATTN_EINVAL;
+    if (dtype != SWIATTN_BF16 && dtype != SWIATTN_F32) return SWIATTN_EINVAL;
+    if (dtype == SWIATTN_BF16 && d != kHD) return SWIATTN_EUNSUPPORTED;
+    const size_t need = swiattn_prefill_backward_workspace(B, N, Hq, Hkv, d, W, dtype);
+    if (!workspace || !aligned256(workspace) || workspace_bytes < need) return SWIATTN_EINVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == SWIATTN_F32) {
+        prof_start(s);
+        cudaError_t e = launch_simt_backward(
+            static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v),
+            gate, static_cast<const float*>(o), lse, static_cast<const float*>(d_o),
+            static_cast<float*>(dq), static_cast<float*>(dk), static_cast<float*>(dv), B, N, Hq, Hkv,
+            d, W, scale, static_cast<float*>(workspace), s);
+        prof_stop(s);
+        return launched(e);
+    }
+    DeviceInfo di;
+    if (!device_info(di)) return SWIATTN_ECUDA;
+    const BwdWs L = bwd_ws_layout(B, N, Hq, Hkv);
+    char* ws = static_cast<char*>(workspace);
+    cudaError_t e = launch_bwd_schedule(gate, q, o, lse, d_o, B, N, Hq, Hkv, W, L, ws, di.sms, s);
+    if (e != cudaSuccess) return SWIATTN_ECUDA;
+    TcBwdArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.d_o = d_o;
+    a.gate = gate;
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.L = &L;
+    a.ws = ws;
+    a.B = B;
+    a.N = N;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.W = W;
+    a.scale = scale;
+    prof_start(s);
+    e = launch_bwd_dkdv(a, di.err, di.sms, s);
+    if (e == cudaSuccess) e = launch_bwd_dq(a, di.err, di.sms, s);
+    prof_stop(s);
+    return launched(e);
+}
+
+size_t swiattn_route_backward_workspace(int64_t tokens, int d_model, int dtype) {
+    (void)dtype;
+    if (tokens < 0 || d_model <= 0) return 0;
+    const size_t n = sizeof(float) * (size_t)route_bwd_chunks(tokens) * (size_t)d_model;
+    return (n + 255) & ~static_cast<size_t>(255);
+}
+
+int swiattn_route_backward(const void* h, const void* w, const float* logits, const void* o_full,
+                           const void* o_swa, const void* d_o, const float* gamma,
+                           const float* d_reg, int64_t tokens, int hd, int d_model, int dtype,
+                           float* d_logits, void* dh, float* dw, float* db, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+    if (tokens < 0 || hd <= 0) return SWIATTN_EINVAL;
+    if (dtype != SWIATTN_BF16 && dtype != SWIATTN_F32) return SWIATTN_EINVAL;
+    if (hd % 8 != 0) return SWIATTN_EINVAL;
+    if ((dh || dw || db) && (d_model <= 0 || d_model % 8 != 0)) return SWIATTN_EINVAL;
+    if (tokens == 0) return SWIATTN_OK;
+    if (!logits || !o_full || !o_swa || !d_o || !d_logits || (d_reg && !gamma))
+        return SWIATTN_EINVAL;
+    if (!aligned16(o_full) || !aligned16(o_swa) || !aligned16(d_o)) return SWIATTN_EINVAL;
+    if ((dh || dw) && (!h || !w || !aligned16(h) || !aligned16(w))) return SWIATTN_EINVAL;
+    if ((dh && !aligned16(dh)) || (dw && !aligned16(dw))) return SWIATTN_EINVAL;
+    if (dw) {
+        const size_t need = swiattn_route_backward_workspace(tokens, d_model, dtype);
+        if (!workspace || !aligned256(workspace) || workspace_bytes < need) return SWIATTN_EINVAL;
+    }
+    return launched(launch_route_backward(h, w, logits, o_full, o_swa, d_o, gamma, d_reg, tokens,
+                                          hd, d_model, dtype, d_logits, dh, dw, db,
+                                          static_cast<float*>(workspace),
+                                          static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

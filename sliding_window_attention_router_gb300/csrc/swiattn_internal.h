@@ -112,6 +112,90 @@ cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const i
                           int Hkv, int d, int W, float scale, int dtype, const DecodeWs& L,
                           char* ws, cudaStream_t s);
 
+// ------------------------------------------------------------ backward ------
+// Far-row scan of launch_schedule on its own: routed_list/routed_count/
+// tile_prefix as in PrefillWs.
+cudaError_t launch_far_scan(const uint8_t* gate, int B, int N, int W, int* routed_list,
+                            int* routed_count, int* tile_prefix, cudaStream_t s);
+
+// Work item of the tensor-core backward kernels (32 bytes).
+//  kBwdKV:    one 128-key block t of (b, kv head h); for each query head of the
+//             group it visits the band query tiles starting at 128*t + 128*u,
+//             u < a0, then the far (compacted) tiles [a1, a2).
+//  kBwdQBand: query tile t (rows 128*t ...) of (b, query head h), window keys.
+//  kBwdQFar:  compacted far tile t of (b, h), keys [0, max i].
+constexpr int kBwdKV = 0;
+constexpr int kBwdQBand = 1;
+constexpr int kBwdQFar = 2;
+struct BwdItem {
+    int kind, b, h, t;
+    int a0, a1, a2, cost;
+};
+static_assert(sizeof(BwdItem) == 32, "BwdItem is read as two int4");
+
+// Rows of a compacted far tile past the routed count carry this row index.
+constexpr int kNoRow = -(1 << 30);
+
+// Workspace layout of swiattn_prefill_backward (tensor-core path; byte
+// offsets from a 256-aligned base).  Npad = N rounded up to 128.
+struct BwdWs {
+    size_t routed_list;   // int32 [B*N]
+    size_t routed_count;  // int32 [B]
+    size_t tile_prefix;   // int32 [B*(NT+1)]
+    size_t rowidx;        // int32 [B*Npad]  far rows (compacted), kNoRow padded per tile
+    size_t d_band;        // f32 [B*Hq*Npad] D_i = <dO_i, O_i>, head-major
+    size_t l_band;        // f32 [B*Hq*Npad] lse_i * log2(e)
+    size_t d_far;         // f32 [B*Hq*Npad] the same for compacted far rows
+    size_t l_far;         // f32 [B*Hq*Npad]
+    size_t qc;            // bf16 [B*Npad*Hq*128] compacted q of far rows (zero pads)
+    size_t doc;           // bf16 [B*Npad*Hq*128] compacted dO of far rows
+    size_t counters;      // int32 [4]: n_kv, next_kv, n_q, next_q
+    size_t items_kv;      // BwdItem [max_kv]
+    size_t items_q;       // BwdItem [max_q]
+    size_t total;
+    int Npad, max_kv, max_q;
+};
+BwdWs bwd_ws_layout(int B, int N, int Hq, int Hkv);
+
+// Scan, row statistics, compaction and work lists of the backward.
+cudaError_t launch_bwd_schedule(const uint8_t* gate, const void* q, const void* o,
+                                const float* lse, const void* d_o, int B, int N, int Hq,
+                                int Hkv, int W, const BwdWs& L, char* ws, int num_sms,
+                                cudaStream_t s);
+
+struct TcBwdArgs {
+    const void* q;     // [B,N,Hq,128] bf16
+    const void* k;     // [B,N,Hkv,128]
+    const void* v;
+    const void* d_o;   // [B,N,Hq,128]
+    const uint8_t* gate;
+    void* dq;          // [B,N,Hq,128] bf16
+    void* dk;          // [B,N,Hkv,128]
+    void* dv;
+    const BwdWs* L;
+    char* ws;
+    int B, N, Hq, Hkv, W;
+    float scale;
+};
+cudaError_t launch_bwd_dkdv(const TcBwdArgs& a, unsigned int* err, int num_sms, cudaStream_t s);
+cudaError_t launch_bwd_dq(const TcBwdArgs& a, unsigned int* err, int num_sms, cudaStream_t s);
+
+// fp32 backward on CUDA cores (dtype SWIATTN_F32, d in {64, 128}); ws holds
+// B*N*Hq floats.
+cudaError_t launch_simt_backward(const float* q, const float* k, const float* v,
+                                 const uint8_t* gate, const float* o, const float* lse,
+                                 const float* d_o, float* dq, float* dk, float* dv, int B, int N,
+                                 int Hq, int Hkv, int d, int W, float scale, float* ws,
+                                 cudaStream_t s);
+
+// Router backward (straight-through gate + regulariser, then the linear map).
+int64_t route_bwd_chunks(int64_t tokens);
+cudaError_t launch_route_backward(const void* h, const void* w, const float* logits,
+                                  const void* o_full, const void* o_swa, const void* d_o,
+                                  const float* gamma, const float* d_reg, int64_t tokens, int hd,
+                                  int d_model, int dtype, float* d_logits, void* dh, float* dw,
+                                  float* db, float* ws, cudaStream_t s);
+
 // Timing hook around the dominant kernel of a call (no-ops unless set).
 void prof_start(cudaStream_t s);
 void prof_stop(cudaStream_t s);

@@ -163,3 +163,9 @@ def dual_8k(seed: int = 0, B: int = 2, N: int = 8192) -> dict:
     nll = (-torch.log1p(-u)).sum(0).to(torch.float32)
     return dict(q=q, k=k, v=v, logits=logits, nll=nll, W=W, B=B, N=N, Hq=Hq, Hkv=Hkv, d=d,
                 gamma_base=1e-3, eps=0.1, alpha=100.0)
+
+
+def output_grad(shape, dtype, seed: int) -> torch.Tensor:
+    """Upstream gradient of an attention output (the training backward's input):
+    iid N(0,1) of the given shape and dtype, from its own seed."""
+    return randn(shape, dtype, _gen(seed))

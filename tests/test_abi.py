@@ -91,6 +91,37 @@ def test_invalid_arguments_rejected_before_launch(lib):
                                    1 << 30, None) == 1
 
 
+def test_backward_workspace_and_validation(lib):
+    import sliding_window_attention_router_gb300 as swa
+    n = swa.prefill_backward_workspace(1, 32768, 16, 16, 128, 1024, swa.BF16)
+    # compacted q and dO of far rows alone are twice the size of q
+    assert n >= 2 * 32768 * 16 * 128 * 2 and n % 256 == 0
+    assert swa.prefill_backward_workspace(1, 100, 6, 4, 128, 8, swa.BF16) == 0   # Hq % Hkv
+    assert swa.prefill_backward_workspace(1, 256, 2, 2, 64, 32, swa.F32) == 256 * 2 * 4
+    assert swa.route_backward_workspace(1000, 256, swa.BF16) >= 16 * 256 * 4
+    vp = ctypes.c_void_p
+    fake = vp(1 << 20)
+    odd = vp((1 << 20) + 8)
+    a10 = [fake] * 10
+    # W < 1; Hq % Hkv; misaligned dq; bf16 d = 64 unsupported; workspace too small; null lse
+    assert lib.swiattn_prefill_backward(*a10, 1, 64, 4, 4, 128, 0, 0.1, 1, fake, 1 << 30, None) == 1
+    assert lib.swiattn_prefill_backward(*a10, 1, 64, 6, 4, 128, 8, 0.1, 1, fake, 1 << 30, None) == 1
+    bad = a10[:7] + [odd] + a10[8:]
+    assert lib.swiattn_prefill_backward(*bad, 1, 64, 4, 4, 128, 8, 0.1, 1, fake, 1 << 30, None) == 1
+    assert lib.swiattn_prefill_backward(*a10, 1, 64, 4, 4, 64, 8, 0.1, 1, fake, 1 << 30, None) == 2
+    assert lib.swiattn_prefill_backward(*a10, 1, 64, 4, 4, 128, 8, 0.1, 1, fake, 16, None) == 1
+    nolse = a10[:5] + [None] + a10[6:]
+    assert lib.swiattn_prefill_backward(*nolse, 1, 64, 4, 4, 128, 8, 0.1, 1, fake, 1 << 30, None) == 1
+    r8 = [fake] * 8
+    # hd not a multiple of 8; d_reg without gamma; dw without workspace; tokens 0 no-op
+    assert lib.swiattn_route_backward(*r8, 10, 12, 16, 1, fake, None, None, None, None, 0, None) == 1
+    nog = r8[:6] + [None, fake]
+    assert lib.swiattn_route_backward(*nog, 10, 16, 16, 1, fake, None, None, None, None, 0, None) == 1
+    assert lib.swiattn_route_backward(*r8, 10, 16, 16, 1, fake, None, fake, None, None, 0, None) == 1
+    assert lib.swiattn_route_backward(*[None] * 8, 0, 16, 16, 1, None, None, None, None, None, 0,
+                                      None) == 0
+
+
 def test_no_gpu_reports_cuda_error_or_runs(lib):
     import torch
     if torch.cuda.is_available():
