@@ -609,6 +609,20 @@ def run_ours(args, dist: Dist):
         print(json.dumps(line), flush=True)
 
 
+def run_backward_only(args):
+    """One backward workload alone (a profiling aid, not the bench line)."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    import sliding_window_attention_router_gb300 as swa
+    swa._load()
+    bw = backward_section(swa, Timer(dev), dev, args.steps, args.warmup, 0, args.only_backward)
+    bms = statistics.mean(bw["step_ms"]) / 1e3
+    bk = statistics.mean(bw["kern_ms"]) / 1e3
+    print(json.dumps({"workload": args.only_backward, "tflops": bw["flops"] / bms / 1e12,
+                      "kernel_tflops": bw["flops"] / bk / 1e12, "ms_per_step": bms * 1e3,
+                      "useful_tflop": bw["flops"] / 1e12}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -623,6 +637,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--ref-step-budget", type=float, default=3.0,
                     help="seconds of oracle work per step of the reference arm")
+    ap.add_argument("--only-backward", choices=["dual_8k", "prefill_32k"], default=None,
+                    help="profiling runs only: time just the training backward on one workload")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -630,6 +646,8 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, dist)
+        elif args.only_backward:
+            run_backward_only(args)
         else:
             run_ours(args, dist)
     finally:

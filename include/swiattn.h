@@ -203,7 +203,8 @@ int swiattn_route_backward(const void* h, const void* w, const float* logits, co
 /* Synchronises `stream`, then returns and clears the device error word of the
  * current device: SWIATTN_OK, SWIATTN_ETIMEOUT if a bounded device wait
  * expired since the last query, or SWIATTN_ECUDA if the synchronisation itself
- * failed. */
+ * failed or a kernel found its shared memory not laid out as it requires (it
+ * then returned without computing). */
 int swiattn_get_device_error(void* stream);
 
 /* Static, NUL-terminated name of a status code. */

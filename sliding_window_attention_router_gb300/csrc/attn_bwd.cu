@@ -37,6 +37,7 @@
 #include "swiattn_internal.h"
 
 #include <cuda_bf16.h>
+#include <climits>
 #include <math.h>
 
 namespace swi {
@@ -152,10 +153,12 @@ __device__ __forceinline__ uint32_t packed_col(int kk) {
     return static_cast<uint32_t>((kk >> 2) * 64 + (kk & 3) * 8);
 }
 
-__device__ __forceinline__ void drain2(uint64_t* bars, uint32_t issued) {
-    for (uint32_t back = 1; back <= 2 && back <= issued; ++back) {
+// After an abort: waits (bounded) for the loads still in flight on a ring of
+// `slots` full-barriers, of which `issued` have been armed so far.
+__device__ __forceinline__ void drain_ring(uint64_t* bars, uint32_t slots, uint32_t issued) {
+    for (uint32_t back = 1; back <= slots && back <= issued; ++back) {
         const uint32_t it = issued - back;
-        mbar_drain(&bars[it % 2], (it / 2) & 1u);
+        mbar_drain(&bars[it % slots], (it / slots) & 1u);
     }
 }
 
@@ -188,23 +191,31 @@ __device__ __forceinline__ void mask_half(float* x, int a, int e, int c0) {
 // =================================================================== dK/dV ==
 namespace kv {
 
+// Query tiles live from S^T(t) to dK += dS^T(t) Q(t): three slots keep their
+// loads a tile and more ahead; dO tiles (with the tile's per-column lse and D)
+// two slots.  The tiles fill 224 KiB; the kernel requires the dynamic shared
+// memory base to be 1024-byte aligned (it is: the window's first KiB is
+// reserved) and checks it instead of padding.
+constexpr int kQSlots = 3;
+constexpr int kDSlots = 2;
 constexpr int kOffK = 0;
 constexpr int kOffV = kOffK + kTileBytes;
-constexpr int kOffQ = kOffV + kTileBytes;        // [2] query tiles
-constexpr int kOffDO = kOffQ + 2 * kTileBytes;   // [2] dO tiles
-constexpr int kOffL = kOffDO + 2 * kTileBytes;   // [2][128] lse * log2 e per column
-constexpr int kOffD = kOffL + 2 * kRowBytes;     // [2][128] D per column
-constexpr int kOffR = kOffD + 2 * kRowBytes;     // [2][128] row index (far tiles)
-constexpr int kOffBar = kOffR + 2 * kRowBytes;
+constexpr int kOffQ = kOffV + kTileBytes;                 // [kQSlots] query tiles
+constexpr int kOffDO = kOffQ + kQSlots * kTileBytes;      // [kDSlots] dO tiles
+constexpr int kOffL = kOffDO + kDSlots * kTileBytes;      // [kDSlots][128] lse * log2 e per column
+constexpr int kOffD = kOffL + kDSlots * kRowBytes;        // [kDSlots][128] D per column
+constexpr int kOffBar = kOffD + kDSlots * kRowBytes;
 
 enum {
     BAR_K_FULL = 0,
     BAR_K_EMPTY,
     BAR_V_FULL,
     BAR_V_EMPTY,
-    BAR_QD_FULL,                      // [2]
-    BAR_QD_EMPTY = BAR_QD_FULL + 2,   // [2]
-    BAR_S_FULL = BAR_QD_EMPTY + 2,
+    BAR_Q_FULL,                             // [kQSlots]
+    BAR_Q_EMPTY = BAR_Q_FULL + kQSlots,     // [kQSlots]
+    BAR_DO_FULL = BAR_Q_EMPTY + kQSlots,    // [kDSlots]
+    BAR_DO_EMPTY = BAR_DO_FULL + kDSlots,   // [kDSlots]
+    BAR_S_FULL = BAR_DO_EMPTY + kDSlots,
     BAR_DP_FULL,
     BAR_P_FULL,
     BAR_DS_FULL,
@@ -217,7 +228,7 @@ enum {
 };
 constexpr int kOffSched = kOffBar + BAR_COUNT * 8;
 constexpr int kOffMisc = kOffSched + kSched * 4;
-constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+constexpr int kSmemBytes = kOffMisc + 16;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Plan {
@@ -271,23 +282,23 @@ __device__ bool producer(const BwdParams& p, uint8_t* smem, uint64_t* bar, volat
         load_tile_pair(&p.tm_v, smem + kOffV, &bar[BAR_V_FULL], pl.kvh, pl.k0, pl.b);
         ++kv_cnt;
         for (int u = 0; u < pl.ntiles; ++u) {
-            const uint32_t st = g % 2, ph = (g / 2) & 1u;
-            if (!mbar_wait_w(&bar[BAR_QD_EMPTY + st], ph ^ 1u, abort_flag, p.err)) return false;
             const Tile t = tile_of(pl, u);
-            uint64_t* fb = &bar[BAR_QD_FULL + st];
-            mbar_arrive_expect_tx_w(fb, 2 * kTileBytes + 2 * kRowBytes + (t.far ? kRowBytes : 0));
-            load_tile_pair(t.far ? &p.tm_qc : &p.tm_q, smem + kOffQ + st * kTileBytes, fb, t.h,
-                           t.row0, pl.b);
-            load_tile_pair(t.far ? &p.tm_doc : &p.tm_do, smem + kOffDO + st * kTileBytes, fb, t.h,
+            const uint32_t qs = g % kQSlots, qph = (g / kQSlots) & 1u;
+            if (!mbar_wait_w(&bar[BAR_Q_EMPTY + qs], qph ^ 1u, abort_flag, p.err)) return false;
+            mbar_arrive_expect_tx_w(&bar[BAR_Q_FULL + qs], kTileBytes);
+            load_tile_pair(t.far ? &p.tm_qc : &p.tm_q, smem + kOffQ + qs * kTileBytes,
+                           &bar[BAR_Q_FULL + qs], t.h, t.row0, pl.b);
+            const uint32_t ds = g % kDSlots, dph = (g / kDSlots) & 1u;
+            if (!mbar_wait_w(&bar[BAR_DO_EMPTY + ds], dph ^ 1u, abort_flag, p.err)) return false;
+            uint64_t* fb = &bar[BAR_DO_FULL + ds];
+            mbar_arrive_expect_tx_w(fb, kTileBytes + 2 * kRowBytes);
+            load_tile_pair(t.far ? &p.tm_doc : &p.tm_do, smem + kOffDO + ds * kTileBytes, fb, t.h,
                            t.row0, pl.b);
             const size_t stat = ((size_t)pl.b * p.Hq + t.h) * p.Npad + t.row0;
-            bulk_load_w(smem + kOffL + st * kRowBytes, (t.far ? p.l_far : p.l_band) + stat,
+            bulk_load_w(smem + kOffL + ds * kRowBytes, (t.far ? p.l_far : p.l_band) + stat,
                         kRowBytes, fb);
-            bulk_load_w(smem + kOffD + st * kRowBytes, (t.far ? p.d_far : p.d_band) + stat,
+            bulk_load_w(smem + kOffD + ds * kRowBytes, (t.far ? p.d_far : p.d_band) + stat,
                         kRowBytes, fb);
-            if (t.far)
-                bulk_load_w(smem + kOffR + st * kRowBytes, p.rowidx + (size_t)pl.b * p.Npad + t.row0,
-                            kRowBytes, fb);
             ++g;
         }
     }
@@ -300,19 +311,29 @@ __device__ bool mma_issuer(const BwdParams& p, uint8_t* smem, uint64_t* bar, vol
     const uint32_t sK = smem_u32(smem + kOffK), sV = smem_u32(smem + kOffV);
     uint32_t g = 0, kv_cnt = 0, acc_cnt = 0;
 
-    auto issue_s = [&](uint32_t st) {   // S^T = K Q^T
-        const uint32_t sQ = smem_u32(smem + kOffQ + st * kTileBytes);
+    // Tile c (a running count over items): query slot c % kQSlots, dO slot
+    // c % kDSlots.
+    auto issue_s = [&](uint32_t c) -> bool {   // S^T = K Q^T
+        const uint32_t qs = c % kQSlots;
+        if (!mbar_wait_w(&bar[BAR_Q_FULL + qs], (c / kQSlots) & 1u, abort_flag, p.err)) return false;
+        tc_fence_after();
+        const uint32_t sQ = smem_u32(smem + kOffQ + qs * kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < kHD / 16; ++kk)
             umma_bf16_w(tS, kmajor_desc(sK, kk), kmajor_desc(sQ, kk), kIdescSS, kk > 0 ? 1u : 0u);
         umma_commit_w(&bar[BAR_S_FULL]);
+        return true;
     };
-    auto issue_dp = [&](uint32_t st) {   // dP^T = V dO^T
-        const uint32_t sD = smem_u32(smem + kOffDO + st * kTileBytes);
+    auto issue_dp = [&](uint32_t c) -> bool {   // dP^T = V dO^T
+        const uint32_t ds = c % kDSlots;
+        if (!mbar_wait_w(&bar[BAR_DO_FULL + ds], (c / kDSlots) & 1u, abort_flag, p.err)) return false;
+        tc_fence_after();
+        const uint32_t sD = smem_u32(smem + kOffDO + ds * kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < kHD / 16; ++kk)
             umma_bf16_w(tDP, kmajor_desc(sV, kk), kmajor_desc(sD, kk), kIdescSS, kk > 0 ? 1u : 0u);
         umma_commit_w(&bar[BAR_DP_FULL]);
+        return true;
     };
 
     for (int k = 0;; ++k) {
@@ -325,40 +346,39 @@ __device__ bool mma_issuer(const BwdParams& p, uint8_t* smem, uint64_t* bar, vol
         if (!mbar_wait_w(&bar[BAR_K_FULL], kv_cnt & 1u, abort_flag, p.err)) return false;
         if (!mbar_wait_w(&bar[BAR_V_FULL], kv_cnt & 1u, abort_flag, p.err)) return false;
         ++kv_cnt;
-        if (!mbar_wait_w(&bar[BAR_QD_FULL + g % 2], (g / 2) & 1u, abort_flag, p.err)) return false;
-        tc_fence_after();
-        issue_s(g % 2);
+        if (!issue_s(g)) return false;
         if (T == 1) umma_commit_w(&bar[BAR_K_EMPTY]);
-        issue_dp(g % 2);
+        if (!issue_dp(g)) return false;
         if (T == 1) umma_commit_w(&bar[BAR_V_EMPTY]);
         for (int t = 0; t < T; ++t) {
-            const uint32_t cur = g + t, st = cur % 2, nst = (cur + 1) % 2;
+            const uint32_t cur = g + t;
             if (!mbar_wait_w(&bar[BAR_P_FULL], cur & 1u, abort_flag, p.err)) return false;
             if (t == 0 && !mbar_wait_w(&bar[BAR_ACC_FREE], (acc_cnt & 1u) ^ 1u, abort_flag, p.err))
                 return false;
             tc_fence_after();
-            const uint32_t sD = smem_u32(smem + kOffDO + st * kTileBytes);
+            const uint32_t sD = smem_u32(smem + kOffDO + (cur % kDSlots) * kTileBytes);
 #pragma unroll
             for (int kk = 0; kk < kBM / 16; ++kk)   // dV += P^T dO
                 umma_bf16_ts_w(tDV, tS + packed_col(kk), mnmajor_desc(sD, kk), kIdescTS,
                                (t > 0 || kk > 0) ? 1u : 0u);
             if (t + 1 < T) {
-                if (!mbar_wait_w(&bar[BAR_QD_FULL + nst], ((cur + 1) / 2) & 1u, abort_flag, p.err))
-                    return false;
-                tc_fence_after();
-                issue_s(nst);
+                if (!issue_s(cur + 1)) return false;
                 if (t + 2 == T) umma_commit_w(&bar[BAR_K_EMPTY]);
             }
             if (!mbar_wait_w(&bar[BAR_DS_FULL], cur & 1u, abort_flag, p.err)) return false;
             tc_fence_after();
-            const uint32_t sQ = smem_u32(smem + kOffQ + st * kTileBytes);
+            const uint32_t sQ = smem_u32(smem + kOffQ + (cur % kQSlots) * kTileBytes);
 #pragma unroll
             for (int kk = 0; kk < kBM / 16; ++kk)   // dK += dS^T Q
                 umma_bf16_ts_w(tDK, tDP + packed_col(kk), mnmajor_desc(sQ, kk), kIdescTS,
                                (t > 0 || kk > 0) ? 1u : 0u);
-            umma_commit_w(&bar[BAR_QD_EMPTY + st]);
+            // Both slots of tile cur are free once these MMAs are done: the
+            // softmax warps finished with the dO slot's lse and D before
+            // signalling DS_FULL.
+            umma_commit_w(&bar[BAR_Q_EMPTY + cur % kQSlots]);
+            umma_commit_w(&bar[BAR_DO_EMPTY + cur % kDSlots]);
             if (t + 1 < T) {
-                issue_dp(nst);
+                if (!issue_dp(cur + 1)) return false;
                 if (t + 2 == T) umma_commit_w(&bar[BAR_V_EMPTY]);
             }
         }
@@ -387,9 +407,10 @@ __device__ bool softmax_role(const BwdParams& p, uint8_t* smem, uint64_t* bar, v
         const int j = pl.k0 + r;   // this thread's key
         const int R = p.routed_count[pl.b];
         for (int u = 0; u < pl.ntiles; ++u) {
-            const uint32_t cur = g + u, st = cur % 2;
+            const uint32_t cur = g + u, st = cur % kDSlots;
             const Tile t = tile_of(pl, u);
-            if (!mbar_wait_w(&bar[BAR_QD_FULL + st], (cur / 2) & 1u, abort_flag, p.err)) return false;
+            if (!mbar_wait_w(&bar[BAR_DO_FULL + st], (cur / kDSlots) & 1u, abort_flag, p.err))
+                return false;
             const float* sL = reinterpret_cast<const float*>(smem + kOffL + st * kRowBytes) + c0;
             const float* sD = reinterpret_cast<const float*>(smem + kOffD + st * kRowBytes) + c0;
             // Visible columns [a, e] of this key: band tiles hold rows
@@ -400,18 +421,34 @@ __device__ bool softmax_role(const BwdParams& p, uint8_t* smem, uint64_t* bar, v
                 a = j - t.row0;
                 e = min(j - t.row0 + p.W - 1, p.N - 1 - t.row0);
             } else {
-                const int* sR = reinterpret_cast<const int*>(smem + kOffR + st * kRowBytes);
+                // Compacted rows ascend; the columns that see key j are those
+                // with row >= j + W among the nvalid real ones.  A tile whose
+                // first row is at least (last key of the block) + W is wholly
+                // visible; otherwise every thread counts the rows below its
+                // target, the tile's 128 row indices spread 4 per lane.
+                const int* gR = p.rowidx + (size_t)pl.b * p.Npad + t.row0;
                 const int nvalid = min(kBM, R - t.row0);
-                const int target = j + p.W;
-                int pos = 0;   // columns of [0, nvalid) whose row is < target (rows ascend)
-#pragma unroll
-                for (int step = 64; step > 0; step >>= 1) {
-                    const int c = pos + step - 1;
-                    if (c < nvalid && sR[c] < target) pos += step;
-                }
-                if (pos < nvalid && sR[pos] < target) ++pos;   // the 128th column
-                a = pos;
                 e = nvalid - 1;
+                if (nvalid == kBM && gR[0] >= pl.k0 + kBN - 1 + p.W) {
+                    a = 0;
+                } else {
+                    const int4 v4 = reinterpret_cast<const int4*>(gR)[lane];
+                    const int cb = 4 * lane;
+                    const int v0 = cb + 0 < nvalid ? v4.x : INT_MAX;
+                    const int v1 = cb + 1 < nvalid ? v4.y : INT_MAX;
+                    const int v2 = cb + 2 < nvalid ? v4.z : INT_MAX;
+                    const int v3 = cb + 3 < nvalid ? v4.w : INT_MAX;
+                    const int target = j + p.W;
+                    int cnt = 0;
+#pragma unroll 4
+                    for (int src = 0; src < 32; ++src) {
+                        cnt += __shfl_sync(0xffffffffu, v0, src) < target;
+                        cnt += __shfl_sync(0xffffffffu, v1, src) < target;
+                        cnt += __shfl_sync(0xffffffffu, v2, src) < target;
+                        cnt += __shfl_sync(0xffffffffu, v3, src) < target;
+                    }
+                    a = cnt;
+                }
             }
             const bool full = __all_sync(0xffffffffu, a <= c0 && e >= c0 + 63);
 
@@ -493,9 +530,12 @@ __device__ bool softmax_role(const BwdParams& p, uint8_t* smem, uint64_t* bar, v
 }
 
 __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant__ BwdParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                               ~static_cast<uintptr_t>(1023));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    if (smem_u32(smem_raw) & 1023u) {   // operand tiles need 1024-byte alignment
+        if (threadIdx.x == 0) atomicOr(p.err, kDevErrLayout);
+        return;
+    }
+    uint8_t* smem = smem_raw;
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kOffBar);
     volatile int* sched = reinterpret_cast<volatile int*>(smem + kOffSched);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
@@ -507,9 +547,13 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
         mbar_init(&bar[BAR_K_EMPTY], 1);
         mbar_init(&bar[BAR_V_FULL], 1);
         mbar_init(&bar[BAR_V_EMPTY], 1);
-        for (int st = 0; st < 2; ++st) {
-            mbar_init(&bar[BAR_QD_FULL + st], 1);
-            mbar_init(&bar[BAR_QD_EMPTY + st], 1);
+        for (int st = 0; st < kQSlots; ++st) {
+            mbar_init(&bar[BAR_Q_FULL + st], 1);
+            mbar_init(&bar[BAR_Q_EMPTY + st], 1);
+        }
+        for (int st = 0; st < kDSlots; ++st) {
+            mbar_init(&bar[BAR_DO_FULL + st], 1);
+            mbar_init(&bar[BAR_DO_EMPTY + st], 1);
         }
         mbar_init(&bar[BAR_S_FULL], 1);
         mbar_init(&bar[BAR_DP_FULL], 1);
@@ -552,7 +596,8 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
         __syncwarp();
         uint32_t g = 0, kv_cnt = 0;
         if (!producer(p, smem, bar, sched, abort_flag, g, kv_cnt)) {
-            drain2(&bar[BAR_QD_FULL], g);
+            drain_ring(&bar[BAR_Q_FULL], kQSlots, g);
+            drain_ring(&bar[BAR_DO_FULL], kDSlots, g);
             if (kv_cnt) {
                 mbar_drain(&bar[BAR_K_FULL], (kv_cnt - 1) & 1u);
                 mbar_drain(&bar[BAR_V_FULL], (kv_cnt - 1) & 1u);
@@ -579,18 +624,24 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
 // ====================================================================== dQ ==
 namespace dqk {
 
+// Key tiles live from S(j) to dQ += dS(j) K(j), value tiles only until dP(j):
+// three key slots and two value slots keep the loads a block and more ahead.
+constexpr int kKSlots = 3;
+constexpr int kVSlots = 2;
 constexpr int kOffQ = 0;
 constexpr int kOffDO = kOffQ + kTileBytes;
-constexpr int kOffK = kOffDO + kTileBytes;       // [2] key tiles
-constexpr int kOffV = kOffK + 2 * kTileBytes;    // [2] value tiles
-constexpr int kOffBar = kOffV + 2 * kTileBytes;
+constexpr int kOffK = kOffDO + kTileBytes;              // [kKSlots] key tiles
+constexpr int kOffV = kOffK + kKSlots * kTileBytes;     // [kVSlots] value tiles
+constexpr int kOffBar = kOffV + kVSlots * kTileBytes;
 
 enum {
     BAR_Q_FULL = 0,
     BAR_Q_EMPTY,
-    BAR_KV_FULL,                       // [2]
-    BAR_KV_EMPTY = BAR_KV_FULL + 2,    // [2]
-    BAR_S_FULL = BAR_KV_EMPTY + 2,     // [2] one per S buffer
+    BAR_K_FULL,                            // [kKSlots]
+    BAR_K_EMPTY = BAR_K_FULL + kKSlots,    // [kKSlots]
+    BAR_V_FULL = BAR_K_EMPTY + kKSlots,    // [kVSlots]
+    BAR_V_EMPTY = BAR_V_FULL + kVSlots,    // [kVSlots]
+    BAR_S_FULL = BAR_V_EMPTY + kVSlots,    // [2] one per S buffer
     BAR_DP_FULL = BAR_S_FULL + 2,
     BAR_DS_FULL,
     BAR_ACC_FULL,
@@ -641,13 +692,16 @@ __device__ bool producer(const BwdParams& p, uint8_t* smem, uint64_t* bar, volat
                        pl.row0, pl.b);
         ++q_cnt;
         for (int j = 0; j < pl.nblk; ++j) {
-            const uint32_t st = g % 2, ph = (g / 2) & 1u;
-            if (!mbar_wait_w(&bar[BAR_KV_EMPTY + st], ph ^ 1u, abort_flag, p.err)) return false;
-            mbar_arrive_expect_tx_w(&bar[BAR_KV_FULL + st], 2 * kTileBytes);
             const int key0 = pl.kv0 + j * kBN;
-            load_tile_pair(&p.tm_k, smem + kOffK + st * kTileBytes, &bar[BAR_KV_FULL + st], pl.kvh,
+            const uint32_t ks = g % kKSlots, kph = (g / kKSlots) & 1u;
+            if (!mbar_wait_w(&bar[BAR_K_EMPTY + ks], kph ^ 1u, abort_flag, p.err)) return false;
+            mbar_arrive_expect_tx_w(&bar[BAR_K_FULL + ks], kTileBytes);
+            load_tile_pair(&p.tm_k, smem + kOffK + ks * kTileBytes, &bar[BAR_K_FULL + ks], pl.kvh,
                            key0, pl.b);
-            load_tile_pair(&p.tm_v, smem + kOffV + st * kTileBytes, &bar[BAR_KV_FULL + st], pl.kvh,
+            const uint32_t vs = g % kVSlots, vph = (g / kVSlots) & 1u;
+            if (!mbar_wait_w(&bar[BAR_V_EMPTY + vs], vph ^ 1u, abort_flag, p.err)) return false;
+            mbar_arrive_expect_tx_w(&bar[BAR_V_FULL + vs], kTileBytes);
+            load_tile_pair(&p.tm_v, smem + kOffV + vs * kTileBytes, &bar[BAR_V_FULL + vs], pl.kvh,
                            key0, pl.b);
             ++g;
         }
@@ -661,20 +715,31 @@ __device__ bool mma_issuer(const BwdParams& p, uint8_t* smem, uint64_t* bar, vol
     const uint32_t sQ = smem_u32(smem + kOffQ), sDO = smem_u32(smem + kOffDO);
     uint32_t g = 0, q_cnt = 0, acc_cnt = 0;
 
-    auto issue_s = [&](uint32_t slot, uint32_t buf) {   // S = Q K^T into S buffer buf
-        const uint32_t sK = smem_u32(smem + kOffK + slot * kTileBytes);
+    // Block c (a running count over items): key slot c % kKSlots, value slot
+    // c % kVSlots, S buffer c % 2.
+    auto issue_s = [&](uint32_t c) -> bool {   // S = Q K^T
+        const uint32_t ks = c % kKSlots, buf = c % 2;
+        if (!mbar_wait_w(&bar[BAR_K_FULL + ks], (c / kKSlots) & 1u, abort_flag, p.err)) return false;
+        tc_fence_after();
+        const uint32_t sK = smem_u32(smem + kOffK + ks * kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < kHD / 16; ++kk)
             umma_bf16_w(tmem + 128 * buf, kmajor_desc(sQ, kk), kmajor_desc(sK, kk), kIdescSS,
                         kk > 0 ? 1u : 0u);
         umma_commit_w(&bar[BAR_S_FULL + buf]);
+        return true;
     };
-    auto issue_dp = [&](uint32_t slot) {   // dP = dO V^T
-        const uint32_t sV = smem_u32(smem + kOffV + slot * kTileBytes);
+    auto issue_dp = [&](uint32_t c) -> bool {   // dP = dO V^T, then the value slot is free
+        const uint32_t vs = c % kVSlots;
+        if (!mbar_wait_w(&bar[BAR_V_FULL + vs], (c / kVSlots) & 1u, abort_flag, p.err)) return false;
+        tc_fence_after();
+        const uint32_t sV = smem_u32(smem + kOffV + vs * kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < kHD / 16; ++kk)
             umma_bf16_w(tDP, kmajor_desc(sDO, kk), kmajor_desc(sV, kk), kIdescSS, kk > 0 ? 1u : 0u);
         umma_commit_w(&bar[BAR_DP_FULL]);
+        umma_commit_w(&bar[BAR_V_EMPTY + vs]);
+        return true;
     };
 
     for (int k = 0;; ++k) {
@@ -686,29 +751,22 @@ __device__ bool mma_issuer(const BwdParams& p, uint8_t* smem, uint64_t* bar, vol
         const int n = pl.nblk;
         if (!mbar_wait_w(&bar[BAR_Q_FULL], q_cnt & 1u, abort_flag, p.err)) return false;
         ++q_cnt;
-        if (!mbar_wait_w(&bar[BAR_KV_FULL + g % 2], (g / 2) & 1u, abort_flag, p.err)) return false;
-        tc_fence_after();
-        issue_s(g % 2, g % 2);
-        issue_dp(g % 2);
+        if (!issue_s(g) || !issue_dp(g)) return false;
         for (int j = 0; j < n; ++j) {
-            const uint32_t cur = g + j, slot = cur % 2, nxt = (cur + 1) % 2;
-            if (j + 1 < n) {
-                if (!mbar_wait_w(&bar[BAR_KV_FULL + nxt], ((cur + 1) / 2) & 1u, abort_flag, p.err))
-                    return false;
-                tc_fence_after();
-                issue_s(nxt, nxt);
-            }
+            const uint32_t cur = g + j;
+            if (j + 1 < n && !issue_s(cur + 1)) return false;
             if (!mbar_wait_w(&bar[BAR_DS_FULL], cur & 1u, abort_flag, p.err)) return false;
             if (j == 0 && !mbar_wait_w(&bar[BAR_ACC_FREE], (acc_cnt & 1u) ^ 1u, abort_flag, p.err))
                 return false;
             tc_fence_after();
-            if (j + 1 < n) issue_dp(nxt);
-            const uint32_t sK = smem_u32(smem + kOffK + slot * kTileBytes);
+            if (j + 1 < n && !issue_dp(cur + 1)) return false;
+            const uint32_t ks = cur % kKSlots;
+            const uint32_t sK = smem_u32(smem + kOffK + ks * kTileBytes);
 #pragma unroll
             for (int kk = 0; kk < kBN / 16; ++kk)   // dQ += dS K
-                umma_bf16_ts_w(tDQ, tmem + 128 * slot + packed_col(kk), mnmajor_desc(sK, kk),
+                umma_bf16_ts_w(tDQ, tmem + 128 * (cur % 2) + packed_col(kk), mnmajor_desc(sK, kk),
                                kIdescTS, (j > 0 || kk > 0) ? 1u : 0u);
-            umma_commit_w(&bar[BAR_KV_EMPTY + slot]);
+            umma_commit_w(&bar[BAR_K_EMPTY + ks]);
         }
         umma_commit_w(&bar[BAR_ACC_FULL]);
         umma_commit_w(&bar[BAR_Q_EMPTY]);
@@ -821,11 +879,15 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__
     if (threadIdx.x == 0) {
         mbar_init(&bar[BAR_Q_FULL], 1);
         mbar_init(&bar[BAR_Q_EMPTY], 1);
-        for (int st = 0; st < 2; ++st) {
-            mbar_init(&bar[BAR_KV_FULL + st], 1);
-            mbar_init(&bar[BAR_KV_EMPTY + st], 1);
-            mbar_init(&bar[BAR_S_FULL + st], 1);
+        for (int st = 0; st < kKSlots; ++st) {
+            mbar_init(&bar[BAR_K_FULL + st], 1);
+            mbar_init(&bar[BAR_K_EMPTY + st], 1);
         }
+        for (int st = 0; st < kVSlots; ++st) {
+            mbar_init(&bar[BAR_V_FULL + st], 1);
+            mbar_init(&bar[BAR_V_EMPTY + st], 1);
+        }
+        for (int st = 0; st < 2; ++st) mbar_init(&bar[BAR_S_FULL + st], 1);
         mbar_init(&bar[BAR_DP_FULL], 1);
         mbar_init(&bar[BAR_DS_FULL], kSoftmaxThreads);
         mbar_init(&bar[BAR_ACC_FULL], 1);
@@ -865,7 +927,8 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__
         __syncwarp();
         uint32_t g = 0, q_cnt = 0;
         if (!producer(p, smem, bar, sched, abort_flag, g, q_cnt)) {
-            drain2(&bar[BAR_KV_FULL], g);
+            drain_ring(&bar[BAR_K_FULL], kKSlots, g);
+            drain_ring(&bar[BAR_V_FULL], kVSlots, g);
             if (q_cnt) mbar_drain(&bar[BAR_Q_FULL], (q_cnt - 1) & 1u);
         }
         __syncwarp();

@@ -13,7 +13,7 @@ namespace swi {
 namespace {
 
 // Device error word: kernels OR kDevErrTimeout into it when a bounded wait
-// expires.  Host code reaches it through cudaGetSymbolAddress, once per device.
+// expires, kDevErrLayout when their shared memory is not laid out as needed.  Host code reaches it through cudaGetSymbolAddress, once per device.
 __device__ unsigned int g_device_error;
 
 constexpr int kMaxDevices = 64;
@@ -147,7 +147,8 @@ int swiattn_get_device_error(void* stream) {
         if (cudaMemcpy(di.err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
             return SWIATTN_ECUDA;
     }
-    return (host & kDevErrTimeout) ? SWIATTN_ETIMEOUT : SWIATTN_OK;
+    if (host & kDevErrTimeout) return SWIATTN_ETIMEOUT;
+    return host ? SWIATTN_ECUDA : SWIATTN_OK;
 }
 
 int swiattn_route(const void* h, const void* w, float bias, int64_t tokens, int d_model, int dtype,

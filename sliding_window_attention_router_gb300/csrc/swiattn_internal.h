@@ -10,6 +10,7 @@ namespace swi {
 
 // Device error word bits (OR-ed by kernels, read by swiattn_get_device_error).
 constexpr unsigned int kDevErrTimeout = 1u;
+constexpr unsigned int kDevErrLayout = 2u;   // shared memory not laid out as a kernel requires
 
 // A healthy wait in these kernels lasts microseconds; after this long a
 // kernel gives up, flags a timeout and returns.
