@@ -20,8 +20,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libswiattn.so")
 
-SOURCES = ["swiattn_api.cu", "route.cu", "schedule.cu", "attn_tc.cu", "attn_prefill.cu", "attn_simt.cu", "decode.cu",
-           "bwd_schedule.cu", "attn_bwd.cu", "bwd_simt.cu"]
+SOURCES = ["swiattn_api.cu", "route.cu", "schedule.cu", "attn_prefill.cu", "attn_simt.cu", "decode.cu",
+           "bwd_schedule.cu", "attn_bwd.cu", "bwd_simt.cu", "attn_dual.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "-I", INCLUDE, "-I", CSRC]

@@ -98,11 +98,14 @@ bool make_tmap_4d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t
 }
 
 DualWs dual_ws_layout(int B, int N, int Hq, int d, int dtype) {
+    auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
     DualWs L;
-    L.mse_part = 0;
-    L.total = dtype == SWIATTN_BF16 ? sizeof(float) * (size_t)B * N * Hq : 0;
-    L.total = (L.total + 255) & ~static_cast<size_t>(255);
-    (void)d;
+    L.mse_part = L.snap = L.counter = L.total = 0;
+    if (dtype != SWIATTN_BF16) return L;
+    const size_t rows = (size_t)B * N * Hq;
+    L.snap = up(sizeof(float) * rows);
+    L.counter = up(L.snap + sizeof(float) * rows * (size_t)d);
+    L.total = up(L.counter + sizeof(int));
     return L;
 }
 
@@ -288,15 +291,15 @@ int swiattn_dual_branch(const void* q, const void* k, const void* v, const float
     a.o_swa = o_swa;
     a.o_gated = o_gated;
     a.mse_part = part;
+    a.snap = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.snap);
+    a.counter = reinterpret_cast<int*>(static_cast<char*>(workspace) + L.counter);
     a.B = B;
     a.N = N;
     a.Hq = Hq;
     a.Hkv = Hkv;
     a.W = W;
     a.scale = scale;
-    prof_start(s);
-    cudaError_t e = launch_tc_attention(a, di.err, di.sms, s);
-    prof_stop(s);
+    cudaError_t e = launch_dual_tc(a, di.err, di.sms, s);
     if (e == cudaSuccess)
         e = launch_dual_epilogue_parts(part, logits, nll, mse, gamma, reg_loss, B, N, Hq,
                                        gamma_base, eps, alpha, s);

@@ -53,6 +53,8 @@ DecodeWs decode_ws_layout(int B, int Lmax, int Hq, int d);
 
 struct DualWs {
     size_t mse_part;  // float [B*N*Hq]
+    size_t snap;      // float [B*N*Hq*128] O_SWA rows, fp32 (tensor-core path)
+    size_t counter;   // int32 work counter
     size_t total;
 };
 DualWs dual_ws_layout(int B, int N, int Hq, int d, int dtype);
@@ -81,12 +83,15 @@ struct TcAttnArgs {
     void* o_gated;         // dual, nullable
     float* lse;            // prefill, nullable
     float* mse_part;       // dual
+    float* snap;           // dual: fp32 O_SWA rows
+    int* counter;          // dual: work counter (zeroed by the launcher)
     int B, N, Hq, Hkv, W;
     float scale;
 };
-// Dual-branch forward (q, k, v, logits, o = O_FULL, o_swa, o_gated, mse_part).
-cudaError_t launch_tc_attention(const TcAttnArgs& a, unsigned int* err, int num_sms,
-                                cudaStream_t s);
+
+// Dual-branch forward, two query tiles per CTA (the launcher records the
+// profile events around the kernel itself).
+cudaError_t launch_dual_tc(const TcAttnArgs& a, unsigned int* err, int num_sms, cudaStream_t s);
 
 // Routed prefill, two query tiles per CTA (work items from launch_schedule).
 cudaError_t launch_prefill_tc(const TcAttnArgs& a, const int* tile_prefix, unsigned int* err,
