@@ -31,45 +31,56 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 
-// <a, b> over one 128-element bf16 row, one warp (4 elements per lane).
-__device__ __forceinline__ float row_dot_bf16(const __nv_bfloat16* a, const __nv_bfloat16* b,
-                                              int lane) {
-    const uint2 ua = reinterpret_cast<const uint2*>(a)[lane];
-    const uint2 ub = reinterpret_cast<const uint2*>(b)[lane];
-    const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&ua);
-    const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&ub);
-    const float2 a0 = __bfloat1622float2(pa[0]), a1 = __bfloat1622float2(pa[1]);
-    const float2 b0 = __bfloat1622float2(pb[0]), b1 = __bfloat1622float2(pb[1]);
-    float acc = a0.x * b0.x + a0.y * b0.y + a1.x * b1.x + a1.y * b1.y;
+// <a, b> of 8 bf16 pairs held in two 16-byte words.
+__device__ __forceinline__ float dot8_bf16(const uint4& a, const uint4& b) {
+    const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+    float acc = 0.f;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    for (int t = 0; t < 4; ++t) {
+        const float2 x = __bfloat1622float2(pa[t]), y = __bfloat1622float2(pb[t]);
+        acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
+    }
     return acc;
 }
 
-// Band statistics, one warp per (b, i, h) with i < Npad (h fastest, so a
-// warp group reads whole contiguous token rows).
+// Band statistics.  One warp per token (b, i): its Hq head rows are one
+// contiguous run, a row of 128 bf16 being 16 lanes x 16 bytes, so the warp
+// covers two rows per step and issues every load of the token before the
+// half-warp reductions.
+constexpr int kMaxHeadPairs = 8;   // 16 heads per pass; more heads take more passes
 __global__ void __launch_bounds__(256) bwd_rowstats_kernel(
     const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ d_o,
     const float* __restrict__ lse, int B, int N, int Npad, int Hq, float* __restrict__ d_band,
     float* __restrict__ l_band) {
-    const int lane = threadIdx.x & 31;
-    const size_t nrows = (size_t)B * Npad * Hq;
-    const size_t stride = (size_t)gridDim.x * (blockDim.x >> 5);
-    for (size_t w = (size_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < nrows;
-         w += stride) {
-        const int h = (int)(w % Hq);
-        const size_t bi = w / Hq;
-        const int i = (int)(bi % Npad), b = (int)(bi / Npad);
-        float dd = 0.f, ll = 0.f;
-        if (i < N) {
-            const size_t row = ((size_t)b * N + i) * Hq + h;
-            dd = row_dot_bf16(d_o + row * kHD, o + row * kHD, lane);
-            ll = lse[row] * kLog2e;
-        }
-        if (lane == 0) {
-            const size_t dst = ((size_t)b * Hq + h) * Npad + i;
-            d_band[dst] = dd;
-            l_band[dst] = ll;
+    const int lane = threadIdx.x & 31, half = lane >> 4, sub = lane & 15;
+    const unsigned tokens = (unsigned)B * (unsigned)Npad;
+    const unsigned stride = gridDim.x * (blockDim.x >> 5);
+    for (unsigned t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < tokens; t += stride) {
+        const int b = (int)(t / (unsigned)Npad), i = (int)(t % (unsigned)Npad);
+        const bool in = i < N;
+        const size_t row0 = ((size_t)b * N + i) * Hq;   // first head row of the token
+        for (int h0 = 0; h0 < Hq; h0 += 2 * kMaxHeadPairs) {
+            uint4 va[kMaxHeadPairs], vb[kMaxHeadPairs];
+#pragma unroll
+            for (int u = 0; u < kMaxHeadPairs; ++u) {
+                const int h = h0 + 2 * u + half;
+                const bool ok = in && h < Hq;
+                va[u] = ok ? reinterpret_cast<const uint4*>(d_o + (row0 + h) * kHD)[sub] : make_uint4(0, 0, 0, 0);
+                vb[u] = ok ? reinterpret_cast<const uint4*>(o + (row0 + h) * kHD)[sub] : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < kMaxHeadPairs; ++u) {
+                float acc = dot8_bf16(va[u], vb[u]);
+#pragma unroll
+                for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+                const int h = h0 + 2 * u + half;
+                if (sub == 0 && h < Hq) {
+                    const size_t dst = ((size_t)b * Hq + h) * Npad + i;
+                    d_band[dst] = acc;
+                    l_band[dst] = in ? lse[row0 + h] * kLog2e : 0.f;
+                }
+            }
         }
     }
 }
@@ -228,32 +239,41 @@ __global__ void __launch_bounds__(kBuildThreads) bwd_build_gather_kernel(
             items_q, &counters[2], &counters[3]);
         return;
     }
-    const int lane = threadIdx.x & 31;
+    // Far rows: half a warp per (compacted row, head), 16 bytes per lane.  The
+    // loop runs per warp (both halves the same trip count), so the half-warp
+    // reductions below are reached by every lane.
+    const int lane = threadIdx.x & 31, half = lane >> 4, sub = lane & 15;
     const size_t warps = (size_t)(gridDim.x - 2) * (blockDim.x >> 5);
     const size_t w0 = (size_t)(blockIdx.x - 2) * (blockDim.x >> 5) + (threadIdx.x >> 5);
     for (int b = 0; b < B; ++b) {
         const int R = routed_count[b];
-        const int Rp = cdiv(R, kBM) * kBM;
-        for (size_t w = w0; w < (size_t)Rp * Hq; w += warps) {
+        const size_t total = (size_t)cdiv(R, kBM) * kBM * Hq;   // (row, head) pairs to write
+        for (size_t ww = w0; 2 * ww < total; ww += warps) {
+            const size_t w = 2 * ww + half;
+            const bool live = w < total;
             const int r = (int)(w / Hq), h = (int)(w % Hq);
-            const size_t dst = ((size_t)b * Npad + r) * Hq + h;
-            uint2 vq = make_uint2(0u, 0u), vd = make_uint2(0u, 0u);
-            float dd = 0.f, ll = 0.f;
+            uint4 vq = make_uint4(0u, 0u, 0u, 0u), vd = vq, vo = vq;
             int i = kNoRow;
-            if (r < R) {
+            size_t src = 0;
+            if (live && r < R) {
                 i = routed_list[(size_t)b * N + r];
-                const size_t src = ((size_t)b * N + i) * Hq + h;
-                vq = reinterpret_cast<const uint2*>(q + src * kHD)[lane];
-                vd = reinterpret_cast<const uint2*>(d_o + src * kHD)[lane];
-                dd = row_dot_bf16(d_o + src * kHD, o + src * kHD, lane);
-                ll = lse[src] * kLog2e;
+                src = ((size_t)b * N + i) * Hq + h;
+                vq = reinterpret_cast<const uint4*>(q + src * kHD)[sub];
+                vd = reinterpret_cast<const uint4*>(d_o + src * kHD)[sub];
+                vo = reinterpret_cast<const uint4*>(o + src * kHD)[sub];
             }
-            reinterpret_cast<uint2*>(qc + dst * kHD)[lane] = vq;
-            reinterpret_cast<uint2*>(doc + dst * kHD)[lane] = vd;
-            if (lane == 0) {
-                d_far[((size_t)b * Hq + h) * Npad + r] = dd;
-                l_far[((size_t)b * Hq + h) * Npad + r] = ll;
-                if (h == 0) rowidx[(size_t)b * Npad + r] = i;
+            float acc = dot8_bf16(vd, vo);
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            if (live) {
+                const size_t dst = ((size_t)b * Npad + r) * Hq + h;
+                reinterpret_cast<uint4*>(qc + dst * kHD)[sub] = vq;
+                reinterpret_cast<uint4*>(doc + dst * kHD)[sub] = vd;
+                if (sub == 0) {
+                    d_far[((size_t)b * Hq + h) * Npad + r] = acc;
+                    l_far[((size_t)b * Hq + h) * Npad + r] = r < R ? lse[src] * kLog2e : 0.f;
+                    if (h == 0) rowidx[(size_t)b * Npad + r] = i;
+                }
             }
         }
     }
@@ -311,7 +331,7 @@ cudaError_t launch_bwd_schedule(const uint8_t* gate, const void* q, const void* 
     if (e != cudaSuccess) return e;
     const auto* ob = static_cast<const __nv_bfloat16*>(o);
     const auto* dob = static_cast<const __nv_bfloat16*>(d_o);
-    bwd_rowstats_kernel<<<num_sms * 8, 256, 0, s>>>(ob, dob, lse, B, N, L.Npad, Hq,
+    bwd_rowstats_kernel<<<num_sms * 4, 256, 0, s>>>(ob, dob, lse, B, N, L.Npad, Hq,
                                                     reinterpret_cast<float*>(ws + L.d_band),
                                                     reinterpret_cast<float*>(ws + L.l_band));
     e = cudaGetLastError();
