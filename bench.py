@@ -46,8 +46,8 @@ L2_FLUSH_BYTES = 256 << 20
 MEASURED_TRAFFIC = {
     # prefill_kernel, long-context prefill N=32768 f=0.13: 1 082 483 456 read + 132 495 104 written
     ("prefill", "2376c004e3f9ab56"): 1082483456 + 132495104,
-    # decode_split_kernel, 16 x 32768 decode: 654 404 352 read + 2 732 800 written
-    ("decode", "ef5ddd11247ce63e"): 654404352 + 2732800,
+    # decode_split_kernel, 16 x 32768 decode: 654 405 376 read + 2 758 912 written
+    ("decode", "023308e7542f8d17"): 654405376 + 2758912,
 }
 KERNEL_SOURCES = {"prefill": ("attn_prefill.cu", "ptx.cuh"), "decode": ("decode.cu",)}
 
@@ -305,6 +305,39 @@ def decode_section(swa, timer, dev, steps, warmup, seed):
     return dict(step_ms=step_ms, kern_ms=kern_ms, bytes=kv_bytes + qo_bytes, n_routed=n_routed)
 
 
+def decode_paged_section(swa, timer, dev, steps, warmup, seed, page_size=64):
+    """The decode workload on a paged cache: the same 16 x 32768 tokens, pages
+    of page_size tokens placed in a shuffled pool."""
+    B, L, H, D, W = 16, 32768, 16, 128, 1024
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    max_pages = L // page_size
+    num_pages = B * max_pages
+    kp = torch.randn(num_pages, page_size, H, D, generator=g, device=dev,
+                     dtype=torch.float32).to(torch.bfloat16)
+    vp = torch.randn(num_pages, page_size, H, D, generator=g, device=dev,
+                     dtype=torch.float32).to(torch.bfloat16)
+    q = torch.randn(B, H, D, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    table = torch.randperm(num_pages, generator=inp._gen(seed)).to(torch.int32).view(B, max_pages)
+    table = table.to(dev)
+    gate = inp.bernoulli_gates((B,), 0.13, inp._gen(seed)).to(dev)
+    sl = torch.full((B,), L, dtype=torch.int32, device=dev)
+    o = torch.empty_like(q)
+    ws = torch.empty(swa.decode_paged_workspace(B, max_pages, page_size, H, H, D, W, torch.bfloat16),
+                     dtype=torch.uint8, device=dev)
+    n_routed = int(gate.sum())
+    entries = n_routed * L + (B - n_routed) * W
+    nbytes = entries * H * D * 2 * 2 + 2 * B * H * D * 2
+
+    def step():
+        swa.decode_paged(q, kp, vp, table, sl, gate, W, out=o, workspace=ws)
+
+    step_ms, kern_ms = timer.run(step, steps, warmup, kernel_events=True)
+    assert swa.get_device_error() == 0
+    del kp, vp
+    return dict(step_ms=step_ms, kern_ms=kern_ms, bytes=nbytes, n_routed=n_routed)
+
+
 def route_section(swa, timer, dev, steps, warmup, seed):
     T, Dm = 32768, 2048
     r = inp.router_inputs(T, Dm, torch.bfloat16, seed)
@@ -536,6 +569,14 @@ def run_ours(args, dist: Dist):
                          "kernel": "decode_split_kernel"},
             "workload": "decode bf16: 16 sequences x 32768 cached tokens, H=16, d=128, W=1024, "
                         "gate Bernoulli(0.13)"}
+        dp = decode_paged_section(swa, timer, dev, ks, kw, seed=dist.rank)
+        dpk = statistics.mean(dp["kern_ms"]) / 1e3
+        dps = statistics.mean(dp["step_ms"]) / 1e3
+        extra["decode_paged"] = {
+            "gbs": dp["bytes"] / dps / 1e9, "ms_per_step": dps * 1e3, "n_routed": dp["n_routed"],
+            "kernel_gbs": dp["bytes"] / dpk / 1e9, "kernel_frac_of_hbm": dp["bytes"] / dpk / 1e9 / hbm,
+            "workload": "decode bf16 on a paged cache: 16 sequences x 32768 tokens in 64-token "
+                        "pages of a shuffled pool, H=16, d=128, W=1024, gate Bernoulli(0.13)"}
         rt = route_section(swa, timer, dev, ks, kw, seed=dist.rank)
         rs = statistics.mean(rt["step_ms"]) / 1e3
         extra["route"] = {"gbs": rt["bytes"] / rs / 1e9, "ms_per_step": rs * 1e3,

@@ -94,7 +94,9 @@ size_t swiattn_decode_workspace(int B, int Lmax, int Hq, int Hkv, int d, int W, 
  * being the query's own, at position L = seq_lens[b]-1.  The query reads cache
  * entries [max(0, L-W+1), L] if gate[b] == 0, else [0, L].
  * q [B,Hq,d]; k_cache, v_cache [B,Lmax,Hkv,d]; seq_lens int32 [B];
- * gate uint8 [B]; o [B,Hq,d]; lse (nullable) fp32 [B,Hq].
+ * gate uint8 [B]; o [B,Hq,d]; lse (nullable) fp32 [B,Hq].  A seq_lens[b]
+ * outside [1, Lmax] (a device-resident input) is clamped into it and
+ * swiattn_get_device_error then reports SWIATTN_EINVAL.
  * d in {64, 128}; Hkv*d/8 (bf16) or Hkv*d/4 (fp32) <= 1024; Hq/Hkv <= 8.
  * workspace: at least swiattn_decode_workspace(...) bytes, scratch only. */
 int swiattn_decode(const void* q, const void* k_cache, const void* v_cache,
@@ -123,6 +125,32 @@ int swiattn_decode_noalloc(const void* q, const void* k_cache, const void* v_cac
                            const int32_t* seq_lens, const uint8_t* gate, void* o, float* lse,
                            int B, int Lmax, int Hq, int Hkv, int d, int W, float scale, int dtype,
                            void* stream);
+
+/* Bytes of device workspace swiattn_decode_paged needs for these sizes
+ * (0 for invalid sizes). */
+size_t swiattn_decode_paged_workspace(int B, int max_pages, int page_size, int Hq, int Hkv, int d,
+                                      int W, int dtype);
+
+/* swiattn_decode over a paged KV cache (a serving cache layout; the report's
+ * decode, section 2 and 6, reads the last W or all cache entries of each
+ * sequence, whatever their placement).  Token t of sequence b is row
+ * t % page_size of physical page block_table[b * max_pages + t / page_size]
+ * of the pool k_pages, v_pages [num_pages, page_size, Hkv, d].
+ * page_size is a power of two; seq_lens[b] <= max_pages * page_size.  The
+ * block table and seq_lens are device arrays: a table entry the call reads
+ * that lies outside [0, num_pages) is read as page 0, and a seq_lens[b]
+ * outside [1, max_pages * page_size] is clamped into it; either way
+ * swiattn_get_device_error then reports SWIATTN_EINVAL (no out-of-range read
+ * is made).  Entries of pages a call does not visit are not read.  Other arguments, layouts
+ * and results are those of swiattn_decode.  A batched step over several
+ * layers is one call with (layer, sequence) flattened into B (one pool, or
+ * per-layer pools laid end to end with the table entries offset).
+ * workspace: at least swiattn_decode_paged_workspace(...) bytes. */
+int swiattn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                         const int32_t* block_table, const int32_t* seq_lens, const uint8_t* gate,
+                         void* o, float* lse, int B, int max_pages, int page_size, int num_pages,
+                         int Hq, int Hkv, int d, int W, float scale, int dtype, void* workspace,
+                         size_t workspace_bytes, void* stream);
 
 /* Bytes of device workspace swiattn_dual_branch needs for these sizes. */
 size_t swiattn_dual_branch_workspace(int B, int N, int Hq, int Hkv, int d, int W, int dtype);
@@ -204,7 +232,8 @@ int swiattn_route_backward(const void* h, const void* w, const float* logits, co
  * current device: SWIATTN_OK, SWIATTN_ETIMEOUT if a bounded device wait
  * expired since the last query, or SWIATTN_ECUDA if the synchronisation itself
  * failed or a kernel found its shared memory not laid out as it requires (it
- * then returned without computing). */
+ * then returned without computing), or SWIATTN_EINVAL if a kernel met an
+ * out-of-range device-resident input (e.g. a paged-decode block table entry). */
 int swiattn_get_device_error(void* stream);
 
 /* Static, NUL-terminated name of a status code. */

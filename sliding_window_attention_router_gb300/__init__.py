@@ -20,7 +20,8 @@ __all__ = [
     "SwiAttnError", "F32", "BF16", "library_path", "route", "prefill", "decode", "dual_branch",
     "prefill_workspace", "decode_workspace", "dual_branch_workspace", "get_device_error",
     "status_string", "num_sms", "set_profile_events", "EXPORTS", "prefill_backward",
-    "prefill_backward_workspace", "route_backward", "route_backward_workspace",
+    "prefill_backward_workspace", "route_backward", "route_backward_workspace", "decode_paged",
+    "decode_paged_workspace",
 ]
 
 F32, BF16 = 0, 1
@@ -36,6 +37,7 @@ EXPORTS = (
     "swiattn_decode", "swiattn_decode_noalloc", "swiattn_dual_branch_workspace",
     "swiattn_dual_branch", "swiattn_prefill_backward_workspace", "swiattn_prefill_backward",
     "swiattn_route_backward_workspace", "swiattn_route_backward",
+    "swiattn_decode_paged_workspace", "swiattn_decode_paged",
     "swiattn_get_device_error", "swiattn_status_string", "swiattn_set_profile_events",
     "swiattn_num_sms",
 )
@@ -80,6 +82,9 @@ def _load() -> ctypes.CDLL:
             lib.swiattn_route_backward_workspace.argtypes = [i64, i32, i32]
             lib.swiattn_route_backward_workspace.restype = sz
             lib.swiattn_route_backward.argtypes = [vp] * 8 + [i64, i32, i32, i32] + [vp] * 5 + [sz, vp]
+            lib.swiattn_decode_paged_workspace.argtypes = [i32] * 8
+            lib.swiattn_decode_paged_workspace.restype = sz
+            lib.swiattn_decode_paged.argtypes = [vp] * 8 + [i32] * 8 + [f32, i32, vp, sz, vp]
             lib.swiattn_get_device_error.argtypes = [vp]
             lib.swiattn_status_string.argtypes = [i32]
             lib.swiattn_status_string.restype = ctypes.c_char_p
@@ -88,7 +93,8 @@ def _load() -> ctypes.CDLL:
             lib.swiattn_set_profile_events.restype = None
             for name in ("swiattn_route", "swiattn_prefill", "swiattn_decode", "swiattn_decode_noalloc",
                          "swiattn_dual_branch", "swiattn_get_device_error", "swiattn_num_sms",
-                         "swiattn_prefill_backward", "swiattn_route_backward"):
+                         "swiattn_prefill_backward", "swiattn_route_backward",
+                         "swiattn_decode_paged"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -304,3 +310,33 @@ def route_backward(logits, o_full, o_swa, d_o, gamma=None, d_reg=None, h=None, w
         _ptr(out.get("dw")), _ptr(out.get("db")), _ptr(ws), 0 if ws is None else ws.numel(),
         _stream()), "swiattn_route_backward")
     return out
+
+
+def decode_paged_workspace(B, max_pages, page_size, Hq, Hkv, d, W, dtype) -> int:
+    return int(_load().swiattn_decode_paged_workspace(B, max_pages, page_size, Hq, Hkv, d, W,
+                                                      _DT.get(dtype, dtype)))
+
+
+def decode_paged(q, k_pages, v_pages, block_table, seq_lens, gate, W: int,
+                 scale: Optional[float] = None, out=None, want_lse=False, workspace=None):
+    """Decode over a paged cache.  q [B,Hq,d]; k_pages, v_pages [num_pages, page_size, Hkv, d];
+    block_table int32 [B, max_pages]; seq_lens int32 [B]; gate uint8 [B]."""
+    _dev(q, "q")
+    _dev(k_pages, "k_pages", q.dtype)
+    _dev(v_pages, "v_pages", q.dtype)
+    _dev(block_table, "block_table", torch.int32)
+    _dev(seq_lens, "seq_lens", torch.int32)
+    _dev(gate, "gate", torch.uint8)
+    B, Hq, d = q.shape
+    num_pages, page_size, Hkv = k_pages.shape[0], k_pages.shape[1], k_pages.shape[2]
+    max_pages = block_table.shape[1]
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o = out if out is not None else torch.empty_like(q)
+    lse = torch.empty((B, Hq), device=q.device, dtype=torch.float32) if want_lse else None
+    ws = _workspace(decode_paged_workspace(B, max_pages, page_size, Hq, Hkv, d, W, q.dtype),
+                    q.device, workspace)
+    _check(_load().swiattn_decode_paged(
+        _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), _ptr(seq_lens), _ptr(gate),
+        _ptr(o), _ptr(lse), B, max_pages, page_size, num_pages, Hq, Hkv, d, W, float(scale),
+        _DT[q.dtype], _ptr(ws), ws.numel(), _stream()), "swiattn_decode_paged")
+    return (o, lse) if want_lse else o

@@ -64,28 +64,64 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
     return r;
 }
 
+// Visited cache entries [lo, lo + n) of sequence b; a length outside
+// [1, Lmax] is clamped into it (the split kernel reports it).
 __device__ __forceinline__ void visited(const int32_t* seq_lens, const uint8_t* gate, int b, int W,
-                                        int& lo, int& n) {
-    const int L = seq_lens[b];
+                                        int Lmax, int& lo, int& n) {
+    const int L = min(max(seq_lens[b], 1), Lmax);
     const int pos = L - 1;
     lo = gate[b] ? 0 : max(0, pos - W + 1);
     n = L - lo;
 }
 
-template <typename T, int D, int G>
+// Where token rows live: a contiguous cache [B, Lmax, Hkv, d] (Lmax rows per
+// sequence), or pages [num_pages, page_size, Hkv, d] found through a block
+// table [B, max_pages] (page_size = 1 << page_lg).
+struct Paging {
+    const int32_t* block_table;   // nullptr: contiguous
+    int max_pages, page_lg, num_pages;
+    unsigned int* err;
+};
+
+template <typename T, int D, int G, bool PAGED>
 __global__ void decode_split_kernel(const T* __restrict__ q, const T* __restrict__ kc,
                                     const T* __restrict__ vc, const int32_t* __restrict__ seq_lens,
                                     const uint8_t* __restrict__ gate, float* __restrict__ part,
                                     int Lmax, int Hq, int Hkv, int W, float scale_log2,
-                                    int max_chunks) {
+                                    int max_chunks, Paging pg) {
     constexpr int VEC = Vec<T>::N;
     constexpr int LPH = D / VEC;   // lanes per KV head
     const int b = blockIdx.y, c = blockIdx.x;
     int lo, n;
-    visited(seq_lens, gate, b, W, lo, n);
+    visited(seq_lens, gate, b, W, Lmax, lo, n);
+    if (c == 0 && threadIdx.x == 0 && pg.err) {
+        const int raw = seq_lens[b];
+        if (raw < 1 || raw > Lmax) atomicOr(pg.err, kDevErrInput);
+    }
     const int t0 = lo + c * kChunk;
     if (c * kChunk >= n) return;
     const int t1 = min(lo + n, t0 + kChunk);
+    // Paged: the physical page of every page this chunk touches, in shared
+    // memory (at most kChunk + 1 of them).  An entry outside [0, num_pages)
+    // is replaced by page 0 and flagged as bad input.
+    __shared__ int s_page[PAGED ? kChunk + 1 : 1];
+    int page_base = 0;
+    if constexpr (PAGED) {
+        page_base = t0 >> pg.page_lg;
+        const int np = ((t1 - 1) >> pg.page_lg) - page_base + 1;
+        for (int k = threadIdx.x; k < np; k += blockDim.x) {
+            // A sequence longer than its table row (seq_lens past
+            // max_pages * page_size) also counts as bad input.
+            const bool in_row = page_base + k < pg.max_pages;
+            int phys = in_row ? pg.block_table[(size_t)b * pg.max_pages + page_base + k] : -1;
+            if (phys < 0 || phys >= pg.num_pages) {
+                atomicOr(pg.err, kDevErrInput);
+                phys = 0;
+            }
+            s_page[k] = phys;
+        }
+        __syncthreads();
+    }
 
     // Threads past Hkv*LPH (block rounded up to whole warps) mirror the last
     // KV head so shuffles stay full-warp; they write nothing.
@@ -109,15 +145,20 @@ __global__ void decode_split_kernel(const T* __restrict__ q, const T* __restrict
         l[g] = 0.f;
     }
 
-    const uint4* kb = reinterpret_cast<const uint4*>(kc) + (size_t)b * Lmax * row_vecs + tid;
-    const uint4* vb = reinterpret_cast<const uint4*>(vc) + (size_t)b * Lmax * row_vecs + tid;
+    const uint4* kb = reinterpret_cast<const uint4*>(kc) + (PAGED ? 0 : (size_t)b * Lmax * row_vecs) + tid;
+    const uint4* vb = reinterpret_cast<const uint4*>(vc) + (PAGED ? 0 : (size_t)b * Lmax * row_vecs) + tid;
     for (int t = t0; t < t1; t += kUnroll) {
         uint4 ku[kUnroll], vu[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             const int tt = min(t + u, t1 - 1);   // clamp: duplicates are masked below
-            ku[u] = ld_stream(kb + (size_t)tt * row_vecs);
-            vu[u] = ld_stream(vb + (size_t)tt * row_vecs);
+            size_t row = (size_t)tt;
+            if constexpr (PAGED) {
+                const int mask = (1 << pg.page_lg) - 1;
+                row = ((size_t)s_page[(tt >> pg.page_lg) - page_base] << pg.page_lg) + (tt & mask);
+            }
+            ku[u] = ld_stream(kb + row * row_vecs);
+            vu[u] = ld_stream(vb + row * row_vecs);
         }
         float s[kUnroll][G];
 #pragma unroll
@@ -181,12 +222,12 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const float* __restri
                                                            const int32_t* __restrict__ seq_lens,
                                                            const uint8_t* __restrict__ gate,
                                                            T* __restrict__ o, float* __restrict__ lse,
-                                                           int Hq, int W, int max_chunks) {
+                                                           int Hq, int W, int Lmax, int max_chunks) {
     __shared__ float red[D / 32];
     const int hq = blockIdx.x, b = blockIdx.y, cidx = threadIdx.x;
     const int lane = cidx & 31, wid = cidx >> 5;
     int lo, n;
-    visited(seq_lens, gate, b, W, lo, n);
+    visited(seq_lens, gate, b, W, Lmax, lo, n);
     const int nc = (n + kChunk - 1) / kChunk;
     const float* base = part + ((size_t)b * max_chunks * Hq + hq) * (D + 2);
     const size_t cstride = (size_t)Hq * (D + 2);
@@ -236,35 +277,57 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const float* __restri
 template <typename T, int D, int G>
 cudaError_t launch_split(const void* q, const void* kc, const void* vc, const int32_t* sl,
                          const uint8_t* gate, float* part, int B, int Lmax, int Hq, int Hkv, int W,
-                         float scale_log2, int max_chunks, cudaStream_t s) {
+                         float scale_log2, int max_chunks, const Paging& pg, cudaStream_t s) {
     const int threads = (Hkv * (D / Vec<T>::N) + 31) / 32 * 32;
     dim3 grid(max_chunks, B);
-    decode_split_kernel<T, D, G><<<grid, threads, 0, s>>>(
-        static_cast<const T*>(q), static_cast<const T*>(kc), static_cast<const T*>(vc), sl, gate,
-        part, Lmax, Hq, Hkv, W, scale_log2, max_chunks);
+    if (pg.block_table)
+        decode_split_kernel<T, D, G, true><<<grid, threads, 0, s>>>(
+            static_cast<const T*>(q), static_cast<const T*>(kc), static_cast<const T*>(vc), sl, gate,
+            part, Lmax, Hq, Hkv, W, scale_log2, max_chunks, pg);
+    else
+        decode_split_kernel<T, D, G, false><<<grid, threads, 0, s>>>(
+            static_cast<const T*>(q), static_cast<const T*>(kc), static_cast<const T*>(vc), sl, gate,
+            part, Lmax, Hq, Hkv, W, scale_log2, max_chunks, pg);
     return cudaGetLastError();
 }
 
 template <typename T, int D>
 cudaError_t launch_typed(const void* q, const void* kc, const void* vc, const int32_t* sl,
                          const uint8_t* gate, void* o, float* lse, int B, int Lmax, int Hq,
-                         int Hkv, int W, float scale, float* part, int max_chunks, cudaStream_t s) {
+                         int Hkv, int W, float scale, float* part, int max_chunks,
+                         const Paging& pg, cudaStream_t s) {
     const float sl2 = scale * 1.4426950408889634f;
     const int G = Hq / Hkv;
     cudaError_t e;
     prof_start(s);
     switch (G) {
-        case 1: e = launch_split<T, D, 1>(q, kc, vc, sl, gate, part, B, Lmax, Hq, Hkv, W, sl2, max_chunks, s); break;
-        case 2: e = launch_split<T, D, 2>(q, kc, vc, sl, gate, part, B, Lmax, Hq, Hkv, W, sl2, max_chunks, s); break;
-        case 4: e = launch_split<T, D, 4>(q, kc, vc, sl, gate, part, B, Lmax, Hq, Hkv, W, sl2, max_chunks, s); break;
-        case 8: e = launch_split<T, D, 8>(q, kc, vc, sl, gate, part, B, Lmax, Hq, Hkv, W, sl2, max_chunks, s); break;
+        case 1: e = launch_split<T, D, 1>(q, kc, vc, sl, gate, part, B, Lmax, Hq, Hkv, W, sl2, max_chunks, pg, s); break;
+        case 2: e = launch_split<T, D, 2>(q, kc, vc, sl, gate, part, B, Lmax, Hq, Hkv, W, sl2, max_chunks, pg, s); break;
+        case 4: e = launch_split<T, D, 4>(q, kc, vc, sl, gate, part, B, Lmax, Hq, Hkv, W, sl2, max_chunks, pg, s); break;
+        case 8: e = launch_split<T, D, 8>(q, kc, vc, sl, gate, part, B, Lmax, Hq, Hkv, W, sl2, max_chunks, pg, s); break;
         default: return cudaErrorInvalidValue;
     }
     prof_stop(s);
     if (e != cudaSuccess) return e;
     decode_combine_kernel<T, D><<<dim3(Hq, B), D, 0, s>>>(part, sl, gate, static_cast<T*>(o), lse,
-                                                          Hq, W, max_chunks);
+                                                          Hq, W, Lmax, max_chunks);
     return cudaGetLastError();
+}
+
+cudaError_t launch_decode_any(const void* q, const void* kc, const void* vc,
+                              const int32_t* seq_lens, const uint8_t* gate, void* o, float* lse,
+                              int B, int Lmax, int Hq, int Hkv, int d, int W, float scale,
+                              int dtype, const DecodeWs& L, char* ws, const Paging& pg,
+                              cudaStream_t s) {
+    float* part = reinterpret_cast<float*>(ws + L.part);
+    if (dtype == 1) {
+        if (d == 128) return launch_typed<__nv_bfloat16, 128>(q, kc, vc, seq_lens, gate, o, lse, B, Lmax, Hq, Hkv, W, scale, part, L.max_chunks, pg, s);
+        if (d == 64) return launch_typed<__nv_bfloat16, 64>(q, kc, vc, seq_lens, gate, o, lse, B, Lmax, Hq, Hkv, W, scale, part, L.max_chunks, pg, s);
+    } else {
+        if (d == 128) return launch_typed<float, 128>(q, kc, vc, seq_lens, gate, o, lse, B, Lmax, Hq, Hkv, W, scale, part, L.max_chunks, pg, s);
+        if (d == 64) return launch_typed<float, 64>(q, kc, vc, seq_lens, gate, o, lse, B, Lmax, Hq, Hkv, W, scale, part, L.max_chunks, pg, s);
+    }
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace
@@ -282,16 +345,21 @@ DecodeWs decode_ws_layout(int B, int Lmax, int Hq, int d) {
 cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const int32_t* seq_lens,
                           const uint8_t* gate, void* o, float* lse, int B, int Lmax, int Hq,
                           int Hkv, int d, int W, float scale, int dtype, const DecodeWs& L,
-                          char* ws, cudaStream_t s) {
-    float* part = reinterpret_cast<float*>(ws + L.part);
-    if (dtype == 1) {
-        if (d == 128) return launch_typed<__nv_bfloat16, 128>(q, kc, vc, seq_lens, gate, o, lse, B, Lmax, Hq, Hkv, W, scale, part, L.max_chunks, s);
-        if (d == 64) return launch_typed<__nv_bfloat16, 64>(q, kc, vc, seq_lens, gate, o, lse, B, Lmax, Hq, Hkv, W, scale, part, L.max_chunks, s);
-    } else {
-        if (d == 128) return launch_typed<float, 128>(q, kc, vc, seq_lens, gate, o, lse, B, Lmax, Hq, Hkv, W, scale, part, L.max_chunks, s);
-        if (d == 64) return launch_typed<float, 64>(q, kc, vc, seq_lens, gate, o, lse, B, Lmax, Hq, Hkv, W, scale, part, L.max_chunks, s);
-    }
-    return cudaErrorInvalidValue;
+                          char* ws, unsigned int* err, cudaStream_t s) {
+    Paging pg{nullptr, 0, 0, 0, err};
+    return launch_decode_any(q, kc, vc, seq_lens, gate, o, lse, B, Lmax, Hq, Hkv, d, W, scale,
+                             dtype, L, ws, pg, s);
+}
+
+cudaError_t launch_decode_paged(const void* q, const void* kp, const void* vp,
+                                const int32_t* block_table, const int32_t* seq_lens,
+                                const uint8_t* gate, void* o, float* lse, int B, int max_pages,
+                                int page_lg, int num_pages, int Hq, int Hkv, int d, int W,
+                                float scale, int dtype, const DecodeWs& L, char* ws,
+                                unsigned int* err, cudaStream_t s) {
+    Paging pg{block_table, max_pages, page_lg, num_pages, err};
+    return launch_decode_any(q, kp, vp, seq_lens, gate, o, lse, B, max_pages << page_lg, Hq, Hkv,
+                             d, W, scale, dtype, L, ws, pg, s);
 }
 
 }  // namespace swi
@@ -352,6 +420,6 @@ extern "C" int swiattn_decode_noalloc(const void* q, const void* k_cache, const 
     // scratch needs no clearing between calls.
     const cudaError_t e = launch_decode(q, k_cache, v_cache, seq_lens, gate, o, lse, B, Lmax, Hq,
                                         Hkv, d, W, scale, dtype, L, reinterpret_cast<char*>(scratch),
-                                        static_cast<cudaStream_t>(stream));
+                                        nullptr, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SWIATTN_OK : SWIATTN_ECUDA;
 }

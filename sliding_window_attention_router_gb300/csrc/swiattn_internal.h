@@ -11,6 +11,7 @@ namespace swi {
 // Device error word bits (OR-ed by kernels, read by swiattn_get_device_error).
 constexpr unsigned int kDevErrTimeout = 1u;
 constexpr unsigned int kDevErrLayout = 2u;   // shared memory not laid out as a kernel requires
+constexpr unsigned int kDevErrInput = 4u;    // a device-resident input was out of range
 
 // A healthy wait in these kernels lasts microseconds; after this long a
 // kernel gives up, flags a timeout and returns.
@@ -113,10 +114,11 @@ cudaError_t launch_dual_epilogue_parts(const float* mse_part, const float* logit
                                        int B, int N, int Hq, float gamma_base, float eps,
                                        float alpha, cudaStream_t s);
 
+// err: device error word (a length outside [1, Lmax] is clamped and reported).
 cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const int32_t* seq_lens,
                           const uint8_t* gate, void* o, float* lse, int B, int Lmax, int Hq,
                           int Hkv, int d, int W, float scale, int dtype, const DecodeWs& L,
-                          char* ws, cudaStream_t s);
+                          char* ws, unsigned int* err, cudaStream_t s);
 
 // ------------------------------------------------------------ backward ------
 // Far-row scan of launch_schedule on its own: routed_list/routed_count/
@@ -201,6 +203,15 @@ cudaError_t launch_route_backward(const void* h, const void* w, const float* log
                                   const float* gamma, const float* d_reg, int64_t tokens, int hd,
                                   int d_model, int dtype, float* d_logits, void* dh, float* dw,
                                   float* db, float* ws, cudaStream_t s);
+
+// Decode over a paged cache: k/v pages [num_pages, 1 << page_lg, Hkv, d],
+// block_table [B, max_pages]; bad table entries are flagged in *err.
+cudaError_t launch_decode_paged(const void* q, const void* kp, const void* vp,
+                                const int32_t* block_table, const int32_t* seq_lens,
+                                const uint8_t* gate, void* o, float* lse, int B, int max_pages,
+                                int page_lg, int num_pages, int Hq, int Hkv, int d, int W,
+                                float scale, int dtype, const DecodeWs& L, char* ws,
+                                unsigned int* err, cudaStream_t s);
 
 // Timing hook around the dominant kernel of a call (no-ops unless set).
 void prof_start(cudaStream_t s);
