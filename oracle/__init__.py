@@ -69,11 +69,16 @@ def _load():
             lib.oracle_prefill_backward_keys.argtypes = ([dp, dp, dp, u8p, dp] + [i64] * 6
                                                          + [ctypes.c_double, i64p, i64, dp, dp])
             lib.oracle_route_backward.argtypes = [dp] * 8 + [i64] * 3 + [dp] * 4
+            lib.oracle_prefill_anchored.argtypes = ([dp, dp, dp, u8p] + [i64] * 7
+                                                    + [ctypes.c_double, dp, dp])
+            lib.oracle_decode_anchored.argtypes = ([dp, dp, dp, i32p, u8p] + [i64] * 7
+                                                   + [ctypes.c_double, dp, dp])
             for name in ("oracle_row_ranges", "oracle_route", "oracle_prefill",
                          "oracle_prefill_rows", "oracle_decode", "oracle_regulariser",
                          "oracle_dual", "oracle_dual_rows", "oracle_num_threads",
                          "oracle_prefill_backward", "oracle_prefill_backward_rows",
-                         "oracle_prefill_backward_keys", "oracle_route_backward"):
+                         "oracle_prefill_backward_keys", "oracle_route_backward",
+                         "oracle_prefill_anchored", "oracle_decode_anchored"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -286,3 +291,34 @@ def route_backward(logits, o_full, o_swa, d_o, gamma, d_reg=None, h=None, w=None
     if h is not None:
         out.update(dh=dh, dw=dw, db=float(db[0]))
     return out
+
+
+def prefill_anchored(q, k, v, gate, W: int, S: int, scale: float, want_lse: bool = False):
+    """Routed prefill where window rows also see the first S keys (global
+    anchors); S = 0 is prefill()."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    g = np.ascontiguousarray(np.asarray(gate, dtype=np.uint8))
+    B, N, Hq, d = q.shape
+    Hkv = k.shape[2]
+    o = np.empty_like(q)
+    lse = np.empty((B, N, Hq), np.float64) if want_lse else None
+    _check(_load().oracle_prefill_anchored(_ptr(q), _ptr(k), _ptr(v), _ptr(g), B, N, Hq, Hkv, d,
+                                           W, S, float(scale), _ptr(o),
+                                           _ptr(lse) if want_lse else None), "prefill_anchored")
+    return (o, lse) if want_lse else o
+
+
+def decode_anchored(q, k_cache, v_cache, seq_lens, gate, W: int, S: int, scale: float,
+                    want_lse: bool = False):
+    """Decode where a window query also sees the first S cache entries."""
+    q, kc, vc = _f64(q), _f64(k_cache), _f64(v_cache)
+    sl = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
+    g = np.ascontiguousarray(np.asarray(gate, dtype=np.uint8))
+    B, Hq, d = q.shape
+    Lmax, Hkv = kc.shape[1], kc.shape[2]
+    o = np.empty_like(q)
+    lse = np.empty((B, Hq), np.float64) if want_lse else None
+    _check(_load().oracle_decode_anchored(_ptr(q), _ptr(kc), _ptr(vc), _ptr(sl), _ptr(g), B, Lmax,
+                                          Hq, Hkv, d, W, S, float(scale), _ptr(o),
+                                          _ptr(lse) if want_lse else None), "decode_anchored")
+    return (o, lse) if want_lse else o

@@ -309,6 +309,102 @@ int oracle_dual_rows(const double *q, const double *k, const double *v, const do
 }
 
 /* ---------------------------------------------------------------------------
+ * Global anchors (SWA glossary, "详细解释", the platform note on 全局锚点重注入,
+ * and "SWA 落地的四个常见坑", pitfall 1, fix 2): besides its window, every
+ * query also attends the first S tokens of the sequence (S = 256 there),
+ * which the window never evicts.  Attention stays causal, so a window row i
+ * visits [0, min(S, i+1)) together with [max(0, i-W+1), i]; a routed row
+ * still visits [0, i].  S = 0 is plain sliding-window attention.
+ * ------------------------------------------------------------------------- */
+
+/* Visited keys of row i, in ascending order, into idx (capacity >= i+1);
+ * returns their count. */
+static int64_t anchored_keys(int routed, int64_t i, int64_t W, int64_t S, int64_t *idx)
+{
+    int64_t n = 0;
+    int64_t lo = routed ? 0 : (i - W + 1 > 0 ? i - W + 1 : 0);
+    for (int64_t j = 0; j < lo && j < S; ++j) idx[n++] = j;
+    for (int64_t j = lo; j <= i; ++j) idx[n++] = j;
+    return n;
+}
+
+/* Softmax attention of one query over an explicit ascending key list. */
+static void attend_list(const double *q, const double *k, const double *v, int64_t stride,
+                        const int64_t *idx, int64_t n, int64_t d, double scale, double *s,
+                        double *o, double *lse)
+{
+    double mx = -INFINITY;
+    for (int64_t t = 0; t < n; ++t) {
+        const double *kj = k + idx[t] * stride;
+        double dot = 0.0;
+        for (int64_t c = 0; c < d; ++c) dot += q[c] * kj[c];
+        s[t] = scale * dot;
+        if (s[t] > mx) mx = s[t];
+    }
+    double den = 0.0;
+    for (int64_t c = 0; c < d; ++c) o[c] = 0.0;
+    for (int64_t t = 0; t < n; ++t) {
+        double p = exp(s[t] - mx);
+        den += p;
+        const double *vj = v + idx[t] * stride;
+        for (int64_t c = 0; c < d; ++c) o[c] += p * vj[c];
+    }
+    for (int64_t c = 0; c < d; ++c) o[c] /= den;
+    if (lse) *lse = mx + log(den);
+}
+
+/* Routed prefill with S global anchors; arguments as oracle_prefill. */
+int oracle_prefill_anchored(const double *q, const double *k, const double *v,
+                            const uint8_t *gate, int64_t B, int64_t N, int64_t Hq, int64_t Hkv,
+                            int64_t d, int64_t W, int64_t S, double scale, double *o, double *lse)
+{
+    if (!shapes_ok(B, N, Hq, Hkv, d, W) || S < 0) return -1;
+    int64_t rows = B * N * Hq;
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)N);
+        int64_t *idx = (int64_t *)malloc(sizeof(int64_t) * (size_t)N);
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t r = 0; r < rows; ++r) {
+            int64_t h = r % Hq, bi = r / Hq, i = bi % N, b = bi / N, kvh = h / (Hq / Hkv);
+            int64_t n = anchored_keys(gate[b * N + i] != 0, i, W, S, idx);
+            attend_list(q + r * d, k + (b * N * Hkv + kvh) * d, v + (b * N * Hkv + kvh) * d,
+                        Hkv * d, idx, n, d, scale, s, o + r * d, lse ? lse + r : NULL);
+        }
+        free(s);
+        free(idx);
+    }
+    return 0;
+}
+
+/* Decode with S global anchors; arguments as oracle_decode. */
+int oracle_decode_anchored(const double *q, const double *kc, const double *vc,
+                           const int32_t *seq_lens, const uint8_t *gate, int64_t B, int64_t Lmax,
+                           int64_t Hq, int64_t Hkv, int64_t d, int64_t W, int64_t S, double scale,
+                           double *o, double *lse)
+{
+    if (!shapes_ok(B, Lmax, Hq, Hkv, d, W) || S < 0) return -1;
+    for (int64_t b = 0; b < B; ++b)
+        if (seq_lens[b] < 1 || seq_lens[b] > Lmax) return -1;
+    int64_t rows = B * Hq;
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)Lmax);
+        int64_t *idx = (int64_t *)malloc(sizeof(int64_t) * (size_t)Lmax);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < rows; ++r) {
+            int64_t b = r / Hq, h = r % Hq, kvh = h / (Hq / Hkv);
+            int64_t n = anchored_keys(gate[b] != 0, (int64_t)seq_lens[b] - 1, W, S, idx);
+            attend_list(q + r * d, kc + (b * Lmax * Hkv + kvh) * d, vc + (b * Lmax * Hkv + kvh) * d,
+                        Hkv * d, idx, n, d, scale, s, o + r * d, lse ? lse + r : NULL);
+        }
+        free(s);
+        free(idx);
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
  * Training backward.
  *
  * Report section 2 (router design): the hard gate is formed with the

@@ -15,7 +15,7 @@ import sys
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-PIN_SUITES = ("test_oracle_pins.py", "test_oracle_backward_pins.py")
+PIN_SUITES = ("test_oracle_pins.py", "test_oracle_backward_pins.py", "test_oracle_anchor_pins.py")
 
 # (name, original text, planted text); the original must occur in the source.
 MUTATIONS = [
@@ -23,7 +23,11 @@ MUTATIONS = [
     ("gate_not_strict", "gate[t] = acc > 0.0 ? 1 : 0;", "gate[t] = acc >= 0.0 ? 1 : 0;"),
     ("gqa_interleaved", "int64_t kvh = h / (Hq / Hkv);\n    int64_t lo, hi;",
      "int64_t kvh = h % Hkv;\n    int64_t lo, hi;"),
-    ("lse_without_max", "if (lse) *lse = mx + log(den);", "if (lse) *lse = log(den);"),
+    ("lse_without_max", "if (lse) *lse = mx + log(den);\n}\n\nstatic int shapes_ok",
+     "if (lse) *lse = log(den);\n}\n\nstatic int shapes_ok"),
+    ("anchored_lse_without_max",
+     "if (lse) *lse = mx + log(den);\n}\n\n/* Routed prefill with S global anchors",
+     "if (lse) *lse = log(den);\n}\n\n/* Routed prefill with S global anchors"),
     ("mse_not_squared", "acc += e * e;", "acc += fabs(e);"),
     ("softplus_unstable_branch", "log1p(exp(-fabs(x)))", "log1p(exp(-x))"),
     ("gamma_without_alpha", "eps + nll[t] + alpha * mse[t]", "eps + nll[t] + mse[t]"),
@@ -40,6 +44,10 @@ MUTATIONS = [
      "g += d_reg[t] * gamma[t] * (1.0 - sg);"),
     ("router_dh_from_logit", "dh[t * D + j] = d_logits[t] * w[j];",
      "dh[t * D + j] = logits[t] * w[j];"),
+    ("anchor_off_by_one", "for (int64_t j = 0; j < lo && j < S; ++j) idx[n++] = j;",
+     "for (int64_t j = 0; j < lo && j <= S; ++j) idx[n++] = j;"),
+    ("anchor_not_causal", "for (int64_t j = 0; j < lo && j < S; ++j) idx[n++] = j;",
+     "for (int64_t j = 0; j < S && j < lo + W; ++j) if (j < lo || j > i) idx[n++] = j;"),
 ]
 
 
