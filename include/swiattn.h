@@ -104,6 +104,23 @@ int swiattn_decode(const void* q, const void* k_cache, const void* v_cache,
                    int Lmax, int Hq, int Hkv, int d, int W, float scale, int dtype,
                    void* workspace, size_t workspace_bytes, void* stream);
 
+/* Bytes of device workspace swiattn_decode_anchored needs (0 for invalid sizes). */
+size_t swiattn_decode_anchored_workspace(int B, int Lmax, int Hq, int Hkv, int d, int W,
+                                         int n_anchor, int dtype);
+
+/* swiattn_decode with global anchors (SWA glossary, "详细解释" platform note on
+ * 全局锚点重注入 and "SWA 落地的四个常见坑" pitfall 1, fix 2: the first tokens'
+ * K/V stay in the cache and every query also attends them).  A window query
+ * at position L-1 reads cache entries [0, min(n_anchor, L)) together with
+ * [max(0, L-W), L-1]; a routed query reads [0, L-1] as before.  n_anchor >= 0;
+ * 0 is swiattn_decode.  Other arguments as swiattn_decode.
+ * workspace: at least swiattn_decode_anchored_workspace(...) bytes. */
+int swiattn_decode_anchored(const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* seq_lens, const uint8_t* gate, void* o, float* lse,
+                            int B, int Lmax, int Hq, int Hkv, int d, int W, int n_anchor,
+                            float scale, int dtype, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
 /* swiattn_decode without a workspace argument, for callers that cannot
  * allocate device memory (for example code that runs inside an allocator-free
  * runtime or a host framework that owns every device allocation and exposes
@@ -129,7 +146,7 @@ int swiattn_decode_noalloc(const void* q, const void* k_cache, const void* v_cac
 /* Bytes of device workspace swiattn_decode_paged needs for these sizes
  * (0 for invalid sizes). */
 size_t swiattn_decode_paged_workspace(int B, int max_pages, int page_size, int Hq, int Hkv, int d,
-                                      int W, int dtype);
+                                      int W, int n_anchor, int dtype);
 
 /* swiattn_decode over a paged KV cache (a serving cache layout; the report's
  * decode, section 2 and 6, reads the last W or all cache entries of each
@@ -142,15 +159,16 @@ size_t swiattn_decode_paged_workspace(int B, int max_pages, int page_size, int H
  * outside [1, max_pages * page_size] is clamped into it; either way
  * swiattn_get_device_error then reports SWIATTN_EINVAL (no out-of-range read
  * is made).  Entries of pages a call does not visit are not read.  Other arguments, layouts
- * and results are those of swiattn_decode.  A batched step over several
+ * and results are those of swiattn_decode_anchored (n_anchor = 0: of
+ * swiattn_decode).  A batched step over several
  * layers is one call with (layer, sequence) flattened into B (one pool, or
  * per-layer pools laid end to end with the table entries offset).
  * workspace: at least swiattn_decode_paged_workspace(...) bytes. */
 int swiattn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
                          const int32_t* block_table, const int32_t* seq_lens, const uint8_t* gate,
                          void* o, float* lse, int B, int max_pages, int page_size, int num_pages,
-                         int Hq, int Hkv, int d, int W, float scale, int dtype, void* workspace,
-                         size_t workspace_bytes, void* stream);
+                         int Hq, int Hkv, int d, int W, int n_anchor, float scale, int dtype,
+                         void* workspace, size_t workspace_bytes, void* stream);
 
 /* Bytes of device workspace swiattn_dual_branch needs for these sizes. */
 size_t swiattn_dual_branch_workspace(int B, int N, int Hq, int Hkv, int d, int W, int dtype);

@@ -21,7 +21,7 @@ __all__ = [
     "prefill_workspace", "decode_workspace", "dual_branch_workspace", "get_device_error",
     "status_string", "num_sms", "set_profile_events", "EXPORTS", "prefill_backward",
     "prefill_backward_workspace", "route_backward", "route_backward_workspace", "decode_paged",
-    "decode_paged_workspace",
+    "decode_paged_workspace", "decode_anchored", "decode_anchored_workspace",
 ]
 
 F32, BF16 = 0, 1
@@ -37,7 +37,8 @@ EXPORTS = (
     "swiattn_decode", "swiattn_decode_noalloc", "swiattn_dual_branch_workspace",
     "swiattn_dual_branch", "swiattn_prefill_backward_workspace", "swiattn_prefill_backward",
     "swiattn_route_backward_workspace", "swiattn_route_backward",
-    "swiattn_decode_paged_workspace", "swiattn_decode_paged",
+    "swiattn_decode_paged_workspace", "swiattn_decode_paged", "swiattn_decode_anchored_workspace",
+    "swiattn_decode_anchored",
     "swiattn_get_device_error", "swiattn_status_string", "swiattn_set_profile_events",
     "swiattn_num_sms",
 )
@@ -82,9 +83,12 @@ def _load() -> ctypes.CDLL:
             lib.swiattn_route_backward_workspace.argtypes = [i64, i32, i32]
             lib.swiattn_route_backward_workspace.restype = sz
             lib.swiattn_route_backward.argtypes = [vp] * 8 + [i64, i32, i32, i32] + [vp] * 5 + [sz, vp]
-            lib.swiattn_decode_paged_workspace.argtypes = [i32] * 8
+            lib.swiattn_decode_paged_workspace.argtypes = [i32] * 9
             lib.swiattn_decode_paged_workspace.restype = sz
-            lib.swiattn_decode_paged.argtypes = [vp] * 8 + [i32] * 8 + [f32, i32, vp, sz, vp]
+            lib.swiattn_decode_paged.argtypes = [vp] * 8 + [i32] * 9 + [f32, i32, vp, sz, vp]
+            lib.swiattn_decode_anchored_workspace.argtypes = [i32] * 8
+            lib.swiattn_decode_anchored_workspace.restype = sz
+            lib.swiattn_decode_anchored.argtypes = [vp] * 7 + [i32] * 7 + [f32, i32, vp, sz, vp]
             lib.swiattn_get_device_error.argtypes = [vp]
             lib.swiattn_status_string.argtypes = [i32]
             lib.swiattn_status_string.restype = ctypes.c_char_p
@@ -94,7 +98,7 @@ def _load() -> ctypes.CDLL:
             for name in ("swiattn_route", "swiattn_prefill", "swiattn_decode", "swiattn_decode_noalloc",
                          "swiattn_dual_branch", "swiattn_get_device_error", "swiattn_num_sms",
                          "swiattn_prefill_backward", "swiattn_route_backward",
-                         "swiattn_decode_paged"):
+                         "swiattn_decode_paged", "swiattn_decode_anchored"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -312,13 +316,41 @@ def route_backward(logits, o_full, o_swa, d_o, gamma=None, d_reg=None, h=None, w
     return out
 
 
-def decode_paged_workspace(B, max_pages, page_size, Hq, Hkv, d, W, dtype) -> int:
+def decode_paged_workspace(B, max_pages, page_size, Hq, Hkv, d, W, dtype, n_anchor=0) -> int:
     return int(_load().swiattn_decode_paged_workspace(B, max_pages, page_size, Hq, Hkv, d, W,
-                                                      _DT.get(dtype, dtype)))
+                                                      n_anchor, _DT.get(dtype, dtype)))
+
+
+def decode_anchored_workspace(B, Lmax, Hq, Hkv, d, W, n_anchor, dtype) -> int:
+    return int(_load().swiattn_decode_anchored_workspace(B, Lmax, Hq, Hkv, d, W, n_anchor,
+                                                         _DT.get(dtype, dtype)))
+
+
+def decode_anchored(q, k_cache, v_cache, seq_lens, gate, W: int, n_anchor: int,
+                    scale: Optional[float] = None, out=None, want_lse=False, workspace=None):
+    """decode() where a window query also sees the first n_anchor cache entries."""
+    _dev(q, "q")
+    _dev(k_cache, "k_cache", q.dtype)
+    _dev(v_cache, "v_cache", q.dtype)
+    _dev(seq_lens, "seq_lens", torch.int32)
+    _dev(gate, "gate", torch.uint8)
+    B, Hq, d = q.shape
+    Lmax, Hkv = k_cache.shape[1], k_cache.shape[2]
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o = out if out is not None else torch.empty_like(q)
+    lse = torch.empty((B, Hq), device=q.device, dtype=torch.float32) if want_lse else None
+    ws = _workspace(decode_anchored_workspace(B, Lmax, Hq, Hkv, d, W, n_anchor, q.dtype),
+                    q.device, workspace)
+    _check(_load().swiattn_decode_anchored(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), _ptr(gate), _ptr(o), _ptr(lse), B,
+        Lmax, Hq, Hkv, d, W, n_anchor, float(scale), _DT[q.dtype], _ptr(ws), ws.numel(),
+        _stream()), "swiattn_decode_anchored")
+    return (o, lse) if want_lse else o
 
 
 def decode_paged(q, k_pages, v_pages, block_table, seq_lens, gate, W: int,
-                 scale: Optional[float] = None, out=None, want_lse=False, workspace=None):
+                 scale: Optional[float] = None, out=None, want_lse=False, workspace=None,
+                 n_anchor: int = 0):
     """Decode over a paged cache.  q [B,Hq,d]; k_pages, v_pages [num_pages, page_size, Hkv, d];
     block_table int32 [B, max_pages]; seq_lens int32 [B]; gate uint8 [B]."""
     _dev(q, "q")
@@ -333,10 +365,10 @@ def decode_paged(q, k_pages, v_pages, block_table, seq_lens, gate, W: int,
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     o = out if out is not None else torch.empty_like(q)
     lse = torch.empty((B, Hq), device=q.device, dtype=torch.float32) if want_lse else None
-    ws = _workspace(decode_paged_workspace(B, max_pages, page_size, Hq, Hkv, d, W, q.dtype),
-                    q.device, workspace)
+    ws = _workspace(decode_paged_workspace(B, max_pages, page_size, Hq, Hkv, d, W, q.dtype,
+                                           n_anchor), q.device, workspace)
     _check(_load().swiattn_decode_paged(
         _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), _ptr(seq_lens), _ptr(gate),
-        _ptr(o), _ptr(lse), B, max_pages, page_size, num_pages, Hq, Hkv, d, W, float(scale),
-        _DT[q.dtype], _ptr(ws), ws.numel(), _stream()), "swiattn_decode_paged")
+        _ptr(o), _ptr(lse), B, max_pages, page_size, num_pages, Hq, Hkv, d, W, n_anchor,
+        float(scale), _DT[q.dtype], _ptr(ws), ws.numel(), _stream()), "swiattn_decode_paged")
     return (o, lse) if want_lse else o

@@ -64,14 +64,24 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
     return r;
 }
 
-// Visited cache entries [lo, lo + n) of sequence b; a length outside
-// [1, Lmax] is clamped into it (the split kernel reports it).
-__device__ __forceinline__ void visited(const int32_t* seq_lens, const uint8_t* gate, int b, int W,
-                                        int Lmax, int& lo, int& n) {
+// Visited cache entries of sequence b: the window (or whole history)
+// [lo, lo + n) and, for a window query with S global anchors, the anchors
+// the window does not reach, [0, na) with na = min(S, lo).  A length outside
+// [1, Lmax] is clamped into it (the split kernel reports it).  Chunks never
+// straddle the two segments: the first ceil(na / kChunk) chunks read anchors.
+struct Visit {
+    int lo, n, na, nca;   // nca: anchor chunks
+};
+__device__ __forceinline__ Visit visited(const int32_t* seq_lens, const uint8_t* gate, int b,
+                                         int W, int S, int Lmax) {
+    Visit v;
     const int L = min(max(seq_lens[b], 1), Lmax);
     const int pos = L - 1;
-    lo = gate[b] ? 0 : max(0, pos - W + 1);
-    n = L - lo;
+    v.lo = gate[b] ? 0 : max(0, pos - W + 1);
+    v.n = L - v.lo;
+    v.na = min(S, v.lo);
+    v.nca = (v.na + kChunk - 1) / kChunk;
+    return v;
 }
 
 // Where token rows live: a contiguous cache [B, Lmax, Hkv, d] (Lmax rows per
@@ -87,20 +97,26 @@ template <typename T, int D, int G, bool PAGED>
 __global__ void decode_split_kernel(const T* __restrict__ q, const T* __restrict__ kc,
                                     const T* __restrict__ vc, const int32_t* __restrict__ seq_lens,
                                     const uint8_t* __restrict__ gate, float* __restrict__ part,
-                                    int Lmax, int Hq, int Hkv, int W, float scale_log2,
+                                    int Lmax, int Hq, int Hkv, int W, int S, float scale_log2,
                                     int max_chunks, Paging pg) {
     constexpr int VEC = Vec<T>::N;
     constexpr int LPH = D / VEC;   // lanes per KV head
     const int b = blockIdx.y, c = blockIdx.x;
-    int lo, n;
-    visited(seq_lens, gate, b, W, Lmax, lo, n);
+    const Visit vis = visited(seq_lens, gate, b, W, S, Lmax);
     if (c == 0 && threadIdx.x == 0 && pg.err) {
         const int raw = seq_lens[b];
         if (raw < 1 || raw > Lmax) atomicOr(pg.err, kDevErrInput);
     }
-    const int t0 = lo + c * kChunk;
-    if (c * kChunk >= n) return;
-    const int t1 = min(lo + n, t0 + kChunk);
+    int t0, t1;   // this chunk's cache entries
+    if (c < vis.nca) {
+        t0 = c * kChunk;
+        t1 = min(vis.na, t0 + kChunk);
+    } else {
+        const int cw = c - vis.nca;
+        if (cw * kChunk >= vis.n) return;
+        t0 = vis.lo + cw * kChunk;
+        t1 = min(vis.lo + vis.n, t0 + kChunk);
+    }
     // Paged: the physical page of every page this chunk touches, in shared
     // memory (at most kChunk + 1 of them).  An entry outside [0, num_pages)
     // is replaced by page 0 and flagged as bad input.
@@ -222,13 +238,13 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const float* __restri
                                                            const int32_t* __restrict__ seq_lens,
                                                            const uint8_t* __restrict__ gate,
                                                            T* __restrict__ o, float* __restrict__ lse,
-                                                           int Hq, int W, int Lmax, int max_chunks) {
+                                                           int Hq, int W, int S, int Lmax,
+                                                           int max_chunks) {
     __shared__ float red[D / 32];
     const int hq = blockIdx.x, b = blockIdx.y, cidx = threadIdx.x;
     const int lane = cidx & 31, wid = cidx >> 5;
-    int lo, n;
-    visited(seq_lens, gate, b, W, Lmax, lo, n);
-    const int nc = (n + kChunk - 1) / kChunk;
+    const Visit vis = visited(seq_lens, gate, b, W, S, Lmax);
+    const int nc = vis.nca + (vis.n + kChunk - 1) / kChunk;
     const float* base = part + ((size_t)b * max_chunks * Hq + hq) * (D + 2);
     const size_t cstride = (size_t)Hq * (D + 2);
     float M = -INFINITY;
@@ -277,65 +293,65 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const float* __restri
 template <typename T, int D, int G>
 cudaError_t launch_split(const void* q, const void* kc, const void* vc, const int32_t* sl,
                          const uint8_t* gate, float* part, int B, int Lmax, int Hq, int Hkv, int W,
-                         float scale_log2, int max_chunks, const Paging& pg, cudaStream_t s) {
+                         int S, float scale_log2, int max_chunks, const Paging& pg, cudaStream_t s) {
     const int threads = (Hkv * (D / Vec<T>::N) + 31) / 32 * 32;
     dim3 grid(max_chunks, B);
     if (pg.block_table)
         decode_split_kernel<T, D, G, true><<<grid, threads, 0, s>>>(
             static_cast<const T*>(q), static_cast<const T*>(kc), static_cast<const T*>(vc), sl, gate,
-            part, Lmax, Hq, Hkv, W, scale_log2, max_chunks, pg);
+            part, Lmax, Hq, Hkv, W, S, scale_log2, max_chunks, pg);
     else
         decode_split_kernel<T, D, G, false><<<grid, threads, 0, s>>>(
             static_cast<const T*>(q), static_cast<const T*>(kc), static_cast<const T*>(vc), sl, gate,
-            part, Lmax, Hq, Hkv, W, scale_log2, max_chunks, pg);
+            part, Lmax, Hq, Hkv, W, S, scale_log2, max_chunks, pg);
     return cudaGetLastError();
 }
 
 template <typename T, int D>
 cudaError_t launch_typed(const void* q, const void* kc, const void* vc, const int32_t* sl,
                          const uint8_t* gate, void* o, float* lse, int B, int Lmax, int Hq,
-                         int Hkv, int W, float scale, float* part, int max_chunks,
+                         int Hkv, int W, int S, float scale, float* part, int max_chunks,
                          const Paging& pg, cudaStream_t s) {
     const float sl2 = scale * 1.4426950408889634f;
     const int G = Hq / Hkv;
     cudaError_t e;
     prof_start(s);
     switch (G) {
-        case 1: e = launch_split<T, D, 1>(q, kc, vc, sl, gate, part, B, Lmax, Hq, Hkv, W, sl2, max_chunks, pg, s); break;
-        case 2: e = launch_split<T, D, 2>(q, kc, vc, sl, gate, part, B, Lmax, Hq, Hkv, W, sl2, max_chunks, pg, s); break;
-        case 4: e = launch_split<T, D, 4>(q, kc, vc, sl, gate, part, B, Lmax, Hq, Hkv, W, sl2, max_chunks, pg, s); break;
-        case 8: e = launch_split<T, D, 8>(q, kc, vc, sl, gate, part, B, Lmax, Hq, Hkv, W, sl2, max_chunks, pg, s); break;
+        case 1: e = launch_split<T, D, 1>(q, kc, vc, sl, gate, part, B, Lmax, Hq, Hkv, W, S, sl2, max_chunks, pg, s); break;
+        case 2: e = launch_split<T, D, 2>(q, kc, vc, sl, gate, part, B, Lmax, Hq, Hkv, W, S, sl2, max_chunks, pg, s); break;
+        case 4: e = launch_split<T, D, 4>(q, kc, vc, sl, gate, part, B, Lmax, Hq, Hkv, W, S, sl2, max_chunks, pg, s); break;
+        case 8: e = launch_split<T, D, 8>(q, kc, vc, sl, gate, part, B, Lmax, Hq, Hkv, W, S, sl2, max_chunks, pg, s); break;
         default: return cudaErrorInvalidValue;
     }
     prof_stop(s);
     if (e != cudaSuccess) return e;
     decode_combine_kernel<T, D><<<dim3(Hq, B), D, 0, s>>>(part, sl, gate, static_cast<T*>(o), lse,
-                                                          Hq, W, Lmax, max_chunks);
+                                                          Hq, W, S, Lmax, max_chunks);
     return cudaGetLastError();
 }
 
 cudaError_t launch_decode_any(const void* q, const void* kc, const void* vc,
                               const int32_t* seq_lens, const uint8_t* gate, void* o, float* lse,
-                              int B, int Lmax, int Hq, int Hkv, int d, int W, float scale,
-                              int dtype, const DecodeWs& L, char* ws, const Paging& pg,
-                              cudaStream_t s) {
+                              int B, int Lmax, int Hq, int Hkv, int d, int W, int S,
+                              float scale, int dtype, const DecodeWs& L, char* ws,
+                              const Paging& pg, cudaStream_t s) {
     float* part = reinterpret_cast<float*>(ws + L.part);
     if (dtype == 1) {
-        if (d == 128) return launch_typed<__nv_bfloat16, 128>(q, kc, vc, seq_lens, gate, o, lse, B, Lmax, Hq, Hkv, W, scale, part, L.max_chunks, pg, s);
-        if (d == 64) return launch_typed<__nv_bfloat16, 64>(q, kc, vc, seq_lens, gate, o, lse, B, Lmax, Hq, Hkv, W, scale, part, L.max_chunks, pg, s);
+        if (d == 128) return launch_typed<__nv_bfloat16, 128>(q, kc, vc, seq_lens, gate, o, lse, B, Lmax, Hq, Hkv, W, S, scale, part, L.max_chunks, pg, s);
+        if (d == 64) return launch_typed<__nv_bfloat16, 64>(q, kc, vc, seq_lens, gate, o, lse, B, Lmax, Hq, Hkv, W, S, scale, part, L.max_chunks, pg, s);
     } else {
-        if (d == 128) return launch_typed<float, 128>(q, kc, vc, seq_lens, gate, o, lse, B, Lmax, Hq, Hkv, W, scale, part, L.max_chunks, pg, s);
-        if (d == 64) return launch_typed<float, 64>(q, kc, vc, seq_lens, gate, o, lse, B, Lmax, Hq, Hkv, W, scale, part, L.max_chunks, pg, s);
+        if (d == 128) return launch_typed<float, 128>(q, kc, vc, seq_lens, gate, o, lse, B, Lmax, Hq, Hkv, W, S, scale, part, L.max_chunks, pg, s);
+        if (d == 64) return launch_typed<float, 64>(q, kc, vc, seq_lens, gate, o, lse, B, Lmax, Hq, Hkv, W, S, scale, part, L.max_chunks, pg, s);
     }
     return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-DecodeWs decode_ws_layout(int B, int Lmax, int Hq, int d) {
+DecodeWs decode_ws_layout(int B, int Lmax, int Hq, int d, int S) {
     DecodeWs L;
     L.chunk = kChunk;
-    L.max_chunks = (Lmax + kChunk - 1) / kChunk;
+    L.max_chunks = (Lmax + kChunk - 1) / kChunk + (min(S, Lmax) + kChunk - 1) / kChunk;
     L.part = 0;
     L.total = sizeof(float) * (size_t)B * L.max_chunks * Hq * (d + 2);
     L.total = (L.total + 255) & ~static_cast<size_t>(255);
@@ -344,22 +360,22 @@ DecodeWs decode_ws_layout(int B, int Lmax, int Hq, int d) {
 
 cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const int32_t* seq_lens,
                           const uint8_t* gate, void* o, float* lse, int B, int Lmax, int Hq,
-                          int Hkv, int d, int W, float scale, int dtype, const DecodeWs& L,
-                          char* ws, unsigned int* err, cudaStream_t s) {
+                          int Hkv, int d, int W, int S, float scale, int dtype,
+                          const DecodeWs& L, char* ws, unsigned int* err, cudaStream_t s) {
     Paging pg{nullptr, 0, 0, 0, err};
-    return launch_decode_any(q, kc, vc, seq_lens, gate, o, lse, B, Lmax, Hq, Hkv, d, W, scale,
+    return launch_decode_any(q, kc, vc, seq_lens, gate, o, lse, B, Lmax, Hq, Hkv, d, W, S, scale,
                              dtype, L, ws, pg, s);
 }
 
 cudaError_t launch_decode_paged(const void* q, const void* kp, const void* vp,
                                 const int32_t* block_table, const int32_t* seq_lens,
                                 const uint8_t* gate, void* o, float* lse, int B, int max_pages,
-                                int page_lg, int num_pages, int Hq, int Hkv, int d, int W,
+                                int page_lg, int num_pages, int Hq, int Hkv, int d, int W, int S,
                                 float scale, int dtype, const DecodeWs& L, char* ws,
                                 unsigned int* err, cudaStream_t s) {
     Paging pg{block_table, max_pages, page_lg, num_pages, err};
     return launch_decode_any(q, kp, vp, seq_lens, gate, o, lse, B, max_pages << page_lg, Hq, Hkv,
-                             d, W, scale, dtype, L, ws, pg, s);
+                             d, W, S, scale, dtype, L, ws, pg, s);
 }
 
 }  // namespace swi
@@ -411,7 +427,7 @@ extern "C" int swiattn_decode_noalloc(const void* q, const void* k_cache, const 
     if (G != 1 && G != 2 && G != 4 && G != 8) return SWIATTN_EUNSUPPORTED;
     if ((int64_t)Hkv * d / (dtype == SWIATTN_BF16 ? 8 : 4) > 1024) return SWIATTN_EUNSUPPORTED;
     if (B > 65535) return SWIATTN_EUNSUPPORTED;
-    const DecodeWs L = decode_ws_layout(B, Lmax, Hq, d);
+    const DecodeWs L = decode_ws_layout(B, Lmax, Hq, d, 0);
     // The partials of this call must fit the fixed scratch array.
     if (L.total > kNoAllocScratchBytes) return SWIATTN_EINVAL;
     float* scratch = decode_scratch_on_current_device();
@@ -419,7 +435,7 @@ extern "C" int swiattn_decode_noalloc(const void* q, const void* k_cache, const 
     // Every chunk's partial is written before the combine reads it, so the
     // scratch needs no clearing between calls.
     const cudaError_t e = launch_decode(q, k_cache, v_cache, seq_lens, gate, o, lse, B, Lmax, Hq,
-                                        Hkv, d, W, scale, dtype, L, reinterpret_cast<char*>(scratch),
+                                        Hkv, d, W, 0, scale, dtype, L, reinterpret_cast<char*>(scratch),
                                         nullptr, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? SWIATTN_OK : SWIATTN_ECUDA;
 }

@@ -219,68 +219,90 @@ int swiattn_prefill(const void* q, const void* k, const void* v, const uint8_t* 
 }
 
 size_t swiattn_decode_workspace(int B, int Lmax, int Hq, int Hkv, int d, int W, int dtype) {
+    return swiattn_decode_anchored_workspace(B, Lmax, Hq, Hkv, d, W, 0, dtype);
+}
+
+size_t swiattn_decode_anchored_workspace(int B, int Lmax, int Hq, int Hkv, int d, int W,
+                                         int n_anchor, int dtype) {
     (void)dtype;
-    if (!attn_shape_ok(B, Lmax, Hq, Hkv, d, W)) return 0;
-    return decode_ws_layout(B, Lmax, Hq, d).total;
+    if (!attn_shape_ok(B, Lmax, Hq, Hkv, d, W) || n_anchor < 0) return 0;
+    return decode_ws_layout(B, Lmax, Hq, d, n_anchor).total;
+}
+
+namespace {
+
+int decode_args_ok(const void* q, const void* k, const void* v, const int32_t* seq_lens,
+                   const uint8_t* gate, const void* o, int B, int Lmax, int Hq, int Hkv, int d,
+                   int W, int S, float scale, int dtype) {
+    if (!attn_shape_ok(B, Lmax, Hq, Hkv, d, W) || S < 0) return SWIATTN_EINVAL;
+    if (dtype != SWIATTN_BF16 && dtype != SWIATTN_F32) return SWIATTN_EINVAL;
+    if (!q || !k || !v || !seq_lens || !gate || !o) return SWIATTN_EINVAL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return SWIATTN_EINVAL;
+    if (!(scale > 0.f)) return SWIATTN_EINVAL;
+    const int G = Hq / Hkv;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return SWIATTN_EUNSUPPORTED;
+    if ((int64_t)Hkv * d / (dtype == SWIATTN_BF16 ? 8 : 4) > 1024) return SWIATTN_EUNSUPPORTED;
+    if (B > 65535) return SWIATTN_EUNSUPPORTED;
+    return SWIATTN_OK;
+}
+
+}  // namespace
+
+int swiattn_decode_anchored(const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* seq_lens, const uint8_t* gate, void* o, float* lse,
+                            int B, int Lmax, int Hq, int Hkv, int d, int W, int n_anchor,
+                            float scale, int dtype, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+    const int st = decode_args_ok(q, k_cache, v_cache, seq_lens, gate, o, B, Lmax, Hq, Hkv, d, W,
+                                  n_anchor, scale, dtype);
+    if (st != SWIATTN_OK) return st;
+    const DecodeWs L = decode_ws_layout(B, Lmax, Hq, d, n_anchor);
+    if (!workspace || !aligned256(workspace) || workspace_bytes < L.total) return SWIATTN_EINVAL;
+    DeviceInfo di;
+    if (!device_info(di)) return SWIATTN_ECUDA;
+    return launched(launch_decode(q, k_cache, v_cache, seq_lens, gate, o, lse, B, Lmax, Hq, Hkv,
+                                  d, W, n_anchor, scale, dtype, L, static_cast<char*>(workspace),
+                                  di.err, static_cast<cudaStream_t>(stream)));
 }
 
 int swiattn_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* seq_lens,
                    const uint8_t* gate, void* o, float* lse, int B, int Lmax, int Hq, int Hkv,
                    int d, int W, float scale, int dtype, void* workspace, size_t workspace_bytes,
                    void* stream) {
-    if (!attn_shape_ok(B, Lmax, Hq, Hkv, d, W)) return SWIATTN_EINVAL;
-    if (dtype != SWIATTN_BF16 && dtype != SWIATTN_F32) return SWIATTN_EINVAL;
-    if (!q || !k_cache || !v_cache || !seq_lens || !gate || !o) return SWIATTN_EINVAL;
-    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return SWIATTN_EINVAL;
-    if (!(scale > 0.f)) return SWIATTN_EINVAL;
-    const int G = Hq / Hkv;
-    if (G != 1 && G != 2 && G != 4 && G != 8) return SWIATTN_EUNSUPPORTED;
-    if ((int64_t)Hkv * d / (dtype == SWIATTN_BF16 ? 8 : 4) > 1024) return SWIATTN_EUNSUPPORTED;
-    if (B > 65535) return SWIATTN_EUNSUPPORTED;
-    const DecodeWs L = decode_ws_layout(B, Lmax, Hq, d);
-    if (!workspace || !aligned256(workspace) || workspace_bytes < L.total) return SWIATTN_EINVAL;
-    DeviceInfo di;
-    if (!device_info(di)) return SWIATTN_ECUDA;
-    return launched(launch_decode(q, k_cache, v_cache, seq_lens, gate, o, lse, B, Lmax, Hq, Hkv,
-                                  d, W, scale, dtype, L, static_cast<char*>(workspace), di.err,
-                                  static_cast<cudaStream_t>(stream)));
+    return swiattn_decode_anchored(q, k_cache, v_cache, seq_lens, gate, o, lse, B, Lmax, Hq, Hkv,
+                                   d, W, 0, scale, dtype, workspace, workspace_bytes, stream);
 }
 
 size_t swiattn_decode_paged_workspace(int B, int max_pages, int page_size, int Hq, int Hkv, int d,
-                                      int W, int dtype) {
+                                      int W, int n_anchor, int dtype) {
     if (page_size <= 0 || (page_size & (page_size - 1)) != 0 || max_pages <= 0) return 0;
     const int64_t max_len = (int64_t)max_pages * page_size;
     if (max_len > (1 << 30)) return 0;
-    return swiattn_decode_workspace(B, (int)max_len, Hq, Hkv, d, W, dtype);
+    return swiattn_decode_anchored_workspace(B, (int)max_len, Hq, Hkv, d, W, n_anchor, dtype);
 }
 
 int swiattn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
                          const int32_t* block_table, const int32_t* seq_lens, const uint8_t* gate,
                          void* o, float* lse, int B, int max_pages, int page_size, int num_pages,
-                         int Hq, int Hkv, int d, int W, float scale, int dtype, void* workspace,
-                         size_t workspace_bytes, void* stream) {
+                         int Hq, int Hkv, int d, int W, int n_anchor, float scale, int dtype,
+                         void* workspace, size_t workspace_bytes, void* stream) {
     if (page_size <= 0 || (page_size & (page_size - 1)) != 0 || max_pages <= 0 || num_pages <= 0)
         return SWIATTN_EINVAL;
     const int64_t max_len = (int64_t)max_pages * page_size;
     if (max_len > (1 << 30)) return SWIATTN_EINVAL;
-    if (!attn_shape_ok(B, (int)max_len, Hq, Hkv, d, W)) return SWIATTN_EINVAL;
-    if (dtype != SWIATTN_BF16 && dtype != SWIATTN_F32) return SWIATTN_EINVAL;
-    if (!q || !k_pages || !v_pages || !block_table || !seq_lens || !gate || !o) return SWIATTN_EINVAL;
-    if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages)) return SWIATTN_EINVAL;
-    if (!(scale > 0.f)) return SWIATTN_EINVAL;
-    const int G = Hq / Hkv;
-    if (G != 1 && G != 2 && G != 4 && G != 8) return SWIATTN_EUNSUPPORTED;
-    if ((int64_t)Hkv * d / (dtype == SWIATTN_BF16 ? 8 : 4) > 1024) return SWIATTN_EUNSUPPORTED;
-    if (B > 65535) return SWIATTN_EUNSUPPORTED;
-    const DecodeWs L = decode_ws_layout(B, (int)max_len, Hq, d);
+    if (!block_table) return SWIATTN_EINVAL;
+    const int st = decode_args_ok(q, k_pages, v_pages, seq_lens, gate, o, B, (int)max_len, Hq, Hkv,
+                                  d, W, n_anchor, scale, dtype);
+    if (st != SWIATTN_OK) return st;
+    const DecodeWs L = decode_ws_layout(B, (int)max_len, Hq, d, n_anchor);
     if (!workspace || !aligned256(workspace) || workspace_bytes < L.total) return SWIATTN_EINVAL;
     DeviceInfo di;
     if (!device_info(di)) return SWIATTN_ECUDA;
     int lg = 0;
     while ((1 << lg) < page_size) ++lg;
     return launched(launch_decode_paged(q, k_pages, v_pages, block_table, seq_lens, gate, o, lse,
-                                        B, max_pages, lg, num_pages, Hq, Hkv, d, W, scale, dtype,
-                                        L, static_cast<char*>(workspace), di.err,
+                                        B, max_pages, lg, num_pages, Hq, Hkv, d, W, n_anchor,
+                                        scale, dtype, L, static_cast<char*>(workspace), di.err,
                                         static_cast<cudaStream_t>(stream)));
 }
 

@@ -50,7 +50,8 @@ struct DecodeWs {
     int max_chunks;
     int chunk;
 };
-DecodeWs decode_ws_layout(int B, int Lmax, int Hq, int d);
+// S: global anchors (extra anchor chunks per sequence; 0 for plain decode).
+DecodeWs decode_ws_layout(int B, int Lmax, int Hq, int d, int S);
 
 struct DualWs {
     size_t mse_part;  // float [B*N*Hq]
@@ -117,8 +118,8 @@ cudaError_t launch_dual_epilogue_parts(const float* mse_part, const float* logit
 // err: device error word (a length outside [1, Lmax] is clamped and reported).
 cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const int32_t* seq_lens,
                           const uint8_t* gate, void* o, float* lse, int B, int Lmax, int Hq,
-                          int Hkv, int d, int W, float scale, int dtype, const DecodeWs& L,
-                          char* ws, unsigned int* err, cudaStream_t s);
+                          int Hkv, int d, int W, int S, float scale, int dtype,
+                          const DecodeWs& L, char* ws, unsigned int* err, cudaStream_t s);
 
 // ------------------------------------------------------------ backward ------
 // Far-row scan of launch_schedule on its own: routed_list/routed_count/
@@ -209,7 +210,7 @@ cudaError_t launch_route_backward(const void* h, const void* w, const float* log
 cudaError_t launch_decode_paged(const void* q, const void* kp, const void* vp,
                                 const int32_t* block_table, const int32_t* seq_lens,
                                 const uint8_t* gate, void* o, float* lse, int B, int max_pages,
-                                int page_lg, int num_pages, int Hq, int Hkv, int d, int W,
+                                int page_lg, int num_pages, int Hq, int Hkv, int d, int W, int S,
                                 float scale, int dtype, const DecodeWs& L, char* ws,
                                 unsigned int* err, cudaStream_t s);
 

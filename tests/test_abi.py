@@ -126,17 +126,25 @@ def test_decode_paged_validation(lib):
     import sliding_window_attention_router_gb300 as swa
     assert swa.decode_paged_workspace(16, 512, 64, 16, 16, 128, 1024, swa.BF16) == \
         swa.decode_workspace(16, 512 * 64, 16, 16, 128, 1024, swa.BF16)
+    # anchors add whole 256-entry chunks of partials per sequence
+    assert swa.decode_anchored_workspace(16, 32768, 16, 16, 128, 1024, 256, swa.BF16) == \
+        swa.decode_workspace(16, 32768 + 256, 16, 16, 128, 1024, swa.BF16)
     assert swa.decode_paged_workspace(2, 8, 48, 4, 4, 128, 64, swa.BF16) == 0   # not a power of 2
     fake = ctypes.c_void_p(1 << 20)
     a8 = [fake] * 8
     # page size not a power of two; no pool pages; unsupported group size
-    assert lib.swiattn_decode_paged(*a8, 2, 8, 48, 16, 4, 4, 128, 64, 0.1, 1, fake, 1 << 30, None) == 1
-    assert lib.swiattn_decode_paged(*a8, 2, 8, 64, 0, 4, 4, 128, 64, 0.1, 1, fake, 1 << 30, None) == 1
-    assert lib.swiattn_decode_paged(*a8, 2, 8, 64, 16, 6, 2, 128, 64, 0.1, 1, fake, 1 << 30, None) == 2
-    # workspace too small; null block table
-    assert lib.swiattn_decode_paged(*a8, 2, 8, 64, 16, 4, 4, 128, 64, 0.1, 1, fake, 8, None) == 1
+    P = lib.swiattn_decode_paged
+    assert P(*a8, 2, 8, 48, 16, 4, 4, 128, 64, 0, 0.1, 1, fake, 1 << 30, None) == 1
+    assert P(*a8, 2, 8, 64, 0, 4, 4, 128, 64, 0, 0.1, 1, fake, 1 << 30, None) == 1
+    assert P(*a8, 2, 8, 64, 16, 6, 2, 128, 64, 0, 0.1, 1, fake, 1 << 30, None) == 2
+    # workspace too small; null block table; negative anchor count
+    assert P(*a8, 2, 8, 64, 16, 4, 4, 128, 64, 0, 0.1, 1, fake, 8, None) == 1
     nt = a8[:3] + [None] + a8[4:]
-    assert lib.swiattn_decode_paged(*nt, 2, 8, 64, 16, 4, 4, 128, 64, 0.1, 1, fake, 1 << 30, None) == 1
+    assert P(*nt, 2, 8, 64, 16, 4, 4, 128, 64, 0, 0.1, 1, fake, 1 << 30, None) == 1
+    assert P(*a8, 2, 8, 64, 16, 4, 4, 128, 64, -1, 0.1, 1, fake, 1 << 30, None) == 1
+    A = lib.swiattn_decode_anchored
+    a7 = [fake] * 7
+    assert A(*a7, 2, 64, 4, 4, 128, 8, -3, 0.1, 1, fake, 1 << 30, None) == 1
 
 
 def test_no_gpu_reports_cuda_error_or_runs(lib):

@@ -143,3 +143,43 @@ def test_length_past_cache_is_clamped_and_reported(swa):
     got = swa.decode(q.cuda(), kc.cuda(), vc.cuda(), long_sl.cuda(), gate.cuda(), 100)
     assert swa.get_device_error() == 1
     assert torch.equal(got, ref)
+
+
+@pytest.mark.parametrize("S", [1, 256, 300, 5000])
+def test_anchored_decode_matches_oracle(swa, S):
+    """Global anchors: a window query also reads the first S cache entries."""
+    B, Lmax, Hq, Hkv, d, W = 6, 3000, 4, 2, 128, 512
+    q, kc, vc, gate, sl = case(B, Lmax, Hq, Hkv, d, torch.bfloat16, 60 + S,
+                               [3000, 1, 100, 513, 2000, 777])
+    gate[:] = torch.tensor([0, 0, 0, 0, 1, 0], dtype=torch.uint8)
+    o, lse = swa.decode_anchored(q.cuda(), kc.cuda(), vc.cuda(), sl.cuda(), gate.cuda(), W, S,
+                                 want_lse=True)
+    assert swa.get_device_error() == 0
+    ref_o, ref_lse = oracle.decode_anchored(f64(q), f64(kc), f64(vc), sl.numpy(), gate.numpy(), W,
+                                            S, 1.0 / math.sqrt(d), want_lse=True)
+    err = np.abs(f64(o) - ref_o)
+    assert err.max() <= 2e-2 and err.mean() <= 2e-3, (err.max(), err.mean())
+    assert np.abs(f64(lse) - ref_lse).max() <= 1e-3
+    # exact visited counts: q = 0 gives lse = ln(number of entries read)
+    o0, lse0 = swa.decode_anchored(torch.zeros_like(q).cuda(), kc.cuda(), vc.cuda(), sl.cuda(),
+                                   gate.cuda(), W, S, want_lse=True)
+    L = sl.numpy().astype(np.int64)
+    lo = np.where(gate.numpy() != 0, 0, np.maximum(0, L - W))
+    n = (L - lo) + np.minimum(S, lo)
+    np.testing.assert_array_equal(np.rint(np.exp(f64(lse0))).astype(np.int64), n[:, None].repeat(Hq, 1))
+
+
+def test_anchored_decode_zero_is_plain_and_paged_matches(swa):
+    B, Lmax, H, d, W, S = 4, 1500, 4, 128, 300, 256
+    q, kc, vc, gate, sl = case(B, Lmax, H, H, d, torch.bfloat16, 70, [1500, 1, 299, 777])
+    gate[:] = torch.tensor([0, 0, 0, 0], dtype=torch.uint8)
+    dev = lambda t: t.cuda()
+    plain = swa.decode(dev(q), dev(kc), dev(vc), dev(sl), dev(gate), W)
+    zero = swa.decode_anchored(dev(q), dev(kc), dev(vc), dev(sl), dev(gate), W, 0)
+    assert torch.equal(plain, zero)
+    anch = swa.decode_anchored(dev(q), dev(kc), dev(vc), dev(sl), dev(gate), W, S)
+    kp, vp, table = paged_copy(kc, vc, 64, seed=71)
+    paged = swa.decode_paged(dev(q), dev(kp), dev(vp), dev(table), dev(sl), dev(gate), W,
+                             n_anchor=S)
+    assert swa.get_device_error() == 0
+    assert torch.equal(paged, anch)
