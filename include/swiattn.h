@@ -85,6 +85,18 @@ int swiattn_prefill(const void* q, const void* k, const void* v, const uint8_t* 
                     float* lse, int B, int N, int Hq, int Hkv, int d, int W, float scale,
                     int dtype, void* workspace, size_t workspace_bytes, void* stream);
 
+/* swiattn_prefill with global anchors (SWA glossary, "详细解释" platform note on
+ * 全局锚点重注入 and "SWA 落地的四个常见坑" pitfall 1, fix 2: every query also
+ * attends the first tokens, which the window never evicts; 256 there).  A
+ * window row i visits [0, min(n_anchor, i-W+1)) together with
+ * [max(0, i-W+1), i]; a routed row visits [0, i] as before.  n_anchor >= 0;
+ * 0 is swiattn_prefill.  Other arguments, and the workspace
+ * (swiattn_prefill_workspace bytes), as swiattn_prefill. */
+int swiattn_prefill_anchored(const void* q, const void* k, const void* v, const uint8_t* gate,
+                             void* o, float* lse, int B, int N, int Hq, int Hkv, int d, int W,
+                             int n_anchor, float scale, int dtype, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
 /* Bytes of device workspace swiattn_decode needs for these sizes. */
 size_t swiattn_decode_workspace(int B, int Lmax, int Hq, int Hkv, int d, int W, int dtype);
 

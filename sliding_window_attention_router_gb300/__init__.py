@@ -38,7 +38,7 @@ EXPORTS = (
     "swiattn_dual_branch", "swiattn_prefill_backward_workspace", "swiattn_prefill_backward",
     "swiattn_route_backward_workspace", "swiattn_route_backward",
     "swiattn_decode_paged_workspace", "swiattn_decode_paged", "swiattn_decode_anchored_workspace",
-    "swiattn_decode_anchored",
+    "swiattn_decode_anchored", "swiattn_prefill_anchored",
     "swiattn_get_device_error", "swiattn_status_string", "swiattn_set_profile_events",
     "swiattn_num_sms",
 )
@@ -89,6 +89,7 @@ def _load() -> ctypes.CDLL:
             lib.swiattn_decode_anchored_workspace.argtypes = [i32] * 8
             lib.swiattn_decode_anchored_workspace.restype = sz
             lib.swiattn_decode_anchored.argtypes = [vp] * 7 + [i32] * 7 + [f32, i32, vp, sz, vp]
+            lib.swiattn_prefill_anchored.argtypes = [vp] * 6 + [i32] * 7 + [f32, i32, vp, sz, vp]
             lib.swiattn_get_device_error.argtypes = [vp]
             lib.swiattn_status_string.argtypes = [i32]
             lib.swiattn_status_string.restype = ctypes.c_char_p
@@ -98,7 +99,8 @@ def _load() -> ctypes.CDLL:
             for name in ("swiattn_route", "swiattn_prefill", "swiattn_decode", "swiattn_decode_noalloc",
                          "swiattn_dual_branch", "swiattn_get_device_error", "swiattn_num_sms",
                          "swiattn_prefill_backward", "swiattn_route_backward",
-                         "swiattn_decode_paged", "swiattn_decode_anchored"):
+                         "swiattn_decode_paged", "swiattn_decode_anchored",
+                         "swiattn_prefill_anchored"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -180,8 +182,9 @@ def _workspace(nbytes: int, device, ws: Optional[torch.Tensor]):
 
 
 def prefill(q, k, v, gate, W: int, scale: Optional[float] = None, out=None, want_lse=False,
-            workspace=None):
-    """Routed prefill.  q [B,N,Hq,d], k/v [B,N,Hkv,d], gate uint8 [B,N] -> o [B,N,Hq,d]."""
+            workspace=None, n_anchor: int = 0):
+    """Routed prefill.  q [B,N,Hq,d], k/v [B,N,Hkv,d], gate uint8 [B,N] -> o [B,N,Hq,d].
+    n_anchor > 0: window rows also see the first n_anchor keys (global anchors)."""
     _dev(q, "q")
     _dev(k, "k", q.dtype)
     _dev(v, "v", q.dtype)
@@ -193,9 +196,15 @@ def prefill(q, k, v, gate, W: int, scale: Optional[float] = None, out=None, want
     lse = torch.empty((B, N, Hq), device=q.device, dtype=torch.float32) if want_lse else None
     nbytes = prefill_workspace(B, N, Hq, Hkv, d, W, q.dtype)
     ws = _workspace(nbytes, q.device, workspace)
-    _check(_load().swiattn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(o), _ptr(lse), B, N,
-                                   Hq, Hkv, d, W, float(scale), _DT[q.dtype], _ptr(ws),
-                                   ws.numel(), _stream()), "swiattn_prefill")
+    if n_anchor:
+        _check(_load().swiattn_prefill_anchored(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(o), _ptr(lse), B, N, Hq, Hkv, d, W,
+            n_anchor, float(scale), _DT[q.dtype], _ptr(ws), ws.numel(), _stream()),
+            "swiattn_prefill_anchored")
+    else:
+        _check(_load().swiattn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(o), _ptr(lse),
+                                       B, N, Hq, Hkv, d, W, float(scale), _DT[q.dtype], _ptr(ws),
+                                       ws.numel(), _stream()), "swiattn_prefill")
     return (o, lse) if want_lse else o
 
 

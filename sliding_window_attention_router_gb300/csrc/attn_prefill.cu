@@ -22,7 +22,10 @@
 //   warps 10-11 idle (complete the third warpgroup for register reconfiguration)
 // TMEM: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
 // Key sets per row (SwiAttn report, section 2; window per the weimeta.cn SWA
-// glossary): window rows [max(0, i-W+1), i], routed rows [0, i].
+// glossary): window rows [max(0, i-W+1), i], routed rows [0, i].  With S
+// global anchors (the glossary's 全局锚点) window rows also see
+// [0, min(S, i-W+1)): a band item then starts with an anchor run of blocks
+// from key 0 before its window run.
 
 #include "ptx.cuh"
 #include "swiattn_internal.h"
@@ -94,19 +97,23 @@ struct PfParams {
     float* lse;
     unsigned int* err;
     int B, N, Hq, Hkv, W, NT;
+    int S;             // global anchors of window rows (0: none)
     float scale_log2;
 };
 
 struct Plan {
     int b, h, kvh, kind;
     int row0;          // band: first query row of tile A; far: first compacted index of tile A
-    int kv0, nblk;     // first key of the block sequence and its length
-    int j0[2], j1[2];  // active block range per tile (j0 > j1: tile empty)
+    int kv0, nblk;     // first key of the window run and the block sequence's length
+    int na;            // anchor blocks at the head of the sequence (keys from 0)
+    int ja1[2];        // anchor run per tile: blocks 0 .. ja1 (-1: none)
+    int j0[2], j1[2];  // window (or far) run per tile (j0 > j1: tile empty)
     int nrows[2];      // valid rows per tile
 };
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 
+template <bool ANCH>
 __device__ __forceinline__ Plan make_plan(const PfParams& p, int idx) {
     const WorkItem it = p.items[idx];
     Plan pl;
@@ -115,6 +122,8 @@ __device__ __forceinline__ Plan make_plan(const PfParams& p, int idx) {
     pl.kvh = it.h / (p.Hq / p.Hkv);
     pl.kind = it.kind;
     pl.row0 = it.tile * 2 * kBM;
+    pl.na = 0;
+    pl.ja1[0] = pl.ja1[1] = -1;
     if (it.kind == kItemFar) {
         const int cnt = p.routed_count[it.b];
         const int* list = p.routed_list + (size_t)it.b * p.N;
@@ -146,17 +155,40 @@ __device__ __forceinline__ Plan make_plan(const PfParams& p, int idx) {
                 pl.j0[x] = (lo_key - pl.kv0) / kBN;
                 pl.j1[x] = (hi_key - pl.kv0) / kBN;
                 last = max(last, pl.j1[x]);
+                const int hi_anchor = min(p.S - 1, hi_key - p.W);   // anchors below the window
+                if (ANCH && hi_anchor >= 0) {
+                    pl.ja1[x] = hi_anchor / kBN;
+                    pl.na = max(pl.na, pl.ja1[x] + 1);
+                }
             } else {
                 pl.j0[x] = 1;
                 pl.j1[x] = 0;
             }
         }
-        pl.nblk = last + 1;
+        // The window runs follow the anchor blocks.
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+            pl.j0[x] += pl.na;
+            pl.j1[x] += pl.na;
+        }
+        pl.nblk = last + 1 + pl.na;
     }
     return pl;
 }
 
 __device__ __forceinline__ bool tile_active(const Plan& pl, int x) { return pl.j0[x] <= pl.j1[x]; }
+template <bool ANCH>
+__device__ __forceinline__ bool blk_active(const Plan& pl, int x, int j) {
+    return (ANCH && j <= pl.ja1[x]) || (j >= pl.j0[x] && j <= pl.j1[x]);
+}
+template <bool ANCH>
+__device__ __forceinline__ int first_blk(const Plan& pl, int x) {
+    return (ANCH && pl.ja1[x] >= 0) ? 0 : pl.j0[x];
+}
+template <bool ANCH>
+__device__ __forceinline__ int blk_key0(const Plan& pl, int j) {
+    return (ANCH && j < pl.na) ? j * kBN : pl.kv0 + (j - (ANCH ? pl.na : 0)) * kBN;
+}
 
 // ----------------------------------------------------------------- roles --
 //
@@ -197,6 +229,7 @@ __device__ bool consume_item(const PfParams& p, uint64_t* bar, volatile int* sch
 // Producer warp (converged, one elected lane issues): per item, the Q tiles,
 // then one K/V slot per step g: step j of an item carries K_j (j < nblk) and
 // V_{j-1} (j >= 1), so a slot is freed by one commit after S(j) and PV(j-1).
+template <bool ANCH>
 __device__ bool producer(const PfParams& p, uint8_t* smem, uint64_t* bar, volatile int* sched,
                          volatile int* abort_flag, uint32_t& g, uint32_t* q_issued) {
     const int n = *p.n_items;
@@ -204,7 +237,7 @@ __device__ bool producer(const PfParams& p, uint8_t* smem, uint64_t* bar, volati
         int idx;
         if (!publish_item(p, bar, sched, k, n, abort_flag, idx)) return false;
         if (idx < 0) break;
-        const Plan pl = make_plan(p, idx);
+        const Plan pl = make_plan<ANCH>(p, idx);
         const CUtensorMap* qm = (pl.kind == kItemFar) ? &p.tm_qc : &p.tm_q;
         auto load_q = [&](int x) -> bool {
             if (!mbar_wait_w(&bar[BAR_Q_EMPTY + x], (q_issued[x] & 1u) ^ 1u, abort_flag, p.err)) return false;
@@ -218,20 +251,20 @@ __device__ bool producer(const PfParams& p, uint8_t* smem, uint64_t* bar, volati
         };
         if (tile_active(pl, 0) && !load_q(0)) return false;
         for (int j = 0; j <= pl.nblk; ++j) {
-            if (j < pl.nblk && tile_active(pl, 1) && j == pl.j0[1] && !load_q(1)) return false;
+            if (j < pl.nblk && tile_active(pl, 1) && j == first_blk<ANCH>(pl, 1) && !load_q(1)) return false;
             const uint32_t st = g % kStages, ph = (g / kStages) & 1u;
             if (!mbar_wait_w(&bar[BAR_KV_EMPTY + st], ph ^ 1u, abort_flag, p.err)) return false;
             const uint32_t bytes = (j < pl.nblk ? kTileBytes : 0) + (j >= 1 ? kTileBytes : 0);
             mbar_arrive_expect_tx_w(&bar[BAR_KV_FULL + st], bytes);
             if (j < pl.nblk) {
                 uint8_t* dst = smem + kOffK + st * kTileBytes;
-                const int key0 = pl.kv0 + j * kBN;
+                const int key0 = blk_key0<ANCH>(pl, j);
                 tma_load_4d_w(dst, &p.tm_k, &bar[BAR_KV_FULL + st], 0, pl.kvh, key0, pl.b);
                 tma_load_4d_w(dst + kHalfBytes, &p.tm_k, &bar[BAR_KV_FULL + st], 64, pl.kvh, key0, pl.b);
             }
             if (j >= 1) {
                 uint8_t* dst = smem + kOffV + st * kTileBytes;
-                const int key0 = pl.kv0 + (j - 1) * kBN;
+                const int key0 = blk_key0<ANCH>(pl, j - 1);
                 tma_load_4d_w(dst, &p.tm_v, &bar[BAR_KV_FULL + st], 0, pl.kvh, key0, pl.b);
                 tma_load_4d_w(dst + kHalfBytes, &p.tm_v, &bar[BAR_KV_FULL + st], 64, pl.kvh, key0, pl.b);
             }
@@ -248,6 +281,7 @@ __device__ void drain_loads(uint64_t* full_bars, uint32_t issued) {
     }
 }
 
+template <bool ANCH>
 __device__ bool mma_issuer(const PfParams& p, uint8_t* smem, uint64_t* bar, volatile int* sched,
                            uint32_t tmem, volatile int* abort_flag) {
     uint32_t g = 0;
@@ -257,7 +291,7 @@ __device__ bool mma_issuer(const PfParams& p, uint8_t* smem, uint64_t* bar, vola
         int idx;
         if (!consume_item(p, bar, sched, k, abort_flag, idx)) return false;
         if (idx < 0) break;
-        const Plan pl = make_plan(p, idx);
+        const Plan pl = make_plan<ANCH>(p, idx);
         int pend[2] = {-1, -1};
         bool first_pv[2] = {true, true};
 
@@ -294,8 +328,8 @@ __device__ bool mma_issuer(const PfParams& p, uint8_t* smem, uint64_t* bar, vola
                     if (!issue_pv(x, pend[x], sV)) return false;
                     pend[x] = -1;
                 }
-                if (j < pl.nblk && j >= pl.j0[x] && j <= pl.j1[x]) {
-                    if (j == pl.j0[x]) {
+                if (j < pl.nblk && blk_active<ANCH>(pl, x, j)) {
+                    if (j == first_blk<ANCH>(pl, x)) {
                         if (!mbar_wait_w(&bar[BAR_Q_FULL + x], q_cnt[x] & 1u, abort_flag, p.err))
                             return false;
                         ++q_cnt[x];
@@ -325,6 +359,9 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
     return mbar_wait_w(bar, parity, abort_flag, err);
 }
 
+// ANCH: the launch has global anchors (p.S > 0); without them the anchor run
+// is compiled out and the loop is the plain window / far walk.
+template <bool ANCH>
 __device__ bool softmax_role(const PfParams& p, uint8_t* smem, uint64_t* bar, volatile int* sched,
                              uint32_t tmem, volatile int* abort_flag, int x, int wq, int lane) {
     const int r = wq * 32 + lane;
@@ -340,7 +377,7 @@ __device__ bool softmax_role(const PfParams& p, uint8_t* smem, uint64_t* bar, vo
         int idx;
         if (!consume_item(p, bar, sched, k, abort_flag, idx)) return false;
         if (idx < 0) break;
-        const Plan pl = make_plan(p, idx);
+        const Plan pl = make_plan<ANCH>(p, idx);
         if (!tile_active(pl, x)) continue;
         const bool far = pl.kind == kItemFar;
         int i = -1;
@@ -353,10 +390,17 @@ __device__ bool softmax_role(const PfParams& p, uint8_t* smem, uint64_t* bar, vo
         const int lo = (i < 0) ? 1 : (far ? 0 : max(0, i - p.W + 1));
         const int hi = (i < 0) ? 0 : i;
 
+        // With anchors the tile first walks its anchor run (blocks 0 .. ja1,
+        // keys from 0, this row's anchors below its window being
+        // [0, min(S, i-W+1))), skipping any block between the two runs.
+        const int e_anc = (ANCH && i >= 0 && !far) ? min(p.S - 1, i - p.W) : -1;
+
         float m2 = -INFINITY, l = 0.f;
-        for (int j = pl.j0[x]; j <= pl.j1[x]; ++j) {
-            const int key0 = pl.kv0 + j * kBN;
-            const int a = lo - key0, e = hi - key0;
+        for (int j = first_blk<ANCH>(pl, x); j <= pl.j1[x]; ++j) {
+            if (ANCH && j > pl.ja1[x] && j < pl.j0[x]) continue;
+            const bool anc = ANCH && j <= pl.ja1[x];
+            const int key0 = blk_key0<ANCH>(pl, j);
+            const int a = (anc ? 0 : lo) - key0, e = (anc ? e_anc : hi) - key0;
             if (!warp_wait(&bar[BAR_S_FULL + x], s_cnt & 1u, abort_flag, p.err)) return false;
             ++s_cnt;
             tc_fence_after();
@@ -486,6 +530,7 @@ __device__ bool softmax_role(const PfParams& p, uint8_t* smem, uint64_t* bar, vo
     return true;
 }
 
+template <bool ANCH>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PfParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -528,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 
     if (warp < 8) {
         warpgroup_reg_inc<kRegsSoftmax>();
-        softmax_role(p, smem, bar, sched, tmem, abort_flag, warp >> 2, warp & 3, lane);
+        softmax_role<ANCH>(p, smem, bar, sched, tmem, abort_flag, warp >> 2, warp & 3, lane);
     } else {
         warpgroup_reg_dec<kRegsOther>();
     }
@@ -541,14 +586,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         }
         __syncwarp();
         uint32_t g = 0, q_issued[2] = {0, 0};
-        if (!producer(p, smem, bar, sched, abort_flag, g, q_issued)) {
+        if (!producer<ANCH>(p, smem, bar, sched, abort_flag, g, q_issued)) {
             drain_loads(&bar[BAR_KV_FULL], g);
             for (int x = 0; x < 2; ++x)
                 if (q_issued[x]) mbar_drain(&bar[BAR_Q_FULL + x], (q_issued[x] - 1) & 1u);
         }
         __syncwarp();
     } else if (warp == 9) {
-        mma_issuer(p, smem, bar, sched, tmem, abort_flag);
+        mma_issuer<ANCH>(p, smem, bar, sched, tmem, abort_flag);
         // Every MMA this warp issued has completed once this arrives.
         umma_commit_w(&bar[BAR_DRAIN]);
         mbar_drain(&bar[BAR_DRAIN], 0);
@@ -590,16 +635,23 @@ cudaError_t launch_prefill_tc(const TcAttnArgs& a, const int* tile_prefix, unsig
     p.Hq = a.Hq;
     p.Hkv = a.Hkv;
     p.W = a.W;
+    p.S = a.n_anchor;
     p.NT = (a.N + kBM - 1) / kBM;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(prefill_kernel<false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(prefill_kernel<true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    prefill_kernel<<<num_sms, kThreads, kSmemBytes, s>>>(p);
+    if (p.S > 0)
+        prefill_kernel<true><<<num_sms, kThreads, kSmemBytes, s>>>(p);
+    else
+        prefill_kernel<false><<<num_sms, kThreads, kSmemBytes, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -5,7 +5,8 @@
 // so that it matches the fp64 definition to ~1e-6.  One warp owns one
 // (batch, row, head); keys are visited one at a time with an online softmax.
 // Key range per row (SwiAttn report, section 2; SWA window per the weimeta.cn
-// glossary): routed [0, i], window [max(0, i-W+1), i].
+// glossary): routed [0, i], window [max(0, i-W+1), i], plus for a window row
+// the global anchors [0, min(S, i-W+1)) (the glossary's 全局锚点).
 
 #include "swiattn_internal.h"
 
@@ -19,7 +20,7 @@ template <int D>
 __global__ void __launch_bounds__(128) simt_attention_kernel(
     const float* __restrict__ q, const float* __restrict__ k, const float* __restrict__ v,
     const uint8_t* __restrict__ gate, int force, float* __restrict__ o, float* __restrict__ lse,
-    int B, int N, int Hq, int Hkv, int W, float scale) {
+    int B, int N, int Hq, int Hkv, int W, int S, float scale) {
     constexpr int PER = D / 32;
     const int lane = threadIdx.x & 31;
     const int64_t row = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
@@ -31,6 +32,7 @@ __global__ void __launch_bounds__(128) simt_attention_kernel(
     const int kvh = h / (Hq / Hkv);
     const bool routed = force >= 0 ? force != 0 : gate[(size_t)b * N + i] != 0;
     const int lo = routed ? 0 : max(0, i - W + 1);
+    const int na = min(S, lo);   // anchors below the window (0 for routed rows)
 
     float qv[PER], acc[PER];
 #pragma unroll
@@ -41,7 +43,8 @@ __global__ void __launch_bounds__(128) simt_attention_kernel(
     float m = -INFINITY, l = 0.f;
     const float* kb = k + ((size_t)b * N * Hkv + kvh) * D;
     const float* vb = v + ((size_t)b * N * Hkv + kvh) * D;
-    for (int j = lo; j <= i; ++j) {
+    for (int jj = 0; jj < na + (i - lo + 1); ++jj) {
+        const int j = jj < na ? jj : lo + (jj - na);
         const float* kj = kb + (size_t)j * Hkv * D;
         float part = 0.f;
 #pragma unroll
@@ -117,8 +120,8 @@ __global__ void dual_epilogue_parts_kernel(const float* __restrict__ part,
 
 cudaError_t launch_simt_attention(const void* q, const void* k, const void* v,
                                   const uint8_t* gate, int force, void* o, float* lse, int B,
-                                  int N, int Hq, int Hkv, int d, int W, float scale, int dtype,
-                                  cudaStream_t s) {
+                                  int N, int Hq, int Hkv, int d, int W, int S, float scale,
+                                  int dtype, cudaStream_t s) {
     if (dtype != 0) return cudaErrorInvalidValue;
     const int64_t rows = (int64_t)B * N * Hq;
     const unsigned blocks = static_cast<unsigned>((rows + 3) / 4);
@@ -128,10 +131,10 @@ cudaError_t launch_simt_attention(const void* q, const void* k, const void* v,
     float* of = static_cast<float*>(o);
     if (d == 64)
         simt_attention_kernel<64><<<blocks, 128, 0, s>>>(qf, kf, vf, gate, force, of, lse, B, N, Hq,
-                                                         Hkv, W, scale);
+                                                         Hkv, W, S, scale);
     else if (d == 128)
         simt_attention_kernel<128><<<blocks, 128, 0, s>>>(qf, kf, vf, gate, force, of, lse, B, N,
-                                                          Hq, Hkv, W, scale);
+                                                          Hq, Hkv, W, S, scale);
     else
         return cudaErrorInvalidValue;
     return cudaGetLastError();

@@ -92,11 +92,19 @@ __device__ __forceinline__ int band_tile_blocks(int b, int r0, int kv0, const in
     return (r0 + nrows - 1 - kv0) / kBN - (lo_key - kv0) / kBN + 1;
 }
 
+// Anchor key blocks a band tile starting at row r0 adds (window rows see the
+// first S keys too): keys [0, min(S, last row - W + 1)).
+__device__ __forceinline__ int anchor_blocks(int r0, int N, int W, int S) {
+    const int last = min(N, r0 + kBM) - 1;
+    const int hi = min(S - 1, last - W);
+    return (S > 0 && last >= r0 && hi >= 0) ? hi / kBN + 1 : 0;
+}
+
 // Cost (key blocks over both tiles) of pair u of the enumeration
 // [far pairs | band pairs] per batch; 0 when the pair has nothing to do.
 __device__ __forceinline__ int pair_cost(int u, const int* routed_list, const int* routed_count,
-                                         const int* tile_prefix, int N, int W, int NT, int NP,
-                                         int& b, int& kind, int& pair) {
+                                         const int* tile_prefix, int N, int W, int S, int NT,
+                                         int NP, int& b, int& kind, int& pair) {
     b = u / (2 * NP);
     const int rem = u % (2 * NP);
     if (rem < NP) {
@@ -116,8 +124,10 @@ __device__ __forceinline__ int pair_cost(int u, const int* routed_list, const in
     pair = rem - NP;
     const int q0 = pair * 2 * kBM;
     const int kv0 = max(0, q0 - W + 1);
-    return band_tile_blocks(b, q0, kv0, tile_prefix, N, W, NT) +
-           band_tile_blocks(b, q0 + kBM, kv0, tile_prefix, N, W, NT);
+    const int na = max(anchor_blocks(q0, N, W, S), anchor_blocks(q0 + kBM, N, W, S));
+    const int cost = band_tile_blocks(b, q0, kv0, tile_prefix, N, W, NT) +
+                     band_tile_blocks(b, q0 + kBM, kv0, tile_prefix, N, W, NT);
+    return cost > 0 ? cost + 2 * na : 0;
 }
 
 // Block 0: counting sort of 256-row pairs by descending cost, Hq items per
@@ -130,7 +140,8 @@ constexpr int kBucketsPerThread = kCostBuckets / kBuildThreads;
 
 __global__ void __launch_bounds__(kBuildThreads) build_and_gather_kernel(
     const int* __restrict__ routed_list, const int* __restrict__ routed_count,
-    const int* __restrict__ tile_prefix, int B, int N, int Hq, int W, WorkItem* __restrict__ items,
+    const int* __restrict__ tile_prefix, int B, int N, int Hq, int W, int S,
+    WorkItem* __restrict__ items,
     int* __restrict__ n_items, const uint4* __restrict__ q, uint4* __restrict__ qc) {
     if (blockIdx.x == 0) {
         __shared__ int hist[kCostBuckets];
@@ -142,7 +153,7 @@ __global__ void __launch_bounds__(kBuildThreads) build_and_gather_kernel(
         __syncthreads();
         for (int u = threadIdx.x; u < U; u += blockDim.x) {
             int b, kind, pair;
-            const int cost = pair_cost(u, routed_list, routed_count, tile_prefix, N, W, NT, NP, b, kind, pair);
+            const int cost = pair_cost(u, routed_list, routed_count, tile_prefix, N, W, S, NT, NP, b, kind, pair);
             if (cost > 0) atomicAdd(&hist[min(cost, kCostBuckets - 1)], 1);
         }
         __syncthreads();
@@ -164,7 +175,7 @@ __global__ void __launch_bounds__(kBuildThreads) build_and_gather_kernel(
         __syncthreads();
         for (int u = threadIdx.x; u < U; u += blockDim.x) {
             int b, kind, pair;
-            const int cost = pair_cost(u, routed_list, routed_count, tile_prefix, N, W, NT, NP, b, kind, pair);
+            const int cost = pair_cost(u, routed_list, routed_count, tile_prefix, N, W, S, NT, NP, b, kind, pair);
             if (cost <= 0) continue;
             const int pos = atomicAdd(&hist[min(cost, kCostBuckets - 1)], 1);
             for (int h = 0; h < Hq; ++h) items[(size_t)pos * Hq + h] = WorkItem{kind, b, h, pair};
@@ -215,14 +226,14 @@ PrefillWs prefill_ws_layout(int B, int N, int Hq, int d) {
     return L;
 }
 
-cudaError_t launch_schedule(const uint8_t* gate, const void* q, int B, int N, int Hq, int W,
+cudaError_t launch_schedule(const uint8_t* gate, const void* q, int B, int N, int Hq, int W, int S,
                             const PrefillWs& L, char* ws, int num_sms, cudaStream_t s) {
     int* list = reinterpret_cast<int*>(ws + L.routed_list);
     int* count = reinterpret_cast<int*>(ws + L.routed_count);
     int* prefix = reinterpret_cast<int*>(ws + L.tile_prefix);
     scan_far_rows_kernel<<<B, kScanThreads, 0, s>>>(gate, N, W, list, count, prefix);
     build_and_gather_kernel<<<1 + num_sms * 2, kBuildThreads, 0, s>>>(
-        list, count, prefix, B, N, Hq, W, reinterpret_cast<WorkItem*>(ws + L.items),
+        list, count, prefix, B, N, Hq, W, S, reinterpret_cast<WorkItem*>(ws + L.items),
         reinterpret_cast<int*>(ws + L.n_items), static_cast<const uint4*>(q),
         reinterpret_cast<uint4*>(ws + L.qc));
     return cudaGetLastError();

@@ -175,14 +175,22 @@ size_t swiattn_prefill_workspace(int B, int N, int Hq, int Hkv, int d, int W, in
 int swiattn_prefill(const void* q, const void* k, const void* v, const uint8_t* gate, void* o,
                     float* lse, int B, int N, int Hq, int Hkv, int d, int W, float scale,
                     int dtype, void* workspace, size_t workspace_bytes, void* stream) {
-    if (!attn_shape_ok(B, N, Hq, Hkv, d, W)) return SWIATTN_EINVAL;
+    return swiattn_prefill_anchored(q, k, v, gate, o, lse, B, N, Hq, Hkv, d, W, 0, scale, dtype,
+                                    workspace, workspace_bytes, stream);
+}
+
+int swiattn_prefill_anchored(const void* q, const void* k, const void* v, const uint8_t* gate,
+                             void* o, float* lse, int B, int N, int Hq, int Hkv, int d, int W,
+                             int n_anchor, float scale, int dtype, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+    if (!attn_shape_ok(B, N, Hq, Hkv, d, W) || n_anchor < 0) return SWIATTN_EINVAL;
     if (!q || !k || !v || !gate || !o) return SWIATTN_EINVAL;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return SWIATTN_EINVAL;
     if (!(scale > 0.f)) return SWIATTN_EINVAL;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (dtype == SWIATTN_F32) {
         return launched(launch_simt_attention(q, k, v, gate, -1, o, lse, B, N, Hq, Hkv, d, W,
-                                              scale, dtype, s));
+                                              n_anchor, scale, dtype, s));
     }
     if (dtype != SWIATTN_BF16) return SWIATTN_EINVAL;
     if (d != kHD) return SWIATTN_EUNSUPPORTED;
@@ -191,7 +199,7 @@ int swiattn_prefill(const void* q, const void* k, const void* v, const uint8_t* 
     DeviceInfo di;
     if (!device_info(di)) return SWIATTN_ECUDA;
     char* ws = static_cast<char*>(workspace);
-    cudaError_t e = launch_schedule(gate, q, B, N, Hq, W, L, ws, di.sms, s);
+    cudaError_t e = launch_schedule(gate, q, B, N, Hq, W, n_anchor, L, ws, di.sms, s);
     if (e != cudaSuccess) return SWIATTN_ECUDA;
     TcAttnArgs a;
     std::memset(&a, 0, sizeof(a));
@@ -211,6 +219,7 @@ int swiattn_prefill(const void* q, const void* k, const void* v, const uint8_t* 
     a.Hq = Hq;
     a.Hkv = Hkv;
     a.W = W;
+    a.n_anchor = n_anchor;
     a.scale = scale;
     prof_start(s);
     e = launch_prefill_tc(a, reinterpret_cast<const int*>(ws + L.tile_prefix), di.err, di.sms, s);
@@ -326,9 +335,9 @@ int swiattn_dual_branch(const void* q, const void* k, const void* v, const float
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (dtype == SWIATTN_F32) {
         cudaError_t e = launch_simt_attention(q, k, v, nullptr, 1, o_full, nullptr, B, N, Hq, Hkv,
-                                              d, W, scale, dtype, s);
+                                              d, W, 0, scale, dtype, s);
         if (e == cudaSuccess)
-            e = launch_simt_attention(q, k, v, nullptr, 0, o_swa, nullptr, B, N, Hq, Hkv, d, W,
+            e = launch_simt_attention(q, k, v, nullptr, 0, o_swa, nullptr, B, N, Hq, Hkv, d, W, 0,
                                       scale, dtype, s);
         if (e == cudaSuccess)
             e = launch_dual_epilogue_f32(static_cast<const float*>(o_full),

@@ -66,7 +66,8 @@ DualWs dual_ws_layout(int B, int N, int Hq, int d, int dtype);
 cudaError_t launch_route(const void* h, const void* w, float bias, int64_t tokens, int d_model,
                          int dtype, float* logits, uint8_t* gate, cudaStream_t s);
 
-cudaError_t launch_schedule(const uint8_t* gate, const void* q, int B, int N, int Hq, int W,
+// S: global anchors of window rows (adds their key blocks to band items' cost).
+cudaError_t launch_schedule(const uint8_t* gate, const void* q, int B, int N, int Hq, int W, int S,
                             const PrefillWs& L, char* ws, int num_sms, cudaStream_t s);
 
 struct TcAttnArgs {
@@ -88,6 +89,7 @@ struct TcAttnArgs {
     float* snap;           // dual: fp32 O_SWA rows
     int* counter;          // dual: work counter (zeroed by the launcher)
     int B, N, Hq, Hkv, W;
+    int n_anchor;          // prefill: global anchors of window rows (0: none)
     float scale;
 };
 
@@ -99,10 +101,11 @@ cudaError_t launch_dual_tc(const TcAttnArgs& a, unsigned int* err, int num_sms, 
 cudaError_t launch_prefill_tc(const TcAttnArgs& a, const int* tile_prefix, unsigned int* err,
                               int num_sms, cudaStream_t s);
 
+// S: global anchors of window rows (0: none).
 cudaError_t launch_simt_attention(const void* q, const void* k, const void* v,
                                   const uint8_t* gate, int force, void* o, float* lse, int B,
-                                  int N, int Hq, int Hkv, int d, int W, float scale, int dtype,
-                                  cudaStream_t s);
+                                  int N, int Hq, int Hkv, int d, int W, int S, float scale,
+                                  int dtype, cudaStream_t s);
 
 cudaError_t launch_dual_epilogue_f32(const float* o_full, const float* o_swa,
                                      const float* logits, const float* nll, float* o_gated,
