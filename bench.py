@@ -73,11 +73,13 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def useful_pairs(gate: np.ndarray, W: int) -> int:
-    """Visited (query, key) pairs per head: routed rows i+1, window rows min(i+1, W)."""
+def useful_pairs(gate: np.ndarray, W: int, S: int = 0) -> int:
+    """Visited (query, key) pairs per head: routed rows i+1, window rows
+    min(i+1, W) plus their global anchors below the window, min(S, i-W+1)."""
     B, N = gate.shape
     i = np.arange(N, dtype=np.int64)[None, :]
-    n = np.where(gate != 0, i + 1, np.minimum(i + 1, W))
+    window = np.minimum(i + 1, W) + np.clip(np.minimum(S, i - W + 1), 0, None)
+    n = np.where(gate != 0, i + 1, window)
     return int(n.sum())
 
 
@@ -278,7 +280,7 @@ def prefill_section(swa, timer, dev, frac, steps, warmup, seed, with_e2e, N=3276
     return res
 
 
-def decode_section(swa, timer, dev, steps, warmup, seed):
+def decode_section(swa, timer, dev, steps, warmup, seed, S=0):
     B, L, H, D, W = 16, 32768, 16, 128, 1024
     g = torch.Generator(device=dev)
     g.manual_seed(seed)
@@ -292,17 +294,68 @@ def decode_section(swa, timer, dev, steps, warmup, seed):
     ws = torch.empty(swa.decode_workspace(B, L, H, H, D, W, torch.bfloat16), dtype=torch.uint8,
                      device=dev)
     n_routed = int(gate.sum())
-    entries = n_routed * L + (B - n_routed) * W
+    entries = n_routed * L + (B - n_routed) * (W + min(S, L - W))
     kv_bytes = entries * H * D * 2 * 2
     qo_bytes = 2 * B * H * D * 2
+    if S:
+        ws = torch.empty(swa.decode_anchored_workspace(B, L, H, H, D, W, S, torch.bfloat16),
+                         dtype=torch.uint8, device=dev)
 
     def step():
-        swa.decode(q, kc, vc, sl, gate, W, out=o, workspace=ws)
+        if S:
+            swa.decode_anchored(q, kc, vc, sl, gate, W, S, out=o, workspace=ws)
+        else:
+            swa.decode(q, kc, vc, sl, gate, W, out=o, workspace=ws)
 
     step_ms, kern_ms = timer.run(step, steps, warmup, kernel_events=True)
     assert swa.get_device_error() == 0
     del kc, vc
     return dict(step_ms=step_ms, kern_ms=kern_ms, bytes=kv_bytes + qo_bytes, n_routed=n_routed)
+
+
+def anchored_prefill_section(swa, timer, dev, steps, warmup, seed, S=256):
+    """The long-context prefill workload with S global anchors per window row
+    (the SWA glossary's 256-token anchor set)."""
+    d = inp.prefill_32k(frac=0.13, seed=seed)
+    B, N, H, D, W = d["B"], d["N"], d["Hq"], d["d"], d["W"]
+    q, k, v, gate = (d[n].to(dev) for n in ("q", "k", "v", "gate"))
+    o = torch.empty_like(q)
+    ws = torch.empty(swa.prefill_workspace(B, N, H, H, D, W, torch.bfloat16), dtype=torch.uint8,
+                     device=dev)
+
+    def step():
+        swa.prefill(q, k, v, gate, W, out=o, workspace=ws, n_anchor=S)
+
+    step_ms, kern_ms = timer.run(step, steps, warmup, kernel_events=True)
+    assert swa.get_device_error() == 0
+    flops = 4.0 * D * H * useful_pairs(d["gate"].numpy(), W, S)
+    return dict(step_ms=step_ms, kern_ms=kern_ms, flops=flops)
+
+
+def static_hybrid_section(swa, timer, dev, steps, warmup, seed):
+    """Comparator: the static 3:1 hybrid (SWA blog, Mellum 2: three window layers
+    then one full-attention layer, W = 1024) on the long-context prefill
+    workload.  A step is one group of four layers (the same Q/K/V per layer);
+    per-layer time compares with one routed layer at the report's average
+    routed fraction."""
+    d = inp.prefill_32k(frac=0.13, seed=seed)
+    B, N, H, D, W = d["B"], d["N"], d["Hq"], d["d"], d["W"]
+    q, k, v = (d[n].to(dev) for n in ("q", "k", "v"))
+    zeros = torch.zeros((B, N), dtype=torch.uint8, device=dev)
+    ones = torch.ones((B, N), dtype=torch.uint8, device=dev)
+    o = torch.empty_like(q)
+    ws = torch.empty(swa.prefill_workspace(B, N, H, H, D, W, torch.bfloat16), dtype=torch.uint8,
+                     device=dev)
+
+    def step():
+        for g in (zeros, zeros, zeros, ones):
+            swa.prefill(q, k, v, g, W, out=o, workspace=ws)
+
+    step_ms, _ = timer.run(step, steps, warmup)
+    assert swa.get_device_error() == 0
+    zc, oc = np.zeros((B, N), np.uint8), np.ones((B, N), np.uint8)
+    flops = 4.0 * D * H * (3 * useful_pairs(zc, W) + useful_pairs(oc, W))
+    return dict(step_ms=step_ms, flops=flops)
 
 
 def decode_paged_section(swa, timer, dev, steps, warmup, seed, page_size=64):
@@ -569,6 +622,13 @@ def run_ours(args, dist: Dist):
                          "kernel": "decode_split_kernel"},
             "workload": "decode bf16: 16 sequences x 32768 cached tokens, H=16, d=128, W=1024, "
                         "gate Bernoulli(0.13)"}
+        da = decode_section(swa, timer, dev, ks, kw, seed=dist.rank, S=256)
+        das = statistics.mean(da["step_ms"]) / 1e3
+        extra["decode_anchored"] = {
+            "gbs": da["bytes"] / das / 1e9, "ms_per_step": das * 1e3,
+            "kernel_gbs": da["bytes"] / (statistics.mean(da["kern_ms"]) / 1e3) / 1e9,
+            "workload": "decode bf16, 16 x 32768 cached tokens, window queries also read the "
+                        "first 256 entries"}
         dp = decode_paged_section(swa, timer, dev, ks, kw, seed=dist.rank)
         dpk = statistics.mean(dp["kern_ms"]) / 1e3
         dps = statistics.mean(dp["step_ms"]) / 1e3
@@ -577,6 +637,22 @@ def run_ours(args, dist: Dist):
             "kernel_gbs": dp["bytes"] / dpk / 1e9, "kernel_frac_of_hbm": dp["bytes"] / dpk / 1e9 / hbm,
             "workload": "decode bf16 on a paged cache: 16 sequences x 32768 tokens in 64-token "
                         "pages of a shuffled pool, H=16, d=128, W=1024, gate Bernoulli(0.13)"}
+        an = anchored_prefill_section(swa, timer, dev, ks, kw, seed=dist.rank)
+        ans = statistics.mean(an["step_ms"]) / 1e3
+        extra["prefill_anchored"] = {
+            "tflops": an["flops"] / ans / 1e12, "ms_per_step": ans * 1e3,
+            "kernel_tflops": an["flops"] / (statistics.mean(an["kern_ms"]) / 1e3) / 1e12,
+            "useful_tflop": an["flops"] / 1e12,
+            "workload": "long-context routed prefill (N=32768, f=0.13) with 256 global anchors "
+                        "per window row"}
+        sh = static_hybrid_section(swa, timer, dev, ks, kw, seed=dist.rank)
+        shs = statistics.mean(sh["step_ms"]) / 1e3
+        extra["static_hybrid_3to1"] = {
+            "ms_per_layer": shs * 1e3 / 4, "routed_ms_per_layer": 1e3 * slowest / args.steps,
+            "tflops": sh["flops"] / shs / 1e12,
+            "workload": "comparator: three window layers and one full layer (W=1024) per group "
+                        "of four, N=32768, H=16, d=128; per-layer time beside one routed layer "
+                        "at routed fraction 0.13"}
         rt = route_section(swa, timer, dev, ks, kw, seed=dist.rank)
         rs = statistics.mean(rt["step_ms"]) / 1e3
         extra["route"] = {"gbs": rt["bytes"] / rs / 1e9, "ms_per_step": rs * 1e3,
