@@ -44,12 +44,18 @@ L2_FLUSH_BYTES = 256 << 20
 # SHA-256 of the kernel's source files at capture time; a kernel whose source
 # has changed since reports null.
 MEASURED_TRAFFIC = {
-    # prefill_kernel, long-context prefill N=32768 f=0.13: 1 082 483 456 read + 132 495 104 written
-    ("prefill", "2376c004e3f9ab56"): 1082483456 + 132495104,
+    # prefill_kernel, long-context prefill N=32768 f=0.13: 1 110 540 800 read + 136 363 520 written
+    ("prefill", "f4d24d0f3fd8fea5"): 1110540800 + 136363520,
     # decode_split_kernel, 16 x 32768 decode: 654 405 376 read + 2 758 912 written
     ("decode", "023308e7542f8d17"): 654405376 + 2758912,
+    # dual_kernel, dual-branch workload B=2 N=8192 GQA 16/4: 155 273 984 read + 272 345 088 written
+    ("dual", "96d14ef8dc35435e"): 155273984 + 272345088,
+    # dkdv_kernel + dq_kernel, backward on the dual workload: (319 030 528 + 21 871 872)
+    # + (257 355 264 + 47 116 032)
+    ("backward", "2a7d1a1f50c044a1"): 319030528 + 21871872 + 257355264 + 47116032,
 }
-KERNEL_SOURCES = {"prefill": ("attn_prefill.cu", "ptx.cuh"), "decode": ("decode.cu",)}
+KERNEL_SOURCES = {"prefill": ("attn_prefill.cu", "ptx.cuh"), "decode": ("decode.cu",),
+                  "dual": ("attn_dual.cu", "ptx.cuh"), "backward": ("attn_bwd.cu", "ptx.cuh")}
 
 
 def kernel_source_hash(kernel: str) -> str:
@@ -665,8 +671,12 @@ def run_ours(args, dist: Dist):
                                          "then routed prefill B=1 H=16 d=128 N=4096 W=1024 on its gates"}
         du = dual_section(swa, timer, dev, ks, kw, seed=dist.rank)
         dm = statistics.mean(du["step_ms"]) / 1e3
+        dk_t = du["flops"] / (statistics.mean(du["kern_ms"]) / 1e3) / 1e12
         extra["dual"] = {"tflops": du["flops"] / dm / 1e12, "ms_per_step": dm * 1e3,
-                         "kernel_tflops": du["flops"] / (statistics.mean(du["kern_ms"]) / 1e3) / 1e12,
+                         "kernel_tflops": dk_t,
+                         "roofline": {"bound": "tensor", "achieved": dk_t, "peak": peak,
+                                      "unit": "TFLOP/s", "frac": dk_t / peak,
+                                      "traffic": measured_traffic("dual"), "kernel": "dual_kernel"},
                          "workload": "dual-branch forward bf16, B=2 Hq=16 Hkv=4 d=128 N=8192 W=1024"}
         for wl, desc in (("dual_8k", "training backward bf16 on the dual-branch workload: B=2 "
                                      "Hq=16 Hkv=4 d=128 N=8192 W=1024, gates = logits > 0"),
@@ -680,7 +690,8 @@ def run_ours(args, dist: Dist):
                 "routed_frac": bw["routed_frac"], "useful_tflop": bw["flops"] / 1e12,
                 "roofline": {"bound": "tensor", "achieved": bw["flops"] / bk / 1e12,
                              "peak": peak, "unit": "TFLOP/s",
-                             "frac": bw["flops"] / bk / 1e12 / peak, "traffic": None,
+                             "frac": bw["flops"] / bk / 1e12 / peak,
+                             "traffic": measured_traffic("backward") if wl == "dual_8k" else None,
                              "kernel": "dkdv_kernel + dq_kernel"},
                 "workload": desc}
         rb = route_backward_section(swa, timer, dev, ks, kw, dist.rank)
