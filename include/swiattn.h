@@ -193,15 +193,19 @@ size_t swiattn_dual_branch_workspace(int B, int N, int Hq, int Hkv, int d, int W
  *   gamma[b,i]    = gamma_base / (eps + nll[b,i] + alpha * mse[b,i])
  *   reg_loss[b,i] = gamma[b,i] * softplus(logits[b,i])
  *   o_gated[b,i,h,:] (nullable) = logits[b,i] > 0 ? o_full : o_swa
+ *   lse_gated[b,i,h] (nullable) = the log-sum-exp of the branch o_gated took
+ *                   (what swiattn_prefill_backward needs with o_gated)
  * logits, nll fp32 [B,N] (nll is treated as a constant input); o_full, o_swa,
- * o_gated [B,N,Hq,d] of `dtype`; mse, gamma, reg_loss fp32 [B,N].
+ * o_gated [B,N,Hq,d] of `dtype`; lse_gated fp32 [B,N,Hq]; mse, gamma, reg_loss
+ * fp32 [B,N].
  * The report's values are gamma_base = 1e-3, eps = 0.1, alpha = 100.
  * workspace: at least swiattn_dual_branch_workspace(...) bytes, scratch only. */
 int swiattn_dual_branch(const void* q, const void* k, const void* v, const float* logits,
-                        const float* nll, void* o_full, void* o_swa, void* o_gated, float* mse,
-                        float* gamma, float* reg_loss, int B, int N, int Hq, int Hkv, int d,
-                        int W, float scale, float gamma_base, float eps, float alpha, int dtype,
-                        void* workspace, size_t workspace_bytes, void* stream);
+                        const float* nll, void* o_full, void* o_swa, void* o_gated,
+                        float* lse_gated, float* mse, float* gamma, float* reg_loss, int B, int N,
+                        int Hq, int Hkv, int d, int W, float scale, float gamma_base, float eps,
+                        float alpha, int dtype, void* workspace, size_t workspace_bytes,
+                        void* stream);
 
 /* Bytes of device workspace swiattn_prefill_backward needs for these sizes. */
 size_t swiattn_prefill_backward_workspace(int B, int N, int Hq, int Hkv, int d, int W, int dtype);

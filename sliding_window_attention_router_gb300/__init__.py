@@ -75,7 +75,7 @@ def _load() -> ctypes.CDLL:
             lib.swiattn_decode_noalloc.argtypes = [vp] * 7 + [i32] * 6 + [f32, i32, vp]
             lib.swiattn_dual_branch_workspace.argtypes = [i32] * 7
             lib.swiattn_dual_branch_workspace.restype = sz
-            lib.swiattn_dual_branch.argtypes = ([vp] * 11 + [i32] * 6 + [f32] * 4
+            lib.swiattn_dual_branch.argtypes = ([vp] * 12 + [i32] * 6 + [f32] * 4
                                                 + [i32, vp, sz, vp])
             lib.swiattn_prefill_backward_workspace.argtypes = [i32] * 7
             lib.swiattn_prefill_backward_workspace.restype = sz
@@ -230,8 +230,8 @@ def decode(q, k_cache, v_cache, seq_lens, gate, W: int, scale: Optional[float] =
 
 
 def dual_branch(q, k, v, logits, nll, W: int, scale: Optional[float] = None, gamma_base=1e-3,
-                eps=0.1, alpha=100.0, want_gated=True, outs=None, workspace=None):
-    """Dual-branch forward: dict(o_full, o_swa, o_gated, mse, gamma, reg_loss)."""
+                eps=0.1, alpha=100.0, want_gated=True, outs=None, workspace=None, want_lse=False):
+    """Dual-branch forward: dict(o_full, o_swa, o_gated, mse, gamma, reg_loss[, lse_gated])."""
     _dev(q, "q")
     _dev(k, "k", q.dtype)
     _dev(v, "v", q.dtype)
@@ -246,10 +246,13 @@ def dual_branch(q, k, v, logits, nll, W: int, scale: Optional[float] = None, gam
                     mse=torch.empty((B, N), device=q.device, dtype=torch.float32),
                     gamma=torch.empty((B, N), device=q.device, dtype=torch.float32),
                     reg_loss=torch.empty((B, N), device=q.device, dtype=torch.float32))
+        if want_lse:
+            outs["lse_gated"] = torch.empty((B, N, Hq), device=q.device, dtype=torch.float32)
     ws = _workspace(dual_branch_workspace(B, N, Hq, Hkv, d, W, q.dtype), q.device, workspace)
     _check(_load().swiattn_dual_branch(
         _ptr(q), _ptr(k), _ptr(v), _ptr(logits), _ptr(nll), _ptr(outs["o_full"]),
-        _ptr(outs["o_swa"]), _ptr(outs.get("o_gated")), _ptr(outs["mse"]), _ptr(outs["gamma"]),
+        _ptr(outs["o_swa"]), _ptr(outs.get("o_gated")), _ptr(outs.get("lse_gated")),
+        _ptr(outs["mse"]), _ptr(outs["gamma"]),
         _ptr(outs["reg_loss"]), B, N, Hq, Hkv, d, W, float(scale), float(gamma_base), float(eps),
         float(alpha), _DT[q.dtype], _ptr(ws), ws.numel(), _stream()), "swiattn_dual_branch")
     return outs

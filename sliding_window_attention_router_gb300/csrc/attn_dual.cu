@@ -85,6 +85,7 @@ struct DuParams {
     __nv_bfloat16* o_full;
     __nv_bfloat16* o_swa;
     __nv_bfloat16* o_gated;  // nullable
+    float* lse_gated;        // [B,N,Hq] lse of the gated output, nullable
     float* snap;             // [B,N,Hq,128] fp32 O_SWA rows (scratch)
     float* mse_part;         // [B,N,Hq]
     unsigned int* err;
@@ -434,6 +435,7 @@ __device__ bool softmax_role(const DuParams& p, uint8_t* smem, uint64_t* bar, vo
         const int wflag = i >= 0 ? 1 : 0;
         const bool has_far = pl.jf1[x] >= 0;
         float m2 = -INFINITY, l = 0.f;
+        float lse_swa = 0.f;   // natural-log lse of the window branch (set at the snapshot)
 
         // Window run: keys [max(0, i-W+1), i].
         for (int j = pl.jw0[x]; j <= pl.jw1[x]; ++j) {
@@ -449,6 +451,7 @@ __device__ bool softmax_role(const DuParams& p, uint8_t* smem, uint64_t* bar, vo
             ++snap_cnt;
             tc_fence_after();
             const float inv = (l > 0.f) ? 1.f / l : 0.f;
+            lse_swa = (m2 + __log2f(l)) * 0.69314718055994531f;
             float* snap_row = p.snap + out_row * kHD;
 #pragma unroll 1
             for (int hh = 0; hh < 2; ++hh) {
@@ -532,6 +535,10 @@ __device__ bool softmax_role(const DuParams& p, uint8_t* smem, uint64_t* bar, vo
             if (p.o_gated) store_half_staged(stg, lane, pg, out_row, wflag, p.o_gated, hh);
         }
         if (i >= 0) p.mse_part[out_row] = mse;
+        if (i >= 0 && p.lse_gated) {
+            const float lse_full = (m2 + __log2f(l)) * 0.69314718055994531f;
+            p.lse_gated[out_row] = (gated_full || !has_far) ? lse_full : lse_swa;
+        }
         tc_fence_before();
         mbar_arrive(&bar[BAR_O_FREE + x]);
     }
@@ -629,6 +636,7 @@ cudaError_t launch_dual_tc(const TcAttnArgs& a, unsigned int* err, int num_sms, 
     p.o_full = static_cast<__nv_bfloat16*>(a.o);
     p.o_swa = static_cast<__nv_bfloat16*>(a.o_swa);
     p.o_gated = static_cast<__nv_bfloat16*>(a.o_gated);
+    p.lse_gated = a.lse;
     p.snap = a.snap;
     p.mse_part = a.mse_part;
     p.err = err;

@@ -77,7 +77,8 @@ __global__ void __launch_bounds__(128) dual_epilogue_f32_kernel(
     const float* __restrict__ of, const float* __restrict__ os, const float* __restrict__ logits,
     const float* __restrict__ nll, float* __restrict__ og, float* __restrict__ mse,
     float* __restrict__ gamma, float* __restrict__ reg, int BN, int HD, float gb, float eps,
-    float alpha) {
+    float alpha, const float* __restrict__ lf, const float* __restrict__ ls,
+    float* __restrict__ lg, int Hq) {
     const int lane = threadIdx.x & 31;
     const int64_t t = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
     if (t >= BN) return;
@@ -97,6 +98,8 @@ __global__ void __launch_bounds__(128) dual_epilogue_f32_kernel(
         gamma[t] = g;
         reg[t] = g * softplus_f(logits[t]);
     }
+    if (lg)
+        for (int h = lane; h < Hq; h += 32) lg[t * Hq + h] = full ? lf[t * Hq + h] : ls[t * Hq + h];
 }
 
 // bf16 dual branch: per-(token, head) squared distances come from the tensor-
@@ -142,13 +145,14 @@ cudaError_t launch_simt_attention(const void* q, const void* k, const void* v,
 
 cudaError_t launch_dual_epilogue_f32(const float* o_full, const float* o_swa,
                                      const float* logits, const float* nll, float* o_gated,
+                                     const float* lse_full, const float* lse_swa, float* lse_gated,
                                      float* mse, float* gamma, float* reg, int B, int N, int Hq,
                                      int d, float gamma_base, float eps, float alpha,
                                      cudaStream_t s) {
     const int BN = B * N;
     dual_epilogue_f32_kernel<<<(BN + 3) / 4, 128, 0, s>>>(o_full, o_swa, logits, nll, o_gated, mse,
                                                           gamma, reg, BN, Hq * d, gamma_base, eps,
-                                                          alpha);
+                                                          alpha, lse_full, lse_swa, lse_gated, Hq);
     return cudaGetLastError();
 }
 

@@ -100,9 +100,13 @@ bool make_tmap_4d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t
 DualWs dual_ws_layout(int B, int N, int Hq, int d, int dtype) {
     auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
     DualWs L;
-    L.mse_part = L.snap = L.counter = L.total = 0;
-    if (dtype != SWIATTN_BF16) return L;
+    L.lse_full = L.lse_swa = L.mse_part = L.snap = L.counter = L.total = 0;
     const size_t rows = (size_t)B * N * Hq;
+    if (dtype != SWIATTN_BF16) {
+        L.lse_swa = up(sizeof(float) * rows);
+        L.total = up(L.lse_swa + sizeof(float) * rows);
+        return L;
+    }
     L.snap = up(sizeof(float) * rows);
     L.counter = up(L.snap + sizeof(float) * rows * (size_t)d);
     L.total = up(L.counter + sizeof(int));
@@ -321,7 +325,8 @@ size_t swiattn_dual_branch_workspace(int B, int N, int Hq, int Hkv, int d, int W
 }
 
 int swiattn_dual_branch(const void* q, const void* k, const void* v, const float* logits,
-                        const float* nll, void* o_full, void* o_swa, void* o_gated, float* mse,
+                        const float* nll, void* o_full, void* o_swa, void* o_gated,
+                        float* lse_gated, float* mse,
                         float* gamma, float* reg_loss, int B, int N, int Hq, int Hkv, int d, int W,
                         float scale, float gamma_base, float eps, float alpha, int dtype,
                         void* workspace, size_t workspace_bytes, void* stream) {
@@ -334,16 +339,25 @@ int swiattn_dual_branch(const void* q, const void* k, const void* v, const float
     if (!(scale > 0.f)) return SWIATTN_EINVAL;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (dtype == SWIATTN_F32) {
-        cudaError_t e = launch_simt_attention(q, k, v, nullptr, 1, o_full, nullptr, B, N, Hq, Hkv,
-                                              d, W, 0, scale, dtype, s);
+        float* lf = nullptr;
+        float* ls = nullptr;
+        if (lse_gated) {   // both branches' lse go through the workspace
+            const DualWs L = dual_ws_layout(B, N, Hq, d, dtype);
+            if (!workspace || !aligned256(workspace) || workspace_bytes < L.total)
+                return SWIATTN_EINVAL;
+            lf = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.lse_full);
+            ls = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.lse_swa);
+        }
+        cudaError_t e = launch_simt_attention(q, k, v, nullptr, 1, o_full, lf, B, N, Hq, Hkv, d, W,
+                                              0, scale, dtype, s);
         if (e == cudaSuccess)
-            e = launch_simt_attention(q, k, v, nullptr, 0, o_swa, nullptr, B, N, Hq, Hkv, d, W, 0,
+            e = launch_simt_attention(q, k, v, nullptr, 0, o_swa, ls, B, N, Hq, Hkv, d, W, 0,
                                       scale, dtype, s);
         if (e == cudaSuccess)
             e = launch_dual_epilogue_f32(static_cast<const float*>(o_full),
                                          static_cast<const float*>(o_swa), logits, nll,
-                                         static_cast<float*>(o_gated), mse, gamma, reg_loss, B, N,
-                                         Hq, d, gamma_base, eps, alpha, s);
+                                         static_cast<float*>(o_gated), lf, ls, lse_gated, mse,
+                                         gamma, reg_loss, B, N, Hq, d, gamma_base, eps, alpha, s);
         return launched(e);
     }
     if (dtype != SWIATTN_BF16) return SWIATTN_EINVAL;
@@ -362,6 +376,7 @@ int swiattn_dual_branch(const void* q, const void* k, const void* v, const float
     a.o = o_full;
     a.o_swa = o_swa;
     a.o_gated = o_gated;
+    a.lse = lse_gated;
     a.mse_part = part;
     a.snap = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.snap);
     a.counter = reinterpret_cast<int*>(static_cast<char*>(workspace) + L.counter);

@@ -54,6 +54,8 @@ struct DecodeWs {
 DecodeWs decode_ws_layout(int B, int Lmax, int Hq, int d, int S);
 
 struct DualWs {
+    size_t lse_full;  // float [B*N*Hq] (fp32 path: lse of both branches)
+    size_t lse_swa;   // float [B*N*Hq]
     size_t mse_part;  // float [B*N*Hq]
     size_t snap;      // float [B*N*Hq*128] O_SWA rows, fp32 (tensor-core path)
     size_t counter;   // int32 work counter
@@ -84,7 +86,7 @@ struct TcAttnArgs {
     void* o;               // prefill output / dual o_full
     void* o_swa;           // dual
     void* o_gated;         // dual, nullable
-    float* lse;            // prefill, nullable
+    float* lse;            // prefill, or dual's lse of the gated output; nullable
     float* mse_part;       // dual
     float* snap;           // dual: fp32 O_SWA rows
     int* counter;          // dual: work counter (zeroed by the launcher)
@@ -109,6 +111,7 @@ cudaError_t launch_simt_attention(const void* q, const void* k, const void* v,
 
 cudaError_t launch_dual_epilogue_f32(const float* o_full, const float* o_swa,
                                      const float* logits, const float* nll, float* o_gated,
+                                     const float* lse_full, const float* lse_swa, float* lse_gated,
                                      float* mse, float* gamma, float* reg, int B, int N, int Hq,
                                      int d, float gamma_base, float eps, float alpha,
                                      cudaStream_t s);

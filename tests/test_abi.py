@@ -59,7 +59,8 @@ def test_workspace_sizes(lib):
     dw = swa.decode_workspace(16, 32768, 16, 16, 128, 1024, bf16)
     assert dw >= 16 * (32768 // 256) * 16 * 130 * 4
     assert swa.dual_branch_workspace(2, 8192, 16, 4, 128, 1024, bf16) >= 2 * 8192 * 16 * 4
-    assert swa.dual_branch_workspace(1, 256, 2, 2, 64, 32, f32) == 0
+    # fp32: both branches' lse (used only when lse_gated is requested)
+    assert swa.dual_branch_workspace(1, 256, 2, 2, 64, 32, f32) == 2 * 256 * 2 * 4
 
 
 def test_invalid_arguments_rejected_before_launch(lib):
@@ -86,7 +87,7 @@ def test_invalid_arguments_rejected_before_launch(lib):
     assert lib.swiattn_decode(*dargs, 2, 64, 6, 2, 128, 8, 0.1, 1, fake, 1 << 30, None) == 2
     assert lib.swiattn_decode(*dargs, 2, 64, 4, 4, 128, 8, 0.1, 1, fake, 8, None) == 1
     # dual: missing output
-    xargs = [fake] * 5 + [None] + [fake] * 5
+    xargs = [fake] * 5 + [None] + [fake] * 6
     assert lib.swiattn_dual_branch(*xargs, 1, 64, 4, 4, 128, 8, 0.1, 1e-3, 0.1, 100.0, 1, fake,
                                    1 << 30, None) == 1
 

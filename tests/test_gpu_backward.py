@@ -225,3 +225,62 @@ def test_route_backward_optional_outputs(swa):
     assert_f32_close(got["d_logits"], ref["d_logits"], "d_logits")
     np.testing.assert_allclose(ref["d_logits"], 0.25 * (f64(do) * (f64(of) - f64(os_))).sum(1),
                                rtol=1e-12)
+
+
+# -------------------------------------------------------- training step ----
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_training_step_through_the_library(swa, dtype):
+    """One training step of a SwiAttn layer through the C ABI: router ->
+    dual-branch forward (gated output and its lse) -> routed attention
+    backward from o_gated / lse_gated, and router backward through the
+    straight-through gate and the regulariser; every gradient against the
+    oracle's."""
+    g = inp._gen(90)
+    B, N, Hq, Hkv, d, W, D = 1, 600, 4, 2, 128, 128, 256
+    r = inp.router_inputs(B * N, D, dtype, 91, frac=0.3)
+    h, w, bias = r["h"], r["w"], r["bias"]
+    for _ in range(10):   # keep every logit at least 1e-3 from the threshold
+        lg0, _ = oracle.route(f64(h), f64(w), bias)
+        bad = np.nonzero(np.abs(lg0) < 1e-3)[0]
+        if bad.size == 0:
+            break
+        inp.redraw_rows(h, bad, r["gen"])
+    q, k, v = inp.attention_qkv(B, N, Hq, Hkv, d, dtype, g)
+    nll = torch.rand(B, N, generator=g) * 3
+    do = inp.output_grad((B, N, Hq, d), dtype, 92)
+    d_reg = torch.ones(B * N)
+    logits, gate = swa.route(h.cuda(), w.cuda(), bias)
+    gate2 = gate.view(B, N)
+    out = swa.dual_branch(q.cuda(), k.cuda(), v.cuda(), logits.view(B, N), nll.cuda(), W,
+                          want_lse=True)
+    dq, dk, dv = swa.prefill_backward(q.cuda(), k.cuda(), v.cuda(), gate2, out["o_gated"],
+                                      out["lse_gated"], do.cuda(), W)
+    rb = swa.route_backward(logits, out["o_full"], out["o_swa"], do.cuda(),
+                            out["gamma"].view(-1), d_reg.cuda(), h.cuda(), w.cuda())
+    assert swa.get_device_error() == 0
+    # oracle: its own router logits and gates, its own branch outputs
+    ref_logits, ref_gate = oracle.route(f64(h), f64(w), bias)
+    assert np.abs(ref_logits).min() >= 1e-3
+    np.testing.assert_array_equal(gate.cpu().numpy(), ref_gate)
+    scale = 1.0 / math.sqrt(d)
+    od = oracle.dual(f64(q), f64(k), f64(v), ref_logits.reshape(B, N), f64(nll), W, scale)
+    rq, rk, rv = oracle.prefill_backward(f64(q), f64(k), f64(v), ref_gate.reshape(B, N), f64(do),
+                                         W, scale)
+    rr = oracle.route_backward(ref_logits, od["o_full"].reshape(B * N, -1),
+                               od["o_swa"].reshape(B * N, -1), f64(do).reshape(B * N, -1),
+                               od["gamma"].ravel(), f64(d_reg), f64(h), f64(w))
+    if dtype == torch.float32:
+        for got, ref, name in ((dq, rq, "dq"), (dk, rk, "dk"), (dv, rv, "dv"),
+                               (rb["d_logits"], rr["d_logits"], "d_logits"),
+                               (rb["dh"], rr["dh"], "dh"), (rb["dw"], rr["dw"], "dw")):
+            assert_f32_close(got, ref, name)
+    else:
+        for got, ref, name in ((dq, rq, "dq"), (dk, rk, "dk"), (dv, rv, "dv")):
+            assert_rel_close(got, ref, name)
+        for got, ref, name in ((rb["d_logits"], rr["d_logits"], "d_logits"),
+                               (rb["dh"], rr["dh"], "dh"), (rb["dw"], rr["dw"], "dw")):
+            assert_rel_close(got, ref, name, ROUTE_REL_MEAN)
+    # lse_gated is the gated branch's log-sum-exp
+    ref_o, ref_lse = oracle.prefill(f64(q), f64(k), f64(v), ref_gate.reshape(B, N), W, scale,
+                                    want_lse=True)
+    assert np.abs(f64(out["lse_gated"]) - ref_lse).max() <= 1e-3
