@@ -44,8 +44,8 @@ L2_FLUSH_BYTES = 256 << 20
 # SHA-256 of the kernel's source files at capture time; a kernel whose source
 # has changed since reports null.
 MEASURED_TRAFFIC = {
-    # prefill_kernel, long-context prefill N=32768 f=0.13: 1 110 540 800 read + 136 363 520 written
-    ("prefill", "f4d24d0f3fd8fea5"): 1110540800 + 136363520,
+    # prefill_kernel, long-context prefill N=32768 f=0.13: 972 332 800 read + 126 025 472 written
+    ("prefill", "654a283632d6b709"): 972332800 + 126025472,
     # decode_split_kernel, 16 x 32768 decode: 654 405 376 read + 2 758 912 written
     ("decode", "023308e7542f8d17"): 654405376 + 2758912,
     # dual_kernel, dual-branch workload B=2 N=8192 GQA 16/4: 155 273 984 read + 272 345 088 written

@@ -177,14 +177,26 @@ __device__ __forceinline__ void store_row64(__nv_bfloat16* dst, const uint32_t* 
 }
 
 // Masks columns outside [a, e] of this warp's 64-column half (column c of
-// the tile is x[c - c0]) by setting the exponent argument to -inf.  Only the
-// branch is warp-uniform; the selects are per lane.
+// the tile is x[c - c0]) by setting the exponent argument to -inf.  Must be
+// reached by the whole warp: it votes for a one-sided mask (visible c <= e,
+// or c >= a, for every lane), which costs one compare and one select per
+// column; the branches follow the votes.
 __device__ __forceinline__ void mask_half(float* x, int a, int e, int c0) {
-    const uint32_t span = static_cast<uint32_t>(e - a);
+    const bool all_pre = __all_sync(0xffffffffu, a <= c0);
+    const bool all_suf = __all_sync(0xffffffffu, e >= c0 + 63);
+    if (all_pre) {
 #pragma unroll
-    for (int c = 0; c < 64; ++c) {
-        const bool ok = static_cast<uint32_t>(c0 + c - a) <= span && e >= a;
-        x[c] = ok ? x[c] : -INFINITY;
+        for (int c = 0; c < 64; ++c) x[c] = c0 + c <= e ? x[c] : -INFINITY;
+    } else if (all_suf) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) x[c] = c0 + c >= a ? x[c] : -INFINITY;
+    } else {
+        const uint32_t span = static_cast<uint32_t>(e - a);
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+            const bool ok = static_cast<uint32_t>(c0 + c - a) <= span && e >= a;
+            x[c] = ok ? x[c] : -INFINITY;
+        }
     }
 }
 

@@ -412,23 +412,38 @@ __device__ bool softmax_role(const PfParams& p, uint8_t* smem, uint64_t* bar, vo
             tmem_ld_wait();
             float* s = reinterpret_cast<float*>(sr);
             const bool full = a <= 0 && e >= kBN - 1;   // every key of the block visible
+            // Warp-uniform classification (every lane votes, the branches
+            // follow the votes, so a warp never runs two paths): a mask that
+            // is one-sided for the whole warp (visible c <= e: diagonal and
+            // far blocks; c >= a: window start) costs one compare and one
+            // select per column; the maximum is then the same three-input
+            // tree as for a full block.
+            const bool all_full = __all_sync(0xffffffffu, full);
+            const bool all_pre = __all_sync(0xffffffffu, a <= 0);
+            const bool all_suf = __all_sync(0xffffffffu, e >= kBN - 1);
             float m8[8];
 #pragma unroll
             for (int t = 0; t < 8; ++t) m8[t] = -INFINITY;
-            if (full) {
+            if (!all_full) {
+                if (all_pre) {
 #pragma unroll
-                for (int cc = 0; cc < kBN; cc += 16)
+                    for (int cc = 0; cc < kBN; ++cc) s[cc] = cc <= e ? s[cc] : -INFINITY;
+                } else if (all_suf) {
 #pragma unroll
-                    for (int t = 0; t < 8; ++t) m8[t] = fmax3(m8[t], s[cc + 2 * t], s[cc + 2 * t + 1]);
-            } else {
-                const uint32_t span = static_cast<uint32_t>(e - a);
+                    for (int cc = 0; cc < kBN; ++cc) s[cc] = cc >= a ? s[cc] : -INFINITY;
+                } else {
+                    const uint32_t span = static_cast<uint32_t>(e - a);
 #pragma unroll
-                for (int cc = 0; cc < kBN; ++cc) {
-                    const bool ok = static_cast<uint32_t>(cc - a) <= span && e >= a;
-                    s[cc] = ok ? s[cc] : -INFINITY;
-                    m8[cc & 7] = fmaxf(m8[cc & 7], s[cc]);
+                    for (int cc = 0; cc < kBN; ++cc) {
+                        const bool ok = static_cast<uint32_t>(cc - a) <= span && e >= a;
+                        s[cc] = ok ? s[cc] : -INFINITY;
+                    }
                 }
             }
+#pragma unroll
+            for (int cc = 0; cc < kBN; cc += 16)
+#pragma unroll
+                for (int t = 0; t < 8; ++t) m8[t] = fmax3(m8[t], s[cc + 2 * t], s[cc + 2 * t + 1]);
             const float mx = fmaxf(fmax3(m8[0], m8[1], m8[2]),
                                    fmax3(fmax3(m8[3], m8[4], m8[5]), m8[6], m8[7]));
             // Running max in scaled log2 units; O and l are rescaled only when
