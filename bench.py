@@ -46,13 +46,13 @@ L2_FLUSH_BYTES = 256 << 20
 MEASURED_TRAFFIC = {
     # prefill_kernel, long-context prefill N=32768 f=0.13: 972 332 800 read + 126 025 472 written
     ("prefill", "654a283632d6b709"): 972332800 + 126025472,
-    # decode_split_kernel, 16 x 32768 decode: 654 405 376 read + 2 758 912 written
-    ("decode", "023308e7542f8d17"): 654405376 + 2758912,
+    # decode_split_kernel, 16 x 32768 decode: 654 404 608 read + 2 771 200 written
+    ("decode", "525498dfbc8e1971"): 654404608 + 2771200,
     # dual_kernel, dual-branch workload B=2 N=8192 GQA 16/4: 155 273 984 read + 272 345 088 written
     ("dual", "96d14ef8dc35435e"): 155273984 + 272345088,
-    # dkdv_kernel + dq_kernel, backward on the dual workload: (319 030 528 + 21 871 872)
-    # + (257 355 264 + 47 116 032)
-    ("backward", "2a7d1a1f50c044a1"): 319030528 + 21871872 + 257355264 + 47116032,
+    # dkdv_kernel + dq_kernel, backward on the dual workload: (319 911 424 + 22 017 024)
+    # + (253 355 520 + 48 199 168)
+    ("backward", "f701359c9e5dddba"): 319911424 + 22017024 + 253355520 + 48199168,
 }
 KERNEL_SOURCES = {"prefill": ("attn_prefill.cu", "ptx.cuh"), "decode": ("decode.cu",),
                   "dual": ("attn_dual.cu", "ptx.cuh"), "backward": ("attn_bwd.cu", "ptx.cuh")}
