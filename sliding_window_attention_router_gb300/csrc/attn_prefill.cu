@@ -16,10 +16,12 @@
 //   warps 0-3   softmax + epilogue of tile A (thread r owns row r = TMEM lane r)
 //               (the epilogue stages rows in shared memory for coalesced stores)
 //   warps 4-7   softmax + epilogue of tile B
-//   warp 8      item claimer and TMA producer: Q tiles, K and V blocks
-//               (converged, elected issue)
+//   warp 8      item claimer and TMA producer: Q tiles of band items, K and V
+//               blocks (converged, elected issue)
 //   warp 9      TMEM allocator and MMA issuer (converged, elected issue)
-//   warps 10-11 idle (complete the third warpgroup for register reconfiguration)
+//   warp 10     Q of far items: gathers the tile's routed rows by row index
+//               straight from Q (cp.async into the swizzled tile layout)
+//   warp 11     idle (completes the third warpgroup for register reconfiguration)
 // TMEM: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
 // Key sets per row (SwiAttn report, section 2; window per the weimeta.cn SWA
 // glossary): window rows [max(0, i-W+1), i], routed rows [0, i].  With S
@@ -69,8 +71,9 @@ enum {
     BAR_DRAIN = BAR_SCHED_EMPTY + kSched,
     BAR_COUNT
 };
-// Consumers of a broadcast item: the MMA warp and the eight softmax warps.
-constexpr uint32_t kSchedConsumers = 1 + 8;
+// Consumers of a broadcast item: the MMA warp, the eight softmax warps and the
+// far-query gatherer.
+constexpr uint32_t kSchedConsumers = 1 + 8 + 1;
 
 constexpr int kOffSched = kOffBar + BAR_COUNT * 8;
 constexpr int kOffMisc = kOffSched + kSched * 4;
@@ -85,7 +88,8 @@ constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, false, false);
 constexpr uint32_t kIdescO = idesc_bf16_f32(kBM, kHD, false, true);
 
 struct PfParams {
-    CUtensorMap tm_q, tm_qc, tm_k, tm_v;
+    CUtensorMap tm_q, tm_k, tm_v;
+    const __nv_bfloat16* q;  // [B, N, Hq, 128]: far tiles gather their rows from it
     const int* routed_list;
     const int* routed_count;
     const int* tile_prefix;
@@ -229,24 +233,30 @@ __device__ bool consume_item(const PfParams& p, uint64_t* bar, volatile int* sch
 // Producer warp (converged, one elected lane issues): per item, the Q tiles,
 // then one K/V slot per step g: step j of an item carries K_j (j < nblk) and
 // V_{j-1} (j >= 1), so a slot is freed by one commit after S(j) and PV(j-1).
+//
+// Each Q slot's barriers see one load per active tile per item, band (TMA,
+// here) or far (the gatherer warp).  Both warps wait for every load's slot in
+// order, so neither waits on a phase more than one ahead of the barrier.
 template <bool ANCH>
 __device__ bool producer(const PfParams& p, uint8_t* smem, uint64_t* bar, volatile int* sched,
-                         volatile int* abort_flag, uint32_t& g, uint32_t* q_issued) {
+                         volatile int* abort_flag, uint32_t& g, uint32_t* q_issued, bool* q_tma_last) {
     const int n = *p.n_items;
     for (int k = 0;; ++k) {
         int idx;
         if (!publish_item(p, bar, sched, k, n, abort_flag, idx)) return false;
         if (idx < 0) break;
         const Plan pl = make_plan<ANCH>(p, idx);
-        const CUtensorMap* qm = (pl.kind == kItemFar) ? &p.tm_qc : &p.tm_q;
+        const bool far = pl.kind == kItemFar;
         auto load_q = [&](int x) -> bool {
             if (!mbar_wait_w(&bar[BAR_Q_EMPTY + x], (q_issued[x] & 1u) ^ 1u, abort_flag, p.err)) return false;
+            ++q_issued[x];
+            q_tma_last[x] = !far;
+            if (far) return true;
             mbar_arrive_expect_tx_w(&bar[BAR_Q_FULL + x], kTileBytes);
             uint8_t* dst = smem + kOffQ + x * kTileBytes;
             const int row = pl.row0 + x * kBM;
-            tma_load_4d_w(dst, qm, &bar[BAR_Q_FULL + x], 0, pl.h, row, pl.b);
-            tma_load_4d_w(dst + kHalfBytes, qm, &bar[BAR_Q_FULL + x], 64, pl.h, row, pl.b);
-            ++q_issued[x];
+            tma_load_4d_w(dst, &p.tm_q, &bar[BAR_Q_FULL + x], 0, pl.h, row, pl.b);
+            tma_load_4d_w(dst + kHalfBytes, &p.tm_q, &bar[BAR_Q_FULL + x], 64, pl.h, row, pl.b);
             return true;
         };
         if (tile_active(pl, 0) && !load_q(0)) return false;
@@ -269,6 +279,70 @@ __device__ bool producer(const PfParams& p, uint8_t* smem, uint64_t* bar, volati
                 tma_load_4d_w(dst + kHalfBytes, &p.tm_v, &bar[BAR_KV_FULL + st], 64, pl.kvh, key0, pl.b);
             }
             ++g;
+        }
+    }
+    return true;
+}
+
+// Far-query gatherer (warp 10).  Row r of far tile x is compacted routed row
+// c = row0 + 128x + r, i.e. query row routed_list[c]; its 256 bytes (head h)
+// are copied in 16-byte chunks with cp.async into the same 128-byte-swizzled
+// K-major layout the TMA writes for band tiles: chunk u of the row (half u/8)
+// lands at 16-byte slot (u%8) ^ (r%8) of the row's 128 bytes.  Rows past the
+// routed count are zero-filled.  Half-warps take one row each, so every load
+// instruction reads two whole rows.  The copies complete, each lane fences its
+// writes for the tensor core's async proxy, then one arrival fills the slot.
+__device__ void gather_far_q(const PfParams& p, uint8_t* smem, uint64_t* bar, const Plan& pl, int x,
+                             int lane) {
+    const int R = p.routed_count[pl.b];
+    const int c0 = pl.row0 + x * kBM;
+    const int* list = p.routed_list + (size_t)pl.b * p.N;
+    int src[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int c = c0 + u * 32 + lane;
+        src[u] = c < R ? list[c] : -1;
+    }
+    const uint32_t tile = smem_u32(smem + kOffQ + x * kTileBytes);
+    const int sub = lane & 15;
+    const uint32_t col = (sub >> 3) * kHalfBytes;
+    const uint32_t slot = sub & 7;
+    const size_t head = (size_t)pl.b * p.N * p.Hq + pl.h;
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {   // rows 32 q4 .. 32 q4 + 31; lane l holds row 32 q4 + l's index
+#pragma unroll 4
+        for (int it = q4 * 16; it < q4 * 16 + 16; ++it) {
+            const int r = 2 * it + (lane >> 4);
+            const int i = __shfl_sync(0xffffffffu, src[q4], r & 31);
+            const uint32_t dst = tile + col + r * 128 + ((slot ^ (r & 7)) << 4);
+            const __nv_bfloat16* s = p.q + (head + (size_t)max(i, 0) * p.Hq) * kHD + sub * 8;
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(s),
+                         "r"(i >= 0 ? 16u : 0u)
+                         : "memory");
+        }
+    }
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar[BAR_Q_FULL + x]);
+    __syncwarp();
+}
+
+template <bool ANCH>
+__device__ bool q_gatherer(const PfParams& p, uint8_t* smem, uint64_t* bar, volatile int* sched,
+                           volatile int* abort_flag, int lane) {
+    uint32_t cnt[2] = {0, 0};
+    for (int k = 0;; ++k) {
+        int idx;
+        if (!consume_item(p, bar, sched, k, abort_flag, idx)) return false;
+        if (idx < 0) break;
+        const Plan pl = make_plan<ANCH>(p, idx);
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+            if (!tile_active(pl, x)) continue;
+            if (!mbar_wait_w(&bar[BAR_Q_EMPTY + x], (cnt[x] & 1u) ^ 1u, abort_flag, p.err)) return false;
+            ++cnt[x];
+            if (pl.kind == kItemFar) gather_far_q(p, smem, bar, pl, x, lane);
         }
     }
     return true;
@@ -595,16 +669,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     if (warp == 8) {
         if (lane == 0) {
             prefetch_tensormap(&p.tm_q);
-            prefetch_tensormap(&p.tm_qc);
             prefetch_tensormap(&p.tm_k);
             prefetch_tensormap(&p.tm_v);
         }
         __syncwarp();
         uint32_t g = 0, q_issued[2] = {0, 0};
-        if (!producer<ANCH>(p, smem, bar, sched, abort_flag, g, q_issued)) {
+        bool q_tma_last[2] = {false, false};
+        if (!producer<ANCH>(p, smem, bar, sched, abort_flag, g, q_issued, q_tma_last)) {
             drain_loads(&bar[BAR_KV_FULL], g);
             for (int x = 0; x < 2; ++x)
-                if (q_issued[x]) mbar_drain(&bar[BAR_Q_FULL + x], (q_issued[x] - 1) & 1u);
+                if (q_tma_last[x]) mbar_drain(&bar[BAR_Q_FULL + x], (q_issued[x] - 1) & 1u);
         }
         __syncwarp();
     } else if (warp == 9) {
@@ -613,6 +687,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         umma_commit_w(&bar[BAR_DRAIN]);
         mbar_drain(&bar[BAR_DRAIN], 0);
         __syncwarp();
+    } else if (warp == 10) {
+        q_gatherer<ANCH>(p, smem, bar, sched, abort_flag, lane);
     }
 
     tc_fence_before();
@@ -631,10 +707,10 @@ cudaError_t launch_prefill_tc(const TcAttnArgs& a, const int* tile_prefix, unsig
     memset(&p, 0, sizeof(p));
     const uint64_t N = a.N, B = a.B;
     bool ok = make_tmap_4d_bf16(&p.tm_q, a.q, kHD, a.Hq, N, B, 64, kBM) &&
-              make_tmap_4d_bf16(&p.tm_qc, a.qc, kHD, a.Hq, N, B, 64, kBM) &&
               make_tmap_4d_bf16(&p.tm_k, a.k, kHD, a.Hkv, N, B, 64, kBN) &&
               make_tmap_4d_bf16(&p.tm_v, a.v, kHD, a.Hkv, N, B, 64, kBN);
     if (!ok) return cudaErrorInvalidValue;
+    p.q = static_cast<const __nv_bfloat16*>(a.q);
     p.routed_list = a.routed_list;
     p.routed_count = a.routed_count;
     p.tile_prefix = tile_prefix;

@@ -1,4 +1,4 @@
-// Gate-driven scheduling for the routed prefill.
+// Gate-driven scheduling for the routed prefill (one launch).
 //
 // A row i of batch b is a "far" row when its gate routes it to full attention
 // and i >= W (for i < W its full range [0, i] equals its window).  Far rows
@@ -130,75 +130,105 @@ __device__ __forceinline__ int pair_cost(int u, const int* routed_list, const in
     return cost > 0 ? cost + 2 * na : 0;
 }
 
-// Block 0: counting sort of 256-row pairs by descending cost, Hq items per
-// pair (one per query head), and reset of the attention kernel's work
-// counter.  Other blocks: compacted queries of far rows,
-// qc[b, r] = q[b, routed_list[b, r]] for r < R_b, zero up to the end of the
-// last 128-row tile.
-constexpr int kBuildThreads = 512;
-constexpr int kBucketsPerThread = kCostBuckets / kBuildThreads;
+// Gate bytes i .. i+15 of one batch row (zero where i+u >= N).  A whole
+// in-range group is one 16-byte load when the row start is 16-byte aligned.
+__device__ __forceinline__ uint4 load_gates16(const uint8_t* g, int i, int N, bool vec) {
+    if (vec && i + 16 <= N) return *reinterpret_cast<const uint4*>(g + i);
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int u = 0; u < 16; ++u)
+        if (i + u < N) w[u >> 2] |= static_cast<uint32_t>(g[i + u] != 0 ? 1u : 0u) << (8 * (u & 3));
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
 
-__global__ void __launch_bounds__(kBuildThreads) build_and_gather_kernel(
-    const int* __restrict__ routed_list, const int* __restrict__ routed_count,
-    const int* __restrict__ tile_prefix, int B, int N, int Hq, int W, int S,
-    WorkItem* __restrict__ items,
-    int* __restrict__ n_items, const uint4* __restrict__ q, uint4* __restrict__ qc) {
-    if (blockIdx.x == 0) {
-        __shared__ int hist[kCostBuckets];
-        __shared__ int warp_tot[32];
-        const int NT = cdiv(N, kBM);
-        const int NP = cdiv(N, 2 * kBM);
-        const int U = B * 2 * NP;
-        for (int c = threadIdx.x; c < kCostBuckets; c += blockDim.x) hist[c] = 0;
-        __syncthreads();
-        for (int u = threadIdx.x; u < U; u += blockDim.x) {
-            int b, kind, pair;
-            const int cost = pair_cost(u, routed_list, routed_count, tile_prefix, N, W, S, NT, NP, b, kind, pair);
-            if (cost > 0) atomicAdd(&hist[min(cost, kCostBuckets - 1)], 1);
-        }
-        __syncthreads();
-        // Exclusive offsets in descending cost order: thread t owns buckets
-        // 4095-8t ... 4095-8t-7.
-        int own = 0;
+__device__ __forceinline__ bool gate_byte(const uint4& v, int u) {
+    const uint32_t w = u < 4 ? v.x : u < 8 ? v.y : u < 12 ? v.z : v.w;
+    return ((w >> (8 * (u & 3))) & 0xFFu) != 0;
+}
+
+// The whole prefill schedule in one CTA.  Per batch: each thread counts the far
+// rows of a contiguous chunk of rows (a multiple of 16, so 16-byte gate groups
+// never straddle two threads), one block scan, then each thread writes its far
+// rows (ascending i) and the prefix counts of the 128-row tiles that start in
+// its chunk.  Then the counting sort of 256-row pairs by descending cost, Hq
+// items per pair (one per query head), and the reset of the attention kernel's
+// work counter.  Far queries are not copied here: the attention kernel gathers
+// them by row index when it loads a far tile.
+constexpr int kPlanThreads = 1024;
+constexpr int kBucketsPerThread = kCostBuckets / kPlanThreads;
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(
+    const uint8_t* __restrict__ gate, int B, int N, int Hq, int W, int S,
+    int* __restrict__ routed_list, int* __restrict__ routed_count, int* __restrict__ tile_prefix,
+    WorkItem* __restrict__ items, int* __restrict__ n_items) {
+    __shared__ int hist[kCostBuckets];
+    __shared__ int warp_tot[32];
+    const int NT = cdiv(N, kBM);
+    const int NP = cdiv(N, 2 * kBM);
+    const int C = cdiv(cdiv(N, kPlanThreads), 16) * 16;
+    for (int b = 0; b < B; ++b) {
+        const uint8_t* g = gate + (size_t)b * N;
+        const bool vec = (reinterpret_cast<uintptr_t>(g) & 15u) == 0;
+        const int i0 = min(N, static_cast<int>(threadIdx.x) * C), i1 = min(N, i0 + C);
+        int cnt = 0;
+        for (int i = i0; i < i1; i += 16) {
+            const uint4 v = load_gates16(g, i, N, vec);
 #pragma unroll
-        for (int k = 0; k < kBucketsPerThread; ++k)
-            own += hist[kCostBuckets - 1 - (threadIdx.x * kBucketsPerThread + k)];
+            for (int u = 0; u < 16; ++u) cnt += (i + u >= W && i + u < i1 && gate_byte(v, u)) ? 1 : 0;
+        }
         int total;
-        int run = block_exclusive_scan(own, warp_tot, &total);
+        int run = block_exclusive_scan(cnt, warp_tot, &total);
+        int* list = routed_list + (size_t)b * N;
+        int* pre = tile_prefix + (size_t)b * (NT + 1);
+        for (int i = i0; i < i1; i += 16) {
+            const uint4 v = load_gates16(g, i, N, vec);
+            if ((i % kBM) == 0) pre[i / kBM] = run;   // 16 divides 128: tile starts begin groups
 #pragma unroll
-        for (int k = 0; k < kBucketsPerThread; ++k) {
-            const int c = kCostBuckets - 1 - (threadIdx.x * kBucketsPerThread + k);
-            const int h = hist[c];
-            hist[c] = run;
-            run += h;
-        }
-        __syncthreads();
-        for (int u = threadIdx.x; u < U; u += blockDim.x) {
-            int b, kind, pair;
-            const int cost = pair_cost(u, routed_list, routed_count, tile_prefix, N, W, S, NT, NP, b, kind, pair);
-            if (cost <= 0) continue;
-            const int pos = atomicAdd(&hist[min(cost, kCostBuckets - 1)], 1);
-            for (int h = 0; h < Hq; ++h) items[(size_t)pos * Hq + h] = WorkItem{kind, b, h, pair};
+            for (int u = 0; u < 16; ++u)
+                if (i + u >= W && i + u < i1 && gate_byte(v, u)) list[run++] = i + u;
         }
         if (threadIdx.x == 0) {
-            n_items[0] = total * Hq;
-            n_items[1] = 0;   // work counter the attention kernel claims items from
+            routed_count[b] = total;
+            pre[NT] = total;
         }
-        return;
     }
-    const int per_row = Hq * (kHD * 2 / 16);
-    const size_t stride = (size_t)(gridDim.x - 1) * blockDim.x;
-    for (int b = 0; b < B; ++b) {
-        const int R = routed_count[b];
-        const int Rp = min(N, cdiv(R, kBM) * kBM);
-        const size_t total = (size_t)Rp * per_row;
-        for (size_t idx = (size_t)(blockIdx.x - 1) * blockDim.x + threadIdx.x; idx < total; idx += stride) {
-            const int r = (int)(idx / per_row);
-            const int c = (int)(idx % per_row);
-            uint4 val = make_uint4(0u, 0u, 0u, 0u);
-            if (r < R) val = q[((size_t)b * N + routed_list[(size_t)b * N + r]) * per_row + c];
-            qc[((size_t)b * N + r) * per_row + c] = val;
-        }
+    __syncthreads();   // the lists, counts and prefixes above are read below
+
+    const int U = B * 2 * NP;
+    for (int c = threadIdx.x; c < kCostBuckets; c += blockDim.x) hist[c] = 0;
+    __syncthreads();
+    for (int u = threadIdx.x; u < U; u += blockDim.x) {
+        int b, kind, pair;
+        const int cost = pair_cost(u, routed_list, routed_count, tile_prefix, N, W, S, NT, NP, b, kind, pair);
+        if (cost > 0) atomicAdd(&hist[min(cost, kCostBuckets - 1)], 1);
+    }
+    __syncthreads();
+    // Exclusive offsets in descending cost order: thread t owns buckets
+    // 4095-4t ... 4095-4t-3.
+    int own = 0;
+#pragma unroll
+    for (int k = 0; k < kBucketsPerThread; ++k)
+        own += hist[kCostBuckets - 1 - (threadIdx.x * kBucketsPerThread + k)];
+    int total;
+    int run = block_exclusive_scan(own, warp_tot, &total);
+#pragma unroll
+    for (int k = 0; k < kBucketsPerThread; ++k) {
+        const int c = kCostBuckets - 1 - (threadIdx.x * kBucketsPerThread + k);
+        const int h = hist[c];
+        hist[c] = run;
+        run += h;
+    }
+    __syncthreads();
+    for (int u = threadIdx.x; u < U; u += blockDim.x) {
+        int b, kind, pair;
+        const int cost = pair_cost(u, routed_list, routed_count, tile_prefix, N, W, S, NT, NP, b, kind, pair);
+        if (cost <= 0) continue;
+        const int pos = atomicAdd(&hist[min(cost, kCostBuckets - 1)], 1);
+        for (int h = 0; h < Hq; ++h) items[(size_t)pos * Hq + h] = WorkItem{kind, b, h, pair};
+    }
+    if (threadIdx.x == 0) {
+        n_items[0] = total * Hq;
+        n_items[1] = 0;   // work counter the attention kernel claims items from
     }
 }
 
@@ -220,22 +250,16 @@ PrefillWs prefill_ws_layout(int B, int N, int Hq, int d) {
     L.max_items = static_cast<int>((size_t)B * 2 * ((N + 2 * kBM - 1) / (2 * kBM)) * Hq);
     L.items = off;
     off = up(off + sizeof(WorkItem) * (size_t)L.max_items);
-    L.qc = off;
-    off = up(off + 2 * (size_t)B * N * Hq * d);
     L.total = off;
     return L;
 }
 
-cudaError_t launch_schedule(const uint8_t* gate, const void* q, int B, int N, int Hq, int W, int S,
-                            const PrefillWs& L, char* ws, int num_sms, cudaStream_t s) {
-    int* list = reinterpret_cast<int*>(ws + L.routed_list);
-    int* count = reinterpret_cast<int*>(ws + L.routed_count);
-    int* prefix = reinterpret_cast<int*>(ws + L.tile_prefix);
-    scan_far_rows_kernel<<<B, kScanThreads, 0, s>>>(gate, N, W, list, count, prefix);
-    build_and_gather_kernel<<<1 + num_sms * 2, kBuildThreads, 0, s>>>(
-        list, count, prefix, B, N, Hq, W, S, reinterpret_cast<WorkItem*>(ws + L.items),
-        reinterpret_cast<int*>(ws + L.n_items), static_cast<const uint4*>(q),
-        reinterpret_cast<uint4*>(ws + L.qc));
+cudaError_t launch_schedule(const uint8_t* gate, int B, int N, int Hq, int W, int S,
+                            const PrefillWs& L, char* ws, cudaStream_t s) {
+    plan_kernel<<<1, kPlanThreads, 0, s>>>(
+        gate, B, N, Hq, W, S, reinterpret_cast<int*>(ws + L.routed_list),
+        reinterpret_cast<int*>(ws + L.routed_count), reinterpret_cast<int*>(ws + L.tile_prefix),
+        reinterpret_cast<WorkItem*>(ws + L.items), reinterpret_cast<int*>(ws + L.n_items));
     return cudaGetLastError();
 }
 

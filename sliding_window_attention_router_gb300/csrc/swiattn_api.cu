@@ -203,14 +203,13 @@ int swiattn_prefill_anchored(const void* q, const void* k, const void* v, const 
     DeviceInfo di;
     if (!device_info(di)) return SWIATTN_ECUDA;
     char* ws = static_cast<char*>(workspace);
-    cudaError_t e = launch_schedule(gate, q, B, N, Hq, W, n_anchor, L, ws, di.sms, s);
+    cudaError_t e = launch_schedule(gate, B, N, Hq, W, n_anchor, L, ws, s);
     if (e != cudaSuccess) return SWIATTN_ECUDA;
     TcAttnArgs a;
     std::memset(&a, 0, sizeof(a));
     a.q = q;
     a.k = k;
     a.v = v;
-    a.qc = ws + L.qc;
     a.routed_list = reinterpret_cast<const int*>(ws + L.routed_list);
     a.routed_count = reinterpret_cast<const int*>(ws + L.routed_count);
     a.n_items = reinterpret_cast<const int*>(ws + L.n_items);

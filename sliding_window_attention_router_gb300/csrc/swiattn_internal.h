@@ -38,7 +38,6 @@ struct PrefillWs {
     size_t tile_prefix;   // int32 [B*(NT+1)] far rows before each 128-row tile
     size_t n_items;       // int32 [4]
     size_t items;         // WorkItem [max_items]
-    size_t qc;            // bf16 [B*N*Hq*d]  compacted queries of far rows
     size_t total;
     int max_items;
 };
@@ -68,15 +67,16 @@ DualWs dual_ws_layout(int B, int N, int Hq, int d, int dtype);
 cudaError_t launch_route(const void* h, const void* w, float bias, int64_t tokens, int d_model,
                          int dtype, float* logits, uint8_t* gate, cudaStream_t s);
 
-// S: global anchors of window rows (adds their key blocks to band items' cost).
-cudaError_t launch_schedule(const uint8_t* gate, const void* q, int B, int N, int Hq, int W, int S,
-                            const PrefillWs& L, char* ws, int num_sms, cudaStream_t s);
+// Far-row lists, tile prefix counts and the cost-sorted work list of the
+// routed prefill, in one single-CTA launch.  S: global anchors of window rows
+// (adds their key blocks to band items' cost).
+cudaError_t launch_schedule(const uint8_t* gate, int B, int N, int Hq, int W, int S,
+                            const PrefillWs& L, char* ws, cudaStream_t s);
 
 struct TcAttnArgs {
     const void* q;     // [B,N,Hq,128] bf16
     const void* k;     // [B,N,Hkv,128]
     const void* v;
-    const void* qc;    // compacted far queries (prefill)
     const int* routed_list;
     const int* routed_count;
     const int* n_items;
@@ -128,7 +128,7 @@ cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const i
                           const DecodeWs& L, char* ws, unsigned int* err, cudaStream_t s);
 
 // ------------------------------------------------------------ backward ------
-// Far-row scan of launch_schedule on its own: routed_list/routed_count/
+// Far-row scan alone (one CTA per batch): routed_list/routed_count/
 // tile_prefix as in PrefillWs.
 cudaError_t launch_far_scan(const uint8_t* gate, int B, int N, int W, int* routed_list,
                             int* routed_count, int* tile_prefix, cudaStream_t s);
