@@ -4,25 +4,29 @@
 // A work item holds 256 query rows of one (batch, head): two 128-row tiles A
 // and B.  Band items take 256 consecutive rows and walk their window keys; far
 // items take 256 compacted routed rows and walk keys [0, max i].  The CTA
-// streams one sequence of 128-key blocks; each tile uses the contiguous run of
+// streams one sequence of 64-key blocks; each tile uses the contiguous run of
 // blocks its rows can see, so every K/V block is loaded once for both tiles.
 //
 // Items are claimed dynamically from the cost-sorted list (longest first).
 //
-// Per tile the chain is S = Q K^T (TMEM) -> softmax (P, bf16, written back
-// over S in TMEM) -> O += P V (P read from TMEM) -> next S.  The two tiles'
-// chains interleave on the tensor core: while warpgroup A turns S_A into P_A,
-// the tensor core runs tile B's PV and next S, and the reverse.
+// Per tile and block: S = Q K^T (TMEM) -> softmax (P, bf16, written back over
+// S in TMEM) -> O += P V (P read from TMEM).  Each tile has two S buffers, so
+// the tensor core computes S of block j+1 while the softmax warps work on
+// block j: per step the MMA warp issues S(j+1) of both tiles, then PV(j) of
+// both tiles as their P become ready.  A tile's softmax thus has a whole step
+// of tensor work (both tiles' PV and next S) to finish in, and the tensor core
+// does not wait on the softmax in steady state.
 //   warps 0-3   softmax + epilogue of tile A (thread r owns row r = TMEM lane r)
 //               (the epilogue stages rows in shared memory for coalesced stores)
 //   warps 4-7   softmax + epilogue of tile B
 //   warp 8      item claimer and TMA producer: Q tiles of band items, K and V
 //               blocks (converged, elected issue)
-//   warp 9      TMEM allocator and MMA issuer (converged, elected issue)
+//   warp 9      TMEM allocator and MMA issuer of tile A (converged, elected issue)
 //   warp 10     Q of far items: gathers the tile's routed rows by row index
 //               straight from Q (cp.async into the swizzled tile layout)
-//   warp 11     idle (completes the third warpgroup for register reconfiguration)
-// TMEM: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
+//   warp 11     MMA issuer of tile B
+// TMEM: S_A0 [0,64), S_A1 [64,128), S_B0 [128,192), S_B1 [192,256),
+// O_A [256,384), O_B [384,512).
 // Key sets per row (SwiAttn report, section 2; window per the weimeta.cn SWA
 // glossary): window rows [max(0, i-W+1), i], routed rows [0, i].  With S
 // global anchors (the glossary's 全局锚点) window rows also see
@@ -38,23 +42,26 @@
 namespace swi {
 namespace {
 
-constexpr int kStages = 2;
+constexpr int kKB = 64;      // keys per block
+constexpr int kStages = 4;
 constexpr int kThreads = 384;   // 3 warpgroups
 // Launched at 168 registers per thread (12 warps x 32 x 168 = 64512); the
 // producer/MMA warpgroup gives up registers to the two softmax warpgroups:
 // 2 x 128 x 216 + 128 x 72 = 64512.
 constexpr uint32_t kRegsSoftmax = 216;
 constexpr uint32_t kRegsOther = 72;
-constexpr int kTileBytes = kBM * kHD * 2;    // 32 KiB
-constexpr int kHalfBytes = kTileBytes / 2;   // 16 KiB
+constexpr int kTileBytes = kBM * kHD * 2;    // 32 KiB: one Q tile
+constexpr int kHalfBytes = kTileBytes / 2;   // 16 KiB: 64 head-dim columns of it
+constexpr int kKVBytes = kKB * kHD * 2;      // 16 KiB: one K or V block
+constexpr int kKVHalf = kKVBytes / 2;        // 8 KiB
 
 constexpr int kSched = 4;                                 // item broadcast ring
 constexpr int kStageBytesPerWarp = 32 * 64 * 2;           // 32 rows x 64 bf16 output columns
 
 constexpr int kOffQ = 0;                                  // Q_A, Q_B
 constexpr int kOffK = kOffQ + 2 * kTileBytes;             // K slots
-constexpr int kOffV = kOffK + kStages * kTileBytes;       // V slots
-constexpr int kOffStage = kOffV + kStages * kTileBytes;   // epilogue staging, 8 warps
+constexpr int kOffV = kOffK + kStages * kKVBytes;         // V slots
+constexpr int kOffStage = kOffV + kStages * kKVBytes;     // epilogue staging, 8 warps
 constexpr int kOffBar = kOffStage + 8 * kStageBytesPerWarp;
 
 enum {
@@ -62,18 +69,19 @@ enum {
     BAR_Q_EMPTY = BAR_Q_FULL + 2,          // [2]
     BAR_KV_FULL = BAR_Q_EMPTY + 2,         // [kStages]: slot of step g holds K_j and V_{j-1}
     BAR_KV_EMPTY = BAR_KV_FULL + kStages,  // [kStages]
-    BAR_S_FULL = BAR_KV_EMPTY + kStages,   // [2]
-    BAR_P_FULL = BAR_S_FULL + 2,           // [2]
-    BAR_O_FULL = BAR_P_FULL + 2,           // [2]
+    BAR_S_FULL = BAR_KV_EMPTY + kStages,   // [4]: tile x, S buffer b at 2x + b
+    BAR_P_FULL = BAR_S_FULL + 4,           // [4]
+    BAR_O_DONE = BAR_P_FULL + 4,           // [2]: a PV other than the run's last completed
+    BAR_O_FULL = BAR_O_DONE + 2,           // [2]: the run's last PV completed
     BAR_O_FREE = BAR_O_FULL + 2,           // [2]
     BAR_SCHED_FULL = BAR_O_FREE + 2,       // [kSched]
     BAR_SCHED_EMPTY = BAR_SCHED_FULL + kSched,
     BAR_DRAIN = BAR_SCHED_EMPTY + kSched,
     BAR_COUNT
 };
-// Consumers of a broadcast item: the MMA warp, the eight softmax warps and the
-// far-query gatherer.
-constexpr uint32_t kSchedConsumers = 1 + 8 + 1;
+// Consumers of a broadcast item: the two MMA warps, the eight softmax warps
+// and the far-query gatherer.
+constexpr uint32_t kSchedConsumers = 2 + 8 + 1;
 
 constexpr int kOffSched = kOffBar + BAR_COUNT * 8;
 constexpr int kOffMisc = kOffSched + kSched * 4;
@@ -81,10 +89,10 @@ constexpr int kSmemBytes = kOffMisc + 16 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 constexpr uint32_t kTmemCols = 512;
-__device__ __forceinline__ uint32_t col_s(int x) { return x ? 128u : 0u; }
+__device__ __forceinline__ uint32_t col_s(int x, uint32_t b) { return x * 128u + b * 64u; }
 __device__ __forceinline__ uint32_t col_o(int x) { return x ? 384u : 256u; }
 
-constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, false, false);
+constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kKB, false, false);
 constexpr uint32_t kIdescO = idesc_bf16_f32(kBM, kHD, false, true);
 
 struct PfParams {
@@ -115,8 +123,6 @@ struct Plan {
     int nrows[2];      // valid rows per tile
 };
 
-__device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
-
 template <bool ANCH>
 __device__ __forceinline__ Plan make_plan(const PfParams& p, int idx) {
     const WorkItem it = p.items[idx];
@@ -138,7 +144,7 @@ __device__ __forceinline__ Plan make_plan(const PfParams& p, int idx) {
             const int r0 = pl.row0 + x * kBM;
             pl.nrows[x] = max(0, min(kBM, cnt - r0));
             pl.j0[x] = 0;
-            pl.j1[x] = pl.nrows[x] > 0 ? list[r0 + pl.nrows[x] - 1] / kBN : -1;
+            pl.j1[x] = pl.nrows[x] > 0 ? list[r0 + pl.nrows[x] - 1] / kKB : -1;
             maxb = max(maxb, pl.j1[x] + 1);
         }
         pl.nblk = maxb;
@@ -156,12 +162,12 @@ __device__ __forceinline__ Plan make_plan(const PfParams& p, int idx) {
             if (has_rows) {
                 const int lo_key = max(0, r0 - p.W + 1);
                 const int hi_key = r0 + pl.nrows[x] - 1;
-                pl.j0[x] = (lo_key - pl.kv0) / kBN;
-                pl.j1[x] = (hi_key - pl.kv0) / kBN;
+                pl.j0[x] = (lo_key - pl.kv0) / kKB;
+                pl.j1[x] = (hi_key - pl.kv0) / kKB;
                 last = max(last, pl.j1[x]);
                 const int hi_anchor = min(p.S - 1, hi_key - p.W);   // anchors below the window
                 if (ANCH && hi_anchor >= 0) {
-                    pl.ja1[x] = hi_anchor / kBN;
+                    pl.ja1[x] = hi_anchor / kKB;
                     pl.na = max(pl.na, pl.ja1[x] + 1);
                 }
             } else {
@@ -191,7 +197,7 @@ __device__ __forceinline__ int first_blk(const Plan& pl, int x) {
 }
 template <bool ANCH>
 __device__ __forceinline__ int blk_key0(const Plan& pl, int j) {
-    return (ANCH && j < pl.na) ? j * kBN : pl.kv0 + (j - (ANCH ? pl.na : 0)) * kBN;
+    return (ANCH && j < pl.na) ? j * kKB : pl.kv0 + (j - (ANCH ? pl.na : 0)) * kKB;
 }
 
 // ----------------------------------------------------------------- roles --
@@ -264,19 +270,19 @@ __device__ bool producer(const PfParams& p, uint8_t* smem, uint64_t* bar, volati
             if (j < pl.nblk && tile_active(pl, 1) && j == first_blk<ANCH>(pl, 1) && !load_q(1)) return false;
             const uint32_t st = g % kStages, ph = (g / kStages) & 1u;
             if (!mbar_wait_w(&bar[BAR_KV_EMPTY + st], ph ^ 1u, abort_flag, p.err)) return false;
-            const uint32_t bytes = (j < pl.nblk ? kTileBytes : 0) + (j >= 1 ? kTileBytes : 0);
+            const uint32_t bytes = (j < pl.nblk ? kKVBytes : 0) + (j >= 1 ? kKVBytes : 0);
             mbar_arrive_expect_tx_w(&bar[BAR_KV_FULL + st], bytes);
             if (j < pl.nblk) {
-                uint8_t* dst = smem + kOffK + st * kTileBytes;
+                uint8_t* dst = smem + kOffK + st * kKVBytes;
                 const int key0 = blk_key0<ANCH>(pl, j);
                 tma_load_4d_w(dst, &p.tm_k, &bar[BAR_KV_FULL + st], 0, pl.kvh, key0, pl.b);
-                tma_load_4d_w(dst + kHalfBytes, &p.tm_k, &bar[BAR_KV_FULL + st], 64, pl.kvh, key0, pl.b);
+                tma_load_4d_w(dst + kKVHalf, &p.tm_k, &bar[BAR_KV_FULL + st], 64, pl.kvh, key0, pl.b);
             }
             if (j >= 1) {
-                uint8_t* dst = smem + kOffV + st * kTileBytes;
+                uint8_t* dst = smem + kOffV + st * kKVBytes;
                 const int key0 = blk_key0<ANCH>(pl, j - 1);
                 tma_load_4d_w(dst, &p.tm_v, &bar[BAR_KV_FULL + st], 0, pl.kvh, key0, pl.b);
-                tma_load_4d_w(dst + kHalfBytes, &p.tm_v, &bar[BAR_KV_FULL + st], 64, pl.kvh, key0, pl.b);
+                tma_load_4d_w(dst + kKVHalf, &p.tm_v, &bar[BAR_KV_FULL + st], 64, pl.kvh, key0, pl.b);
             }
             ++g;
         }
@@ -355,72 +361,79 @@ __device__ void drain_loads(uint64_t* full_bars, uint32_t issued) {
     }
 }
 
+// MMA warp of tile x (one per tile, converged, elected issue).  Step j of an
+// item (slot g holds K_j and V_{j-1}): S(j), if the tile's run contains block
+// j, into the S buffer not holding block j-1's P; then PV(j-1) once the
+// softmax has written P(j-1).  A tile's S buffer is reused two blocks later,
+// after the PV that read it (this warp issues both, in that order).  Each PV
+// but the run's last commits BAR_O_DONE (the softmax waits on it before
+// rescaling O); the last commits BAR_O_FULL.  Both MMA warps walk every step
+// and release the slot with one commit each; the tensor core interleaves
+// their MMAs, which touch disjoint TMEM columns.
 template <bool ANCH>
 __device__ bool mma_issuer(const PfParams& p, uint8_t* smem, uint64_t* bar, volatile int* sched,
-                           uint32_t tmem, volatile int* abort_flag) {
-    uint32_t g = 0;
-    uint32_t q_cnt[2] = {0, 0}, p_cnt[2] = {0, 0}, o_cnt[2] = {0, 0};
+                           uint32_t tmem, volatile int* abort_flag, int x) {
+    uint32_t g = 0, q_cnt = 0, s_cnt = 0, o_cnt = 0;
+    // Shared-memory descriptors of the operand tiles, formed once: the start
+    // address is the low field, so a byte offset o within a tile adds o >> 4
+    // (no carry: every address in the 227 KiB window is below 2^18).
+    const uint64_t dQ = sdesc_sw128(smem_u32(smem + kOffQ + x * kTileBytes), 16, 1024);
+    const uint64_t dK0 = sdesc_sw128(smem_u32(smem + kOffK), 16, 1024);
+    const uint64_t dV0 = sdesc_sw128(smem_u32(smem + kOffV), kKVHalf, 1024);
 
     for (int k = 0;; ++k) {
         int idx;
         if (!consume_item(p, bar, sched, k, abort_flag, idx)) return false;
         if (idx < 0) break;
         const Plan pl = make_plan<ANCH>(p, idx);
-        int pend[2] = {-1, -1};
-        bool first_pv[2] = {true, true};
-
-        auto issue_pv = [&](int x, int jj, uint32_t sV) -> bool {
-            if (!mbar_wait_w(&bar[BAR_P_FULL + x], p_cnt[x] & 1u, abort_flag, p.err)) return false;
-            ++p_cnt[x];
-            if (first_pv[x]) {
-                if (!mbar_wait_w(&bar[BAR_O_FREE + x], (o_cnt[x] & 1u) ^ 1u, abort_flag, p.err))
-                    return false;
-                ++o_cnt[x];
-            }
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk) {
-                const uint64_t bdesc = sdesc_sw128(sV + kk * 16 * 128, kHalfBytes, 1024);
-                umma_bf16_ts_w(tmem + col_o(x), tmem + col_s(x) + kk * 8, bdesc, kIdescO,
-                               (first_pv[x] && kk == 0) ? 0u : 1u);
-            }
-            first_pv[x] = false;
-            if (jj == pl.j1[x]) umma_commit_w(&bar[BAR_O_FULL + x]);
-            return true;
-        };
+        bool pend = false;   // block j-1 awaits its PV
+        bool first_pv = true;
 
         for (int j = 0; j <= pl.nblk; ++j) {
             const uint32_t st = g % kStages, ph = (g / kStages) & 1u;
             if (!mbar_wait_w(&bar[BAR_KV_FULL + st], ph, abort_flag, p.err)) return false;
             tc_fence_after();
-            const uint32_t sK = smem_u32(smem + kOffK + st * kTileBytes);
-            const uint32_t sV = smem_u32(smem + kOffV + st * kTileBytes);
-#pragma unroll
-            for (int x = 0; x < 2; ++x) {
-                // PV of the previous block first: P_x lives in S_x's columns.
-                if (pend[x] >= 0) {
-                    if (!issue_pv(x, pend[x], sV)) return false;
-                    pend[x] = -1;
+            const bool now = j < pl.nblk && blk_active<ANCH>(pl, x, j);
+            if (now) {
+                if (j == first_blk<ANCH>(pl, x)) {
+                    if (!mbar_wait_w(&bar[BAR_Q_FULL + x], q_cnt & 1u, abort_flag, p.err)) return false;
+                    ++q_cnt;
+                    tc_fence_after();
                 }
-                if (j < pl.nblk && blk_active<ANCH>(pl, x, j)) {
-                    if (j == first_blk<ANCH>(pl, x)) {
-                        if (!mbar_wait_w(&bar[BAR_Q_FULL + x], q_cnt[x] & 1u, abort_flag, p.err))
-                            return false;
-                        ++q_cnt[x];
-                        tc_fence_after();
-                    }
-                    const uint32_t sQ = smem_u32(smem + kOffQ + x * kTileBytes);
+                const uint32_t b = s_cnt & 1u;
+                const uint64_t dK = dK0 + st * (kKVBytes >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < kHD / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                        umma_bf16_w(tmem + col_s(x), sdesc_sw128(sQ + off, 16, 1024),
-                                    sdesc_sw128(sK + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
-                    }
-                    umma_commit_w(&bar[BAR_S_FULL + x]);
-                    if (j == pl.j1[x]) umma_commit_w(&bar[BAR_Q_EMPTY + x]);
-                    pend[x] = j;
+                for (int kk = 0; kk < kHD / 16; ++kk) {
+                    const uint32_t offq = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+                    const uint32_t offk = (kk >> 2) * kKVHalf + (kk & 3) * 32;
+                    umma_bf16_w(tmem + col_s(x, b), dQ + (offq >> 4), dK + (offk >> 4), kIdescS,
+                                kk > 0 ? 1u : 0u);
                 }
+                umma_commit_w(&bar[BAR_S_FULL + 2 * x + b]);
+                if (j == pl.j1[x]) umma_commit_w(&bar[BAR_Q_EMPTY + x]);
+                ++s_cnt;
             }
+            if (pend) {
+                const uint32_t n = s_cnt - (now ? 2u : 1u);   // block j-1's S
+                const uint32_t b = n & 1u;
+                if (!mbar_wait_w(&bar[BAR_P_FULL + 2 * x + b], (n >> 1) & 1u, abort_flag, p.err))
+                    return false;
+                if (first_pv) {
+                    if (!mbar_wait_w(&bar[BAR_O_FREE + x], (o_cnt & 1u) ^ 1u, abort_flag, p.err))
+                        return false;
+                    ++o_cnt;
+                }
+                tc_fence_after();
+                const uint64_t dV = dV0 + st * (kKVBytes >> 4);
+#pragma unroll
+                for (int kk = 0; kk < kKB / 16; ++kk)
+                    umma_bf16_ts_w(tmem + col_o(x), tmem + col_s(x, b) + kk * 8,
+                                   dV + ((kk * 16 * 128) >> 4), kIdescO,
+                                   (first_pv && kk == 0) ? 0u : 1u);
+                first_pv = false;
+                umma_commit_w(&bar[(j - 1 == pl.j1[x]) ? BAR_O_FULL + x : BAR_O_DONE + x]);
+            }
+            pend = now;
             umma_commit_w(&bar[BAR_KV_EMPTY + st]);
             ++g;
         }
@@ -440,12 +453,11 @@ __device__ bool softmax_role(const PfParams& p, uint8_t* smem, uint64_t* bar, vo
                              uint32_t tmem, volatile int* abort_flag, int x, int wq, int lane) {
     const int r = wq * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-    const uint32_t tS = lane_base + col_s(x);
     const uint32_t tO = lane_base + col_o(x);
     const float sl = p.scale_log2;
     // This warp's 4 KiB staging area for coalesced output stores.
     const uint32_t stg = smem_u32(smem + kOffStage + (x * 4 + wq) * kStageBytesPerWarp);
-    uint32_t s_cnt = 0, o_cnt = 0;
+    uint32_t s_cnt = 0, o_cnt = 0, od_cnt = 0;
 
     for (int k = 0;; ++k) {
         int idx;
@@ -470,22 +482,23 @@ __device__ bool softmax_role(const PfParams& p, uint8_t* smem, uint64_t* bar, vo
         const int e_anc = (ANCH && i >= 0 && !far) ? min(p.S - 1, i - p.W) : -1;
 
         float m2 = -INFINITY, l = 0.f;
+        bool first = true;
         for (int j = first_blk<ANCH>(pl, x); j <= pl.j1[x]; ++j) {
             if (ANCH && j > pl.ja1[x] && j < pl.j0[x]) continue;
             const bool anc = ANCH && j <= pl.ja1[x];
             const int key0 = blk_key0<ANCH>(pl, j);
             const int a = (anc ? 0 : lo) - key0, e = (anc ? e_anc : hi) - key0;
-            if (!warp_wait(&bar[BAR_S_FULL + x], s_cnt & 1u, abort_flag, p.err)) return false;
-            ++s_cnt;
+            const uint32_t b = s_cnt & 1u;
+            if (!warp_wait(&bar[BAR_S_FULL + 2 * x + b], (s_cnt >> 1) & 1u, abort_flag, p.err))
+                return false;
             tc_fence_after();
-            uint32_t sr[128];
+            const uint32_t tS = lane_base + col_s(x, b);
+            uint32_t sr[kKB];
             tmem_ld32(tS + 0, sr);
             tmem_ld32(tS + 32, sr + 32);
-            tmem_ld32(tS + 64, sr + 64);
-            tmem_ld32(tS + 96, sr + 96);
             tmem_ld_wait();
             float* s = reinterpret_cast<float*>(sr);
-            const bool full = a <= 0 && e >= kBN - 1;   // every key of the block visible
+            const bool full = a <= 0 && e >= kKB - 1;   // every key of the block visible
             // Warp-uniform classification (every lane votes, the branches
             // follow the votes, so a warp never runs two paths): a mask that
             // is one-sided for the whole warp (visible c <= e: diagonal and
@@ -494,28 +507,28 @@ __device__ bool softmax_role(const PfParams& p, uint8_t* smem, uint64_t* bar, vo
             // tree as for a full block.
             const bool all_full = __all_sync(0xffffffffu, full);
             const bool all_pre = __all_sync(0xffffffffu, a <= 0);
-            const bool all_suf = __all_sync(0xffffffffu, e >= kBN - 1);
+            const bool all_suf = __all_sync(0xffffffffu, e >= kKB - 1);
             float m8[8];
 #pragma unroll
             for (int t = 0; t < 8; ++t) m8[t] = -INFINITY;
             if (!all_full) {
                 if (all_pre) {
 #pragma unroll
-                    for (int cc = 0; cc < kBN; ++cc) s[cc] = cc <= e ? s[cc] : -INFINITY;
+                    for (int cc = 0; cc < kKB; ++cc) s[cc] = cc <= e ? s[cc] : -INFINITY;
                 } else if (all_suf) {
 #pragma unroll
-                    for (int cc = 0; cc < kBN; ++cc) s[cc] = cc >= a ? s[cc] : -INFINITY;
+                    for (int cc = 0; cc < kKB; ++cc) s[cc] = cc >= a ? s[cc] : -INFINITY;
                 } else {
                     const uint32_t span = static_cast<uint32_t>(e - a);
 #pragma unroll
-                    for (int cc = 0; cc < kBN; ++cc) {
+                    for (int cc = 0; cc < kKB; ++cc) {
                         const bool ok = static_cast<uint32_t>(cc - a) <= span && e >= a;
                         s[cc] = ok ? s[cc] : -INFINITY;
                     }
                 }
             }
 #pragma unroll
-            for (int cc = 0; cc < kBN; cc += 16)
+            for (int cc = 0; cc < kKB; cc += 16)
 #pragma unroll
                 for (int t = 0; t < 8; ++t) m8[t] = fmax3(m8[t], s[cc + 2 * t], s[cc + 2 * t + 1]);
             const float mx = fmaxf(fmax3(m8[0], m8[1], m8[2]),
@@ -529,7 +542,37 @@ __device__ bool softmax_role(const PfParams& p, uint8_t* smem, uint64_t* bar, vo
                 alpha = ex2_approx(m2 - mnew);
                 m2 = mnew;
             }
-            // O_X is stable here: S_X(j) completing implies the earlier PV_X did.
+            const float mb = (m2 == -INFINITY) ? 0.f : m2;
+            const float2 sl2 = make_float2(sl, sl), nmb = make_float2(-mb, -mb);
+            float2 r4[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) r4[t] = make_float2(0.f, 0.f);
+            // p = 2^(s * scale * log2 e - m) on the MUFU (a masked key's
+            // weight is exactly 0); scale-and-subtract and the row sums use
+            // packed fp32 pairs.  P goes over the S columns just read.
+            {
+                uint32_t pk[kKB / 2];
+#pragma unroll
+                for (int pp = 0; pp < kKB / 2; ++pp) {
+                    const float2 xv = ffma2(make_float2(s[2 * pp], s[2 * pp + 1]), sl2, nmb);
+                    float2 pv;
+                    pv.x = ex2_approx(xv.x);
+                    pv.y = ex2_approx(xv.y);
+                    r4[pp & 3] = fadd2(r4[pp & 3], pv);
+                    pk[pp] = pack_bf16x2(pv.x, pv.y);
+                }
+                tmem_st32(tS, pk);
+            }
+            const float2 rs2 = fadd2(fadd2(r4[0], r4[1]), fadd2(r4[2], r4[3]));
+            const float rs = rs2.x + rs2.y;
+            // O may be rescaled only once the previous block's PV has landed
+            // (it was issued after this block's S, so it has normally completed
+            // by now); the first block of the run has no earlier PV.
+            if (!first) {
+                if (!warp_wait(&bar[BAR_O_DONE + x], od_cnt & 1u, abort_flag, p.err)) return false;
+                ++od_cnt;
+                tc_fence_after();
+            }
             const bool need = resc && l > 0.f;
             if (__any_sync(0xffffffffu, need)) {
                 const float f = need ? alpha : 1.f;
@@ -543,36 +586,12 @@ __device__ bool softmax_role(const PfParams& p, uint8_t* smem, uint64_t* bar, vo
                     tmem_st32(tO + q4 * 32, orr);
                 }
             }
-            const float mb = (m2 == -INFINITY) ? 0.f : m2;
-            const float2 sl2 = make_float2(sl, sl), nmb = make_float2(-mb, -mb);
-            float2 r4[4];
-#pragma unroll
-            for (int t = 0; t < 4; ++t) r4[t] = make_float2(0.f, 0.f);
-            // p = 2^(s * scale * log2 e - m) on the MUFU (a masked key's
-            // weight is exactly 0); scale-and-subtract and the row sums use
-            // packed fp32 pairs.
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int pp = 0; pp < 32; ++pp) {
-                    const int cc = hh * 64 + 2 * pp;
-                    const float2 xv = ffma2(make_float2(s[cc], s[cc + 1]), sl2, nmb);
-                    float2 pv;
-                    pv.x = ex2_approx(xv.x);
-                    pv.y = ex2_approx(xv.y);
-                    r4[pp & 3] = fadd2(r4[pp & 3], pv);
-                    pk[pp] = pack_bf16x2(pv.x, pv.y);
-                }
-                // P over the S columns this half has already consumed.
-                tmem_st32(tS + hh * 32, pk);
-            }
-            const float2 rs2 = fadd2(fadd2(r4[0], r4[1]), fadd2(r4[2], r4[3]));
-            const float rs = rs2.x + rs2.y;
             tmem_st_wait();
             l = l * alpha + rs;
+            first = false;
+            ++s_cnt;
             tc_fence_before();
-            mbar_arrive(&bar[BAR_P_FULL + x]);
+            mbar_arrive(&bar[BAR_P_FULL + 2 * x + b]);
         }
 
         // Epilogue: O/l as bf16.  Each thread stages its row (64 columns at a
@@ -634,20 +653,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         for (int x = 0; x < 2; ++x) {
             mbar_init(&bar[BAR_Q_FULL + x], 1);
             mbar_init(&bar[BAR_Q_EMPTY + x], 1);
-            mbar_init(&bar[BAR_S_FULL + x], 1);
-            mbar_init(&bar[BAR_P_FULL + x], kBM);
+            mbar_init(&bar[BAR_O_DONE + x], 1);
             mbar_init(&bar[BAR_O_FULL + x], 1);
             mbar_init(&bar[BAR_O_FREE + x], kBM);
         }
+        for (int sb = 0; sb < 4; ++sb) {
+            mbar_init(&bar[BAR_S_FULL + sb], 1);
+            mbar_init(&bar[BAR_P_FULL + sb], kBM);
+        }
         for (int st = 0; st < kStages; ++st) {
             mbar_init(&bar[BAR_KV_FULL + st], 1);
-            mbar_init(&bar[BAR_KV_EMPTY + st], 1);
+            mbar_init(&bar[BAR_KV_EMPTY + st], 2);   // one commit per MMA warp
         }
         for (int st = 0; st < kSched; ++st) {
             mbar_init(&bar[BAR_SCHED_FULL + st], 1);
             mbar_init(&bar[BAR_SCHED_EMPTY + st], kSchedConsumers);
         }
-        mbar_init(&bar[BAR_DRAIN], 1);
+        mbar_init(&bar[BAR_DRAIN], 2);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -681,9 +703,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 if (q_tma_last[x]) mbar_drain(&bar[BAR_Q_FULL + x], (q_issued[x] - 1) & 1u);
         }
         __syncwarp();
-    } else if (warp == 9) {
-        mma_issuer<ANCH>(p, smem, bar, sched, tmem, abort_flag);
-        // Every MMA this warp issued has completed once this arrives.
+    } else if (warp == 9 || warp == 11) {
+        mma_issuer<ANCH>(p, smem, bar, sched, tmem, abort_flag, warp == 9 ? 0 : 1);
+        // Every MMA both warps issued has completed once this phase completes.
         umma_commit_w(&bar[BAR_DRAIN]);
         mbar_drain(&bar[BAR_DRAIN], 0);
         __syncwarp();
@@ -707,8 +729,8 @@ cudaError_t launch_prefill_tc(const TcAttnArgs& a, const int* tile_prefix, unsig
     memset(&p, 0, sizeof(p));
     const uint64_t N = a.N, B = a.B;
     bool ok = make_tmap_4d_bf16(&p.tm_q, a.q, kHD, a.Hq, N, B, 64, kBM) &&
-              make_tmap_4d_bf16(&p.tm_k, a.k, kHD, a.Hkv, N, B, 64, kBN) &&
-              make_tmap_4d_bf16(&p.tm_v, a.v, kHD, a.Hkv, N, B, 64, kBN);
+              make_tmap_4d_bf16(&p.tm_k, a.k, kHD, a.Hkv, N, B, 64, kKB) &&
+              make_tmap_4d_bf16(&p.tm_v, a.v, kHD, a.Hkv, N, B, 64, kKB);
     if (!ok) return cudaErrorInvalidValue;
     p.q = static_cast<const __nv_bfloat16*>(a.q);
     p.routed_list = a.routed_list;
