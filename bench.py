@@ -48,8 +48,8 @@ MEASURED_TRAFFIC = {
     ("prefill", "654a283632d6b709"): 972332800 + 126025472,
     # decode_split_kernel, 16 x 32768 decode: 654 404 608 read + 2 771 200 written
     ("decode", "525498dfbc8e1971"): 654404608 + 2771200,
-    # dual_kernel, dual-branch workload B=2 N=8192 GQA 16/4: 155 273 984 read + 272 345 088 written
-    ("dual", "96d14ef8dc35435e"): 155273984 + 272345088,
+    # dual_kernel, dual-branch workload B=2 N=8192 GQA 16/4: 158 522 880 read + 271 861 760 written
+    ("dual", "022299affd4ac4fb"): 158522880 + 271861760,
     # dkdv_kernel + dq_kernel, backward on the dual workload: (319 911 424 + 22 017 024)
     # + (253 355 520 + 48 199 168)
     ("backward", "f701359c9e5dddba"): 319911424 + 22017024 + 253355520 + 48199168,

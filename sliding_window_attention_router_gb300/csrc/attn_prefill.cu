@@ -565,16 +565,23 @@ __device__ bool softmax_role(const PfParams& p, uint8_t* smem, uint64_t* bar, vo
             }
             const float2 rs2 = fadd2(fadd2(r4[0], r4[1]), fadd2(r4[2], r4[3]));
             const float rs = rs2.x + rs2.y;
-            // O may be rescaled only once the previous block's PV has landed
-            // (it was issued after this block's S, so it has normally completed
-            // by now); the first block of the run has no earlier PV.
-            if (!first) {
-                if (!warp_wait(&bar[BAR_O_DONE + x], od_cnt & 1u, abort_flag, p.err)) return false;
-                ++od_cnt;
-                tc_fence_after();
-            }
+            // O may be rescaled only once the previous block's PV has landed.
+            // Its commit is BAR_O_DONE phase od_cnt (every PV of the run but
+            // the last commits one); that phase is waited for only when some
+            // row rescales.  Skipping the wait otherwise keeps the parity test
+            // unambiguous: S(j) completing implies PV(j-2) did (same issuing
+            // thread, issued before it), and PV(j) needs this block's P, so
+            // the barrier is at phase od_cnt or just past it.
             const bool need = resc && l > 0.f;
-            if (__any_sync(0xffffffffu, need)) {
+            const bool any_need = __any_sync(0xffffffffu, need);
+            if (!first) {
+                if (any_need) {
+                    if (!warp_wait(&bar[BAR_O_DONE + x], od_cnt & 1u, abort_flag, p.err)) return false;
+                    tc_fence_after();
+                }
+                ++od_cnt;
+            }
+            if (any_need) {
                 const float f = need ? alpha : 1.f;
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
