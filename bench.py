@@ -44,8 +44,8 @@ L2_FLUSH_BYTES = 256 << 20
 # SHA-256 of the kernel's source files at capture time; a kernel whose source
 # has changed since reports null.
 MEASURED_TRAFFIC = {
-    # prefill_kernel, long-context prefill N=32768 f=0.13: 972 332 800 read + 126 025 472 written
-    ("prefill", "654a283632d6b709"): 972332800 + 126025472,
+    # prefill_kernel, long-context prefill N=32768 f=0.13: 1 142 919 424 read + 127 038 720 written
+    ("prefill", "ccb76205e85abea5"): 1142919424 + 127038720,
     # decode_split_kernel, 16 x 32768 decode: 654 404 608 read + 2 771 200 written
     ("decode", "525498dfbc8e1971"): 654404608 + 2771200,
     # dual_kernel, dual-branch workload B=2 N=8192 GQA 16/4: 158 522 880 read + 271 861 760 written
@@ -413,7 +413,8 @@ def route_section(swa, timer, dev, steps, warmup, seed):
 
 
 def layer_4k_section(swa, timer, dev, steps, warmup, seed):
-    """Single-layer prefill: router GEMV + gate, then routed prefill on its gates."""
+    """Single-layer prefill: router GEMV + gate, then routed prefill on its gates,
+    timed as the fused call (route_prefill) and as the two separate calls."""
     d = inp.prefill_4k(seed=seed)
     B, N, H, D, W = d["B"], d["N"], d["Hq"], d["d"], d["W"]
     h, w = d["h"].to(dev), d["w"].to(dev)
@@ -424,14 +425,26 @@ def layer_4k_section(swa, timer, dev, steps, warmup, seed):
     ws = torch.empty(swa.prefill_workspace(B, N, H, H, D, W, torch.bfloat16), dtype=torch.uint8,
                      device=dev)
 
-    def step():
+    wsf = torch.empty(swa.route_prefill_workspace(B, N, H, H, D, W, torch.bfloat16),
+                      dtype=torch.uint8, device=dev)
+    logits_f = torch.empty((B, N), dtype=torch.float32, device=dev)
+    gate_f = torch.empty((B, N), dtype=torch.uint8, device=dev)
+    o_f = torch.empty_like(q)
+
+    def separate():
         swa.route(h, w, d["bias"], logits=logits, gate=gate)
         swa.prefill(q, k, v, gate.view(B, N), W, out=o, workspace=ws)
 
-    step_ms, _ = timer.run(step, steps, warmup)
+    def fused():
+        swa.route_prefill(h, w, d["bias"], q, k, v, W, out=o_f, logits=logits_f, gate=gate_f,
+                          workspace=wsf)
+
+    sep_ms, _ = timer.run(separate, steps, warmup)
+    step_ms, _ = timer.run(fused, steps, warmup)
     assert swa.get_device_error() == 0
+    assert torch.equal(gate_f.view(-1), gate)
     pairs = useful_pairs(gate.view(B, N).cpu().numpy(), W)
-    return dict(step_ms=step_ms, flops=4.0 * D * H * pairs,
+    return dict(step_ms=step_ms, separate_ms=sep_ms, flops=4.0 * D * H * pairs,
                 routed_frac=float(gate.float().mean()))
 
 
@@ -666,9 +679,11 @@ def run_ours(args, dist: Dist):
         l4 = layer_4k_section(swa, timer, dev, ks, kw, seed=dist.rank)
         l4s = statistics.mean(l4["step_ms"]) / 1e3
         extra["layer_4k"] = {"tflops": l4["flops"] / l4s / 1e12, "ms_per_step": l4s * 1e3,
+                             "separate_calls_ms_per_step": statistics.mean(l4["separate_ms"]),
                              "routed_frac": l4["routed_frac"],
                              "workload": "single-layer prefill bf16: router GEMV over h [4096, 2048] "
-                                         "then routed prefill B=1 H=16 d=128 N=4096 W=1024 on its gates"}
+                                         "then routed prefill B=1 H=16 d=128 N=4096 W=1024 on its "
+                                         "gates, as one fused call (route_prefill)"}
         du = dual_section(swa, timer, dev, ks, kw, seed=dist.rank)
         dm = statistics.mean(du["step_ms"]) / 1e3
         dk_t = du["flops"] / (statistics.mean(du["kern_ms"]) / 1e3) / 1e12
@@ -729,7 +744,7 @@ def run_ours(args, dist: Dist):
                          "peak_source": f"{peaks_src} bf16 dense (burst)"},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": 3 * args.steps,
+            "gpu_launches": 2 * args.steps,   # plan_kernel + prefill_kernel per step
             "clocks": clk,
             "wall_s_headline": wall,
         }

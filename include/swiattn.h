@@ -97,6 +97,29 @@ int swiattn_prefill_anchored(const void* q, const void* k, const void* v, const 
                              int n_anchor, float scale, int dtype, void* workspace,
                              size_t workspace_bytes, void* stream);
 
+/* Bytes of device workspace swiattn_route_prefill needs (0 for invalid sizes). */
+size_t swiattn_route_prefill_workspace(int B, int N, int Hq, int Hkv, int d, int W, int dtype);
+
+/* One layer's router and routed prefill in one call (report section 2: the
+ * router's hard gate decides, per token, the key set of the prefill):
+ *   logits[b*N+i] = h[b*N+i,:] . w + bias,  gate[b*N+i] = logits > 0,
+ * then o = swiattn_prefill_anchored(q, k, v, gate, ...).  h [B*N, d_model]
+ * and w [d_model] of `dtype` (16-byte aligned; d_model a multiple of 8 for
+ * bf16, 4 for fp32); logits fp32 [B*N] and gate uint8 [B*N] are written (the
+ * gates are the prefill's); the remaining arguments as
+ * swiattn_prefill_anchored (n_anchor 0: no anchors).  For bf16 the router GEMV
+ * and the prefill schedule are one launch (the CTA that finishes the GEMV last
+ * plans the prefill over all gates), so the call is two kernel launches and a
+ * 4-byte reset of a counter in the workspace.  Results equal those of
+ * swiattn_route followed by swiattn_prefill_anchored bit for bit.
+ * workspace: at least swiattn_route_prefill_workspace(...) bytes, 256-byte
+ * aligned, scratch only; calls that share one must not overlap in time. */
+int swiattn_route_prefill(const void* h, const void* w, float bias, int d_model, const void* q,
+                          const void* k, const void* v, void* o, float* lse, float* logits,
+                          uint8_t* gate, int B, int N, int Hq, int Hkv, int d, int W, int n_anchor,
+                          float scale, int dtype, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
 /* Bytes of device workspace swiattn_decode needs for these sizes. */
 size_t swiattn_decode_workspace(int B, int Lmax, int Hq, int Hkv, int d, int W, int dtype);
 

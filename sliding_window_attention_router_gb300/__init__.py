@@ -38,7 +38,8 @@ EXPORTS = (
     "swiattn_dual_branch", "swiattn_prefill_backward_workspace", "swiattn_prefill_backward",
     "swiattn_route_backward_workspace", "swiattn_route_backward",
     "swiattn_decode_paged_workspace", "swiattn_decode_paged", "swiattn_decode_anchored_workspace",
-    "swiattn_decode_anchored", "swiattn_prefill_anchored",
+    "swiattn_decode_anchored", "swiattn_prefill_anchored", "swiattn_route_prefill_workspace",
+    "swiattn_route_prefill",
     "swiattn_get_device_error", "swiattn_status_string", "swiattn_set_profile_events",
     "swiattn_num_sms",
 )
@@ -90,6 +91,10 @@ def _load() -> ctypes.CDLL:
             lib.swiattn_decode_anchored_workspace.restype = sz
             lib.swiattn_decode_anchored.argtypes = [vp] * 7 + [i32] * 7 + [f32, i32, vp, sz, vp]
             lib.swiattn_prefill_anchored.argtypes = [vp] * 6 + [i32] * 7 + [f32, i32, vp, sz, vp]
+            lib.swiattn_route_prefill_workspace.argtypes = [i32] * 7
+            lib.swiattn_route_prefill_workspace.restype = sz
+            lib.swiattn_route_prefill.argtypes = ([vp, vp, f32, i32] + [vp] * 7 + [i32] * 7 +
+                                                  [f32, i32, vp, sz, vp])
             lib.swiattn_get_device_error.argtypes = [vp]
             lib.swiattn_status_string.argtypes = [i32]
             lib.swiattn_status_string.restype = ctypes.c_char_p
@@ -100,7 +105,7 @@ def _load() -> ctypes.CDLL:
                          "swiattn_dual_branch", "swiattn_get_device_error", "swiattn_num_sms",
                          "swiattn_prefill_backward", "swiattn_route_backward",
                          "swiattn_decode_paged", "swiattn_decode_anchored",
-                         "swiattn_prefill_anchored"):
+                         "swiattn_prefill_anchored", "swiattn_route_prefill"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -206,6 +211,40 @@ def prefill(q, k, v, gate, W: int, scale: Optional[float] = None, out=None, want
                                        B, N, Hq, Hkv, d, W, float(scale), _DT[q.dtype], _ptr(ws),
                                        ws.numel(), _stream()), "swiattn_prefill")
     return (o, lse) if want_lse else o
+
+
+def route_prefill_workspace(B, N, Hq, Hkv, d, W, dtype) -> int:
+    return int(_load().swiattn_route_prefill_workspace(B, N, Hq, Hkv, d, W, _DT.get(dtype, dtype)))
+
+
+def route_prefill(h, w, bias: float, q, k, v, W: int, scale: Optional[float] = None,
+                  n_anchor: int = 0, out=None, want_lse=False, logits=None, gate=None,
+                  workspace=None):
+    """One layer's router and routed prefill in one call.  h [B*N, d_model] (or
+    [B, N, d_model]), w [d_model]; q [B,N,Hq,d], k/v [B,N,Hkv,d].  Returns
+    (o, logits fp32 [B,N], gate uint8 [B,N]) (and lse when want_lse)."""
+    _dev(q, "q")
+    _dev(k, "k", q.dtype)
+    _dev(v, "v", q.dtype)
+    _dev(h, "h", q.dtype)
+    _dev(w, "w", q.dtype)
+    B, N, Hq, d = q.shape
+    Hkv = k.shape[2]
+    D = h.shape[-1]
+    if h.numel() != B * N * D or w.numel() != D:
+        raise ValueError("h must hold B*N rows of d_model values and w d_model values")
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o = out if out is not None else torch.empty_like(q)
+    lse = torch.empty((B, N, Hq), device=q.device, dtype=torch.float32) if want_lse else None
+    logits = logits if logits is not None else torch.empty((B, N), device=q.device,
+                                                           dtype=torch.float32)
+    gate = gate if gate is not None else torch.empty((B, N), device=q.device, dtype=torch.uint8)
+    ws = _workspace(route_prefill_workspace(B, N, Hq, Hkv, d, W, q.dtype), q.device, workspace)
+    _check(_load().swiattn_route_prefill(
+        _ptr(h), _ptr(w), float(bias), D, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+        _ptr(logits), _ptr(gate), B, N, Hq, Hkv, d, W, n_anchor, float(scale), _DT[q.dtype],
+        _ptr(ws), ws.numel(), _stream()), "swiattn_route_prefill")
+    return (o, logits, gate, lse) if want_lse else (o, logits, gate)
 
 
 def decode(q, k_cache, v_cache, seq_lens, gate, W: int, scale: Optional[float] = None, out=None,

@@ -1,0 +1,57 @@
+// Router logit of one token by one warp (SwiAttn report, section 2, router
+// design): logit_t = <h_t, w> + b, gate_t = 1(logit_t > 0), fp32 accumulate.
+// The hidden row streams through 16-byte loads, four in flight per lane.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+namespace swi {
+
+__device__ __forceinline__ float route_dot16(const uint4& a, const uint4& b, __nv_bfloat16) {
+    const __nv_bfloat162* x = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* y = reinterpret_cast<const __nv_bfloat162*>(&b);
+    float acc = 0.f;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        const float2 u = __bfloat1622float2(x[t]);
+        const float2 v = __bfloat1622float2(y[t]);
+        acc = fmaf(u.x, v.x, acc);
+        acc = fmaf(u.y, v.y, acc);
+    }
+    return acc;
+}
+
+__device__ __forceinline__ float route_dot16(const uint4& a, const uint4& b, float) {
+    const float4 x = *reinterpret_cast<const float4*>(&a);
+    const float4 y = *reinterpret_cast<const float4*>(&b);
+    return fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, x.w * y.w)));
+}
+
+// Whole warp: token t's logit and gate (lane 0 writes them).  nvec = 16-byte
+// vectors per hidden row.
+template <typename T>
+__device__ __forceinline__ void route_token(const uint4* __restrict__ h, const uint4* __restrict__ w,
+                                            float bias, int64_t t, int nvec, float* __restrict__ logits,
+                                            uint8_t* __restrict__ gate) {
+    const int lane = threadIdx.x & 31;
+    const uint4* row = h + t * nvec;
+    float acc = 0.f;
+    int v = lane;
+    for (; v + 96 < nvec; v += 128) {
+        const uint4 a0 = __ldcs(row + v), a1 = __ldcs(row + v + 32);
+        const uint4 a2 = __ldcs(row + v + 64), a3 = __ldcs(row + v + 96);
+        acc += route_dot16(a0, __ldg(w + v), T()) + route_dot16(a1, __ldg(w + v + 32), T()) +
+               route_dot16(a2, __ldg(w + v + 64), T()) + route_dot16(a3, __ldg(w + v + 96), T());
+    }
+    for (; v < nvec; v += 32) acc += route_dot16(__ldcs(row + v), __ldg(w + v), T());
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) {
+        const float lg = acc + bias;
+        logits[t] = lg;
+        gate[t] = lg > 0.f ? 1 : 0;
+    }
+}
+
+}  // namespace swi

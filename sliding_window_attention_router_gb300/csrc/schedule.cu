@@ -8,6 +8,7 @@
 // such tiles (256 rows, one head); the list is sorted by cost (key blocks),
 // longest first, for the persistent attention kernel.
 
+#include "route_gemv.cuh"
 #include "swiattn_internal.h"
 
 #include <cuda_bf16.h>
@@ -132,12 +133,15 @@ __device__ __forceinline__ int pair_cost(int u, const int* routed_list, const in
 
 // Gate bytes i .. i+15 of one batch row (zero where i+u >= N).  A whole
 // in-range group is one 16-byte load when the row start is 16-byte aligned.
+// The loads bypass L1: in the fused router + schedule kernel other CTAs wrote
+// the gates moments before.
 __device__ __forceinline__ uint4 load_gates16(const uint8_t* g, int i, int N, bool vec) {
-    if (vec && i + 16 <= N) return *reinterpret_cast<const uint4*>(g + i);
+    if (vec && i + 16 <= N) return __ldcg(reinterpret_cast<const uint4*>(g + i));
     uint32_t w[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
     for (int u = 0; u < 16; ++u)
-        if (i + u < N) w[u >> 2] |= static_cast<uint32_t>(g[i + u] != 0 ? 1u : 0u) << (8 * (u & 3));
+        if (i + u < N)
+            w[u >> 2] |= static_cast<uint32_t>(__ldcg(g + i + u) != 0 ? 1u : 0u) << (8 * (u & 3));
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
@@ -157,10 +161,11 @@ __device__ __forceinline__ bool gate_byte(const uint4& v, int u) {
 constexpr int kPlanThreads = 1024;
 constexpr int kBucketsPerThread = kCostBuckets / kPlanThreads;
 
-__global__ void __launch_bounds__(kPlanThreads) plan_kernel(
-    const uint8_t* __restrict__ gate, int B, int N, int Hq, int W, int S,
-    int* __restrict__ routed_list, int* __restrict__ routed_count, int* __restrict__ tile_prefix,
-    WorkItem* __restrict__ items, int* __restrict__ n_items) {
+// Every thread of a kPlanThreads-thread block calls it.
+__device__ void plan_block(const uint8_t* __restrict__ gate, int B, int N, int Hq, int W, int S,
+                           int* __restrict__ routed_list, int* __restrict__ routed_count,
+                           int* __restrict__ tile_prefix, WorkItem* __restrict__ items,
+                           int* __restrict__ n_items) {
     __shared__ int hist[kCostBuckets];
     __shared__ int warp_tot[32];
     const int NT = cdiv(N, kBM);
@@ -232,6 +237,41 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(
     }
 }
 
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(
+    const uint8_t* __restrict__ gate, int B, int N, int Hq, int W, int S,
+    int* __restrict__ routed_list, int* __restrict__ routed_count, int* __restrict__ tile_prefix,
+    WorkItem* __restrict__ items, int* __restrict__ n_items) {
+    plan_block(gate, B, N, Hq, W, S, routed_list, routed_count, tile_prefix, items, n_items);
+}
+
+// Router GEMV fused with the schedule: every CTA computes logits and gates of
+// its tokens (one warp per token); the CTA that finishes last (ticket from a
+// counter zeroed before the launch) then plans the prefill over all gates.
+// Every thread fences its gate writes before the CTA takes its ticket, and
+// the last CTA fences after taking it, before reading the gates.
+template <typename T>
+__global__ void __launch_bounds__(kPlanThreads) route_plan_kernel(
+    const uint4* __restrict__ h, const uint4* __restrict__ w, float bias, int nvec,
+    float* __restrict__ logits, uint8_t* __restrict__ gate, int B, int N, int Hq, int W, int S,
+    unsigned int* __restrict__ ticket, int* __restrict__ routed_list,
+    int* __restrict__ routed_count, int* __restrict__ tile_prefix, WorkItem* __restrict__ items,
+    int* __restrict__ n_items) {
+    __shared__ int last;
+    const int64_t tokens = (int64_t)B * N;
+    const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t t = warp0; t < tokens; t += nwarps) route_token<T>(h, w, bias, t, nvec, logits, gate);
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        last = atomicAdd(ticket, 1u) == gridDim.x - 1 ? 1 : 0;
+        if (last) __threadfence();
+    }
+    __syncthreads();
+    if (!last) return;
+    plan_block(gate, B, N, Hq, W, S, routed_list, routed_count, tile_prefix, items, n_items);
+}
+
 }  // namespace
 
 PrefillWs prefill_ws_layout(int B, int N, int Hq, int d) {
@@ -260,6 +300,32 @@ cudaError_t launch_schedule(const uint8_t* gate, int B, int N, int Hq, int W, in
         gate, B, N, Hq, W, S, reinterpret_cast<int*>(ws + L.routed_list),
         reinterpret_cast<int*>(ws + L.routed_count), reinterpret_cast<int*>(ws + L.tile_prefix),
         reinterpret_cast<WorkItem*>(ws + L.items), reinterpret_cast<int*>(ws + L.n_items));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_route_plan(const void* h, const void* w, float bias, int d_model, int dtype,
+                              float* logits, uint8_t* gate, int B, int N, int Hq, int W, int S,
+                              const PrefillWs& L, char* ws, unsigned int* ticket, int num_sms,
+                              cudaStream_t s) {
+    cudaError_t e = cudaMemsetAsync(ticket, 0, sizeof(unsigned int), s);
+    if (e != cudaSuccess) return e;
+    const int64_t tokens = (int64_t)B * N;
+    const int64_t want = (tokens + kPlanThreads / 32 - 1) / (kPlanThreads / 32);
+    const int blocks = static_cast<int>(want < (int64_t)num_sms ? want : (int64_t)num_sms);
+    int* list = reinterpret_cast<int*>(ws + L.routed_list);
+    int* count = reinterpret_cast<int*>(ws + L.routed_count);
+    int* prefix = reinterpret_cast<int*>(ws + L.tile_prefix);
+    WorkItem* items = reinterpret_cast<WorkItem*>(ws + L.items);
+    int* n_items = reinterpret_cast<int*>(ws + L.n_items);
+    if (dtype == 1) {
+        route_plan_kernel<__nv_bfloat16><<<blocks, kPlanThreads, 0, s>>>(
+            static_cast<const uint4*>(h), static_cast<const uint4*>(w), bias, d_model / 8, logits,
+            gate, B, N, Hq, W, S, ticket, list, count, prefix, items, n_items);
+    } else {
+        route_plan_kernel<float><<<blocks, kPlanThreads, 0, s>>>(
+            static_cast<const uint4*>(h), static_cast<const uint4*>(w), bias, d_model / 4, logits,
+            gate, B, N, Hq, W, S, ticket, list, count, prefix, items, n_items);
+    }
     return cudaGetLastError();
 }
 

@@ -183,28 +183,23 @@ int swiattn_prefill(const void* q, const void* k, const void* v, const uint8_t* 
                                     workspace, workspace_bytes, stream);
 }
 
-int swiattn_prefill_anchored(const void* q, const void* k, const void* v, const uint8_t* gate,
-                             void* o, float* lse, int B, int N, int Hq, int Hkv, int d, int W,
-                             int n_anchor, float scale, int dtype, void* workspace,
-                             size_t workspace_bytes, void* stream) {
+namespace {
+
+int prefill_args_ok(const void* q, const void* k, const void* v, const void* o, int B, int N,
+                    int Hq, int Hkv, int d, int W, int n_anchor, float scale) {
     if (!attn_shape_ok(B, N, Hq, Hkv, d, W) || n_anchor < 0) return SWIATTN_EINVAL;
-    if (!q || !k || !v || !gate || !o) return SWIATTN_EINVAL;
+    if (!q || !k || !v || !o) return SWIATTN_EINVAL;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return SWIATTN_EINVAL;
     if (!(scale > 0.f)) return SWIATTN_EINVAL;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (dtype == SWIATTN_F32) {
-        return launched(launch_simt_attention(q, k, v, gate, -1, o, lse, B, N, Hq, Hkv, d, W,
-                                              n_anchor, scale, dtype, s));
-    }
-    if (dtype != SWIATTN_BF16) return SWIATTN_EINVAL;
-    if (d != kHD) return SWIATTN_EUNSUPPORTED;
-    const PrefillWs L = prefill_ws_layout(B, N, Hq, d);
-    if (!workspace || !aligned256(workspace) || workspace_bytes < L.total) return SWIATTN_EINVAL;
-    DeviceInfo di;
-    if (!device_info(di)) return SWIATTN_ECUDA;
-    char* ws = static_cast<char*>(workspace);
-    cudaError_t e = launch_schedule(gate, B, N, Hq, W, n_anchor, L, ws, s);
-    if (e != cudaSuccess) return SWIATTN_ECUDA;
+    return SWIATTN_OK;
+}
+
+// The attention launch of the tensor-core prefill, once the schedule has been
+// enqueued on s (workspace laid out by prefill_ws_layout).
+int launch_prefill_after_plan(const void* q, const void* k, const void* v, const uint8_t* gate,
+                              void* o, float* lse, int B, int N, int Hq, int Hkv, int W,
+                              int n_anchor, float scale, const PrefillWs& L, char* ws,
+                              const DeviceInfo& di, cudaStream_t s) {
     TcAttnArgs a;
     std::memset(&a, 0, sizeof(a));
     a.q = q;
@@ -225,9 +220,75 @@ int swiattn_prefill_anchored(const void* q, const void* k, const void* v, const 
     a.n_anchor = n_anchor;
     a.scale = scale;
     prof_start(s);
-    e = launch_prefill_tc(a, reinterpret_cast<const int*>(ws + L.tile_prefix), di.err, di.sms, s);
+    cudaError_t e = launch_prefill_tc(a, reinterpret_cast<const int*>(ws + L.tile_prefix), di.err,
+                                      di.sms, s);
     prof_stop(s);
     return launched(e);
+}
+
+}  // namespace
+
+int swiattn_prefill_anchored(const void* q, const void* k, const void* v, const uint8_t* gate,
+                             void* o, float* lse, int B, int N, int Hq, int Hkv, int d, int W,
+                             int n_anchor, float scale, int dtype, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+    const int ok = prefill_args_ok(q, k, v, o, B, N, Hq, Hkv, d, W, n_anchor, scale);
+    if (ok != SWIATTN_OK) return ok;
+    if (!gate) return SWIATTN_EINVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == SWIATTN_F32) {
+        return launched(launch_simt_attention(q, k, v, gate, -1, o, lse, B, N, Hq, Hkv, d, W,
+                                              n_anchor, scale, dtype, s));
+    }
+    if (dtype != SWIATTN_BF16) return SWIATTN_EINVAL;
+    if (d != kHD) return SWIATTN_EUNSUPPORTED;
+    const PrefillWs L = prefill_ws_layout(B, N, Hq, d);
+    if (!workspace || !aligned256(workspace) || workspace_bytes < L.total) return SWIATTN_EINVAL;
+    DeviceInfo di;
+    if (!device_info(di)) return SWIATTN_ECUDA;
+    char* ws = static_cast<char*>(workspace);
+    if (launch_schedule(gate, B, N, Hq, W, n_anchor, L, ws, s) != cudaSuccess) return SWIATTN_ECUDA;
+    return launch_prefill_after_plan(q, k, v, gate, o, lse, B, N, Hq, Hkv, W, n_anchor, scale, L,
+                                     ws, di, s);
+}
+
+size_t swiattn_route_prefill_workspace(int B, int N, int Hq, int Hkv, int d, int W, int dtype) {
+    const size_t base = swiattn_prefill_workspace(B, N, Hq, Hkv, d, W, dtype);
+    if (base == 0 || dtype != SWIATTN_BF16) return base;
+    return base + 256;   // the ticket of the fused router + schedule kernel
+}
+
+int swiattn_route_prefill(const void* h, const void* w, float bias, int d_model, const void* q,
+                          const void* k, const void* v, void* o, float* lse, float* logits,
+                          uint8_t* gate, int B, int N, int Hq, int Hkv, int d, int W, int n_anchor,
+                          float scale, int dtype, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+    const int ok = prefill_args_ok(q, k, v, o, B, N, Hq, Hkv, d, W, n_anchor, scale);
+    if (ok != SWIATTN_OK) return ok;
+    if (dtype != SWIATTN_BF16 && dtype != SWIATTN_F32) return SWIATTN_EINVAL;
+    if (d_model <= 0 || d_model % (dtype == SWIATTN_BF16 ? 8 : 4) != 0) return SWIATTN_EINVAL;
+    if (!h || !w || !logits || !gate || !aligned16(h) || !aligned16(w)) return SWIATTN_EINVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t tokens = (int64_t)B * N;
+    if (dtype == SWIATTN_F32) {
+        if (launch_route(h, w, bias, tokens, d_model, dtype, logits, gate, s) != cudaSuccess)
+            return SWIATTN_ECUDA;
+        return launched(launch_simt_attention(q, k, v, gate, -1, o, lse, B, N, Hq, Hkv, d, W,
+                                              n_anchor, scale, dtype, s));
+    }
+    if (d != kHD) return SWIATTN_EUNSUPPORTED;
+    const PrefillWs L = prefill_ws_layout(B, N, Hq, d);
+    if (!workspace || !aligned256(workspace) || workspace_bytes < L.total + 256)
+        return SWIATTN_EINVAL;
+    DeviceInfo di;
+    if (!device_info(di)) return SWIATTN_ECUDA;
+    char* ws = static_cast<char*>(workspace);
+    unsigned int* ticket = reinterpret_cast<unsigned int*>(ws + L.total);
+    if (launch_route_plan(h, w, bias, d_model, dtype, logits, gate, B, N, Hq, W, n_anchor, L, ws,
+                          ticket, di.sms, s) != cudaSuccess)
+        return SWIATTN_ECUDA;
+    return launch_prefill_after_plan(q, k, v, gate, o, lse, B, N, Hq, Hkv, W, n_anchor, scale, L,
+                                     ws, di, s);
 }
 
 size_t swiattn_decode_workspace(int B, int Lmax, int Hq, int Hkv, int d, int W, int dtype) {

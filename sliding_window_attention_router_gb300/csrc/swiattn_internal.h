@@ -73,6 +73,14 @@ cudaError_t launch_route(const void* h, const void* w, float bias, int64_t token
 cudaError_t launch_schedule(const uint8_t* gate, int B, int N, int Hq, int W, int S,
                             const PrefillWs& L, char* ws, cudaStream_t s);
 
+// Router GEMV over the B*N tokens (logits, gates) fused with the schedule
+// above: the last CTA to finish plans over the gates.  ticket: a 4-byte
+// counter in device memory, zeroed here before the launch.
+cudaError_t launch_route_plan(const void* h, const void* w, float bias, int d_model, int dtype,
+                              float* logits, uint8_t* gate, int B, int N, int Hq, int W, int S,
+                              const PrefillWs& L, char* ws, unsigned int* ticket, int num_sms,
+                              cudaStream_t s);
+
 struct TcAttnArgs {
     const void* q;     // [B,N,Hq,128] bf16
     const void* k;     // [B,N,Hkv,128]

@@ -94,6 +94,36 @@ def test_invalid_arguments_rejected_before_launch(lib):
                                    1 << 30, None) == 1
 
 
+def test_route_prefill_workspace_and_validation(lib):
+    import sliding_window_attention_router_gb300 as swa
+    bf16 = swa.BF16
+    base = swa.prefill_workspace(2, 4096, 16, 4, 128, 1024, bf16)
+    # the prefill's workspace plus the counter that elects the planning CTA
+    assert swa.route_prefill_workspace(2, 4096, 16, 4, 128, 1024, bf16) == base + 256
+    assert swa.route_prefill_workspace(1, 0, 16, 16, 128, 1024, bf16) == 0
+    vp = ctypes.c_void_p
+    fake = vp(1 << 20)          # never dereferenced: validation fails first
+    odd = vp((1 << 20) + 8)
+    ws = 1 << 30
+
+    def call(h=fake, w=fake, d_model=1024, logits=fake, gate=fake, W=64, S=0, d=128, scale=0.1,
+             dt=1, nbytes=ws, Hq=4):
+        return lib.swiattn_route_prefill(h, w, 0.0, d_model, fake, fake, fake, fake, None, logits,
+                                         gate, 1, 256, Hq, 4, d, W, S, scale, dt, fake, nbytes,
+                                         None)
+    assert call(d_model=1020) == 1          # not a multiple of 8 (bf16)
+    assert call(h=odd) == 1                 # misaligned hidden states
+    assert call(logits=None) == 1           # router outputs are required
+    assert call(gate=None) == 1
+    assert call(W=0) == 1
+    assert call(S=-1) == 1
+    assert call(scale=0.0) == 1
+    assert call(Hq=6) == 1                  # Hq % Hkv != 0
+    assert call(dt=7) == 1
+    assert call(nbytes=16) == 1             # workspace too small
+    assert call(d=64) == 2                  # bf16 head dim 64: not on the tensor-core path
+
+
 def test_backward_workspace_and_validation(lib):
     import sliding_window_attention_router_gb300 as swa
     n = swa.prefill_backward_workspace(1, 32768, 16, 16, 128, 1024, swa.BF16)
