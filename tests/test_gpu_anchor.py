@@ -48,6 +48,8 @@ CASES = [  # B, N, Hq, Hkv, W, S, frac
     (1, 100, 2, 2, 1000, 256, 0.2),
     (1, 1000, 2, 2, 128, 5000, 0.1),
     (1, 700, 4, 4, 129, 129, 1.0),
+    (1, 400, 2, 2, 64, 63, 0.2),     # 64-key block edges of the tensor-core kernel
+    (1, 400, 2, 2, 65, 65, 0.2),
 ]
 
 

@@ -238,6 +238,13 @@ EDGE = [
     (1, 700, 2, 2, 129, "ones"),
     (1, 700, 2, 2, 64, "single"),
     (3, 520, 8, 2, 200, "runs"),
+    # 64-key block edges of the tensor-core kernel
+    (1, 64, 2, 2, 64, "rand"),
+    (1, 65, 2, 2, 63, "rand"),
+    (1, 191, 2, 2, 65, "runs"),
+    (1, 192, 2, 2, 64, "ones"),
+    (1, 193, 2, 2, 127, "alt"),
+    (2, 257, 2, 2, 65, "rand"),
 ]
 
 
