@@ -216,6 +216,12 @@ class Timer:
             torch.cuda.synchronize()
 
     def run(self, fn, steps: int, warmup: int, kernel_events: bool = False):
+        """Warm up, then time `steps` calls (L2 flushed before each).  With
+        kernel_events, a second loop of `steps` calls times the library's
+        dominant kernel alone through its event hook; the step times come from
+        the first loop, which records nothing between the library's launches
+        (a recorded event there would serialise a programmatic dependent
+        launch)."""
         import sliding_window_attention_router_gb300 as swa
         for _ in range(warmup):
             self.flush.zero_()
@@ -223,26 +229,29 @@ class Timer:
         torch.cuda.synchronize()
         starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
         stops = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-        ks = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-        ke = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-        if kernel_events:
-            # torch creates events lazily: record once so the handles exist
-            # before the library records them around its kernel.
-            for e in ks + ke:
-                e.record()
-            torch.cuda.synchronize()
         for s in range(steps):
             self.flush.zero_()
-            if kernel_events:
-                swa.set_profile_events(ks[s], ke[s])
             starts[s].record()
             fn()
             stops[s].record()
-        if kernel_events:
-            swa.set_profile_events(None, None)
         torch.cuda.synchronize()
         step_ms = [a.elapsed_time(b) for a, b in zip(starts, stops)]
-        kern_ms = [a.elapsed_time(b) for a, b in zip(ks, ke)] if kernel_events else None
+        if not kernel_events:
+            return step_ms, None
+        ks = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ke = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        # torch creates events lazily: record once so the handles exist
+        # before the library records them around its kernel.
+        for e in ks + ke:
+            e.record()
+        torch.cuda.synchronize()
+        for s in range(steps):
+            self.flush.zero_()
+            swa.set_profile_events(ks[s], ke[s])
+            fn()
+        swa.set_profile_events(None, None)
+        torch.cuda.synchronize()
+        kern_ms = [a.elapsed_time(b) for a, b in zip(ks, ke)]
         return step_ms, kern_ms
 
 

@@ -113,7 +113,11 @@ __global__ void decode_split_kernel(const T* __restrict__ q, const T* __restrict
         t1 = min(vis.na, t0 + kChunk);
     } else {
         const int cw = c - vis.nca;
-        if (cw * kChunk >= vis.n) return;
+        if (cw * kChunk >= vis.n) {
+            // No entries for this chunk: let the dependent combine launch.
+            asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+            return;
+        }
         t0 = vis.lo + cw * kChunk;
         t1 = min(vis.lo + vis.n, t0 + kChunk);
     }
@@ -215,24 +219,32 @@ __global__ void decode_split_kernel(const T* __restrict__ q, const T* __restrict
         }
     }
 
-    if (!active) return;
+    if (active) {
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-        const int hq = kvh * G + g;
-        float* dst = part + (((size_t)b * max_chunks + c) * Hq + hq) * (D + 2);
+        for (int g = 0; g < G; ++g) {
+            const int hq = kvh * G + g;
+            float* dst = part + (((size_t)b * max_chunks + c) * Hq + hq) * (D + 2);
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) dst[sub * VEC + e] = acc[g][e];
-        if (sub == 0) {
-            dst[D] = m[g];
-            dst[D + 1] = l[g];
+            for (int e = 0; e < VEC; ++e) dst[sub * VEC + e] = acc[g][e];
+            if (sub == 0) {
+                dst[D] = m[g];
+                dst[D + 1] = l[g];
+            }
         }
     }
+    // The combine kernel is launched as a programmatic dependent of this one:
+    // once every CTA has come this far it may be scheduled (it waits for this
+    // grid's completion and memory before reading any partial), which hides
+    // its launch behind the last CTAs' tail.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Log-sum-exp merge of the chunk partials of one (sequence, query head):
 // block (hq, b), D threads, thread c owns output column c.  The maximum over
-// chunks is a block reduction; the weighted sums run 8 chunks per iteration
-// so their loads are in flight together.
+// chunks is a block reduction; the weighted sums run 32 chunks per iteration
+// so their loads are in flight together (a routed 32K-token sequence has 128
+// chunks: four rounds).  Launched as a programmatic dependent of the split
+// kernel, it first waits for that grid's completion.
 template <typename T, int D>
 __global__ void __launch_bounds__(D) decode_combine_kernel(const float* __restrict__ part,
                                                            const int32_t* __restrict__ seq_lens,
@@ -241,6 +253,7 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const float* __restri
                                                            int Hq, int W, int S, int Lmax,
                                                            int max_chunks) {
     __shared__ float red[D / 32];
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int hq = blockIdx.x, b = blockIdx.y, cidx = threadIdx.x;
     const int lane = cidx & 31, wid = cidx >> 5;
     const Visit vis = visited(seq_lens, gate, b, W, S, Lmax);
@@ -258,17 +271,18 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const float* __restri
     for (int w = 1; w < D / 32; ++w) M = fmaxf(M, red[w]);
     float L = 0.f, acc = 0.f;
     int c = 0;
-    for (; c + 8 <= nc; c += 8) {
-        float mv[8], lv[8], ov[8];
+    constexpr int kRound = 32;
+    for (; c + kRound <= nc; c += kRound) {
+        float mv[kRound], lv[kRound], ov[kRound];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < kRound; ++u) {
             const float* pc = base + (size_t)(c + u) * cstride;
             mv[u] = pc[D];
             lv[u] = pc[D + 1];
             ov[u] = pc[cidx];
         }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < kRound; ++u) {
             const float w = ex2f(mv[u] - M);
             L = fmaf(lv[u], w, L);
             acc = fmaf(ov[u], w, acc);
@@ -325,8 +339,18 @@ cudaError_t launch_typed(const void* q, const void* kc, const void* vc, const in
     }
     prof_stop(s);
     if (e != cudaSuccess) return e;
-    decode_combine_kernel<T, D><<<dim3(Hq, B), D, 0, s>>>(part, sl, gate, static_cast<T*>(o), lse,
-                                                          Hq, W, S, Lmax, max_chunks);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(Hq, B);
+    cfg.blockDim = dim3(D);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<T, D>, static_cast<const float*>(part), sl,
+                           gate, static_cast<T*>(o), lse, Hq, W, S, Lmax, max_chunks);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
