@@ -239,16 +239,34 @@ __global__ void __launch_bounds__(256) route_bwd_dh_kernel(
     }
 }
 
-// dw[c] = sum over chunks of the partials (chunk order); db = sum d_logits
-// (block 0, fixed-order tree).
+// dw[c] = sum over chunks of the partials: a block takes 32 columns and warp
+// w sums chunks w, w+8, w+16, ... for its lane's column, then the eight warp
+// sums are added in warp order (a fixed order, so dw is bitwise repeatable).
+// db = sum d_logits (block 0, fixed-order tree).
+constexpr int kReduceCols = 32;
+constexpr int kReduceWarps = 8;
+
 __global__ void __launch_bounds__(256) route_bwd_reduce_kernel(
     const float* __restrict__ part, int64_t chunks, int d_model, const float* __restrict__ d_logits,
     int64_t tokens, float* __restrict__ dw, float* __restrict__ db) {
-    const int c = blockIdx.x * blockDim.x + threadIdx.x;
-    if (dw && part && c < d_model) {
+    __shared__ float wsum[kReduceWarps][kReduceCols];
+    const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
+    const int c = blockIdx.x * kReduceCols + lane;
+    const bool do_dw = dw && part;
+    if (do_dw) {
         float acc = 0.f;
-        for (int64_t k = 0; k < chunks; ++k) acc += part[k * d_model + c];
-        dw[c] = acc;
+        if (c < d_model) {
+#pragma unroll 8
+            for (int64_t k = wp; k < chunks; k += kReduceWarps) acc += part[k * d_model + c];
+        }
+        wsum[wp][lane] = acc;
+    }
+    __syncthreads();
+    if (do_dw && wp == 0 && c < d_model) {
+        float t = 0.f;
+#pragma unroll
+        for (int u = 0; u < kReduceWarps; ++u) t += wsum[u][lane];
+        dw[c] = t;
     }
     if (db && blockIdx.x == 0) {
         __shared__ float red[256];
@@ -285,7 +303,8 @@ cudaError_t route_backward_t(const void* h, const void* w, const float* logits, 
         if (e != cudaSuccess) return e;
     }
     if (dw || db) {
-        route_bwd_reduce_kernel<<<(d_model + 255) / 256 > 0 ? (d_model + 255) / 256 : 1, 256, 0, s>>>(
+        const int blocks_r = (d_model + kReduceCols - 1) / kReduceCols;
+        route_bwd_reduce_kernel<<<blocks_r > 0 ? blocks_r : 1, kReduceWarps * 32, 0, s>>>(
             ws, chunks, d_model, d_logits, tokens, dw, db);
         e = cudaGetLastError();
     }
