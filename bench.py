@@ -280,13 +280,16 @@ def prefill_section(swa, timer, dev, frac, steps, warmup, seed, with_e2e, N=3276
     res = dict(d=d, flops=flops, pairs=pairs, step_ms=step_ms, kern_ms=kern_ms,
                realised_frac=float(d["gate"].float().mean()), t_from=t_from, t_to=t_to)
     if with_e2e:
+        # End to end through the host-buffer entry point: every step copies
+        # q, k, v, gate from pinned host memory, runs the prefill and copies o
+        # back, all enqueued by swiattn_prefill_host on the current stream.
         o_host = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        ws_host = torch.empty(swa.prefill_host_workspace(B, N, H, H, D, W, torch.bfloat16),
+                              dtype=torch.uint8, device=dev)
 
         def e2e_step():
-            qd, kd, vd, gd = (t.to(dev, non_blocking=True) for t in
-                              (host["q"], host["k"], host["v"], host["gate"]))
-            swa.prefill(qd, kd, vd, gd, W, scale, out=o, workspace=ws)
-            o_host.copy_(o, non_blocking=True)
+            swa.prefill_host(host["q"], host["k"], host["v"], host["gate"], W, scale, out=o_host,
+                             workspace=ws_host, device=dev)
 
         e2e_ms, _ = timer.run(e2e_step, max(3, steps // 2), 2)
         h2d = sum(host[n].numel() * host[n].element_size() for n in host)

@@ -97,6 +97,25 @@ int swiattn_prefill_anchored(const void* q, const void* k, const void* v, const 
                              int n_anchor, float scale, int dtype, void* workspace,
                              size_t workspace_bytes, void* stream);
 
+/* Bytes of device workspace swiattn_prefill_host needs: device copies of q, k,
+ * v, gate and o (and lse) plus the prefill's own workspace (0 for invalid sizes). */
+size_t swiattn_prefill_host_workspace(int B, int N, int Hq, int Hkv, int d, int W, int dtype);
+
+/* swiattn_prefill_anchored from and to HOST memory, for callers that keep
+ * tensors on the host: enqueues on `stream` the copies of q, k, v, gate to
+ * device staging inside `workspace` (one cudaMemcpyAsync each), the prefill,
+ * and the copies of o (and lse, when lse_host is not null) back to the host.
+ * q_host, k_host, v_host, gate_host, o_host, lse_host are host pointers with
+ * the layouts of swiattn_prefill; with page-locked (pinned) host memory every
+ * copy is asynchronous, with pageable memory the CUDA runtime synchronises
+ * around it.  The results are in o_host once the stream reaches the end of the
+ * call.  workspace: device memory of at least swiattn_prefill_host_workspace
+ * bytes, 256-byte aligned; other arguments as swiattn_prefill_anchored. */
+int swiattn_prefill_host(const void* q_host, const void* k_host, const void* v_host,
+                         const uint8_t* gate_host, void* o_host, float* lse_host, int B, int N,
+                         int Hq, int Hkv, int d, int W, int n_anchor, float scale, int dtype,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
 /* Bytes of device workspace swiattn_route_prefill needs (0 for invalid sizes). */
 size_t swiattn_route_prefill_workspace(int B, int N, int Hq, int Hkv, int d, int W, int dtype);
 

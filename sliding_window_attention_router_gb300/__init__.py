@@ -39,7 +39,7 @@ EXPORTS = (
     "swiattn_route_backward_workspace", "swiattn_route_backward",
     "swiattn_decode_paged_workspace", "swiattn_decode_paged", "swiattn_decode_anchored_workspace",
     "swiattn_decode_anchored", "swiattn_prefill_anchored", "swiattn_route_prefill_workspace",
-    "swiattn_route_prefill",
+    "swiattn_route_prefill", "swiattn_prefill_host_workspace", "swiattn_prefill_host",
     "swiattn_get_device_error", "swiattn_status_string", "swiattn_set_profile_events",
     "swiattn_num_sms",
 )
@@ -91,6 +91,9 @@ def _load() -> ctypes.CDLL:
             lib.swiattn_decode_anchored_workspace.restype = sz
             lib.swiattn_decode_anchored.argtypes = [vp] * 7 + [i32] * 7 + [f32, i32, vp, sz, vp]
             lib.swiattn_prefill_anchored.argtypes = [vp] * 6 + [i32] * 7 + [f32, i32, vp, sz, vp]
+            lib.swiattn_prefill_host_workspace.argtypes = [i32] * 7
+            lib.swiattn_prefill_host_workspace.restype = sz
+            lib.swiattn_prefill_host.argtypes = [vp] * 6 + [i32] * 7 + [f32, i32, vp, sz, vp]
             lib.swiattn_route_prefill_workspace.argtypes = [i32] * 7
             lib.swiattn_route_prefill_workspace.restype = sz
             lib.swiattn_route_prefill.argtypes = ([vp, vp, f32, i32] + [vp] * 7 + [i32] * 7 +
@@ -105,7 +108,8 @@ def _load() -> ctypes.CDLL:
                          "swiattn_dual_branch", "swiattn_get_device_error", "swiattn_num_sms",
                          "swiattn_prefill_backward", "swiattn_route_backward",
                          "swiattn_decode_paged", "swiattn_decode_anchored",
-                         "swiattn_prefill_anchored", "swiattn_route_prefill"):
+                         "swiattn_prefill_anchored", "swiattn_route_prefill",
+                         "swiattn_prefill_host"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -210,6 +214,48 @@ def prefill(q, k, v, gate, W: int, scale: Optional[float] = None, out=None, want
         _check(_load().swiattn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(o), _ptr(lse),
                                        B, N, Hq, Hkv, d, W, float(scale), _DT[q.dtype], _ptr(ws),
                                        ws.numel(), _stream()), "swiattn_prefill")
+    return (o, lse) if want_lse else o
+
+
+def prefill_host_workspace(B, N, Hq, Hkv, d, W, dtype) -> int:
+    return int(_load().swiattn_prefill_host_workspace(B, N, Hq, Hkv, d, W, _DT.get(dtype, dtype)))
+
+
+def _host(t: torch.Tensor, name: str, dtype=None):
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+def prefill_host(q, k, v, gate, W: int, scale: Optional[float] = None, n_anchor: int = 0,
+                 out=None, want_lse=False, workspace=None, device=None):
+    """Routed prefill from and to host memory (swiattn_prefill_host): q, k, v,
+    gate are CPU tensors (pinned for asynchronous copies); the output is a CPU
+    tensor (pinned when allocated here), valid once the current stream of
+    `device` has passed the call.  workspace: a device uint8 tensor of at least
+    prefill_host_workspace(...) bytes."""
+    _host(q, "q")
+    _host(k, "k", q.dtype)
+    _host(v, "v", q.dtype)
+    _host(gate, "gate", torch.uint8)
+    B, N, Hq, d = q.shape
+    Hkv = k.shape[2]
+    dev = torch.device(device) if device is not None else torch.device("cuda",
+                                                                        torch.cuda.current_device())
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o = out if out is not None else torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    _host(o, "out", q.dtype)
+    lse = torch.empty((B, N, Hq), dtype=torch.float32, pin_memory=True) if want_lse else None
+    ws = _workspace(prefill_host_workspace(B, N, Hq, Hkv, d, W, q.dtype), dev, workspace)
+    with torch.cuda.device(dev):
+        _check(_load().swiattn_prefill_host(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(o), _ptr(lse), B, N, Hq, Hkv, d, W,
+            n_anchor, float(scale), _DT[q.dtype], _ptr(ws), ws.numel(), _stream()),
+            "swiattn_prefill_host")
     return (o, lse) if want_lse else o
 
 

@@ -252,6 +252,69 @@ int swiattn_prefill_anchored(const void* q, const void* k, const void* v, const 
                                      ws, di, s);
 }
 
+namespace {
+
+// Device staging of swiattn_prefill_host, after the prefill workspace.
+struct HostStage {
+    size_t q, k, v, gate, o, lse, total;
+};
+HostStage host_stage_layout(size_t base, int B, int N, int Hq, int Hkv, int d, int esize) {
+    auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+    const size_t rows = (size_t)B * N;
+    HostStage H;
+    H.q = up(base);
+    H.k = up(H.q + rows * Hq * d * esize);
+    H.v = up(H.k + rows * Hkv * d * esize);
+    H.gate = up(H.v + rows * Hkv * d * esize);
+    H.o = up(H.gate + rows);
+    H.lse = up(H.o + rows * Hq * d * esize);
+    H.total = up(H.lse + rows * Hq * sizeof(float));
+    return H;
+}
+
+}  // namespace
+
+size_t swiattn_prefill_host_workspace(int B, int N, int Hq, int Hkv, int d, int W, int dtype) {
+    const size_t base = swiattn_prefill_workspace(B, N, Hq, Hkv, d, W, dtype);
+    if (base == 0 || (dtype != SWIATTN_BF16 && dtype != SWIATTN_F32)) return 0;
+    return host_stage_layout(base, B, N, Hq, Hkv, d, dtype == SWIATTN_BF16 ? 2 : 4).total;
+}
+
+int swiattn_prefill_host(const void* q_host, const void* k_host, const void* v_host,
+                         const uint8_t* gate_host, void* o_host, float* lse_host, int B, int N,
+                         int Hq, int Hkv, int d, int W, int n_anchor, float scale, int dtype,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+    if (dtype != SWIATTN_BF16 && dtype != SWIATTN_F32) return SWIATTN_EINVAL;
+    const size_t need = swiattn_prefill_host_workspace(B, N, Hq, Hkv, d, W, dtype);
+    if (need == 0 || n_anchor < 0 || !(scale > 0.f)) return SWIATTN_EINVAL;
+    if (!q_host || !k_host || !v_host || !gate_host || !o_host) return SWIATTN_EINVAL;
+    if (!workspace || !aligned256(workspace) || workspace_bytes < need) return SWIATTN_EINVAL;
+    const int es = dtype == SWIATTN_BF16 ? 2 : 4;
+    const size_t base = swiattn_prefill_workspace(B, N, Hq, Hkv, d, W, dtype);
+    const HostStage H = host_stage_layout(base, B, N, Hq, Hkv, d, es);
+    char* ws = static_cast<char*>(workspace);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t rows = (size_t)B * N;
+    const size_t qb = rows * Hq * d * es, kvb = rows * Hkv * d * es;
+    if (cudaMemcpyAsync(ws + H.gate, gate_host, rows, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(ws + H.q, q_host, qb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(ws + H.k, k_host, kvb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(ws + H.v, v_host, kvb, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return SWIATTN_ECUDA;
+    float* lse_dev = lse_host ? reinterpret_cast<float*>(ws + H.lse) : nullptr;
+    const int rc = swiattn_prefill_anchored(ws + H.q, ws + H.k, ws + H.v,
+                                            reinterpret_cast<const uint8_t*>(ws + H.gate),
+                                            ws + H.o, lse_dev, B, N, Hq, Hkv, d, W, n_anchor, scale,
+                                            dtype, ws, base, stream);
+    if (rc != SWIATTN_OK) return rc;
+    if (cudaMemcpyAsync(o_host, ws + H.o, qb, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return SWIATTN_ECUDA;
+    if (lse_host && cudaMemcpyAsync(lse_host, lse_dev, rows * Hq * sizeof(float),
+                                    cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return SWIATTN_ECUDA;
+    return SWIATTN_OK;
+}
+
 size_t swiattn_route_prefill_workspace(int B, int N, int Hq, int Hkv, int d, int W, int dtype) {
     const size_t base = swiattn_prefill_workspace(B, N, Hq, Hkv, d, W, dtype);
     if (base == 0 || dtype != SWIATTN_BF16) return base;

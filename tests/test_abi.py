@@ -124,6 +124,25 @@ def test_route_prefill_workspace_and_validation(lib):
     assert call(d=64) == 2                  # bf16 head dim 64: not on the tensor-core path
 
 
+def test_prefill_host_workspace_and_validation(lib):
+    import sliding_window_attention_router_gb300 as swa
+    bf16 = swa.BF16
+    base = swa.prefill_workspace(1, 4096, 16, 16, 128, 1024, bf16)
+    n = swa.prefill_host_workspace(1, 4096, 16, 16, 128, 1024, bf16)
+    # staging for q, k, v (8 MiB each), gate, o, lse on top of the prefill's workspace
+    assert n >= base + 4 * 4096 * 16 * 128 * 2 + 4096 + 4096 * 16 * 4 and n % 256 == 0
+    assert swa.prefill_host_workspace(1, 0, 16, 16, 128, 1024, bf16) == 0
+    vp = ctypes.c_void_p
+    fake = vp(1 << 20)
+    args = [fake] * 5 + [None]
+    assert lib.swiattn_prefill_host(None, *args[1:], 1, 64, 4, 4, 128, 8, 0, 0.1, 1, fake, 1 << 30,
+                                    None) == 1                                  # missing q
+    assert lib.swiattn_prefill_host(*args, 1, 64, 4, 4, 128, 8, 0, 0.1, 1, fake, 16, None) == 1
+    assert lib.swiattn_prefill_host(*args, 1, 64, 4, 4, 128, 8, 0, 0.1, 7, fake, 1 << 30, None) == 1
+    assert lib.swiattn_prefill_host(*args, 1, 64, 4, 4, 128, 8, -1, 0.1, 1, fake, 1 << 30, None) == 1
+    assert lib.swiattn_prefill_host(*args, 1, 64, 4, 4, 128, 8, 0, 0.0, 1, fake, 1 << 30, None) == 1
+
+
 def test_backward_workspace_and_validation(lib):
     import sliding_window_attention_router_gb300 as swa
     n = swa.prefill_backward_workspace(1, 32768, 16, 16, 128, 1024, swa.BF16)
