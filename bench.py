@@ -561,6 +561,23 @@ def oracle_sample(d, budget_s: float, seed: int = 0):
     return dict(flops_per_s=f / t, seconds=t, rows=nrows, cores=oracle.num_threads())
 
 
+def oracle_single_core_4k(budget_s: float = 3.0):
+    """The oracle on one host core, on a sample of the single-layer 4K
+    workload (gates from the oracle's own router): a per-core reference point
+    beside the all-core baseline."""
+    import oracle
+    d = inp.prefill_4k(seed=0)
+    _, gate = oracle.route(d["h"].to(torch.float64).numpy(), d["w"].to(torch.float64).numpy(),
+                           d["bias"])
+    dd = dict(d, gate=torch.from_numpy(np.ascontiguousarray(gate.reshape(1, -1))))
+    prev = oracle.num_threads()
+    oracle.set_num_threads(1)
+    try:
+        return oracle_sample(dd, budget_s)
+    finally:
+        oracle.set_num_threads(prev)
+
+
 # ------------------------------------------------------------------ arms --
 def run_reference(args, dist: Dist):
     if dist.rank != 0:
@@ -734,6 +751,11 @@ def run_ours(args, dist: Dist):
                "kind": "oracle",
                "sample": f"{r['rows']} random (row, head) outputs of the N=32768 workload, "
                          f"{r['seconds']:.1f} s of fp64 oracle work on {r['cores']} threads"}
+        r1 = oracle_single_core_4k()
+        cpu["single_core_prefill_4k"] = {
+            "value": r1["flops_per_s"] / 1e12, "unit": "TFLOP/s", "cores": r1["cores"],
+            "sample": f"{r1['rows']} random (row, head) outputs of the single-layer N=4096 "
+                      f"workload, {r1['seconds']:.1f} s on one core"}
 
     if dist.rank == 0:
         d = main["d"]

@@ -55,6 +55,7 @@ def _load():
                                                 + [ctypes.c_double, i64p, i64, dp, dp])
             lib.oracle_decode.argtypes = ([dp, dp, dp, i32p, u8p] + [i64] * 6
                                           + [ctypes.c_double, dp, dp])
+            lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
             lib.oracle_softplus.argtypes = [ctypes.c_double]
             lib.oracle_softplus.restype = ctypes.c_double
             lib.oracle_regulariser.argtypes = [dp, dp, dp, i64] + [ctypes.c_double] * 3 + [dp, dp]
@@ -95,6 +96,11 @@ def _ptr(a: np.ndarray):
 def _check(rc: int, name: str):
     if rc != 0:
         raise ValueError(f"{name}: invalid arguments")
+
+
+def set_num_threads(n: int) -> None:
+    """Threads of the OpenMP loops that follow (timing only)."""
+    _load().oracle_set_num_threads(int(n))
 
 
 def num_threads() -> int:

@@ -629,3 +629,15 @@ int oracle_num_threads(void)
     return 1;
 #endif
 }
+
+/* Threads for the calls that follow (n >= 1; no effect without OpenMP).
+ * Timing only: the results do not depend on the thread count. */
+int oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+    return 0;
+}
