@@ -141,11 +141,15 @@ __device__ __forceinline__ void load_tile_pair(const CUtensorMap* map, uint8_t* 
 
 // K-step kk of a 128-deep K-major operand in a two-half SW128 tile.
 __device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk) {
-    return sdesc_sw128(tile + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
+    // The start address is the descriptor's low field (16-byte units, no carry
+    // within shared memory): the tile's descriptor plus the step's offset, so
+    // the per-step descriptors of one tile share one computed base.
+    return sdesc_sw128(tile, 16, 1024) +
+           static_cast<uint64_t>(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
 }
 // K-step kk (16 rows) of an MN-major B operand (rows = K, 128 columns = N).
 __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int kk) {
-    return sdesc_sw128(tile + kk * 16 * 128, kHalfBytes, 1024);
+    return sdesc_sw128(tile, kHalfBytes, 1024) + static_cast<uint64_t>((kk * 16 * 128) >> 4);
 }
 // TMEM column of K-step kk of a bf16 operand packed per column half: keys or
 // queries 0-63 at columns [0, 32), 64-127 at [64, 96) of the 128-column block.
