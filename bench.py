@@ -50,9 +50,9 @@ MEASURED_TRAFFIC = {
     ("decode", "731602d165ca105b"): 654405120 + 2784512,
     # dual_kernel, dual-branch workload B=2 N=8192 GQA 16/4: 158 522 880 read + 271 861 760 written
     ("dual", "022299affd4ac4fb"): 158522880 + 271861760,
-    # dkdv_kernel + dq_kernel, backward on the dual workload: (319 911 424 + 22 017 024)
-    # + (253 355 520 + 48 199 168)
-    ("backward", "f701359c9e5dddba"): 319911424 + 22017024 + 253355520 + 48199168,
+    # dkdv_kernel + dq_kernel, backward on the dual workload: (314 070 528 + 21 010 176)
+    # + (257 931 520 + 47 250 432)
+    ("backward", "bc05ca26b24fe4aa"): 314070528 + 21010176 + 257931520 + 47250432,
 }
 KERNEL_SOURCES = {"prefill": ("attn_prefill.cu", "ptx.cuh"), "decode": ("decode.cu",),
                   "dual": ("attn_dual.cu", "ptx.cuh"), "backward": ("attn_bwd.cu", "ptx.cuh")}
