@@ -298,7 +298,7 @@ def prefill_section(swa, timer, dev, frac, steps, warmup, seed, with_e2e, N=3276
     return res
 
 
-def decode_section(swa, timer, dev, steps, warmup, seed, S=0):
+def decode_section(swa, timer, dev, steps, warmup, seed, S=0, sweep_routed=()):
     B, L, H, D, W = 16, 32768, 16, 128, 1024
     g = torch.Generator(device=dev)
     g.manual_seed(seed)
@@ -327,8 +327,21 @@ def decode_section(swa, timer, dev, steps, warmup, seed, S=0):
 
     step_ms, kern_ms = timer.run(step, steps, warmup, kernel_events=True)
     assert swa.get_device_error() == 0
+    sweep = []
+    if sweep_routed:
+        # The same caches with the first n sequences routed, n = 0 .. B.
+        for n in sweep_routed:
+            gate.zero_()
+            gate[:n] = 1
+            sbytes = (n * L + (B - n) * W) * H * D * 2 * 2 + qo_bytes
+            sm, km = timer.run(step, max(3, steps // 2), 2, kernel_events=True)
+            sweep.append({"n_routed": n, "gbs": sbytes / (statistics.mean(sm) / 1e3) / 1e9,
+                          "kernel_gbs": sbytes / (statistics.mean(km) / 1e3) / 1e9,
+                          "ms_per_step": statistics.mean(sm)})
+        assert swa.get_device_error() == 0
     del kc, vc
-    return dict(step_ms=step_ms, kern_ms=kern_ms, bytes=kv_bytes + qo_bytes, n_routed=n_routed)
+    return dict(step_ms=step_ms, kern_ms=kern_ms, bytes=kv_bytes + qo_bytes, n_routed=n_routed,
+                sweep=sweep)
 
 
 def anchored_prefill_section(swa, timer, dev, steps, warmup, seed, S=256):
@@ -657,7 +670,8 @@ def run_ours(args, dist: Dist):
             "kernel_tflops": easy["flops"] / (statistics.mean(easy["kern_ms"]) / 1e3) / 1e12,
             "ms_per_step": statistics.mean(easy["step_ms"]),
             "realised_frac": easy["realised_frac"], "useful_tflop": easy["flops"] / 1e12}
-        dec = decode_section(swa, timer, dev, ks, kw, seed=dist.rank)
+        dec = decode_section(swa, timer, dev, ks, kw, seed=dist.rank,
+                             sweep_routed=(0, 1, 2, 4, 8, 12, 16))
         dk = statistics.mean(dec["kern_ms"]) / 1e3
         ds = statistics.mean(dec["step_ms"]) / 1e3
         hbm = float(peaks["hbm_gbs"])
@@ -669,7 +683,8 @@ def run_ours(args, dist: Dist):
                          "traffic": measured_traffic("decode"),
                          "kernel": "decode_split_kernel"},
             "workload": "decode bf16: 16 sequences x 32768 cached tokens, H=16, d=128, W=1024, "
-                        "gate Bernoulli(0.13)"}
+                        "gate Bernoulli(0.13)",
+            "sweep_n_routed": dec["sweep"]}
         da = decode_section(swa, timer, dev, ks, kw, seed=dist.rank, S=256)
         das = statistics.mean(da["step_ms"]) / 1e3
         extra["decode_anchored"] = {

@@ -21,7 +21,8 @@
 namespace swi {
 namespace {
 
-constexpr int kChunk = 256;   // tokens per split
+constexpr int kChunk = 256;   // largest chunk (tokens per split)
+constexpr int kMinChunk = 64;
 constexpr int kUnroll = 8;    // tokens in flight per thread
 
 template <typename T>
@@ -68,10 +69,20 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
 // [lo, lo + n) and, for a window query with S global anchors, the anchors
 // the window does not reach, [0, na) with na = min(S, lo).  A length outside
 // [1, Lmax] is clamped into it (the split kernel reports it).  Chunks never
-// straddle the two segments: the first ceil(na / kChunk) chunks read anchors.
+// straddle the two segments: the first ceil(na / chunk) chunks read anchors.
+// The chunk length is about (na + n) / 8 rounded up to a power of two within
+// [64, 256]: short visited ranges (windows) still split over several CTAs,
+// long ones stream 256 tokens per CTA.  It depends on the sequence alone, so
+// a sequence's result does not depend on the rest of the batch.
 struct Visit {
     int lo, n, na, nca;   // nca: anchor chunks
+    int chunk;
 };
+__device__ __forceinline__ int chunk_of(int m) {
+    int c = kMinChunk;
+    while (c < kChunk && c * 8 < m) c <<= 1;
+    return c;
+}
 __device__ __forceinline__ Visit visited(const int32_t* seq_lens, const uint8_t* gate, int b,
                                          int W, int S, int Lmax) {
     Visit v;
@@ -80,7 +91,8 @@ __device__ __forceinline__ Visit visited(const int32_t* seq_lens, const uint8_t*
     v.lo = gate[b] ? 0 : max(0, pos - W + 1);
     v.n = L - v.lo;
     v.na = min(S, v.lo);
-    v.nca = (v.na + kChunk - 1) / kChunk;
+    v.chunk = chunk_of(v.na + v.n);
+    v.nca = (v.na + v.chunk - 1) / v.chunk;
     return v;
 }
 
@@ -109,17 +121,17 @@ __global__ void decode_split_kernel(const T* __restrict__ q, const T* __restrict
     }
     int t0, t1;   // this chunk's cache entries
     if (c < vis.nca) {
-        t0 = c * kChunk;
-        t1 = min(vis.na, t0 + kChunk);
+        t0 = c * vis.chunk;
+        t1 = min(vis.na, t0 + vis.chunk);
     } else {
         const int cw = c - vis.nca;
-        if (cw * kChunk >= vis.n) {
+        if (cw * vis.chunk >= vis.n) {
             // No entries for this chunk: let the dependent combine launch.
             asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
             return;
         }
-        t0 = vis.lo + cw * kChunk;
-        t1 = min(vis.lo + vis.n, t0 + kChunk);
+        t0 = vis.lo + cw * vis.chunk;
+        t1 = min(vis.lo + vis.n, t0 + vis.chunk);
     }
     // Paged: the physical page of every page this chunk touches, in shared
     // memory (at most kChunk + 1 of them).  An entry outside [0, num_pages)
@@ -257,7 +269,7 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const float* __restri
     const int hq = blockIdx.x, b = blockIdx.y, cidx = threadIdx.x;
     const int lane = cidx & 31, wid = cidx >> 5;
     const Visit vis = visited(seq_lens, gate, b, W, S, Lmax);
-    const int nc = vis.nca + (vis.n + kChunk - 1) / kChunk;
+    const int nc = vis.nca + (vis.n + vis.chunk - 1) / vis.chunk;
     const float* base = part + ((size_t)b * max_chunks * Hq + hq) * (D + 2);
     const size_t cstride = (size_t)Hq * (D + 2);
     float M = -INFINITY;
@@ -375,7 +387,10 @@ cudaError_t launch_decode_any(const void* q, const void* kc, const void* vc,
 DecodeWs decode_ws_layout(int B, int Lmax, int Hq, int d, int S) {
     DecodeWs L;
     L.chunk = kChunk;
-    L.max_chunks = (Lmax + kChunk - 1) / kChunk + (min(S, Lmax) + kChunk - 1) / kChunk;
+    // At most ceil(m / chunk) + 1 chunks for m = na + n <= Lmax + min(S, Lmax)
+    // visited entries: 9 while the chunk is below 256, else ceil(m / 256) + 1.
+    const int longest = (Lmax + min(S, Lmax) + kChunk - 1) / kChunk + 1;
+    L.max_chunks = longest > 9 ? longest : 9;
     L.part = 0;
     L.total = sizeof(float) * (size_t)B * L.max_chunks * Hq * (d + 2);
     L.total = (L.total + 255) & ~static_cast<size_t>(255);
