@@ -46,8 +46,8 @@ L2_FLUSH_BYTES = 256 << 20
 MEASURED_TRAFFIC = {
     # prefill_kernel, long-context prefill N=32768 f=0.13: 1 142 919 424 read + 127 038 720 written
     ("prefill", "ccb76205e85abea5"): 1142919424 + 127038720,
-    # decode_split_kernel, 16 x 32768 decode: 654 405 120 read + 2 784 512 written
-    ("decode", "731602d165ca105b"): 654405120 + 2784512,
+    # decode_split_kernel, 16 x 32768 decode: 654 409 472 read + 3 369 472 written
+    ("decode", "e855b4984bd61652"): 654409472 + 3369472,
     # dual_kernel, dual-branch workload B=2 N=8192 GQA 16/4: 158 522 880 read + 271 861 760 written
     ("dual", "022299affd4ac4fb"): 158522880 + 271861760,
     # dkdv_kernel + dq_kernel, backward on the dual workload: (314 070 528 + 21 010 176)
