@@ -49,7 +49,7 @@ extern "C" {
 typedef enum {
     SWIATTN_OK = 0,
     SWIATTN_EINVAL = 1,        /* bad pointer, size, alignment or workspace too small */
-    SWIATTN_EUNSUPPORTED = 2,  /* valid request this build does not implement (e.g. d) */
+    SWIATTN_EUNSUPPORTED = 2,  /* valid request the library does not implement (e.g. d) */
     SWIATTN_ECUDA = 3,         /* a CUDA runtime/driver call failed (launch, symbol, map) */
     SWIATTN_ETIMEOUT = 4       /* a device-side bounded wait expired (from get_device_error) */
 } swiattn_status;
