@@ -252,46 +252,55 @@ __global__ void decode_split_kernel(const T* __restrict__ q, const T* __restrict
 }
 
 // Log-sum-exp merge of the chunk partials of one (sequence, query head):
-// block (hq, b), D threads, thread c owns output column c.  The maximum over
-// chunks is a block reduction; the weighted sums run 32 chunks per iteration
-// so their loads are in flight together (a routed 32K-token sequence has 128
-// chunks: four rounds).  Launched as a programmatic dependent of the split
-// kernel, it first waits for that grid's completion.
+// block (hq, b) of 1024 threads = 1024/D groups of D, thread (g, c) owns
+// output column c for the chunks g, g + 1024/D, ...  The maximum over chunks
+// is a block reduction; each group loads 16 of its chunks per round, so a
+// routed 32K-token sequence's 128 partials arrive in one round; the groups'
+// sums are then added in group order, so the result depends only on the
+// sequence's own chunk count.  Launched as a programmatic dependent of the
+// split kernel, it reads the visit (an input) and then waits for that grid's
+// completion before touching any partial.
 template <typename T, int D>
-__global__ void __launch_bounds__(D) decode_combine_kernel(const float* __restrict__ part,
-                                                           const int32_t* __restrict__ seq_lens,
-                                                           const uint8_t* __restrict__ gate,
-                                                           T* __restrict__ o, float* __restrict__ lse,
-                                                           int Hq, int W, int S, int Lmax,
-                                                           int max_chunks) {
-    __shared__ float red[D / 32];
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int hq = blockIdx.x, b = blockIdx.y, cidx = threadIdx.x;
-    const int lane = cidx & 31, wid = cidx >> 5;
+__global__ void __launch_bounds__(1024) decode_combine_kernel(const float* __restrict__ part,
+                                                              const int32_t* __restrict__ seq_lens,
+                                                              const uint8_t* __restrict__ gate,
+                                                              T* __restrict__ o, float* __restrict__ lse,
+                                                              int Hq, int W, int S, int Lmax,
+                                                              int max_chunks) {
+    constexpr int NG = 1024 / D;    // chunk groups
+    constexpr int kRound = 16;      // chunks per group and load round
+    __shared__ float red[32];
+    __shared__ float s_acc[NG][D];
+    __shared__ float s_l[NG];
+    const int hq = blockIdx.x, b = blockIdx.y;
+    const int col = threadIdx.x % D, grp = threadIdx.x / D;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    // The visit comes from the call's inputs, so it is read before waiting.
     const Visit vis = visited(seq_lens, gate, b, W, S, Lmax);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int nc = vis.nca + (vis.n + vis.chunk - 1) / vis.chunk;
     const float* base = part + ((size_t)b * max_chunks * Hq + hq) * (D + 2);
     const size_t cstride = (size_t)Hq * (D + 2);
     float M = -INFINITY;
-    for (int c = cidx; c < nc; c += D) M = fmaxf(M, base[c * cstride + D]);
+    for (int c = threadIdx.x; c < nc; c += 1024) M = fmaxf(M, base[c * cstride + D]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     if (lane == 0) red[wid] = M;
     __syncthreads();
     M = red[0];
 #pragma unroll
-    for (int w = 1; w < D / 32; ++w) M = fmaxf(M, red[w]);
+    for (int w = 1; w < 32; ++w) M = fmaxf(M, red[w]);
+    // Group g sums chunks g, g + NG, ...; the groups are then added in order.
     float L = 0.f, acc = 0.f;
-    int c = 0;
-    constexpr int kRound = 32;
-    for (; c + kRound <= nc; c += kRound) {
+    for (int c0 = grp; c0 < nc; c0 += NG * kRound) {
         float mv[kRound], lv[kRound], ov[kRound];
 #pragma unroll
         for (int u = 0; u < kRound; ++u) {
-            const float* pc = base + (size_t)(c + u) * cstride;
-            mv[u] = pc[D];
-            lv[u] = pc[D + 1];
-            ov[u] = pc[cidx];
+            const int c = c0 + u * NG;
+            const float* pc = base + (size_t)(c < nc ? c : 0) * cstride;
+            mv[u] = c < nc ? pc[D] : -INFINITY;
+            lv[u] = c < nc ? pc[D + 1] : 0.f;
+            ov[u] = c < nc ? pc[col] : 0.f;
         }
 #pragma unroll
         for (int u = 0; u < kRound; ++u) {
@@ -300,20 +309,24 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const float* __restri
             acc = fmaf(ov[u], w, acc);
         }
     }
-    for (; c < nc; ++c) {
-        const float* pc = base + (size_t)c * cstride;
-        const float w = ex2f(pc[D] - M);
-        L = fmaf(pc[D + 1], w, L);
-        acc = fmaf(pc[cidx], w, acc);
+    s_acc[grp][col] = acc;
+    if (col == 0) s_l[grp] = L;
+    __syncthreads();
+    if (grp != 0) return;
+    float A = s_acc[0][col], Lt = s_l[0];
+#pragma unroll
+    for (int g = 1; g < NG; ++g) {
+        A += s_acc[g][col];
+        Lt += s_l[g];
     }
-    const float val = acc / L;
-    T* dst = o + ((size_t)b * Hq + hq) * D + cidx;
+    const float val = A / Lt;
+    T* dst = o + ((size_t)b * Hq + hq) * D + col;
     if constexpr (sizeof(T) == 2) {
         *dst = __float2bfloat16_rn(val);
     } else {
         *dst = val;
     }
-    if (lse && cidx == 0) lse[(size_t)b * Hq + hq] = (M + __log2f(L)) * 0.69314718055994531f;
+    if (lse && col == 0) lse[(size_t)b * Hq + hq] = (M + __log2f(Lt)) * 0.69314718055994531f;
 }
 
 template <typename T, int D, int G>
@@ -353,7 +366,7 @@ cudaError_t launch_typed(const void* q, const void* kc, const void* vc, const in
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(Hq, B);
-    cfg.blockDim = dim3(D);
+    cfg.blockDim = dim3(1024);
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
