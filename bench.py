@@ -47,23 +47,30 @@ MEASURED_TRAFFIC = {
     # prefill_kernel, long-context prefill N=32768 f=0.13: 1 142 919 424 read + 127 038 720 written
     ("prefill", "ccb76205e85abea5"): 1142919424 + 127038720,
     # decode_split_kernel, 16 x 32768 decode: 654 409 472 read + 3 369 472 written
-    ("decode", "e855b4984bd61652"): 654409472 + 3369472,
+    ("decode", "a9ba9aaf8fae9108"): 654409472 + 3369472,
     # dual_kernel, dual-branch workload B=2 N=8192 GQA 16/4: 158 522 880 read + 271 861 760 written
     ("dual", "022299affd4ac4fb"): 158522880 + 271861760,
     # dkdv_kernel + dq_kernel, backward on the dual workload: (314 070 528 + 21 010 176)
     # + (257 931 520 + 47 250 432)
     ("backward", "bc05ca26b24fe4aa"): 314070528 + 21010176 + 257931520 + 47250432,
 }
-KERNEL_SOURCES = {"prefill": ("attn_prefill.cu", "ptx.cuh"), "decode": ("decode.cu",),
+# Source text each stored count depends on: whole files, or a file up to a
+# marker (the decode split kernel sits before the combine in its file).
+KERNEL_SOURCES = {"prefill": ("attn_prefill.cu", "ptx.cuh"),
+                  "decode": (("decode.cu", "// Log-sum-exp merge of the chunk partials"),),
                   "dual": ("attn_dual.cu", "ptx.cuh"), "backward": ("attn_bwd.cu", "ptx.cuh")}
 
 
 def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES[kernel]:
+    for entry in KERNEL_SOURCES[kernel]:
+        name, marker = (entry, None) if isinstance(entry, str) else entry
         path = os.path.join(ROOT, "sliding_window_attention_router_gb300", "csrc", name)
         with open(path, "rb") as f:
-            h.update(f.read())
+            data = f.read()
+        if marker is not None:
+            data = data[:data.index(marker.encode())]
+        h.update(data)
     return h.hexdigest()[:16]
 
 
