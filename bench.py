@@ -45,20 +45,22 @@ L2_FLUSH_BYTES = 256 << 20
 # has changed since reports null.
 MEASURED_TRAFFIC = {
     # prefill_kernel, long-context prefill N=32768 f=0.13: 1 142 919 424 read + 127 038 720 written
-    ("prefill", "ccb76205e85abea5"): 1142919424 + 127038720,
+    ("prefill", "2291c7922c10153b"): 1142919424 + 127038720,
     # decode_split_kernel, 16 x 32768 decode: 654 409 472 read + 3 369 472 written
     ("decode", "a9ba9aaf8fae9108"): 654409472 + 3369472,
     # dual_kernel, dual-branch workload B=2 N=8192 GQA 16/4: 158 522 880 read + 271 861 760 written
-    ("dual", "022299affd4ac4fb"): 158522880 + 271861760,
+    ("dual", "cd1b81dfd8c7475b"): 158522880 + 271861760,
     # dkdv_kernel + dq_kernel, backward on the dual workload: (314 070 528 + 21 010 176)
     # + (257 931 520 + 47 250 432)
-    ("backward", "bc05ca26b24fe4aa"): 314070528 + 21010176 + 257931520 + 47250432,
+    ("backward", "8cc041104e26e910"): 314070528 + 21010176 + 257931520 + 47250432,
 }
 # Source text each stored count depends on: whole files, or a file up to a
-# marker (the decode split kernel sits before the combine in its file).
-KERNEL_SOURCES = {"prefill": ("attn_prefill.cu", "ptx.cuh"),
+# marker (the device code of a kernel file, before its host launcher; the
+# decode split kernel, before the combine).
+KERNEL_SOURCES = {"prefill": (("attn_prefill.cu", "cudaError_t launch_prefill_tc("), "ptx.cuh"),
                   "decode": (("decode.cu", "// Log-sum-exp merge of the chunk partials"),),
-                  "dual": ("attn_dual.cu", "ptx.cuh"), "backward": ("attn_bwd.cu", "ptx.cuh")}
+                  "dual": (("attn_dual.cu", "cudaError_t launch_dual_tc("), "ptx.cuh"),
+                  "backward": (("attn_bwd.cu", "cudaError_t launch_bwd_dkdv("), "ptx.cuh")}
 
 
 def kernel_source_hash(kernel: str) -> str:

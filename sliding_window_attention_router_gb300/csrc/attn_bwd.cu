@@ -1007,14 +1007,9 @@ cudaError_t launch_bwd_dkdv(const TcBwdArgs& a, unsigned int* err, int num_sms, 
     p.items = reinterpret_cast<const BwdItem*>(a.ws + a.L->items_kv);
     p.n_items = counters;
     p.next_item = counters + 1;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(kv::dkdv_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kv::kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static std::atomic<uint64_t> smem_allowed{0};
+    const cudaError_t e = allow_dynamic_smem(kv::dkdv_kernel, kv::kSmemBytes, smem_allowed);
+    if (e != cudaSuccess) return e;
     kv::dkdv_kernel<<<num_sms, kThreads, kv::kSmemBytes, s>>>(p);
     return cudaGetLastError();
 }
@@ -1026,14 +1021,9 @@ cudaError_t launch_bwd_dq(const TcBwdArgs& a, unsigned int* err, int num_sms, cu
     p.items = reinterpret_cast<const BwdItem*>(a.ws + a.L->items_q);
     p.n_items = counters + 2;
     p.next_item = counters + 3;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(dqk::dq_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             dqk::kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static std::atomic<uint64_t> smem_allowed{0};
+    const cudaError_t e = allow_dynamic_smem(dqk::dq_kernel, dqk::kSmemBytes, smem_allowed);
+    if (e != cudaSuccess) return e;
     dqk::dq_kernel<<<num_sms, kThreads, dqk::kSmemBytes, s>>>(p);
     return cudaGetLastError();
 }

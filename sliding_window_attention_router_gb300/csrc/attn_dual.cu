@@ -660,14 +660,10 @@ cudaError_t launch_dual_tc(const TcAttnArgs& a, unsigned int* err, int num_sms, 
     p.NP = (a.N + 2 * kBM - 1) / (2 * kBM);
     p.n_items = p.NP * a.B * a.Hq;
     p.scale_log2 = a.scale * 1.4426950408889634f;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(dual_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
-    cudaError_t e = cudaMemsetAsync(a.counter, 0, sizeof(int), s);
+    static std::atomic<uint64_t> smem_allowed{0};
+    cudaError_t e = allow_dynamic_smem(dual_kernel, kSmemBytes, smem_allowed);
+    if (e != cudaSuccess) return e;
+    e = cudaMemsetAsync(a.counter, 0, sizeof(int), s);
     if (e != cudaSuccess) return e;
     prof_start(s);
     dual_kernel<<<num_sms, kThreads, kSmemBytes, s>>>(p);

@@ -758,16 +758,10 @@ cudaError_t launch_prefill_tc(const TcAttnArgs& a, const int* tile_prefix, unsig
     p.S = a.n_anchor;
     p.NT = (a.N + kBM - 1) / kBM;
     p.scale_log2 = a.scale * 1.4426950408889634f;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_kernel<false>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(prefill_kernel<true>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static std::atomic<uint64_t> smem_plain{0}, smem_anchored{0};
+    cudaError_t e = p.S > 0 ? allow_dynamic_smem(prefill_kernel<true>, kSmemBytes, smem_anchored)
+                            : allow_dynamic_smem(prefill_kernel<false>, kSmemBytes, smem_plain);
+    if (e != cudaSuccess) return e;
     if (p.S > 0)
         prefill_kernel<true><<<num_sms, kThreads, kSmemBytes, s>>>(p);
     else

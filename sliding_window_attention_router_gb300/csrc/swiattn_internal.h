@@ -3,6 +3,7 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 
@@ -17,6 +18,22 @@ constexpr unsigned int kDevErrInput = 4u;    // a device-resident input was out 
 // kernel gives up, flags a timeout and returns.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
 constexpr uint64_t kDrainLimitNs = 100000000ull;   // 0.1 s, waits while aborting
+
+// Lets `kernel` use `bytes` of dynamic shared memory on the current device.
+// The attribute belongs to the device's context, so it is set once per
+// device (devices 0-63 are remembered in `done`; others set it every call),
+// and concurrent callers may both set it, which is harmless.
+template <typename K>
+cudaError_t allow_dynamic_smem(K kernel, int bytes, std::atomic<uint64_t>& done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
 
 // ------------------------------------------------------------ tiling --------
 constexpr int kBM = 128;   // query rows per tile (TMEM lanes)
