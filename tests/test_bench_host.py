@@ -69,3 +69,19 @@ def test_reference_arm_prints_one_json_line():
     assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["steps"] == 1
+
+
+def test_traffic_counts_resolve_for_the_current_sources():
+    """Every stored DRAM count is keyed by the source text of its kernel (a
+    whole file or a file up to a marker).  Each marker must still occur once
+    in its file, and every kernel with a stored count has a source entry."""
+    import bench
+    csrc = os.path.join(ROOT, "sliding_window_attention_router_gb300", "csrc")
+    for kernel, entries in bench.KERNEL_SOURCES.items():
+        for entry in entries:
+            name, marker = (entry, None) if isinstance(entry, str) else entry
+            text = open(os.path.join(csrc, name)).read()
+            if marker is not None:
+                assert text.count(marker) == 1, (kernel, name, marker)
+        assert len(bench.kernel_source_hash(kernel)) == 16
+    assert {k for k, _ in bench.MEASURED_TRAFFIC} == set(bench.KERNEL_SOURCES)
