@@ -1,6 +1,7 @@
 """Host-side logic of bench.py on the CPU: the whole-job aggregation across
-ranks (two gloo processes), the useful-pair count, and the reference arm's
-JSON line (the fp64 oracle timed on a small sample)."""
+ranks (two gloo processes), the useful-pair count, the reference arm's
+JSON line (the fp64 oracle timed on a small sample), and the source keys of
+the stored DRAM counts."""
 import json
 import os
 import subprocess
