@@ -79,8 +79,8 @@ def test_anchors_cover_everything_is_causal_and_routed_rows_unchanged():
 
 def test_decode_anchored_equals_last_prefill_row():
     rng = np.random.default_rng(5)
-    N, H, d, W, S = 50, 2, 8, 6, 9
-    q, k, v = (rng.standard_normal((1, N, H, d)) for _ in range(3))
+    N, Hq, Hkv, d, W, S = 50, 4, 2, 8, 6, 9
+    q, k, v = (rng.standard_normal((1, N, h, d)) for h in (Hq, Hkv, Hkv))
     for g in (0, 1):
         gate = np.full((1, N), g, np.uint8)
         full = oracle.prefill_anchored(q, k, v, gate, W, S, 0.3)

@@ -5,7 +5,9 @@ temporary directory, on the CPU), then runs the pin suites against that copy
 and expects them to fail.  The mistakes are the kind a restatement of the
 pages could make: an off-by-one window, a non-strict gate, the wrong GQA
 grouping, a missing square, a dropped softmax term in the gradient, the wrong
-sigmoid derivative in the straight-through gate.
+sigmoid derivative in the straight-through gate, an inverted decode gate, an
+averaged instead of summed divergence, unscaled scores, a subtracted router
+bias.
 """
 import os
 import shutil
@@ -48,6 +50,29 @@ MUTATIONS = [
      "for (int64_t j = 0; j < lo && j <= S; ++j) idx[n++] = j;"),
     ("anchor_not_causal", "for (int64_t j = 0; j < lo && j < S; ++j) idx[n++] = j;",
      "for (int64_t j = 0; j < S && j < lo + W; ++j) if (j < lo || j > i) idx[n++] = j;"),
+    ("decode_gate_inverted", "key_range(gate[b] != 0, (int64_t)seq_lens[b] - 1, W, &lo, &hi);",
+     "key_range(gate[b] == 0, (int64_t)seq_lens[b] - 1, W, &lo, &hi);"),
+    ("decode_gqa_interleaved", "kvh = h / (Hq / Hkv);\n            int64_t lo, hi;",
+     "kvh = h % Hkv;\n            int64_t lo, hi;"),
+    ("decode_anchored_gqa_interleaved",
+     "kvh = h / (Hq / Hkv);\n            int64_t n = anchored_keys(gate[b] != 0,",
+     "kvh = h % Hkv;\n            int64_t n = anchored_keys(gate[b] != 0,"),
+    ("prefill_anchored_gqa_interleaved",
+     "kvh = h / (Hq / Hkv);\n            int64_t n = anchored_keys(gate[b * N + i] != 0,",
+     "kvh = h % Hkv;\n            int64_t n = anchored_keys(gate[b * N + i] != 0,"),
+    ("mse_averaged", "*mse = acc;", "*mse = acc / (double)(Hq * d);"),
+    ("softplus_missing_max", "return (x > 0.0 ? x : 0.0) + log1p(exp(-fabs(x)));",
+     "return x + log1p(exp(-fabs(x)));"),
+    ("scores_unscaled", "kj = k + (lo + t) * kstride;\n        double dot = 0.0;\n"
+     "        for (int64_t c = 0; c < d; ++c) dot += q[c] * kj[c];\n        s[t] = scale * dot;",
+     "kj = k + (lo + t) * kstride;\n        double dot = 0.0;\n"
+     "        for (int64_t c = 0; c < d; ++c) dot += q[c] * kj[c];\n        s[t] = dot;"),
+    ("anchored_scores_unscaled", "kj = k + idx[t] * stride;\n        double dot = 0.0;\n"
+     "        for (int64_t c = 0; c < d; ++c) dot += q[c] * kj[c];\n        s[t] = scale * dot;",
+     "kj = k + idx[t] * stride;\n        double dot = 0.0;\n"
+     "        for (int64_t c = 0; c < d; ++c) dot += q[c] * kj[c];\n        s[t] = dot;"),
+    ("router_bias_subtracted", "acc += bias;", "acc -= bias;"),
+    ("gamma_without_eps", "eps + nll[t] + alpha * mse[t]", "nll[t] + alpha * mse[t]"),
 ]
 
 
