@@ -182,9 +182,9 @@ int swiattn_decode_anchored(const void* q, const void* k_cache, const void* v_ca
  * convenience.  Arguments, layouts and results are those of swiattn_decode.
  *  - The split-KV partials go to one fixed 16 MiB device array inside the
  *    library, which every GPU that loads the library holds until the process
- *    exits.  A call whose partials, B * ceil(Lmax/256) * Hq * (d+2) * 4 bytes
- *    rounded up to 256, exceed 16 MiB returns SWIATTN_EINVAL and launches
- *    nothing (e.g. B=16, Hq=16, d=128 allows Lmax up to 32 256).
+ *    exits.  A call whose partials, B * max(9, ceil(Lmax/256) + 1) * Hq *
+ *    (d+2) * 4 bytes rounded up to 256, exceed 16 MiB returns SWIATTN_EINVAL
+ *    and launches nothing (e.g. B=16, Hq=16, d=128 allows Lmax up to 32 000).
  *  - The call allocates nothing.  Its first call on a device looks up that
  *    array's device address (once per device, with the device current); make
  *    that first call before any stream capture.

@@ -69,7 +69,7 @@ def test_noalloc_decode_rejects_partials_beyond_scratch(swa):
     sl = torch.full((B,), 8, dtype=torch.int32, device="cuda")
     gate = torch.zeros(B, dtype=torch.uint8, device="cuda")
     small = torch.zeros(B, 8, Hkv, d, dtype=torch.bfloat16, device="cuda")
-    # Lmax = 32 512 needs 127 chunks of partials: 16.9 MB > 16 MiB.  The caches
+    # Lmax = 32 512 needs 128 chunks of partials: 17.0 MB > 16 MiB.  The caches
     # are never read because validation rejects the call first.
     rc = _call_noalloc(lib, q, small, small, sl, gate, o, lse, W, 0.1, swa.BF16)
     assert rc == 0
