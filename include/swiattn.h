@@ -151,7 +151,13 @@ size_t swiattn_decode_workspace(int B, int Lmax, int Hq, int Hkv, int d, int W, 
  * gate uint8 [B]; o [B,Hq,d]; lse (nullable) fp32 [B,Hq].  A seq_lens[b]
  * outside [1, Lmax] (a device-resident input) is clamped into it and
  * swiattn_get_device_error then reports SWIATTN_EINVAL.
- * d in {64, 128}; Hkv*d/8 (bf16) or Hkv*d/4 (fp32) <= 1024; Hq/Hkv <= 8.
+ * d in {64, 128}; Hq/Hkv in {1, 2, 4, 8}.  One thread per 16 bytes of a
+ * token row (Hkv*d/8 threads for bf16, Hkv*d/4 for fp32, rounded up to 32)
+ * must fit one block of the split kernel on the device: at most 1024 threads,
+ * fewer where the kernel's register use takes more (e.g. 896 for bf16, d=128,
+ * Hq = Hkv; 256 for Hq = 8*Hkv).  A larger request returns
+ * SWIATTN_EUNSUPPORTED and launches nothing; so do swiattn_decode_anchored,
+ * swiattn_decode_paged and swiattn_decode_noalloc, whose limits are these.
  * workspace: at least swiattn_decode_workspace(...) bytes, scratch only. */
 int swiattn_decode(const void* q, const void* k_cache, const void* v_cache,
                    const int32_t* seq_lens, const uint8_t* gate, void* o, float* lse, int B,

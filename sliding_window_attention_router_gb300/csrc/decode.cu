@@ -16,6 +16,7 @@
 
 #include <cuda_bf16.h>
 #include <math.h>
+#include <atomic>
 #include <mutex>
 
 namespace swi {
@@ -430,6 +431,51 @@ cudaError_t launch_decode_paged(const void* q, const void* kp, const void* vp,
                              d, W, S, scale, dtype, L, ws, pg, s);
 }
 
+namespace {
+
+// Largest block the split kernel can launch with: its register use bounds it
+// below 1024 threads (read from the compiled kernel, cached per kind).
+template <typename T, int D, int G>
+int split_block_cap(bool paged) {
+    static std::atomic<int> cap[2];
+    int c = cap[paged].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+    cudaFuncAttributes attr;
+    const cudaError_t e = paged ? cudaFuncGetAttributes(&attr, decode_split_kernel<T, D, G, true>)
+                                : cudaFuncGetAttributes(&attr, decode_split_kernel<T, D, G, false>);
+    if (e != cudaSuccess) return 0;
+    c = attr.maxThreadsPerBlock;
+    cap[paged].store(c, std::memory_order_relaxed);
+    return c;
+}
+
+template <typename T, int D>
+int split_block_cap(int G, bool paged) {
+    switch (G) {
+        case 1: return split_block_cap<T, D, 1>(paged);
+        case 2: return split_block_cap<T, D, 2>(paged);
+        case 4: return split_block_cap<T, D, 4>(paged);
+        case 8: return split_block_cap<T, D, 8>(paged);
+        default: return 0;
+    }
+}
+
+}  // namespace
+
+int decode_block_check(int dtype, int d, int Hq, int Hkv, bool paged) {
+    const int G = Hq / Hkv;
+    int cap = 0;
+    if (dtype == SWIATTN_BF16)
+        cap = d == 128 ? split_block_cap<__nv_bfloat16, 128>(G, paged)
+                       : split_block_cap<__nv_bfloat16, 64>(G, paged);
+    else
+        cap = d == 128 ? split_block_cap<float, 128>(G, paged) : split_block_cap<float, 64>(G, paged);
+    if (cap <= 0) return SWIATTN_OK;   // limit unknown: the launch itself decides
+    const int vec = dtype == SWIATTN_BF16 ? 8 : 4;
+    const int64_t threads = ((int64_t)Hkv * d / vec + 31) / 32 * 32;
+    return threads <= cap ? SWIATTN_OK : SWIATTN_EUNSUPPORTED;
+}
+
 }  // namespace swi
 
 // ------------------------------------------------------ no-allocation variant --
@@ -484,6 +530,8 @@ extern "C" int swiattn_decode_noalloc(const void* q, const void* k_cache, const 
     if (L.total > kNoAllocScratchBytes) return SWIATTN_EINVAL;
     float* scratch = decode_scratch_on_current_device();
     if (!scratch) return SWIATTN_ECUDA;
+    const int fit = decode_block_check(dtype, d, Hq, Hkv, false);
+    if (fit != SWIATTN_OK) return fit;
     // Every chunk's partial is written before the combine reads it, so the
     // scratch needs no clearing between calls.
     const cudaError_t e = launch_decode(q, k_cache, v_cache, seq_lens, gate, o, lse, B, Lmax, Hq,

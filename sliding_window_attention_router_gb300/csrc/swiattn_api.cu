@@ -396,6 +396,8 @@ int swiattn_decode_anchored(const void* q, const void* k_cache, const void* v_ca
     if (!workspace || !aligned256(workspace) || workspace_bytes < L.total) return SWIATTN_EINVAL;
     DeviceInfo di;
     if (!device_info(di)) return SWIATTN_ECUDA;
+    const int fit = decode_block_check(dtype, d, Hq, Hkv, false);
+    if (fit != SWIATTN_OK) return fit;
     return launched(launch_decode(q, k_cache, v_cache, seq_lens, gate, o, lse, B, Lmax, Hq, Hkv,
                                   d, W, n_anchor, scale, dtype, L, static_cast<char*>(workspace),
                                   di.err, static_cast<cudaStream_t>(stream)));
@@ -434,6 +436,8 @@ int swiattn_decode_paged(const void* q, const void* k_pages, const void* v_pages
     if (!workspace || !aligned256(workspace) || workspace_bytes < L.total) return SWIATTN_EINVAL;
     DeviceInfo di;
     if (!device_info(di)) return SWIATTN_ECUDA;
+    const int fit = decode_block_check(dtype, d, Hq, Hkv, true);
+    if (fit != SWIATTN_OK) return fit;
     int lg = 0;
     while ((1 << lg) < page_size) ++lg;
     return launched(launch_decode_paged(q, k_pages, v_pages, block_table, seq_lens, gate, o, lse,

@@ -146,6 +146,14 @@ cudaError_t launch_dual_epilogue_parts(const float* mse_part, const float* logit
                                        int B, int N, int Hq, float gamma_base, float eps,
                                        float alpha, cudaStream_t s);
 
+// SWIATTN_OK when the decode split kernel for these sizes fits one block on
+// the current device (one thread per 16 bytes of a token row, all KV heads;
+// the kernel's register use caps the block below 1024 threads for most
+// kinds), SWIATTN_EUNSUPPORTED when it does not.  When the kernel's
+// attributes cannot be read it answers SWIATTN_OK and the launch decides.
+// Hq/Hkv must be 1, 2, 4 or 8.
+int decode_block_check(int dtype, int d, int Hq, int Hkv, bool paged);
+
 // err: device error word (a length outside [1, Lmax] is clamped and reported).
 cudaError_t launch_decode(const void* q, const void* kc, const void* vc, const int32_t* seq_lens,
                           const uint8_t* gate, void* o, float* lse, int B, int Lmax, int Hq,

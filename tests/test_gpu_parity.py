@@ -316,6 +316,35 @@ def test_decode_edges(swa):
             assert np.abs(f64(o) - ref).max() <= BF16_MAX
 
 
+def test_decode_wide_token_rows(swa):
+    """One block reads a token row of every KV head (one thread per 16 bytes).
+    Rows within the split kernel's block limit are computed; a wider valid row
+    is refused with SWIATTN_EUNSUPPORTED before any launch, never with a CUDA
+    error.  512 threads (32 heads, Hq = Hkv) and 256 threads (16 heads,
+    Hq = 8 Hkv) are within every limit the kernel's register use allows."""
+    g = inp._gen(78)
+    computed = []
+    for Hkv, G in ((32, 1), (56, 1), (64, 1), (16, 8), (32, 8)):
+        Hq, d, B, Lmax, W = Hkv * G, 128, 2, 150, 40
+        kc = inp.randn((B, Lmax, Hkv, d), torch.bfloat16, g)
+        vc = inp.randn((B, Lmax, Hkv, d), torch.bfloat16, g)
+        q = inp.randn((B, Hq, d), torch.bfloat16, g)
+        sl = torch.tensor([150, 77], dtype=torch.int32)
+        gate = torch.tensor([1, 0], dtype=torch.uint8)
+        scale = 1 / math.sqrt(d)
+        try:
+            o = swa.decode(*cuda(q, kc, vc, sl, gate), W, scale)
+        except swa.SwiAttnError as e:
+            assert e.status == 2, (Hkv, G, str(e))   # SWIATTN_EUNSUPPORTED
+            continue
+        torch.cuda.synchronize()
+        ref = oracle.decode(f64(q), f64(kc), f64(vc), sl.numpy(), gate.numpy(), W, scale)
+        assert np.abs(f64(o) - ref).max() <= BF16_MAX, (Hkv, G)
+        computed.append((Hkv, G))
+    assert (32, 1) in computed and (16, 8) in computed
+    assert swa.get_device_error() == 0
+
+
 # -------------------------------------------------------- cross-API invariants --
 def test_cross_api_invariants(swa):
     g = inp._gen(31)
