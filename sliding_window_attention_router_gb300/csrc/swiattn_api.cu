@@ -6,6 +6,7 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -63,7 +64,8 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-cudaEvent_t g_prof_start = nullptr, g_prof_stop = nullptr;
+// Profiling hook events: set by one thread, read by every launching thread.
+std::atomic<cudaEvent_t> g_prof_start{nullptr}, g_prof_stop{nullptr};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
@@ -78,10 +80,12 @@ bool attn_shape_ok(int B, int N, int Hq, int Hkv, int d, int W) {
 }  // namespace
 
 void prof_start(cudaStream_t s) {
-    if (g_prof_start && g_prof_stop) cudaEventRecord(g_prof_start, s);
+    cudaEvent_t a = g_prof_start.load(std::memory_order_acquire);
+    if (a && g_prof_stop.load(std::memory_order_acquire)) cudaEventRecord(a, s);
 }
 void prof_stop(cudaStream_t s) {
-    if (g_prof_start && g_prof_stop) cudaEventRecord(g_prof_stop, s);
+    cudaEvent_t b = g_prof_stop.load(std::memory_order_acquire);
+    if (b && g_prof_start.load(std::memory_order_acquire)) cudaEventRecord(b, s);
 }
 
 bool make_tmap_4d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
@@ -132,8 +136,8 @@ const char* swiattn_status_string(int status) {
 
 void swiattn_set_profile_events(void* start, void* stop) {
     std::lock_guard<std::mutex> lk(g_mu);
-    g_prof_start = static_cast<cudaEvent_t>(start);
-    g_prof_stop = static_cast<cudaEvent_t>(stop);
+    g_prof_start.store(static_cast<cudaEvent_t>(start), std::memory_order_release);
+    g_prof_stop.store(static_cast<cudaEvent_t>(stop), std::memory_order_release);
 }
 
 int swiattn_num_sms(void) {
