@@ -204,3 +204,34 @@ def test_no_gpu_reports_cuda_error_or_runs(lib):
     if torch.cuda.is_available():
         pytest.skip("GPU present")
     assert lib.swiattn_num_sms() == -1
+
+
+def _decode_chunk_len(m):
+    """Chunk length of a decode visit of m = na + n cache entries (na anchors,
+    then the window or history n): the smallest power of two from 64 up to 256
+    tokens with chunk * 8 >= m.  The two segments never share a chunk."""
+    c = 64
+    while c < 256 and c * 8 < m:
+        c *= 2
+    return c
+
+
+def test_decode_workspace_holds_every_chunk_partial(lib):
+    """The split kernel writes one partial per (sequence, chunk, query head) and
+    the combine reads them back; the workspace must hold the most chunks any
+    visit of up to Lmax entries (plus up to S anchors) can have."""
+    import sliding_window_attention_router_gb300 as swa
+    Hq, d = 256, 64                  # a chunk's partials: 256 * 66 floats = 67 584 bytes
+    per_chunk = Hq * (d + 2) * 4
+    for Lmax in (1, 7, 63, 64, 65, 200, 511, 512, 513, 1024, 1025, 2047, 2048, 2049, 4096, 5000):
+        for S in (0, 1, 63, 64, 300, 4096):
+            size = swa.decode_anchored_workspace(1, Lmax, Hq, Hq, d, 16, S, swa.BF16)
+            assert size % per_chunk == 0
+            max_chunks = size // per_chunk
+            for lo_span in range(1, Lmax + 1):
+                n = lo_span                                  # visited window / history
+                na = min(S, Lmax - n)                        # anchors below it
+                m = na + n
+                c = _decode_chunk_len(m)
+                need = -(-na // c) + -(-n // c)
+                assert need <= max_chunks, (Lmax, S, n, na, need, max_chunks)
