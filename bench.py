@@ -441,9 +441,9 @@ def route_section(swa, timer, dev, steps, warmup, seed):
     def step():
         swa.route(h, w, r["bias"], logits=logits, gate=gate)
 
-    step_ms, _ = timer.run(step, steps, warmup)
+    step_ms, kern_ms = timer.run(step, steps, warmup, kernel_events=True)
     nbytes = T * Dm * 2 + Dm * 2 + T * 5
-    return dict(step_ms=step_ms, bytes=nbytes)
+    return dict(step_ms=step_ms, kern_ms=kern_ms, bytes=nbytes)
 
 
 def layer_4k_section(swa, timer, dev, steps, warmup, seed):
@@ -551,9 +551,9 @@ def route_backward_section(swa, timer, dev, steps, warmup, seed):
     def step():
         swa.route_backward(logits, of, os_, do, gamma, d_reg, h, w, workspace=ws)
 
-    step_ms, _ = timer.run(step, steps, warmup)
+    step_ms, kern_ms = timer.run(step, steps, warmup, kernel_events=True)
     nbytes = 3 * T * HD * 2 + 2 * T * Dm * 2 + T * 16 + Dm * 4
-    return dict(step_ms=step_ms, bytes=nbytes)
+    return dict(step_ms=step_ms, kern_ms=kern_ms, bytes=nbytes)
 
 
 # ------------------------------------------------------------ CPU oracle --
@@ -684,16 +684,19 @@ def run_ours(args, dist: Dist):
         dk = statistics.mean(dec["kern_ms"]) / 1e3
         ds = statistics.mean(dec["step_ms"]) / 1e3
         hbm = float(peaks["hbm_gbs"])
-        extra["decode"] = {
-            "gbs": dec["bytes"] / ds / 1e9, "ms_per_step": ds * 1e3, "n_routed": dec["n_routed"],
-            "bytes_per_step": dec["bytes"],
-            "roofline": {"bound": "hbm", "achieved": dec["bytes"] / dk / 1e9, "peak": hbm,
-                         "unit": "GB/s", "frac": dec["bytes"] / dk / 1e9 / hbm,
+        decode_entry = {
+            "gbs": round(dec["bytes"] / ds / 1e9, 1), "ms_per_step": round(ds * 1e3, 4),
+            "n_routed": dec["n_routed"], "bytes_per_step": dec["bytes"],
+            "roofline": {"bound": "hbm", "achieved": round(dec["bytes"] / dk / 1e9, 1),
+                         "peak": hbm, "unit": "GB/s",
+                         "frac": round(dec["bytes"] / dk / 1e9 / hbm, 4),
                          "traffic": measured_traffic("decode"),
                          "kernel": "decode_split_kernel"},
             "workload": "decode bf16: 16 sequences x 32768 cached tokens, H=16, d=128, W=1024, "
                         "gate Bernoulli(0.13)",
-            "sweep_n_routed": dec["sweep"]}
+            "sweep": {"columns": ["n_routed", "step GB/s", "kernel GB/s", "kernel frac of HBM"],
+                      "rows": [[r["n_routed"], round(r["gbs"], 1), round(r["kernel_gbs"], 1),
+                                round(r["kernel_gbs"] / hbm, 4)] for r in dec["sweep"]]}}
         da = decode_section(swa, timer, dev, ks, kw, seed=dist.rank, S=256)
         das = statistics.mean(da["step_ms"]) / 1e3
         extra["decode_anchored"] = {
@@ -727,7 +730,12 @@ def run_ours(args, dist: Dist):
                         "at routed fraction 0.13"}
         rt = route_section(swa, timer, dev, ks, kw, seed=dist.rank)
         rs = statistics.mean(rt["step_ms"]) / 1e3
+        rk = statistics.mean(rt["kern_ms"]) / 1e3
         extra["route"] = {"gbs": rt["bytes"] / rs / 1e9, "ms_per_step": rs * 1e3,
+                          "roofline": {"bound": "hbm", "achieved": rt["bytes"] / rk / 1e9,
+                                       "peak": hbm, "unit": "GB/s",
+                                       "frac": rt["bytes"] / rk / 1e9 / hbm,
+                                       "traffic": None, "kernel": "route_kernel"},
                           "workload": "router GEMV, 32768 tokens x d_model 2048, bf16"}
         l4 = layer_4k_section(swa, timer, dev, ks, kw, seed=dist.rank)
         l4s = statistics.mean(l4["step_ms"]) / 1e3
@@ -764,9 +772,15 @@ def run_ours(args, dist: Dist):
                 "workload": desc}
         rb = route_backward_section(swa, timer, dev, ks, kw, dist.rank)
         rbs = statistics.mean(rb["step_ms"]) / 1e3
+        rbk = statistics.mean(rb["kern_ms"]) / 1e3
         extra["route_backward"] = {
             "gbs": rb["bytes"] / rbs / 1e9, "ms_per_step": rbs * 1e3,
+            "roofline": {"bound": "hbm", "achieved": rb["bytes"] / rbk / 1e9, "peak": hbm,
+                         "unit": "GB/s", "frac": rb["bytes"] / rbk / 1e9 / hbm, "traffic": None,
+                         "kernel": "route_bwd_logit_kernel + route_bwd_dh_kernel + "
+                                   "route_bwd_reduce_kernel"},
             "workload": "router backward bf16: 16384 tokens, 2048 outputs per token, d_model 2048"}
+        extra["decode"] = decode_entry
 
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:

@@ -151,7 +151,8 @@ size_t swiattn_decode_workspace(int B, int Lmax, int Hq, int Hkv, int d, int W, 
  * gate uint8 [B]; o [B,Hq,d]; lse (nullable) fp32 [B,Hq].  A seq_lens[b]
  * outside [1, Lmax] (a device-resident input) is clamped into it and
  * swiattn_get_device_error then reports SWIATTN_EINVAL.
- * d in {64, 128}; Hq/Hkv in {1, 2, 4, 8}.  One thread per 16 bytes of a
+ * d in {64, 128}; Hq/Hkv in {1, 2, 4, 8}; Lmax <= 2^30 (larger:
+ * SWIATTN_EUNSUPPORTED).  One thread per 16 bytes of a
  * token row (Hkv*d/8 threads for bf16, Hkv*d/4 for fp32, rounded up to 32)
  * must fit one block of the split kernel on the device: at most 1024 threads,
  * fewer where the kernel's register use takes more (e.g. 896 for bf16, d=128,
@@ -185,7 +186,9 @@ int swiattn_decode_anchored(const void* q, const void* k_cache, const void* v_ca
  * allocate device memory (for example code that runs inside an allocator-free
  * runtime or a host framework that owns every device allocation and exposes
  * none to plug-ins).  The paper has no counterpart: this is a deployment
- * convenience.  Arguments, layouts and results are those of swiattn_decode.
+ * convenience.  Arguments, layouts, results and the device-side report of a
+ * seq_lens[b] outside [1, Lmax] (clamped, then SWIATTN_EINVAL from
+ * swiattn_get_device_error) are those of swiattn_decode.
  *  - The split-KV partials go to one fixed 16 MiB device array inside the
  *    library, which every GPU that loads the library holds until the process
  *    exits.  A call whose partials, B * max(9, ceil(Lmax/256) + 1) * Hq *

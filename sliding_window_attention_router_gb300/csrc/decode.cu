@@ -17,7 +17,6 @@
 #include <cuda_bf16.h>
 #include <math.h>
 #include <atomic>
-#include <mutex>
 
 namespace swi {
 namespace {
@@ -403,8 +402,9 @@ DecodeWs decode_ws_layout(int B, int Lmax, int Hq, int d, int S) {
     L.chunk = kChunk;
     // At most ceil(m / chunk) + 1 chunks for m = na + n <= Lmax + min(S, Lmax)
     // visited entries: 9 while the chunk is below 256, else ceil(m / 256) + 1.
-    const int longest = (Lmax + min(S, Lmax) + kChunk - 1) / kChunk + 1;
-    L.max_chunks = longest > 9 ? longest : 9;
+    const int64_t m = (int64_t)Lmax + (S < Lmax ? S : Lmax);
+    const int64_t longest = (m + kChunk - 1) / kChunk + 1;
+    L.max_chunks = longest > 9 ? (int)longest : 9;
     L.part = 0;
     L.total = sizeof(float) * (size_t)B * L.max_chunks * Hq * (d + 2);
     L.total = (L.total + 255) & ~static_cast<size_t>(255);
@@ -477,65 +477,3 @@ int decode_block_check(int dtype, int d, int Hq, int Hkv, bool paged) {
 }
 
 }  // namespace swi
-
-// ------------------------------------------------------ no-allocation variant --
-// Scratch for swiattn_decode_noalloc: the split-KV partials live in this
-// fixed device array instead of a caller workspace.  Every GPU that loads the
-// library holds it (16 MiB) until the process exits.
-namespace {
-
-constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
-static __device__ __align__(256) float g_decode_scratch[kNoAllocScratchBytes / sizeof(float)];
-
-constexpr int kNoAllocMaxDevices = 64;
-std::mutex g_scratch_mu;
-float* g_scratch_ptr[kNoAllocMaxDevices];
-
-// Device address of g_decode_scratch on the current device.  The host-side
-// name only stands in for the array, so the address is looked up once per
-// device, with that device current.
-float* decode_scratch_on_current_device() {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return nullptr;
-    std::lock_guard<std::mutex> lk(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
-        void* ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_decode_scratch) != cudaSuccess) return nullptr;
-        g_scratch_ptr[dev] = static_cast<float*>(ptr);
-    }
-    return g_scratch_ptr[dev];
-}
-
-}  // namespace
-
-extern "C" int swiattn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
-                                      const int32_t* seq_lens, const uint8_t* gate, void* o,
-                                      float* lse, int B, int Lmax, int Hq, int Hkv, int d, int W,
-                                      float scale, int dtype, void* stream) {
-    using namespace swi;
-    if (B <= 0 || Lmax <= 0 || Hq <= 0 || Hkv <= 0 || W <= 0 || Hq % Hkv != 0) return SWIATTN_EINVAL;
-    if (d != 64 && d != 128) return SWIATTN_EINVAL;
-    if (dtype != SWIATTN_BF16 && dtype != SWIATTN_F32) return SWIATTN_EINVAL;
-    if (!q || !k_cache || !v_cache || !seq_lens || !gate || !o) return SWIATTN_EINVAL;
-    const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_cache) |
-                          reinterpret_cast<uintptr_t>(v_cache);
-    if (mis & 15u) return SWIATTN_EINVAL;
-    if (!(scale > 0.f)) return SWIATTN_EINVAL;
-    const int G = Hq / Hkv;
-    if (G != 1 && G != 2 && G != 4 && G != 8) return SWIATTN_EUNSUPPORTED;
-    if ((int64_t)Hkv * d / (dtype == SWIATTN_BF16 ? 8 : 4) > 1024) return SWIATTN_EUNSUPPORTED;
-    if (B > 65535) return SWIATTN_EUNSUPPORTED;
-    const DecodeWs L = decode_ws_layout(B, Lmax, Hq, d, 0);
-    // The partials of this call must fit the fixed scratch array.
-    if (L.total > kNoAllocScratchBytes) return SWIATTN_EINVAL;
-    float* scratch = decode_scratch_on_current_device();
-    if (!scratch) return SWIATTN_ECUDA;
-    const int fit = decode_block_check(dtype, d, Hq, Hkv, false);
-    if (fit != SWIATTN_OK) return fit;
-    // Every chunk's partial is written before the combine reads it, so the
-    // scratch needs no clearing between calls.
-    const cudaError_t e = launch_decode(q, k_cache, v_cache, seq_lens, gate, o, lse, B, Lmax, Hq,
-                                        Hkv, d, W, 0, scale, dtype, L, reinterpret_cast<char*>(scratch),
-                                        nullptr, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? SWIATTN_OK : SWIATTN_ECUDA;
-}

@@ -170,8 +170,11 @@ int swiattn_route(const void* h, const void* w, float bias, int64_t tokens, int 
     if (d_model % (dtype == SWIATTN_BF16 ? 8 : 4) != 0) return SWIATTN_EINVAL;
     if (tokens == 0) return SWIATTN_OK;
     if (!h || !w || !logits || !gate || !aligned16(h) || !aligned16(w)) return SWIATTN_EINVAL;
-    return launched(launch_route(h, w, bias, tokens, d_model, dtype, logits, gate,
-                                 static_cast<cudaStream_t>(stream)));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    prof_start(s);
+    const cudaError_t e = launch_route(h, w, bias, tokens, d_model, dtype, logits, gate, s);
+    prof_stop(s);
+    return launched(e);
 }
 
 size_t swiattn_prefill_workspace(int B, int N, int Hq, int Hkv, int d, int W, int dtype) {
@@ -383,7 +386,32 @@ int decode_args_ok(const void* q, const void* k, const void* v, const int32_t* s
     if (G != 1 && G != 2 && G != 4 && G != 8) return SWIATTN_EUNSUPPORTED;
     if ((int64_t)Hkv * d / (dtype == SWIATTN_BF16 ? 8 : 4) > 1024) return SWIATTN_EUNSUPPORTED;
     if (B > 65535) return SWIATTN_EUNSUPPORTED;
+    if (Lmax > (1 << 30)) return SWIATTN_EUNSUPPORTED;
     return SWIATTN_OK;
+}
+
+// Scratch of swiattn_decode_noalloc: its split-KV partials live in this fixed
+// device array instead of a caller workspace.  Every GPU that loads the
+// library holds it (16 MiB) until the process exits.
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
+static __device__ __align__(256) float g_decode_scratch[kNoAllocScratchBytes / sizeof(float)];
+
+std::mutex g_scratch_mu;
+float* g_scratch_ptr[kMaxDevices];
+
+// Device address of g_decode_scratch on the current device.  In host code the
+// array's name only stands in for it, so the address is looked up once per
+// device, with that device current.
+float* decode_scratch_on_current_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_decode_scratch) != cudaSuccess) return nullptr;
+        g_scratch_ptr[dev] = static_cast<float*>(ptr);
+    }
+    return g_scratch_ptr[dev];
 }
 
 }  // namespace
@@ -413,6 +441,29 @@ int swiattn_decode(const void* q, const void* k_cache, const void* v_cache, cons
                    void* stream) {
     return swiattn_decode_anchored(q, k_cache, v_cache, seq_lens, gate, o, lse, B, Lmax, Hq, Hkv,
                                    d, W, 0, scale, dtype, workspace, workspace_bytes, stream);
+}
+
+int swiattn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* seq_lens, const uint8_t* gate, void* o, float* lse,
+                           int B, int Lmax, int Hq, int Hkv, int d, int W, float scale, int dtype,
+                           void* stream) {
+    const int st = decode_args_ok(q, k_cache, v_cache, seq_lens, gate, o, B, Lmax, Hq, Hkv, d, W,
+                                  0, scale, dtype);
+    if (st != SWIATTN_OK) return st;
+    const DecodeWs L = decode_ws_layout(B, Lmax, Hq, d, 0);
+    // The partials of this call must fit the fixed scratch array.
+    if (L.total > kNoAllocScratchBytes) return SWIATTN_EINVAL;
+    DeviceInfo di;
+    if (!device_info(di)) return SWIATTN_ECUDA;
+    float* scratch = decode_scratch_on_current_device();
+    if (!scratch) return SWIATTN_ECUDA;
+    const int fit = decode_block_check(dtype, d, Hq, Hkv, false);
+    if (fit != SWIATTN_OK) return fit;
+    // Every chunk's partial is written before the combine reads it, so the
+    // scratch needs no clearing between calls.
+    return launched(launch_decode(q, k_cache, v_cache, seq_lens, gate, o, lse, B, Lmax, Hq, Hkv,
+                                  d, W, 0, scale, dtype, L, reinterpret_cast<char*>(scratch),
+                                  di.err, static_cast<cudaStream_t>(stream)));
 }
 
 size_t swiattn_decode_paged_workspace(int B, int max_pages, int page_size, int Hq, int Hkv, int d,
@@ -615,10 +666,13 @@ int swiattn_route_backward(const void* h, const void* w, const float* logits, co
         const size_t need = swiattn_route_backward_workspace(tokens, d_model, dtype);
         if (!workspace || !aligned256(workspace) || workspace_bytes < need) return SWIATTN_EINVAL;
     }
-    return launched(launch_route_backward(h, w, logits, o_full, o_swa, d_o, gamma, d_reg, tokens,
-                                          hd, d_model, dtype, d_logits, dh, dw, db,
-                                          static_cast<float*>(workspace),
-                                          static_cast<cudaStream_t>(stream)));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    prof_start(s);
+    const cudaError_t e = launch_route_backward(h, w, logits, o_full, o_swa, d_o, gamma, d_reg,
+                                                tokens, hd, d_model, dtype, d_logits, dh, dw, db,
+                                                static_cast<float*>(workspace), s);
+    prof_stop(s);
+    return launched(e);
 }
 
 }  // extern "C"

@@ -88,6 +88,14 @@ def test_invalid_arguments_rejected_before_launch(lib):
     dargs = [fake] * 7
     assert lib.swiattn_decode(*dargs, 2, 64, 6, 2, 128, 8, 0.1, 1, fake, 1 << 30, None) == 2
     assert lib.swiattn_decode(*dargs, 2, 64, 4, 4, 128, 8, 0.1, 1, fake, 8, None) == 1
+    # decode: caches longer than 2^30 entries are refused by every decode call
+    assert lib.swiattn_decode(*dargs, 1, (1 << 30) + 1, 4, 4, 128, 8, 0.1, 1, fake, 1 << 40,
+                              None) == 2
+    assert lib.swiattn_decode_noalloc(*dargs, 1, (1 << 30) + 1, 4, 4, 128, 8, 0.1, 1, None) == 2
+    # the no-allocation decode validates like swiattn_decode: Hq/Hkv = 3, bad scale, misaligned q
+    assert lib.swiattn_decode_noalloc(*dargs, 2, 64, 6, 2, 128, 8, 0.1, 1, None) == 2
+    assert lib.swiattn_decode_noalloc(*dargs, 2, 64, 4, 4, 128, 8, 0.0, 1, None) == 1
+    assert lib.swiattn_decode_noalloc(odd, *dargs[1:], 2, 64, 4, 4, 128, 8, 0.1, 1, None) == 1
     # dual: missing output
     xargs = [fake] * 5 + [None] + [fake] * 6
     assert lib.swiattn_dual_branch(*xargs, 1, 64, 4, 4, 128, 8, 0.1, 1e-3, 0.1, 100.0, 1, fake,

@@ -137,63 +137,63 @@ def test_prefill_4k_bf16_routed(swa):
     assert_bf16_close(o, ref, "prefill 4k")
 
 
-# -------------------------------------------------- long prefill 32K (sampled) --
-def _sample_rows(gate, N, H, W, rng, n_random=192):
-    routed = np.nonzero(gate[0])[0]
-    far = routed[routed >= W]
-    picks = {0, 1, 127, 128, W - 1, W, W + 1, N - 1, N - 128, N - 129}
-    picks.update(far[::128].tolist())          # first row of every far tile
-    picks.update(far[127::128].tolist())       # last row of every far tile
-    if far.size:
-        picks.update([int(far[0]), int(far[-1])])
-    picks.update(rng.integers(0, N, n_random).tolist())
-    rows = sorted(i for i in picks if 0 <= i < N)
-    return np.array([[0, i, int(rng.integers(0, H))] for i in rows], np.int64)
+# ------------------------------------------------------ long prefill 32K --
+# lse = m + log(sum p) in fp32: the sum of up to 32768 terms carries a
+# relative error of at most n * 2^-24 (2e-3 at n = 32768), which is the
+# absolute error of lse; the exponentials' own error (ex2.approx, a few ulp)
+# is far below it.
+LSE_TOL = 3e-3
 
 
 @pytest.mark.parametrize("frac", [0.13, 0.05])
-def test_prefill_32k_bf16_sampled(swa, frac):
+def test_prefill_32k_bf16_full(swa, frac):
+    """Every (row, head) output and lse of the long-context workload against the
+    oracle: max-abs 2e-2 and mean-abs 2e-3 over all 67M output elements."""
     d = inp.prefill_32k(frac=frac, seed=0)
-    N, H, W = d["N"], d["Hq"], d["W"]
+    W = d["W"]
     q, k, v, gate = cuda(d["q"], d["k"], d["v"], d["gate"])
     scale = 1 / math.sqrt(d["d"])
     o, lse = swa.prefill(q, k, v, gate, W, scale, want_lse=True)
     torch.cuda.synchronize()
     assert swa.get_device_error() == 0
-    rng = np.random.default_rng(1)
-    sel = _sample_rows(d["gate"].numpy(), N, H, W, rng)
-    ref, ref_lse = oracle.prefill_rows(f64(d["q"]), f64(d["k"]), f64(d["v"]), d["gate"].numpy(), W,
-                                       scale, sel, want_lse=True)
-    got = o[sel[:, 0], sel[:, 1], sel[:, 2]]
-    assert_bf16_close(got, ref, f"32k f={frac}")
-    got_lse = lse[sel[:, 0], sel[:, 1], sel[:, 2]]
-    np.testing.assert_allclose(f64(got_lse), ref_lse, atol=5e-2)
     assert torch.isfinite(o.float()).all()
+    got, got_lse = f64(o), f64(lse)
+    del o, lse, q, k, v
+    ref, ref_lse = oracle.prefill(f64(d["q"]), f64(d["k"]), f64(d["v"]), d["gate"].numpy(), W,
+                                  scale, want_lse=True)
+    err = np.abs(got - ref)
+    assert err.max() <= BF16_MAX and err.mean() <= BF16_MEAN, (frac, err.max(), err.mean())
+    assert np.abs(got_lse - ref_lse).max() <= LSE_TOL
 
 
 # ------------------------------------------------------ decode 16 x 32K --
 def test_decode_16x32k_bf16(swa):
+    """Every head of every sequence (routed ones read 32768 entries, window
+    ones the last 1024) against the oracle, max-abs and mean-abs."""
     d = inp.decode_16x32k(seed=0)
     scale = 1 / math.sqrt(d["d"])
     q, kc, vc, sl, gate = cuda(d["q"], d["k_cache"], d["v_cache"], d["seq_lens"], d["gate"])
     o, lse = swa.decode(q, kc, vc, sl, gate, d["W"], scale, want_lse=True)
     torch.cuda.synchronize()
     assert swa.get_device_error() == 0
-    heads = [0, 7, 15]
-    for b in range(d["B"]):
-        for h in heads:
-            kb = f64(d["k_cache"][b:b + 1, :, h:h + 1])
-            vb = f64(d["v_cache"][b:b + 1, :, h:h + 1])
-            qb = f64(d["q"][b:b + 1, h:h + 1])
-            ref, ref_lse = oracle.decode(qb, kb, vb, d["seq_lens"][b:b + 1].numpy(),
-                                         d["gate"][b:b + 1].numpy(), d["W"], scale, want_lse=True)
-            err = np.abs(f64(o[b, h]) - ref[0, 0]).max()
-            assert err <= BF16_MAX, (b, h, err)
-            assert abs(float(lse[b, h]) - ref_lse[0, 0]) < 5e-2
+    got, got_lse = f64(o), f64(lse)
+    ref = np.empty_like(got)
+    ref_lse = np.empty_like(got_lse)
+    for b in range(d["B"]):   # one sequence at a time keeps the fp64 caches at 1 GiB
+        r, rl = oracle.decode(f64(d["q"][b:b + 1]), f64(d["k_cache"][b:b + 1]),
+                              f64(d["v_cache"][b:b + 1]), d["seq_lens"][b:b + 1].numpy(),
+                              d["gate"][b:b + 1].numpy(), d["W"], scale, want_lse=True)
+        ref[b], ref_lse[b] = r[0], rl[0]
+    err = np.abs(got - ref)
+    assert err.max() <= BF16_MAX and err.mean() <= BF16_MEAN, (err.max(), err.mean())
+    assert np.abs(got_lse - ref_lse).max() <= LSE_TOL
+    assert int(d["gate"].sum()) >= 1 and int(d["gate"].sum()) < d["B"]   # both kinds present
 
 
 # ------------------------------------------------- dual branch 8K, GQA --
-def test_dual_8k_gqa_bf16_sampled(swa):
+def test_dual_8k_gqa_bf16_full(swa):
+    """Every token of the dual-branch workload: both branch outputs, the
+    divergence, gamma and the regulariser against the oracle."""
     d = inp.dual_8k(seed=0)
     B, N, Hq, W = d["B"], d["N"], d["Hq"], d["W"]
     scale = 1 / math.sqrt(d["d"])
@@ -208,19 +208,19 @@ def test_dual_8k_gqa_bf16_sampled(swa):
     torch.testing.assert_close(out["o_full"][:, :W], out["o_swa"][:, :W], rtol=0, atol=0)
     sel_full = (d["logits"] > 0)[..., None, None].cuda()
     assert torch.equal(out["o_gated"], torch.where(sel_full, out["o_full"], out["o_swa"]))
-    rng = np.random.default_rng(2)
-    toks = sorted({0, W - 1, W, W + 1, N - 1, 2 * W + 7} | set(rng.integers(0, N, 40).tolist()))
-    sel = np.array([[b, i] for b in range(B) for i in toks[b::2]], np.int64)
-    ref = oracle.dual_rows(f64(d["q"]), f64(d["k"]), f64(d["v"]), f64(d["logits"]), f64(d["nll"]),
-                           W, scale, sel, d["gamma_base"], d["eps"], d["alpha"])
-    of = out["o_full"][sel[:, 0], sel[:, 1]]
-    os_ = out["o_swa"][sel[:, 0], sel[:, 1]]
-    assert_bf16_close(of, ref["o_full"], "o_full")
-    assert_bf16_close(os_, ref["o_swa"], "o_swa")
-    got_mse = mse[sel[:, 0], sel[:, 1]]
-    np.testing.assert_allclose(got_mse, ref["mse"], rtol=3e-2, atol=1e-3)
-    np.testing.assert_allclose(f64(out["gamma"])[sel[:, 0], sel[:, 1]], ref["gamma"], rtol=3e-2)
-    np.testing.assert_allclose(f64(out["reg_loss"])[sel[:, 0], sel[:, 1]], ref["reg"], rtol=3e-2)
+    got_full, got_swa = f64(out["o_full"]), f64(out["o_swa"])
+    gamma, reg = f64(out["gamma"]), f64(out["reg_loss"])
+    del out
+    ref = oracle.dual(f64(d["q"]), f64(d["k"]), f64(d["v"]), f64(d["logits"]), f64(d["nll"]),
+                      W, scale, d["gamma_base"], d["eps"], d["alpha"])
+    for name, got in (("o_full", got_full), ("o_swa", got_swa)):
+        err = np.abs(got - ref[name])
+        assert err.max() <= BF16_MAX and err.mean() <= BF16_MEAN, (name, err.max(), err.mean())
+    # mse sums 2048 squared differences of outputs that each carry a relative
+    # error of order 2^-8 (bf16 probabilities): a few per cent of mse.
+    np.testing.assert_allclose(mse, ref["mse"], rtol=3e-2, atol=1e-3)
+    np.testing.assert_allclose(gamma, ref["gamma"], rtol=3e-2)
+    np.testing.assert_allclose(reg, ref["reg"], rtol=3e-2)
 
 
 # ------------------------------------------------------------ edge cases --

@@ -32,8 +32,9 @@ def _call_noalloc(lib, q, kc, vc, sl, gate, o, lse, W, scale, dtype):
     vp = ctypes.c_void_p
     return lib.swiattn_decode_noalloc(
         vp(q.data_ptr()), vp(kc.data_ptr()), vp(vc.data_ptr()), vp(sl.data_ptr()),
-        vp(gate.data_ptr()), vp(o.data_ptr()), vp(lse.data_ptr()), B, Lmax, Hq, Hkv, d, W,
-        float(scale), dtype, vp(torch.cuda.current_stream().cuda_stream))
+        vp(gate.data_ptr()), vp(o.data_ptr()), vp(lse.data_ptr() if lse is not None else None),
+        B, Lmax, Hq, Hkv, d, W, float(scale), dtype,
+        vp(torch.cuda.current_stream().cuda_stream))
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
@@ -80,3 +81,68 @@ def test_noalloc_decode_rejects_partials_beyond_scratch(swa):
                                     vp(torch.cuda.current_stream().cuda_stream))
     assert rc == 1   # SWIATTN_EINVAL, nothing launched
     torch.cuda.synchronize()
+
+
+def test_noalloc_decode_without_lse(swa):
+    """lse is optional, as for swiattn_decode."""
+    lib = swa._load()
+    g = inp._gen(2025)
+    B, Lmax, Hq, Hkv, d, W = 3, 700, 4, 4, 64, 100
+    kc = inp.randn((B, Lmax, Hkv, d), torch.bfloat16, g).cuda()
+    vc = inp.randn((B, Lmax, Hkv, d), torch.bfloat16, g).cuda()
+    q = inp.randn((B, Hq, d), torch.bfloat16, g).cuda()
+    sl = torch.tensor([700, 99, 350], dtype=torch.int32).cuda()
+    gate = torch.tensor([1, 0, 0], dtype=torch.uint8).cuda()
+    ref = swa.decode(q, kc, vc, sl, gate, W, 0.125)
+    o = torch.empty_like(q)
+    assert _call_noalloc(lib, q, kc, vc, sl, gate, o, None, W, 0.125, swa.BF16) == 0
+    torch.cuda.synchronize()
+    assert (o.float() - ref.float()).abs().max().item() <= 2e-2
+    assert swa.get_device_error() == 0
+
+
+def test_noalloc_decode_reports_out_of_range_lengths(swa):
+    """A device-resident length outside [1, Lmax] is clamped into it and
+    reported through swiattn_get_device_error, as swiattn_decode does; the
+    clamped results equal swiattn_decode's."""
+    lib = swa._load()
+    g = inp._gen(2026)
+    B, Lmax, Hq, Hkv, d, W = 4, 300, 4, 2, 128, 64
+    kc = inp.randn((B, Lmax, Hkv, d), torch.bfloat16, g).cuda()
+    vc = inp.randn((B, Lmax, Hkv, d), torch.bfloat16, g).cuda()
+    q = inp.randn((B, Hq, d), torch.bfloat16, g).cuda()
+    sl = torch.tensor([0, Lmax + 1, 150, -7], dtype=torch.int32).cuda()
+    gate = torch.tensor([1, 0, 1, 0], dtype=torch.uint8).cuda()
+    assert swa.get_device_error() == 0
+    ref = swa.decode(q, kc, vc, sl, gate, W, 0.1)
+    assert swa.get_device_error() == 1   # SWIATTN_EINVAL from swiattn_decode
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device="cuda")
+    assert _call_noalloc(lib, q, kc, vc, sl, gate, o, lse, W, 0.1, swa.BF16) == 0
+    assert swa.get_device_error() == 1   # the same report from the no-allocation call
+    assert torch.equal(o, ref)
+    assert swa.get_device_error() == 0   # reading the report cleared it
+
+
+def test_noalloc_decode_scratch_boundary(swa):
+    """The header's example bound: B=16, Hq=16, d=128 fits Lmax = 32000 and
+    not 32001 (max(9, ceil(Lmax/256) + 1) chunks of (d+2) floats per
+    sequence and head).  The rejected call launches nothing, so its caches,
+    smaller than Lmax, are never read."""
+    lib = swa._load()
+    B, Hq, Hkv, d, W = 16, 16, 16, 128, 1024
+    assert swa.decode_workspace(B, 32000, Hq, Hkv, d, W, swa.BF16) <= 16 << 20
+    assert swa.decode_workspace(B, 32001, Hq, Hkv, d, W, swa.BF16) > 16 << 20
+    q = torch.zeros(B, Hq, d, dtype=torch.bfloat16, device="cuda")
+    o = torch.empty_like(q)
+    sl = torch.full((B,), 8, dtype=torch.int32, device="cuda")
+    gate = torch.zeros(B, dtype=torch.uint8, device="cuda")
+    small = torch.zeros(B, 8, Hkv, d, dtype=torch.bfloat16, device="cuda")
+    vp = ctypes.c_void_p
+    rc = lib.swiattn_decode_noalloc(vp(q.data_ptr()), vp(small.data_ptr()), vp(small.data_ptr()),
+                                    vp(sl.data_ptr()), vp(gate.data_ptr()), vp(o.data_ptr()),
+                                    vp(None), B, 32001, Hq, Hkv, d, W, 0.1, swa.BF16,
+                                    vp(torch.cuda.current_stream().cuda_stream))
+    assert rc == 1   # SWIATTN_EINVAL, nothing launched
+    torch.cuda.synchronize()
+    assert swa.get_device_error() == 0
