@@ -325,18 +325,31 @@ int swiattn_get_device_error(void* stream);
 const char* swiattn_status_string(int status);
 
 /* Timing hook.  When both are non-NULL, every later swiattn_prefill,
- * swiattn_decode, swiattn_dual_branch and swiattn_prefill_backward call
- * records `start` (a cudaEvent_t passed as void*) on its stream immediately
- * before launching its dominant kernel (the attention kernel, the decode
- * split kernel, or the backward's two attention kernels, dK/dV then dQ) and
- * `stop` immediately after it, so cudaEventElapsedTime gives that kernel's
- * device time alone.  Passing NULL, NULL turns the hook off.  Process-wide setting;
+ * swiattn_decode, swiattn_dual_branch, swiattn_prefill_backward, swiattn_route
+ * and swiattn_route_backward call records `start` (a cudaEvent_t passed as
+ * void*) on its stream immediately before launching its dominant kernel (the
+ * attention kernel, the decode split kernel, the backward's two attention
+ * kernels, dK/dV then dQ, the router GEMV, or the router backward's three
+ * kernels) and `stop` immediately after it, so cudaEventElapsedTime gives that
+ * kernel's device time alone.  Passing NULL, NULL turns the hook off.  Process-wide setting;
  * the events stay owned by the caller and must outlive their use. */
 void swiattn_set_profile_events(void* start, void* stop);
 
 /* Number of SMs of the current device (the persistent kernels launch one CTA
  * per SM), or -1 on a CUDA error. */
 int swiattn_num_sms(void);
+
+/* Failure-detection aid with no counterpart in the paper: sets, on the
+ * current device, how long a device-side wait of the tensor-core kernels
+ * (routed prefill, dual branch, backward) may last before the kernel gives up,
+ * records SWIATTN_ETIMEOUT for swiattn_get_device_error and returns early
+ * without computing the rest of its work; ns = 0 restores the default of 2 s.
+ * A tiny limit lets a test make such a wait run out on purpose and check that
+ * the kernel stops cleanly (it still waits, with a separate fixed bound, for
+ * its own copies and tensor-core operations in flight before it exits) and
+ * that the next call computes normally.  Outputs of a call that timed out are
+ * unspecified.  Synchronous; call it with no kernel of this library running. */
+int swiattn_set_wait_limit_ns(uint64_t ns);
 
 #ifdef __cplusplus
 }

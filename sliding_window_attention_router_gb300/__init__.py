@@ -41,7 +41,7 @@ EXPORTS = (
     "swiattn_decode_anchored", "swiattn_prefill_anchored", "swiattn_route_prefill_workspace",
     "swiattn_route_prefill", "swiattn_prefill_host_workspace", "swiattn_prefill_host",
     "swiattn_get_device_error", "swiattn_status_string", "swiattn_set_profile_events",
-    "swiattn_num_sms",
+    "swiattn_num_sms", "swiattn_set_wait_limit_ns",
 )
 
 
@@ -102,6 +102,7 @@ def _load() -> ctypes.CDLL:
             lib.swiattn_status_string.argtypes = [i32]
             lib.swiattn_status_string.restype = ctypes.c_char_p
             lib.swiattn_num_sms.argtypes = []
+            lib.swiattn_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
             lib.swiattn_set_profile_events.argtypes = [vp, vp]
             lib.swiattn_set_profile_events.restype = None
             for name in ("swiattn_route", "swiattn_prefill", "swiattn_decode", "swiattn_decode_noalloc",
@@ -153,6 +154,12 @@ def set_profile_events(start: Optional[torch.cuda.Event], stop: Optional[torch.c
     else:
         _load().swiattn_set_profile_events(ctypes.c_void_p(start.cuda_event),
                                            ctypes.c_void_p(stop.cuda_event))
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    """Limit of the tensor-core kernels' device waits on the current device
+    (0 restores the default); a failure-detection test aid."""
+    _check(_load().swiattn_set_wait_limit_ns(int(ns)), "swiattn_set_wait_limit_ns")
 
 
 def get_device_error() -> int:

@@ -280,8 +280,14 @@ __device__ __forceinline__ Tile tile_of(const Plan& pl, int u) {
     return t;
 }
 
+// Loads issued so far on each ring of the dK/dV producer (a drain after an
+// abort waits for the last one of each ring that can still be in flight).
+struct KvIssued {
+    uint32_t q, d, k, v;
+};
+
 __device__ bool producer(const BwdParams& p, uint8_t* smem, uint64_t* bar, volatile int* sched,
-                         volatile int* abort_flag, uint32_t& g, uint32_t& kv_cnt) {
+                         volatile int* abort_flag, KvIssued& n_is) {
     const int n = p.n_items[0];
     for (int k = 0;; ++k) {
         int idx;
@@ -290,21 +296,23 @@ __device__ bool producer(const BwdParams& p, uint8_t* smem, uint64_t* bar, volat
             return false;
         if (idx < 0) break;
         const Plan pl = make_plan(p, idx);
-        if (!mbar_wait_w(&bar[BAR_K_EMPTY], (kv_cnt & 1u) ^ 1u, abort_flag, p.err)) return false;
+        if (!mbar_wait_w(&bar[BAR_K_EMPTY], (n_is.k & 1u) ^ 1u, abort_flag, p.err)) return false;
         mbar_arrive_expect_tx_w(&bar[BAR_K_FULL], kTileBytes);
         load_tile_pair(&p.tm_k, smem + kOffK, &bar[BAR_K_FULL], pl.kvh, pl.k0, pl.b);
-        if (!mbar_wait_w(&bar[BAR_V_EMPTY], (kv_cnt & 1u) ^ 1u, abort_flag, p.err)) return false;
+        ++n_is.k;
+        if (!mbar_wait_w(&bar[BAR_V_EMPTY], (n_is.v & 1u) ^ 1u, abort_flag, p.err)) return false;
         mbar_arrive_expect_tx_w(&bar[BAR_V_FULL], kTileBytes);
         load_tile_pair(&p.tm_v, smem + kOffV, &bar[BAR_V_FULL], pl.kvh, pl.k0, pl.b);
-        ++kv_cnt;
+        ++n_is.v;
         for (int u = 0; u < pl.ntiles; ++u) {
             const Tile t = tile_of(pl, u);
-            const uint32_t qs = g % kQSlots, qph = (g / kQSlots) & 1u;
+            const uint32_t qs = n_is.q % kQSlots, qph = (n_is.q / kQSlots) & 1u;
             if (!mbar_wait_w(&bar[BAR_Q_EMPTY + qs], qph ^ 1u, abort_flag, p.err)) return false;
             mbar_arrive_expect_tx_w(&bar[BAR_Q_FULL + qs], kTileBytes);
             load_tile_pair(t.far ? &p.tm_qc : &p.tm_q, smem + kOffQ + qs * kTileBytes,
                            &bar[BAR_Q_FULL + qs], t.h, t.row0, pl.b);
-            const uint32_t ds = g % kDSlots, dph = (g / kDSlots) & 1u;
+            ++n_is.q;
+            const uint32_t ds = n_is.d % kDSlots, dph = (n_is.d / kDSlots) & 1u;
             if (!mbar_wait_w(&bar[BAR_DO_EMPTY + ds], dph ^ 1u, abort_flag, p.err)) return false;
             uint64_t* fb = &bar[BAR_DO_FULL + ds];
             mbar_arrive_expect_tx_w(fb, kTileBytes + 2 * kRowBytes);
@@ -315,7 +323,7 @@ __device__ bool producer(const BwdParams& p, uint8_t* smem, uint64_t* bar, volat
                         kRowBytes, fb);
             bulk_load_w(smem + kOffD + ds * kRowBytes, (t.far ? p.d_far : p.d_band) + stat,
                         kRowBytes, fb);
-            ++g;
+            ++n_is.d;
         }
     }
     return true;
@@ -610,14 +618,12 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
             prefetch_tensormap(&p.tm_v);
         }
         __syncwarp();
-        uint32_t g = 0, kv_cnt = 0;
-        if (!producer(p, smem, bar, sched, abort_flag, g, kv_cnt)) {
-            drain_ring(&bar[BAR_Q_FULL], kQSlots, g);
-            drain_ring(&bar[BAR_DO_FULL], kDSlots, g);
-            if (kv_cnt) {
-                mbar_drain(&bar[BAR_K_FULL], (kv_cnt - 1) & 1u);
-                mbar_drain(&bar[BAR_V_FULL], (kv_cnt - 1) & 1u);
-            }
+        KvIssued n_is{0, 0, 0, 0};
+        if (!producer(p, smem, bar, sched, abort_flag, n_is)) {
+            drain_ring(&bar[BAR_Q_FULL], kQSlots, n_is.q);
+            drain_ring(&bar[BAR_DO_FULL], kDSlots, n_is.d);
+            drain_ring(&bar[BAR_K_FULL], 1, n_is.k);
+            drain_ring(&bar[BAR_V_FULL], 1, n_is.v);
         }
         __syncwarp();
     } else if (warp == 9) {
@@ -690,8 +696,13 @@ __device__ __forceinline__ Plan make_plan(const BwdParams& p, int idx) {
     return pl;
 }
 
+// Loads issued so far on each ring of the dQ producer (see KvIssued).
+struct QIssued {
+    uint32_t q, k, v;
+};
+
 __device__ bool producer(const BwdParams& p, uint8_t* smem, uint64_t* bar, volatile int* sched,
-                         volatile int* abort_flag, uint32_t& g, uint32_t& q_cnt) {
+                         volatile int* abort_flag, QIssued& n_is) {
     const int n = p.n_items[0];
     for (int k = 0;; ++k) {
         int idx;
@@ -700,26 +711,27 @@ __device__ bool producer(const BwdParams& p, uint8_t* smem, uint64_t* bar, volat
             return false;
         if (idx < 0) break;
         const Plan pl = make_plan(p, idx);
-        if (!mbar_wait_w(&bar[BAR_Q_EMPTY], (q_cnt & 1u) ^ 1u, abort_flag, p.err)) return false;
+        if (!mbar_wait_w(&bar[BAR_Q_EMPTY], (n_is.q & 1u) ^ 1u, abort_flag, p.err)) return false;
         mbar_arrive_expect_tx_w(&bar[BAR_Q_FULL], 2 * kTileBytes);
         load_tile_pair(pl.far ? &p.tm_qc : &p.tm_q, smem + kOffQ, &bar[BAR_Q_FULL], pl.h, pl.row0,
                        pl.b);
         load_tile_pair(pl.far ? &p.tm_doc : &p.tm_do, smem + kOffDO, &bar[BAR_Q_FULL], pl.h,
                        pl.row0, pl.b);
-        ++q_cnt;
+        ++n_is.q;
         for (int j = 0; j < pl.nblk; ++j) {
             const int key0 = pl.kv0 + j * kBN;
-            const uint32_t ks = g % kKSlots, kph = (g / kKSlots) & 1u;
+            const uint32_t ks = n_is.k % kKSlots, kph = (n_is.k / kKSlots) & 1u;
             if (!mbar_wait_w(&bar[BAR_K_EMPTY + ks], kph ^ 1u, abort_flag, p.err)) return false;
             mbar_arrive_expect_tx_w(&bar[BAR_K_FULL + ks], kTileBytes);
             load_tile_pair(&p.tm_k, smem + kOffK + ks * kTileBytes, &bar[BAR_K_FULL + ks], pl.kvh,
                            key0, pl.b);
-            const uint32_t vs = g % kVSlots, vph = (g / kVSlots) & 1u;
+            ++n_is.k;
+            const uint32_t vs = n_is.v % kVSlots, vph = (n_is.v / kVSlots) & 1u;
             if (!mbar_wait_w(&bar[BAR_V_EMPTY + vs], vph ^ 1u, abort_flag, p.err)) return false;
             mbar_arrive_expect_tx_w(&bar[BAR_V_FULL + vs], kTileBytes);
             load_tile_pair(&p.tm_v, smem + kOffV + vs * kTileBytes, &bar[BAR_V_FULL + vs], pl.kvh,
                            key0, pl.b);
-            ++g;
+            ++n_is.v;
         }
     }
     return true;
@@ -941,11 +953,11 @@ __global__ void __launch_bounds__(kThreads, 1) dq_kernel(const __grid_constant__
             prefetch_tensormap(&p.tm_v);
         }
         __syncwarp();
-        uint32_t g = 0, q_cnt = 0;
-        if (!producer(p, smem, bar, sched, abort_flag, g, q_cnt)) {
-            drain_ring(&bar[BAR_K_FULL], kKSlots, g);
-            drain_ring(&bar[BAR_V_FULL], kVSlots, g);
-            if (q_cnt) mbar_drain(&bar[BAR_Q_FULL], (q_cnt - 1) & 1u);
+        QIssued n_is{0, 0, 0};
+        if (!producer(p, smem, bar, sched, abort_flag, n_is)) {
+            drain_ring(&bar[BAR_K_FULL], kKSlots, n_is.k);
+            drain_ring(&bar[BAR_V_FULL], kVSlots, n_is.v);
+            drain_ring(&bar[BAR_Q_FULL], 1, n_is.q);
         }
         __syncwarp();
     } else if (warp == 9) {
@@ -1027,5 +1039,7 @@ cudaError_t launch_bwd_dq(const TcBwdArgs& a, unsigned int* err, int num_sms, cu
     dqk::dq_kernel<<<num_sms, kThreads, dqk::kSmemBytes, s>>>(p);
     return cudaGetLastError();
 }
+
+cudaError_t bwd_set_wait_limit(uint64_t ns) { return set_wait_limit_of_unit(ns); }
 
 }  // namespace swi

@@ -671,4 +671,6 @@ cudaError_t launch_dual_tc(const TcAttnArgs& a, unsigned int* err, int num_sms, 
     return cudaGetLastError();
 }
 
+cudaError_t dual_set_wait_limit(uint64_t ns) { return set_wait_limit_of_unit(ns); }
+
 }  // namespace swi

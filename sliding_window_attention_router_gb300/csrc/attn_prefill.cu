@@ -769,4 +769,6 @@ cudaError_t launch_prefill_tc(const TcAttnArgs& a, const int* tile_prefix, unsig
     return cudaGetLastError();
 }
 
+cudaError_t prefill_set_wait_limit(uint64_t ns) { return set_wait_limit_of_unit(ns); }
+
 }  // namespace swi

@@ -23,6 +23,7 @@ namespace {
 
 constexpr int kChunk = 256;   // largest chunk (tokens per split)
 constexpr int kMinChunk = 64;
+constexpr int kSplit = 8;     // a visit shorter than kSplit * kChunk splits into about kSplit chunks
 constexpr int kUnroll = 8;    // tokens in flight per thread
 
 template <typename T>
@@ -80,7 +81,7 @@ struct Visit {
 };
 __device__ __forceinline__ int chunk_of(int m) {
     int c = kMinChunk;
-    while (c < kChunk && c * 8 < m) c <<= 1;
+    while (c < kChunk && c * kSplit < m) c <<= 1;
     return c;
 }
 __device__ __forceinline__ Visit visited(const int32_t* seq_lens, const uint8_t* gate, int b,
@@ -96,6 +97,47 @@ __device__ __forceinline__ Visit visited(const int32_t* seq_lens, const uint8_t*
     return v;
 }
 
+__device__ __forceinline__ int chunks_of(const Visit& v) {
+    return v.nca + (v.n + v.chunk - 1) / v.chunk;
+}
+
+// Batches up to this size dispatch their chunks longest visit first.
+constexpr int kOrderMaxB = 32;
+
+// CTA (blockIdx.x, blockIdx.y) -> (sequence b, chunk c).  For B <= 32 warp 0
+// enumerates the real chunks of the batch, sequences with more chunks first
+// (ties by index), and the linear CTA index picks one: the longest visits are
+// dispatched first, and every real chunk precedes every CTA that has no chunk
+// (b = -1), so no CTA slot is spent on empty ones before real work starts.
+// Which CTA computes a chunk does not change that chunk's partial, so the
+// results stay batch-invariant.  Larger batches keep the direct mapping
+// (b = blockIdx.y, c = blockIdx.x; chunks past the visit are empty).
+__device__ __forceinline__ void cta_chunk(const int32_t* seq_lens, const uint8_t* gate, int B,
+                                          int W, int S, int Lmax, int& b, int& c) {
+    if (B > kOrderMaxB) {
+        b = blockIdx.y;
+        c = blockIdx.x;
+        return;
+    }
+    __shared__ int s_bc[2];
+    if (threadIdx.x < 32) {
+        const int l = threadIdx.x;
+        const int n = l < B ? chunks_of(visited(seq_lens, gate, l, W, S, Lmax)) : 0;
+        int start = 0;   // chunks of the sequences ordered before sequence l
+        for (int o = 0; o < B; ++o) {
+            const int no = __shfl_sync(0xffffffffu, n, o);
+            if (no > n || (no == n && o < l)) start += no;
+        }
+        const int64_t i = blockIdx.x + (int64_t)blockIdx.y * gridDim.x;
+        const unsigned hit = __ballot_sync(0xffffffffu, l < B && i >= start && i < start + n);
+        if (l == 0) s_bc[0] = hit ? __ffs(hit) - 1 : -1;
+        if (hit && l == __ffs(hit) - 1) s_bc[1] = static_cast<int>(i - start);
+    }
+    __syncthreads();
+    b = s_bc[0];
+    c = s_bc[1];
+}
+
 // Where token rows live: a contiguous cache [B, Lmax, Hkv, d] (Lmax rows per
 // sequence), or pages [num_pages, page_size, Hkv, d] found through a block
 // table [B, max_pages] (page_size = 1 << page_lg).
@@ -105,15 +147,25 @@ struct Paging {
     unsigned int* err;
 };
 
-template <typename T, int D, int G, bool PAGED>
-__global__ void decode_split_kernel(const T* __restrict__ q, const T* __restrict__ kc,
+// NG thread groups per CTA (1 or 2) split a chunk's tokens between them, in
+// alternating runs of kUnroll tokens, and merge their partials through shared
+// memory at the end: twice the loads in flight per chunk where a token row
+// takes at most 256 threads.
+template <typename T, int D, int G, bool PAGED, int NG>
+__device__ __forceinline__ void decode_split_body(const T* __restrict__ q, const T* __restrict__ kc,
                                     const T* __restrict__ vc, const int32_t* __restrict__ seq_lens,
                                     const uint8_t* __restrict__ gate, float* __restrict__ part,
                                     int Lmax, int Hq, int Hkv, int W, int S, float scale_log2,
-                                    int max_chunks, Paging pg) {
+                                    int B, int max_chunks, Paging pg) {
     constexpr int VEC = Vec<T>::N;
     constexpr int LPH = D / VEC;   // lanes per KV head
-    const int b = blockIdx.y, c = blockIdx.x;
+    int b, c;
+    cta_chunk(seq_lens, gate, B, W, S, Lmax, b, c);
+    if (b < 0) {
+        // No chunk for this CTA: let the dependent combine launch.
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        return;
+    }
     const Visit vis = visited(seq_lens, gate, b, W, S, Lmax);
     if (c == 0 && threadIdx.x == 0 && pg.err) {
         const int raw = seq_lens[b];
@@ -155,10 +207,13 @@ __global__ void decode_split_kernel(const T* __restrict__ q, const T* __restrict
         __syncthreads();
     }
 
-    // Threads past Hkv*LPH (block rounded up to whole warps) mirror the last
-    // KV head so shuffles stay full-warp; they write nothing.
-    const int active = threadIdx.x < Hkv * LPH;
-    const int tid = active ? threadIdx.x : (Hkv - 1) * LPH + (threadIdx.x % LPH);
+    // Thread group grp (tpg threads, whole warps) takes runs grp, grp + NG, ...
+    // of kUnroll tokens.  Threads past Hkv*LPH in a group mirror the last KV
+    // head so shuffles stay full-warp; they write nothing.
+    const int tpg = blockDim.x / NG;
+    const int grp = threadIdx.x / tpg, tig = threadIdx.x % tpg;
+    const int active = tig < Hkv * LPH;
+    const int tid = active ? tig : (Hkv - 1) * LPH + (tig % LPH);
     const int kvh = tid / LPH, sub = tid % LPH;
     const size_t row_vecs = (size_t)Hkv * LPH;   // uint4 per token row (all KV heads)
 
@@ -179,7 +234,7 @@ __global__ void decode_split_kernel(const T* __restrict__ q, const T* __restrict
 
     const uint4* kb = reinterpret_cast<const uint4*>(kc) + (PAGED ? 0 : (size_t)b * Lmax * row_vecs) + tid;
     const uint4* vb = reinterpret_cast<const uint4*>(vc) + (PAGED ? 0 : (size_t)b * Lmax * row_vecs) + tid;
-    for (int t = t0; t < t1; t += kUnroll) {
+    for (int t = t0 + grp * kUnroll; t < t1; t += NG * kUnroll) {
         uint4 ku[kUnroll], vu[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
@@ -231,7 +286,36 @@ __global__ void decode_split_kernel(const T* __restrict__ q, const T* __restrict
         }
     }
 
-    if (active) {
+    if constexpr (NG == 2) {
+        // Group 1 hands its (m, l, o) to group 0, which merges them by
+        // log-sum-exp (group 0 always has a token, so its m is finite).
+        extern __shared__ float s_merge[];
+        constexpr int PER = G * (VEC + 2);
+        float* mine = s_merge + (size_t)tig * PER;
+        if (grp == 1) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) mine[g * (VEC + 2) + e] = acc[g][e];
+                mine[g * (VEC + 2) + VEC] = m[g];
+                mine[g * (VEC + 2) + VEC + 1] = l[g];
+            }
+        }
+        __syncthreads();
+        if (grp == 0) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float m1 = mine[g * (VEC + 2) + VEC], l1 = mine[g * (VEC + 2) + VEC + 1];
+                const float mx = fmaxf(m[g], m1);
+                const float a0 = ex2f(m[g] - mx), a1 = ex2f(m1 - mx);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) acc[g][e] = acc[g][e] * a0 + mine[g * (VEC + 2) + e] * a1;
+                l[g] = l[g] * a0 + l1 * a1;
+                m[g] = mx;
+            }
+        }
+    }
+    if (active && grp == 0) {
 #pragma unroll
         for (int g = 0; g < G; ++g) {
             const int hq = kvh * G + g;
@@ -249,6 +333,28 @@ __global__ void decode_split_kernel(const T* __restrict__ q, const T* __restrict
     // grid's completion and memory before reading any partial), which hides
     // its launch behind the last CTAs' tail.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename T, int D, int G, bool PAGED>
+__global__ void decode_split_kernel(const T* __restrict__ q, const T* __restrict__ kc,
+                                    const T* __restrict__ vc, const int32_t* __restrict__ seq_lens,
+                                    const uint8_t* __restrict__ gate, float* __restrict__ part,
+                                    int Lmax, int Hq, int Hkv, int W, int S, float scale_log2,
+                                    int B, int max_chunks, Paging pg) {
+    decode_split_body<T, D, G, PAGED, 1>(q, kc, vc, seq_lens, gate, part, Lmax, Hq, Hkv, W, S,
+                                         scale_log2, B, max_chunks, pg);
+}
+
+// Two thread groups per CTA, at most 512 threads.  (Two such CTAs per SM would
+// cap registers at 64, and the kernel then spills.)
+template <typename T, int D, int G, bool PAGED>
+__global__ void __launch_bounds__(512, 1)
+decode_split2_kernel(const T* __restrict__ q, const T* __restrict__ kc,
+                     const T* __restrict__ vc, const int32_t* __restrict__ seq_lens,
+                     const uint8_t* __restrict__ gate, float* __restrict__ part, int Lmax, int Hq,
+                     int Hkv, int W, int S, float scale_log2, int B, int max_chunks, Paging pg) {
+    decode_split_body<T, D, G, PAGED, 2>(q, kc, vc, seq_lens, gate, part, Lmax, Hq, Hkv, W, S,
+                                         scale_log2, B, max_chunks, pg);
 }
 
 // Log-sum-exp merge of the chunk partials of one (sequence, query head):
@@ -329,20 +435,45 @@ __global__ void __launch_bounds__(1024) decode_combine_kernel(const float* __res
     if (lse && col == 0) lse[(size_t)b * Hq + hq] = (M + __log2f(Lt)) * 0.69314718055994531f;
 }
 
+// Thread groups per CTA for a token row of tpg threads and G query heads per
+// KV head: two groups when the row takes at most 256 threads and G <= 2 (the
+// merge buffer is then at most 20 KiB), else one.  It depends on the shapes
+// alone, so a sequence's result does not depend on the rest of the batch.
+inline int split_groups(int tpg, int G) { return (tpg <= 256 && G <= 2) ? 2 : 1; }
+
+template <typename T, int D, int G, int NG>
+void launch_split_ng(const void* q, const void* kc, const void* vc, const int32_t* sl,
+                     const uint8_t* gate, float* part, int B, int Lmax, int Hq, int Hkv, int W,
+                     int S, float scale_log2, int max_chunks, const Paging& pg, int tpg,
+                     cudaStream_t s) {
+    const dim3 grid(max_chunks, B);
+    const size_t smem = NG > 1 ? sizeof(float) * tpg * G * (Vec<T>::N + 2) : 0;
+    using Kern = void (*)(const T*, const T*, const T*, const int32_t*, const uint8_t*, float*,
+                          int, int, int, int, int, float, int, int, Paging);
+    Kern kern;
+    if constexpr (NG == 2)
+        kern = pg.block_table ? decode_split2_kernel<T, D, G, true> : decode_split2_kernel<T, D, G, false>;
+    else
+        kern = pg.block_table ? decode_split_kernel<T, D, G, true> : decode_split_kernel<T, D, G, false>;
+    kern<<<grid, NG * tpg, smem, s>>>(static_cast<const T*>(q), static_cast<const T*>(kc),
+                                      static_cast<const T*>(vc), sl, gate, part, Lmax, Hq, Hkv, W,
+                                      S, scale_log2, B, max_chunks, pg);
+}
+
 template <typename T, int D, int G>
 cudaError_t launch_split(const void* q, const void* kc, const void* vc, const int32_t* sl,
                          const uint8_t* gate, float* part, int B, int Lmax, int Hq, int Hkv, int W,
                          int S, float scale_log2, int max_chunks, const Paging& pg, cudaStream_t s) {
-    const int threads = (Hkv * (D / Vec<T>::N) + 31) / 32 * 32;
-    dim3 grid(max_chunks, B);
-    if (pg.block_table)
-        decode_split_kernel<T, D, G, true><<<grid, threads, 0, s>>>(
-            static_cast<const T*>(q), static_cast<const T*>(kc), static_cast<const T*>(vc), sl, gate,
-            part, Lmax, Hq, Hkv, W, S, scale_log2, max_chunks, pg);
-    else
-        decode_split_kernel<T, D, G, false><<<grid, threads, 0, s>>>(
-            static_cast<const T*>(q), static_cast<const T*>(kc), static_cast<const T*>(vc), sl, gate,
-            part, Lmax, Hq, Hkv, W, S, scale_log2, max_chunks, pg);
+    const int tpg = (Hkv * (D / Vec<T>::N) + 31) / 32 * 32;
+    if constexpr (G <= 2) {
+        if (split_groups(tpg, G) == 2) {
+            launch_split_ng<T, D, G, 2>(q, kc, vc, sl, gate, part, B, Lmax, Hq, Hkv, W, S,
+                                        scale_log2, max_chunks, pg, tpg, s);
+            return cudaGetLastError();
+        }
+    }
+    launch_split_ng<T, D, G, 1>(q, kc, vc, sl, gate, part, B, Lmax, Hq, Hkv, W, S, scale_log2,
+                                max_chunks, pg, tpg, s);
     return cudaGetLastError();
 }
 
@@ -400,11 +531,13 @@ cudaError_t launch_decode_any(const void* q, const void* kc, const void* vc,
 DecodeWs decode_ws_layout(int B, int Lmax, int Hq, int d, int S) {
     DecodeWs L;
     L.chunk = kChunk;
-    // At most ceil(m / chunk) + 1 chunks for m = na + n <= Lmax + min(S, Lmax)
-    // visited entries: 9 while the chunk is below 256, else ceil(m / 256) + 1.
+    // A visit of m = na + n <= Lmax + min(S, Lmax) entries has at most
+    // ceil(m / chunk) + 1 chunks (ceil(a/c) + ceil(b/c) <= ceil((a+b)/c) + 1
+    // for its two segments): kSplit + 1 while the chunk is below 256 (then
+    // chunk * kSplit >= m), else ceil(m / 256) + 1.
     const int64_t m = (int64_t)Lmax + (S < Lmax ? S : Lmax);
     const int64_t longest = (m + kChunk - 1) / kChunk + 1;
-    L.max_chunks = longest > 9 ? (int)longest : 9;
+    L.max_chunks = longest > kSplit + 1 ? (int)longest : kSplit + 1;
     L.part = 0;
     L.total = sizeof(float) * (size_t)B * L.max_chunks * Hq * (d + 2);
     L.total = (L.total + 255) & ~static_cast<size_t>(255);

@@ -57,31 +57,63 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // try_wait that lets the hardware suspend the thread (for up to about
-// 0.1 ms) until the phase completes, so waiting warps do not take issue slots
+// hint_ns) until the phase completes, so waiting warps do not take issue slots
 // from working ones.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(100000u)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
         : "memory");
     return ok != 0;
 }
 
+// Limit of the bounded waits below, one copy per translation unit that
+// includes this header (kWaitLimitNs unless lowered on purpose, see
+// set_wait_limit_of_unit).
+static __device__ unsigned long long g_wait_limit_ns = kWaitLimitNs;
+
+// Sets this translation unit's copy of the wait limit on the current device
+// (synchronous; 0 restores kWaitLimitNs).
+static inline cudaError_t set_wait_limit_of_unit(uint64_t ns) {
+    const unsigned long long v = ns ? ns : kWaitLimitNs;
+    return cudaMemcpyToSymbol(g_wait_limit_ns, &v, sizeof(v));
+}
+
 // Bounded wait for the phase with the given parity.  Returns false when the
-// CTA-wide abort flag is raised or after kWaitLimitNs; in the latter case the
-// waiter raises the abort flag and records SWIATTN_DEVERR_TIMEOUT in *err.
+// CTA-wide abort flag is raised or after g_wait_limit_ns; in the latter case
+// the waiter raises the abort flag and records SWIATTN_DEVERR_TIMEOUT in *err.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           unsigned int* err) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    for (;;) {
-        if (mbar_try_wait_sleep(bar, parity)) return true;
+    const uint64_t limit = g_wait_limit_ns;
+    // A limit below 0.1 ms polls without suspending (a suspended waiter may
+    // sleep until the phase completes, past such a limit) and also bounds the
+    // number of polls (the global timer may tick more coarsely than such a
+    // limit); otherwise the waiter suspends for up to 0.1 ms at a time.
+    const bool poll = limit < 100000ull;
+    for (uint64_t polls = 1;; ++polls) {
+        if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait_sleep(bar, parity, 100000u))
+            return true;
         if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > limit || (poll && polls > limit)) {
             *abort_flag = 1;
             atomicOr(err, kDevErrTimeout);
             return false;
@@ -164,6 +196,20 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
         : "memory");
 }
 
+// Copies a 128-row x 32-byte matrix (one 16-element K slice of a bf16
+// operand tile, described by a shared-memory descriptor) from shared memory
+// into TMEM lanes 0-127, 8 consecutive 32-bit columns from taddr: lane r holds
+// row r's 16 elements, two per column, in order -- the layout the MMA reads an
+// A operand from TMEM in.  Asynchronous; executed in issue order with this
+// thread's later MMAs, and covered by its later commits.  Warp-converged,
+// elected issue.
+__device__ __forceinline__ void tmem_cp_128x256b_w(uint32_t taddr, uint64_t s_desc) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.cp.cta_group::1.128x256b [%0], %1;\n\t}" ::"r"(taddr), "l"(s_desc)
+        : "memory");
+}
+
 // Arrive once on bar when every tcgen05 operation this thread issued so far
 // has completed.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
@@ -195,6 +241,17 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
           "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
           "=r"(r[31])
         : "r"(taddr)
+        : "memory");
+}
+
+// 32 lanes x 32 bit, 16 consecutive columns from taddr (thread t: lane base + t).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
         : "memory");
 }
 

@@ -1,6 +1,6 @@
 // Router logit of one token by one warp (SwiAttn report, section 2, router
 // design): logit_t = <h_t, w> + b, gate_t = 1(logit_t > 0), fp32 accumulate.
-// The hidden row streams through 16-byte loads, four in flight per lane.
+// The hidden row streams through 16-byte loads, eight in flight per lane.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -28,8 +28,6 @@ __device__ __forceinline__ float route_dot16(const uint4& a, const uint4& b, flo
     return fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, x.w * y.w)));
 }
 
-// Whole warp: token t's logit and gate (lane 0 writes them).  nvec = 16-byte
-// vectors per hidden row.
 template <typename T>
 __device__ __forceinline__ void route_token(const uint4* __restrict__ h, const uint4* __restrict__ w,
                                             float bias, int64_t t, int nvec, float* __restrict__ logits,
@@ -38,11 +36,14 @@ __device__ __forceinline__ void route_token(const uint4* __restrict__ h, const u
     const uint4* row = h + t * nvec;
     float acc = 0.f;
     int v = lane;
-    for (; v + 96 < nvec; v += 128) {
-        const uint4 a0 = __ldcs(row + v), a1 = __ldcs(row + v + 32);
-        const uint4 a2 = __ldcs(row + v + 64), a3 = __ldcs(row + v + 96);
-        acc += route_dot16(a0, __ldg(w + v), T()) + route_dot16(a1, __ldg(w + v + 32), T()) +
-               route_dot16(a2, __ldg(w + v + 64), T()) + route_dot16(a3, __ldg(w + v + 96), T());
+    for (; v + 224 < nvec; v += 256) {
+        uint4 a[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) a[u] = __ldcs(row + v + 32 * u);
+        float p = 0.f;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) p += route_dot16(a[u], __ldg(w + v + 32 * u), T());
+        acc += p;
     }
     for (; v < nvec; v += 32) acc += route_dot16(__ldcs(row + v), __ldg(w + v), T());
 #pragma unroll

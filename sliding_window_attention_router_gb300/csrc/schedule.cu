@@ -5,8 +5,9 @@
 // are compacted (ascending i) so that 128 of them share one query tile that
 // walks keys [0, max i]; every other row is served by the 128-row band tile
 // that holds it, which walks only the window keys.  Work items are pairs of
-// such tiles (256 rows, one head); the list is sorted by cost (key blocks),
-// longest first, for the persistent attention kernel.
+// such tiles (256 rows, one head).  For the persistent attention kernel the
+// list holds the far pairs longest first (cost in key blocks), then the band
+// pairs in row order, the heads of a pair adjacent.
 
 #include "route_gemv.cuh"
 #include "swiattn_internal.h"
@@ -154,9 +155,9 @@ __device__ __forceinline__ bool gate_byte(const uint4& v, int u) {
 // rows of a contiguous chunk of rows (a multiple of 16, so 16-byte gate groups
 // never straddle two threads), one block scan, then each thread writes its far
 // rows (ascending i) and the prefix counts of the 128-row tiles that start in
-// its chunk.  Then the counting sort of 256-row pairs by descending cost, Hq
-// items per pair (one per query head), and the reset of the attention kernel's
-// work counter.  Far queries are not copied here: the attention kernel gathers
+// its chunk.  Then the work list, Hq items per 256-row pair (one per query
+// head): far pairs sorted by descending cost, then band pairs in order; and
+// the reset of the attention kernel's work counter.  Far queries are not copied here: the attention kernel gathers
 // them by row index when it loads a far tile.
 constexpr int kPlanThreads = 1024;
 constexpr int kBucketsPerThread = kCostBuckets / kPlanThreads;
@@ -199,13 +200,16 @@ __device__ void plan_block(const uint8_t* __restrict__ gate, int B, int N, int H
     }
     __syncthreads();   // the lists, counts and prefixes above are read below
 
+    // Far pairs: counting sort by descending cost (they cost up to N / 128
+    // key blocks per tile, so longest first matters for the balance of the
+    // persistent kernel).
     const int U = B * 2 * NP;
     for (int c = threadIdx.x; c < kCostBuckets; c += blockDim.x) hist[c] = 0;
     __syncthreads();
     for (int u = threadIdx.x; u < U; u += blockDim.x) {
         int b, kind, pair;
         const int cost = pair_cost(u, routed_list, routed_count, tile_prefix, N, W, S, NT, NP, b, kind, pair);
-        if (cost > 0) atomicAdd(&hist[min(cost, kCostBuckets - 1)], 1);
+        if (kind == kItemFar && cost > 0) atomicAdd(&hist[min(cost, kCostBuckets - 1)], 1);
     }
     __syncthreads();
     // Exclusive offsets in descending cost order: thread t owns buckets
@@ -214,8 +218,8 @@ __device__ void plan_block(const uint8_t* __restrict__ gate, int B, int N, int H
 #pragma unroll
     for (int k = 0; k < kBucketsPerThread; ++k)
         own += hist[kCostBuckets - 1 - (threadIdx.x * kBucketsPerThread + k)];
-    int total;
-    int run = block_exclusive_scan(own, warp_tot, &total);
+    int far_total;
+    int run = block_exclusive_scan(own, warp_tot, &far_total);
 #pragma unroll
     for (int k = 0; k < kBucketsPerThread; ++k) {
         const int c = kCostBuckets - 1 - (threadIdx.x * kBucketsPerThread + k);
@@ -227,12 +231,36 @@ __device__ void plan_block(const uint8_t* __restrict__ gate, int B, int N, int H
     for (int u = threadIdx.x; u < U; u += blockDim.x) {
         int b, kind, pair;
         const int cost = pair_cost(u, routed_list, routed_count, tile_prefix, N, W, S, NT, NP, b, kind, pair);
-        if (cost <= 0) continue;
+        if (kind != kItemFar || cost <= 0) continue;
         const int pos = atomicAdd(&hist[min(cost, kCostBuckets - 1)], 1);
         for (int h = 0; h < Hq; ++h) items[(size_t)pos * Hq + h] = WorkItem{kind, b, h, pair};
     }
+    // Band pairs follow, in (batch, pair) order with the heads of a pair
+    // adjacent: their costs are nearly equal (the window and one tile), and
+    // the CTAs that run them at the same time then walk overlapping windows
+    // of the same heads, which L2 serves.  Each thread takes a contiguous run
+    // of pairs; one scan places the runs.
+    const int V = B * NP;
+    const int CB = cdiv(V, kPlanThreads);
+    const int v0 = min(V, static_cast<int>(threadIdx.x) * CB), v1 = min(V, v0 + CB);
+    int nb = 0;
+    for (int v = v0; v < v1; ++v) {
+        int b, kind, pair;
+        const int u = (v / NP) * 2 * NP + NP + v % NP;
+        nb += pair_cost(u, routed_list, routed_count, tile_prefix, N, W, S, NT, NP, b, kind, pair) > 0;
+    }
+    int band_total;
+    int pos = far_total + block_exclusive_scan(nb, warp_tot, &band_total);
+    for (int v = v0; v < v1; ++v) {
+        int b, kind, pair;
+        const int u = (v / NP) * 2 * NP + NP + v % NP;
+        if (pair_cost(u, routed_list, routed_count, tile_prefix, N, W, S, NT, NP, b, kind, pair) <= 0)
+            continue;
+        for (int h = 0; h < Hq; ++h) items[(size_t)pos * Hq + h] = WorkItem{kind, b, h, pair};
+        ++pos;
+    }
     if (threadIdx.x == 0) {
-        n_items[0] = total * Hq;
+        n_items[0] = (far_total + band_total) * Hq;
         n_items[1] = 0;   // work counter the attention kernel claims items from
     }
 }

@@ -140,6 +140,13 @@ void swiattn_set_profile_events(void* start, void* stop) {
     g_prof_stop.store(static_cast<cudaEvent_t>(stop), std::memory_order_release);
 }
 
+int swiattn_set_wait_limit_ns(uint64_t ns) {
+    if (prefill_set_wait_limit(ns) != cudaSuccess || dual_set_wait_limit(ns) != cudaSuccess ||
+        bwd_set_wait_limit(ns) != cudaSuccess)
+        return SWIATTN_ECUDA;
+    return SWIATTN_OK;
+}
+
 int swiattn_num_sms(void) {
     DeviceInfo di;
     return device_info(di) ? di.sms : -1;

@@ -15,9 +15,17 @@ constexpr unsigned int kDevErrLayout = 2u;   // shared memory not laid out as a 
 constexpr unsigned int kDevErrInput = 4u;    // a device-resident input was out of range
 
 // A healthy wait in these kernels lasts microseconds; after this long a
-// kernel gives up, flags a timeout and returns.
+// kernel gives up, flags a timeout and returns (the default; a test may lower
+// it through swiattn_set_wait_limit_ns).  Waits while aborting keep their own
+// fixed limit.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
 constexpr uint64_t kDrainLimitNs = 100000000ull;   // 0.1 s, waits while aborting
+
+// Per translation unit setters of the wait limit (current device; 0 restores
+// the default): the routed prefill, the dual-branch forward, the backward.
+cudaError_t prefill_set_wait_limit(uint64_t ns);
+cudaError_t dual_set_wait_limit(uint64_t ns);
+cudaError_t bwd_set_wait_limit(uint64_t ns);
 
 // Lets `kernel` use `bytes` of dynamic shared memory on the current device.
 // The attribute belongs to the device's context, so it is set once per
