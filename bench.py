@@ -44,15 +44,15 @@ L2_FLUSH_BYTES = 256 << 20
 # SHA-256 of the kernel's source files at capture time; a kernel whose source
 # has changed since reports null.
 MEASURED_TRAFFIC = {
-    # prefill_kernel, long-context prefill N=32768 f=0.13: 1 142 919 424 read + 127 038 720 written
-    ("prefill", "2291c7922c10153b"): 1142919424 + 127038720,
-    # decode_split_kernel, 16 x 32768 decode: 654 409 472 read + 3 369 472 written
-    ("decode", "a9ba9aaf8fae9108"): 654409472 + 3369472,
-    # dual_kernel, dual-branch workload B=2 N=8192 GQA 16/4: 158 522 880 read + 271 861 760 written
-    ("dual", "cd1b81dfd8c7475b"): 158522880 + 271861760,
-    # dkdv_kernel + dq_kernel, backward on the dual workload: (314 070 528 + 21 010 176)
-    # + (257 931 520 + 47 250 432)
-    ("backward", "8cc041104e26e910"): 314070528 + 21010176 + 257931520 + 47250432,
+    # prefill_kernel, long-context prefill N=32768 f=0.13: 1 110 817 280 read + 123 436 032 written
+    ("prefill", "a40402c51fd49dcd"): 1110817280 + 123436032,
+    # decode_split2_kernel, 16 x 32768 decode: 654 458 112 read + 3 557 376 written
+    ("decode", "f7f22a7889623302"): 654458112 + 3557376,
+    # dual_kernel, dual-branch workload B=2 N=8192 GQA 16/4: 148 151 040 read + 271 419 648 written
+    ("dual", "8d3e62db38f8aca6"): 148151040 + 271419648,
+    # dkdv_kernel + dq_kernel, backward on the dual workload: (314 131 968 + 22 016 768)
+    # + (258 405 376 + 47 600 640)
+    ("backward", "061e05be4060ff07"): 314131968 + 22016768 + 258405376 + 47600640,
 }
 # Source text each stored count depends on: whole files, or a file up to a
 # marker (the device code of a kernel file, before its host launcher; the
@@ -691,7 +691,7 @@ def run_ours(args, dist: Dist):
                          "peak": hbm, "unit": "GB/s",
                          "frac": round(dec["bytes"] / dk / 1e9 / hbm, 4),
                          "traffic": measured_traffic("decode"),
-                         "kernel": "decode_split_kernel"},
+                         "kernel": "decode_split2_kernel"},
             "workload": "decode bf16: 16 sequences x 32768 cached tokens, H=16, d=128, W=1024, "
                         "gate Bernoulli(0.13)",
             "sweep": {"columns": ["n_routed", "step GB/s", "kernel GB/s", "kernel frac of HBM"],
@@ -838,6 +838,25 @@ def run_backward_only(args):
                       "useful_tflop": bw["flops"] / 1e12}), flush=True)
 
 
+def run_section_only(args):
+    """The decode (16 x 32K) or dual-branch (8K) section alone (a profiling
+    aid, not the bench line)."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    import sliding_window_attention_router_gb300 as swa
+    swa._load()
+    timer = Timer(dev)
+    if args.only == "decode":
+        r = decode_section(swa, timer, dev, args.steps, args.warmup, 0)
+        k = statistics.mean(r["kern_ms"]) / 1e3
+        print(json.dumps({"section": "decode", "kernel_gbs": r["bytes"] / k / 1e9,
+                          "bytes_per_step": r["bytes"], "n_routed": r["n_routed"]}), flush=True)
+    else:
+        r = dual_section(swa, timer, dev, args.steps, args.warmup, 0)
+        k = statistics.mean(r["kern_ms"]) / 1e3
+        print(json.dumps({"section": "dual", "kernel_tflops": r["flops"] / k / 1e12}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -854,6 +873,8 @@ def main():
                     help="seconds of oracle work per step of the reference arm")
     ap.add_argument("--only-backward", choices=["dual_8k", "prefill_32k"], default=None,
                     help="profiling runs only: time just the training backward on one workload")
+    ap.add_argument("--only", choices=["decode", "dual"], default=None,
+                    help="profiling runs only: time just the decode or the dual-branch section")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -863,6 +884,8 @@ def main():
             run_reference(args, dist)
         elif args.only_backward:
             run_backward_only(args)
+        elif args.only:
+            run_section_only(args)
         else:
             run_ours(args, dist)
     finally:
