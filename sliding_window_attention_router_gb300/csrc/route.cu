@@ -1,6 +1,6 @@
 // Router GEMV + hard gate (SwiAttn report, section 2, router design):
 // logit_t = <h_t, w> + b, gate_t = 1(sigmoid(logit_t) > 0.5) = 1(logit_t > 0).
-// HBM-bound: one warp per token (route_gemv.cuh).
+// HBM-bound: each warp takes two tokens at a time (route_gemv.cuh).
 
 #include "route_gemv.cuh"
 #include "swiattn_internal.h"
@@ -18,7 +18,9 @@ __global__ void __launch_bounds__(256) route_kernel(const uint4* __restrict__ h,
                                                     uint8_t* __restrict__ gate) {
     const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    for (int64_t t = warp0; t < tokens; t += nwarps) route_token<T>(h, w, bias, t, nvec, logits, gate);
+    int64_t t = warp0;
+    for (; t + nwarps < tokens; t += 2 * nwarps) route_token2<T>(h, w, bias, t, t + nwarps, nvec, logits, gate);
+    if (t < tokens) route_token<T>(h, w, bias, t, nvec, logits, gate);
 }
 
 }  // namespace

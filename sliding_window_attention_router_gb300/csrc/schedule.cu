@@ -6,8 +6,9 @@
 // walks keys [0, max i]; every other row is served by the 128-row band tile
 // that holds it, which walks only the window keys.  Work items are pairs of
 // such tiles (256 rows, one head).  For the persistent attention kernel the
-// list holds the far pairs longest first (cost in key blocks), then the band
-// pairs in row order, the heads of a pair adjacent.
+// list holds the far pairs head by head, longest first within a head (cost
+// in key blocks), then the band pairs in row order, the heads of a pair
+// adjacent.
 
 #include "route_gemv.cuh"
 #include "swiattn_internal.h"
@@ -202,7 +203,10 @@ __device__ void plan_block(const uint8_t* __restrict__ gate, int B, int N, int H
 
     // Far pairs: counting sort by descending cost (they cost up to N / 128
     // key blocks per tile, so longest first matters for the balance of the
-    // persistent kernel).
+    // persistent kernel), listed head by head: the CTAs that take them at the
+    // same time then walk the K/V prefix of few heads, from key 0 up, and
+    // share it in L2 (with the heads interleaved, the 32K workload read
+    // 2.2x its algorithmic bytes from HBM; head by head, 1.45x).
     const int U = B * 2 * NP;
     for (int c = threadIdx.x; c < kCostBuckets; c += blockDim.x) hist[c] = 0;
     __syncthreads();
@@ -233,7 +237,7 @@ __device__ void plan_block(const uint8_t* __restrict__ gate, int B, int N, int H
         const int cost = pair_cost(u, routed_list, routed_count, tile_prefix, N, W, S, NT, NP, b, kind, pair);
         if (kind != kItemFar || cost <= 0) continue;
         const int pos = atomicAdd(&hist[min(cost, kCostBuckets - 1)], 1);
-        for (int h = 0; h < Hq; ++h) items[(size_t)pos * Hq + h] = WorkItem{kind, b, h, pair};
+        for (int h = 0; h < Hq; ++h) items[(size_t)h * far_total + pos] = WorkItem{kind, b, h, pair};
     }
     // Band pairs follow, in (batch, pair) order with the heads of a pair
     // adjacent: their costs are nearly equal (the window and one tile), and
@@ -273,7 +277,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(
 }
 
 // Router GEMV fused with the schedule: every CTA computes logits and gates of
-// its tokens (one warp per token); the CTA that finishes last (ticket from a
+// its tokens (each warp two tokens at a time); the CTA that finishes last (ticket from a
 // counter zeroed before the launch) then plans the prefill over all gates.
 // Every thread fences its gate writes before the CTA takes its ticket, and
 // the last CTA fences after taking it, before reading the gates.
@@ -288,7 +292,9 @@ __global__ void __launch_bounds__(kPlanThreads) route_plan_kernel(
     const int64_t tokens = (int64_t)B * N;
     const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    for (int64_t t = warp0; t < tokens; t += nwarps) route_token<T>(h, w, bias, t, nvec, logits, gate);
+    int64_t t = warp0;
+    for (; t + nwarps < tokens; t += 2 * nwarps) route_token2<T>(h, w, bias, t, t + nwarps, nvec, logits, gate);
+    if (t < tokens) route_token<T>(h, w, bias, t, nvec, logits, gate);
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
