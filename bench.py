@@ -44,8 +44,9 @@ L2_FLUSH_BYTES = 256 << 20
 # SHA-256 of the kernel's source files at capture time; a kernel whose source
 # has changed since reports null.
 MEASURED_TRAFFIC = {
-    # prefill_kernel, long-context prefill N=32768 f=0.13: 1 110 817 280 read + 123 436 032 written
-    ("prefill", "a40402c51fd49dcd"): 1110817280 + 123436032,
+    # prefill_kernel, long-context prefill N=32768 f=0.13 (far items head by head):
+    # 686 008 064 read + 120 857 088 written
+    ("prefill", "055e5142999f96a7"): 686008064 + 120857088,
     # decode_split2_kernel, 16 x 32768 decode: 654 458 112 read + 3 557 376 written
     ("decode", "f7f22a7889623302"): 654458112 + 3557376,
     # dual_kernel, dual-branch workload B=2 N=8192 GQA 16/4: 148 151 040 read + 271 419 648 written
@@ -56,8 +57,10 @@ MEASURED_TRAFFIC = {
 }
 # Source text each stored count depends on: whole files, or a file up to a
 # marker (the device code of a kernel file, before its host launcher; the
-# decode split kernel, before the combine).
-KERNEL_SOURCES = {"prefill": (("attn_prefill.cu", "cudaError_t launch_prefill_tc("), "ptx.cuh"),
+# decode split kernel, before the combine).  The prefill's count also depends
+# on the order of its work list (schedule.cu).
+KERNEL_SOURCES = {"prefill": (("attn_prefill.cu", "cudaError_t launch_prefill_tc("), "ptx.cuh",
+                              "schedule.cu"),
                   "decode": (("decode.cu", "// Log-sum-exp merge of the chunk partials"),),
                   "dual": (("attn_dual.cu", "cudaError_t launch_dual_tc("), "ptx.cuh"),
                   "backward": (("attn_bwd.cu", "cudaError_t launch_bwd_dkdv("), "ptx.cuh")}

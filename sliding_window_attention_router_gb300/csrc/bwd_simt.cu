@@ -208,7 +208,11 @@ __global__ void __launch_bounds__(256) route_bwd_logit_kernel(
 constexpr int kRouteChunk = 64;   // tokens per block of the dh/dw pass
 
 // dh = d_logit * w and per-chunk partial sums of d_logit * h (one block per
-// chunk of kRouteChunk tokens; threads stride over 8-column groups).
+// chunk of kRouteChunk tokens; threads stride over 8-column groups).  The
+// h rows of kRouteUnroll tokens are loaded before any is used, so that many
+// loads are in flight per thread; the sums still run in token order.
+constexpr int kRouteUnroll = 8;
+
 template <typename T>
 __global__ void __launch_bounds__(256) route_bwd_dh_kernel(
     const T* __restrict__ h, const T* __restrict__ w, const float* __restrict__ d_logits,
@@ -220,19 +224,27 @@ __global__ void __launch_bounds__(256) route_bwd_dh_kernel(
         load8<T>(w + c, wv);
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-        for (int64_t t = t0; t < t1; ++t) {
-            const float dl = d_logits[t];
-            if (part) {
-                float hv[8];
-                load8<T>(h + t * d_model + c, hv);
+        for (int64_t tb = t0; tb < t1; tb += kRouteUnroll) {
+            float hv[kRouteUnroll][8], dl[kRouteUnroll];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[e] += dl * hv[e];
+            for (int u = 0; u < kRouteUnroll; ++u) {
+                const int64_t t = min(tb + u, t1 - 1);   // clamp: duplicates are not used below
+                dl[u] = d_logits[t];
+                if (part) load8<T>(h + t * d_model + c, hv[u]);
             }
-            if (dh) {
-                float o[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) o[e] = dl * wv[e];
-                store8<T>(dh + t * d_model + c, o);
+            for (int u = 0; u < kRouteUnroll; ++u) {
+                if (tb + u >= t1) break;
+                if (part) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[e] += dl[u] * hv[u][e];
+                }
+                if (dh) {
+                    float o[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[e] = dl[u] * wv[e];
+                    store8<T>(dh + (tb + u) * d_model + c, o);
+                }
             }
         }
         if (part) store8<float>(part + (int64_t)blockIdx.x * d_model + c, acc);
@@ -240,19 +252,20 @@ __global__ void __launch_bounds__(256) route_bwd_dh_kernel(
 }
 
 // dw[c] = sum over chunks of the partials: a block takes 32 columns and warp
-// w sums chunks w, w+8, w+16, ... for its lane's column, then the eight warp
-// sums are added in warp order (a fixed order, so dw is bitwise repeatable).
-// db = sum d_logits (block 0, fixed-order tree).
+// w sums chunks w, w+16, w+32, ... for its lane's column, then the sixteen
+// warp sums are added in warp order (a fixed order, so dw is bitwise
+// repeatable).  db = sum d_logits (the last block, fixed-order tree).
 constexpr int kReduceCols = 32;
-constexpr int kReduceWarps = 8;
+constexpr int kReduceWarps = 16;
 
-__global__ void __launch_bounds__(256) route_bwd_reduce_kernel(
+__global__ void __launch_bounds__(kReduceWarps * 32) route_bwd_reduce_kernel(
     const float* __restrict__ part, int64_t chunks, int d_model, const float* __restrict__ d_logits,
     int64_t tokens, float* __restrict__ dw, float* __restrict__ db) {
     __shared__ float wsum[kReduceWarps][kReduceCols];
     const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
     const int c = blockIdx.x * kReduceCols + lane;
-    const bool do_dw = dw && part;
+    const bool last = blockIdx.x == gridDim.x - 1;
+    const bool do_dw = dw && part && c - lane < d_model;
     if (do_dw) {
         float acc = 0.f;
         if (c < d_model) {
@@ -268,8 +281,8 @@ __global__ void __launch_bounds__(256) route_bwd_reduce_kernel(
         for (int u = 0; u < kReduceWarps; ++u) t += wsum[u][lane];
         dw[c] = t;
     }
-    if (db && blockIdx.x == 0) {
-        __shared__ float red[256];
+    if (db && last) {
+        __shared__ float red[kReduceWarps * 32];
         float acc = 0.f;
         for (int64_t t = threadIdx.x; t < tokens; t += blockDim.x) acc += d_logits[t];
         red[threadIdx.x] = acc;
@@ -303,8 +316,9 @@ cudaError_t route_backward_t(const void* h, const void* w, const float* logits, 
         if (e != cudaSuccess) return e;
     }
     if (dw || db) {
-        const int blocks_r = (d_model + kReduceCols - 1) / kReduceCols;
-        route_bwd_reduce_kernel<<<blocks_r > 0 ? blocks_r : 1, kReduceWarps * 32, 0, s>>>(
+        // One block per 32 columns of dw, and one more for db.
+        const int blocks_r = (dw ? (d_model + kReduceCols - 1) / kReduceCols : 0) + 1;
+        route_bwd_reduce_kernel<<<blocks_r, kReduceWarps * 32, 0, s>>>(
             ws, chunks, d_model, d_logits, tokens, dw, db);
         e = cudaGetLastError();
     }
