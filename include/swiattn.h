@@ -159,7 +159,9 @@ size_t swiattn_decode_workspace(int B, int Lmax, int Hq, int Hkv, int d, int W, 
  * Hq = Hkv; 256 for Hq = 8*Hkv).  A larger request returns
  * SWIATTN_EUNSUPPORTED and launches nothing; so do swiattn_decode_anchored,
  * swiattn_decode_paged and swiattn_decode_noalloc, whose limits are these.
- * workspace: at least swiattn_decode_workspace(...) bytes, scratch only. */
+ * workspace: at least swiattn_decode_workspace(...) bytes, scratch only; for
+ * B <= 32 the call first clears a 4-byte chunk counter in it on `stream`
+ * (cudaMemsetAsync), then launches its two kernels there. */
 int swiattn_decode(const void* q, const void* k_cache, const void* v_cache,
                    const int32_t* seq_lens, const uint8_t* gate, void* o, float* lse, int B,
                    int Lmax, int Hq, int Hkv, int d, int W, float scale, int dtype,
@@ -191,9 +193,10 @@ int swiattn_decode_anchored(const void* q, const void* k_cache, const void* v_ca
  * swiattn_get_device_error) are those of swiattn_decode.
  *  - The split-KV partials go to one fixed 16 MiB device array inside the
  *    library, which every GPU that loads the library holds until the process
- *    exits.  A call whose partials, B * max(9, ceil(Lmax/256) + 1) * Hq *
- *    (d+2) * 4 bytes rounded up to 256, exceed 16 MiB returns SWIATTN_EINVAL
- *    and launches nothing (e.g. B=16, Hq=16, d=128 allows Lmax up to 32 000).
+ *    exits.  A call whose partials, B * max(17, ceil(Lmax/256) + 1) * Hq *
+ *    (d+2) * 4 bytes rounded up to 256, plus 256 bytes, exceed 16 MiB returns
+ *    SWIATTN_EINVAL and launches nothing (e.g. B=16, Hq=16, d=128 allows Lmax
+ *    up to 32 000).
  *  - The call allocates nothing.  Its first call on a device looks up that
  *    array's device address (once per device, with the device current); make
  *    that first call before any stream capture.

@@ -16,6 +16,7 @@
 
 #include <cuda_bf16.h>
 #include <math.h>
+#include <algorithm>
 #include <atomic>
 
 namespace swi {
@@ -23,7 +24,7 @@ namespace {
 
 constexpr int kChunk = 256;   // largest chunk (tokens per split)
 constexpr int kMinChunk = 64;
-constexpr int kSplit = 8;     // a visit shorter than kSplit * kChunk splits into about kSplit chunks
+constexpr int kSplit = 16;    // a visit shorter than kSplit * kChunk splits into about kSplit chunks
 constexpr int kUnroll = 8;    // tokens in flight per thread
 
 template <typename T>
@@ -71,9 +72,9 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
 // the window does not reach, [0, na) with na = min(S, lo).  A length outside
 // [1, Lmax] is clamped into it (the split kernel reports it).  Chunks never
 // straddle the two segments: the first ceil(na / chunk) chunks read anchors.
-// The chunk length is about (na + n) / 8 rounded up to a power of two within
+// The chunk length is about (na + n) / 16 rounded up to a power of two within
 // [64, 256]: short visited ranges (windows) still split over several CTAs,
-// long ones stream 256 tokens per CTA.  It depends on the sequence alone, so
+// long ones stream 256 tokens per chunk.  It depends on the sequence alone, so
 // a sequence's result does not depend on the rest of the batch.
 struct Visit {
     int lo, n, na, nca;   // nca: anchor chunks
@@ -104,40 +105,6 @@ __device__ __forceinline__ int chunks_of(const Visit& v) {
 // Batches up to this size dispatch their chunks longest visit first.
 constexpr int kOrderMaxB = 32;
 
-// CTA (blockIdx.x, blockIdx.y) -> (sequence b, chunk c).  For B <= 32 warp 0
-// enumerates the real chunks of the batch, sequences with more chunks first
-// (ties by index), and the linear CTA index picks one: the longest visits are
-// dispatched first, and every real chunk precedes every CTA that has no chunk
-// (b = -1), so no CTA slot is spent on empty ones before real work starts.
-// Which CTA computes a chunk does not change that chunk's partial, so the
-// results stay batch-invariant.  Larger batches keep the direct mapping
-// (b = blockIdx.y, c = blockIdx.x; chunks past the visit are empty).
-__device__ __forceinline__ void cta_chunk(const int32_t* seq_lens, const uint8_t* gate, int B,
-                                          int W, int S, int Lmax, int& b, int& c) {
-    if (B > kOrderMaxB) {
-        b = blockIdx.y;
-        c = blockIdx.x;
-        return;
-    }
-    __shared__ int s_bc[2];
-    if (threadIdx.x < 32) {
-        const int l = threadIdx.x;
-        const int n = l < B ? chunks_of(visited(seq_lens, gate, l, W, S, Lmax)) : 0;
-        int start = 0;   // chunks of the sequences ordered before sequence l
-        for (int o = 0; o < B; ++o) {
-            const int no = __shfl_sync(0xffffffffu, n, o);
-            if (no > n || (no == n && o < l)) start += no;
-        }
-        const int64_t i = blockIdx.x + (int64_t)blockIdx.y * gridDim.x;
-        const unsigned hit = __ballot_sync(0xffffffffu, l < B && i >= start && i < start + n);
-        if (l == 0) s_bc[0] = hit ? __ffs(hit) - 1 : -1;
-        if (hit && l == __ffs(hit) - 1) s_bc[1] = static_cast<int>(i - start);
-    }
-    __syncthreads();
-    b = s_bc[0];
-    c = s_bc[1];
-}
-
 // Where token rows live: a contiguous cache [B, Lmax, Hkv, d] (Lmax rows per
 // sequence), or pages [num_pages, page_size, Hkv, d] found through a block
 // table [B, max_pages] (page_size = 1 << page_lg).
@@ -156,33 +123,66 @@ __device__ __forceinline__ void decode_split_body(const T* __restrict__ q, const
                                     const T* __restrict__ vc, const int32_t* __restrict__ seq_lens,
                                     const uint8_t* __restrict__ gate, float* __restrict__ part,
                                     int Lmax, int Hq, int Hkv, int W, int S, float scale_log2,
-                                    int B, int max_chunks, Paging pg) {
+                                    int B, int max_chunks, Paging pg, int* claim) {
     constexpr int VEC = Vec<T>::N;
     constexpr int LPH = D / VEC;   // lanes per KV head
-    int b, c;
-    cta_chunk(seq_lens, gate, B, W, S, Lmax, b, c);
-    if (b < 0) {
-        // No chunk for this CTA: let the dependent combine launch.
-        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-        return;
+    // For B <= 32 the CTAs are persistent: warp 0 keeps the batch's chunk
+    // ranking (sequences with more chunks first, ties by index) in registers
+    // and claims chunk after chunk for the CTA from the workspace counter, so
+    // the longest visits start first and no CTA is launched without work.
+    // Larger batches map CTA (x, y) to chunk x of sequence y, one per CTA.
+    __shared__ int s_bc[2][2];
+    int rk_n = 0, rk_start = 0, rk_total = 0;
+    if (B <= kOrderMaxB && threadIdx.x < 32) {
+        const int l = threadIdx.x;
+        rk_n = l < B ? chunks_of(visited(seq_lens, gate, l, W, S, Lmax)) : 0;
+        for (int o = 0; o < B; ++o) {
+            const int no = __shfl_sync(0xffffffffu, rk_n, o);
+            if (no > rk_n || (no == rk_n && o < l)) rk_start += no;
+            rk_total += no;
+        }
     }
+    for (int it = 0;; ++it) {
+    // Chunk of this iteration (b < 0: none).  The two slots alternate, so
+    // warp 0 never overwrites a slot another warp has yet to read.
+    int* bc = s_bc[it & 1];
+    if (threadIdx.x < 32) {
+        const int l = threadIdx.x;
+        int cb = -1, cc = 0;
+        if (B > kOrderMaxB) {
+            if (it == 0 && (int)blockIdx.x < chunks_of(visited(seq_lens, gate, blockIdx.y, W, S, Lmax))) {
+                cb = blockIdx.y;
+                cc = blockIdx.x;
+            }
+        } else {
+            int i = 0;
+            if (l == 0) i = atomicAdd(claim, 1);
+            i = __shfl_sync(0xffffffffu, i, 0);
+            if (i < rk_total) {
+                const unsigned hit = __ballot_sync(0xffffffffu, l < B && i >= rk_start && i < rk_start + rk_n);
+                cb = __ffs(hit) - 1;
+                cc = i - __shfl_sync(0xffffffffu, rk_start, cb);
+            }
+        }
+        if (l == 0) {
+            bc[0] = cb;
+            bc[1] = cc;
+        }
+    }
+    __syncthreads();
+    const int b = bc[0], c = bc[1];
+    if (b < 0) break;
     const Visit vis = visited(seq_lens, gate, b, W, S, Lmax);
     if (c == 0 && threadIdx.x == 0 && pg.err) {
         const int raw = seq_lens[b];
         if (raw < 1 || raw > Lmax) atomicOr(pg.err, kDevErrInput);
     }
-    int t0, t1;   // this chunk's cache entries
+    int t0, t1;   // this chunk's cache entries (the chunk is never empty)
     if (c < vis.nca) {
         t0 = c * vis.chunk;
         t1 = min(vis.na, t0 + vis.chunk);
     } else {
-        const int cw = c - vis.nca;
-        if (cw * vis.chunk >= vis.n) {
-            // No entries for this chunk: let the dependent combine launch.
-            asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-            return;
-        }
-        t0 = vis.lo + cw * vis.chunk;
+        t0 = vis.lo + (c - vis.nca) * vis.chunk;
         t1 = min(vis.lo + vis.n, t0 + vis.chunk);
     }
     // Paged: the physical page of every page this chunk touches, in shared
@@ -328,6 +328,7 @@ __device__ __forceinline__ void decode_split_body(const T* __restrict__ q, const
             }
         }
     }
+    }   // next chunk
     // The combine kernel is launched as a programmatic dependent of this one:
     // once every CTA has come this far it may be scheduled (it waits for this
     // grid's completion and memory before reading any partial), which hides
@@ -340,9 +341,9 @@ __global__ void decode_split_kernel(const T* __restrict__ q, const T* __restrict
                                     const T* __restrict__ vc, const int32_t* __restrict__ seq_lens,
                                     const uint8_t* __restrict__ gate, float* __restrict__ part,
                                     int Lmax, int Hq, int Hkv, int W, int S, float scale_log2,
-                                    int B, int max_chunks, Paging pg) {
+                                    int B, int max_chunks, Paging pg, int* claim) {
     decode_split_body<T, D, G, PAGED, 1>(q, kc, vc, seq_lens, gate, part, Lmax, Hq, Hkv, W, S,
-                                         scale_log2, B, max_chunks, pg);
+                                         scale_log2, B, max_chunks, pg, claim);
 }
 
 // Two thread groups per CTA, at most 512 threads.  (Two such CTAs per SM would
@@ -352,9 +353,10 @@ __global__ void __launch_bounds__(512, 1)
 decode_split2_kernel(const T* __restrict__ q, const T* __restrict__ kc,
                      const T* __restrict__ vc, const int32_t* __restrict__ seq_lens,
                      const uint8_t* __restrict__ gate, float* __restrict__ part, int Lmax, int Hq,
-                     int Hkv, int W, int S, float scale_log2, int B, int max_chunks, Paging pg) {
+                     int Hkv, int W, int S, float scale_log2, int B, int max_chunks, Paging pg,
+                     int* claim) {
     decode_split_body<T, D, G, PAGED, 2>(q, kc, vc, seq_lens, gate, part, Lmax, Hq, Hkv, W, S,
-                                         scale_log2, B, max_chunks, pg);
+                                         scale_log2, B, max_chunks, pg, claim);
 }
 
 // Log-sum-exp merge of the chunk partials of one (sequence, query head):
@@ -441,56 +443,83 @@ __global__ void __launch_bounds__(1024) decode_combine_kernel(const float* __res
 // alone, so a sequence's result does not depend on the rest of the batch.
 inline int split_groups(int tpg, int G) { return (tpg <= 256 && G <= 2) ? 2 : 1; }
 
+inline int num_sms_of_current_device() {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64) {
+        const int c = cache[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64) cache[dev].store(sms, std::memory_order_relaxed);
+    return sms;
+}
+
+// B <= 32: as many persistent CTAs as fit on the GPU at once (at most one per
+// chunk slot), after clearing the claim counter on the stream; larger
+// batches: one CTA per (chunk, sequence) slot.
 template <typename T, int D, int G, int NG>
-void launch_split_ng(const void* q, const void* kc, const void* vc, const int32_t* sl,
-                     const uint8_t* gate, float* part, int B, int Lmax, int Hq, int Hkv, int W,
-                     int S, float scale_log2, int max_chunks, const Paging& pg, int tpg,
-                     cudaStream_t s) {
-    const dim3 grid(max_chunks, B);
+cudaError_t launch_split_ng(const void* q, const void* kc, const void* vc, const int32_t* sl,
+                            const uint8_t* gate, float* part, int* claim, int B, int Lmax, int Hq,
+                            int Hkv, int W, int S, float scale_log2, int max_chunks,
+                            const Paging& pg, int tpg, cudaStream_t s) {
     const size_t smem = NG > 1 ? sizeof(float) * tpg * G * (Vec<T>::N + 2) : 0;
     using Kern = void (*)(const T*, const T*, const T*, const int32_t*, const uint8_t*, float*,
-                          int, int, int, int, int, float, int, int, Paging);
+                          int, int, int, int, int, float, int, int, Paging, int*);
     Kern kern;
     if constexpr (NG == 2)
         kern = pg.block_table ? decode_split2_kernel<T, D, G, true> : decode_split2_kernel<T, D, G, false>;
     else
         kern = pg.block_table ? decode_split_kernel<T, D, G, true> : decode_split_kernel<T, D, G, false>;
+    dim3 grid(max_chunks, B);
+    if (B <= kOrderMaxB) {
+        int per_sm = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NG * tpg, smem);
+        if (e != cudaSuccess) return e;
+        const int sms = num_sms_of_current_device();
+        if (sms <= 0) return cudaErrorInvalidDevice;
+        const int64_t slots = (int64_t)max_chunks * B;
+        grid = dim3((unsigned)std::min<int64_t>(slots, (int64_t)sms * std::max(per_sm, 1)));
+        e = cudaMemsetAsync(claim, 0, sizeof(int), s);
+        if (e != cudaSuccess) return e;
+    }
     kern<<<grid, NG * tpg, smem, s>>>(static_cast<const T*>(q), static_cast<const T*>(kc),
                                       static_cast<const T*>(vc), sl, gate, part, Lmax, Hq, Hkv, W,
-                                      S, scale_log2, B, max_chunks, pg);
+                                      S, scale_log2, B, max_chunks, pg, claim);
+    return cudaGetLastError();
 }
 
 template <typename T, int D, int G>
 cudaError_t launch_split(const void* q, const void* kc, const void* vc, const int32_t* sl,
-                         const uint8_t* gate, float* part, int B, int Lmax, int Hq, int Hkv, int W,
-                         int S, float scale_log2, int max_chunks, const Paging& pg, cudaStream_t s) {
+                         const uint8_t* gate, float* part, int* claim, int B, int Lmax, int Hq,
+                         int Hkv, int W, int S, float scale_log2, int max_chunks, const Paging& pg,
+                         cudaStream_t s) {
     const int tpg = (Hkv * (D / Vec<T>::N) + 31) / 32 * 32;
     if constexpr (G <= 2) {
-        if (split_groups(tpg, G) == 2) {
-            launch_split_ng<T, D, G, 2>(q, kc, vc, sl, gate, part, B, Lmax, Hq, Hkv, W, S,
-                                        scale_log2, max_chunks, pg, tpg, s);
-            return cudaGetLastError();
-        }
+        if (split_groups(tpg, G) == 2)
+            return launch_split_ng<T, D, G, 2>(q, kc, vc, sl, gate, part, claim, B, Lmax, Hq, Hkv,
+                                               W, S, scale_log2, max_chunks, pg, tpg, s);
     }
-    launch_split_ng<T, D, G, 1>(q, kc, vc, sl, gate, part, B, Lmax, Hq, Hkv, W, S, scale_log2,
-                                max_chunks, pg, tpg, s);
-    return cudaGetLastError();
+    return launch_split_ng<T, D, G, 1>(q, kc, vc, sl, gate, part, claim, B, Lmax, Hq, Hkv, W, S,
+                                       scale_log2, max_chunks, pg, tpg, s);
 }
 
 template <typename T, int D>
 cudaError_t launch_typed(const void* q, const void* kc, const void* vc, const int32_t* sl,
                          const uint8_t* gate, void* o, float* lse, int B, int Lmax, int Hq,
-                         int Hkv, int W, int S, float scale, float* part, int max_chunks,
-                         const Paging& pg, cudaStream_t s) {
+                         int Hkv, int W, int S, float scale, float* part, int* claim,
+                         int max_chunks, const Paging& pg, cudaStream_t s) {
     const float sl2 = scale * 1.4426950408889634f;
     const int G = Hq / Hkv;
     cudaError_t e;
     prof_start(s);
     switch (G) {
-        case 1: e = launch_split<T, D, 1>(q, kc, vc, sl, gate, part, B, Lmax, Hq, Hkv, W, S, sl2, max_chunks, pg, s); break;
-        case 2: e = launch_split<T, D, 2>(q, kc, vc, sl, gate, part, B, Lmax, Hq, Hkv, W, S, sl2, max_chunks, pg, s); break;
-        case 4: e = launch_split<T, D, 4>(q, kc, vc, sl, gate, part, B, Lmax, Hq, Hkv, W, S, sl2, max_chunks, pg, s); break;
-        case 8: e = launch_split<T, D, 8>(q, kc, vc, sl, gate, part, B, Lmax, Hq, Hkv, W, S, sl2, max_chunks, pg, s); break;
+        case 1: e = launch_split<T, D, 1>(q, kc, vc, sl, gate, part, claim, B, Lmax, Hq, Hkv, W, S, sl2, max_chunks, pg, s); break;
+        case 2: e = launch_split<T, D, 2>(q, kc, vc, sl, gate, part, claim, B, Lmax, Hq, Hkv, W, S, sl2, max_chunks, pg, s); break;
+        case 4: e = launch_split<T, D, 4>(q, kc, vc, sl, gate, part, claim, B, Lmax, Hq, Hkv, W, S, sl2, max_chunks, pg, s); break;
+        case 8: e = launch_split<T, D, 8>(q, kc, vc, sl, gate, part, claim, B, Lmax, Hq, Hkv, W, S, sl2, max_chunks, pg, s); break;
         default: return cudaErrorInvalidValue;
     }
     prof_stop(s);
@@ -516,12 +545,13 @@ cudaError_t launch_decode_any(const void* q, const void* kc, const void* vc,
                               float scale, int dtype, const DecodeWs& L, char* ws,
                               const Paging& pg, cudaStream_t s) {
     float* part = reinterpret_cast<float*>(ws + L.part);
+    int* claim = reinterpret_cast<int*>(ws + L.claim);
     if (dtype == 1) {
-        if (d == 128) return launch_typed<__nv_bfloat16, 128>(q, kc, vc, seq_lens, gate, o, lse, B, Lmax, Hq, Hkv, W, S, scale, part, L.max_chunks, pg, s);
-        if (d == 64) return launch_typed<__nv_bfloat16, 64>(q, kc, vc, seq_lens, gate, o, lse, B, Lmax, Hq, Hkv, W, S, scale, part, L.max_chunks, pg, s);
+        if (d == 128) return launch_typed<__nv_bfloat16, 128>(q, kc, vc, seq_lens, gate, o, lse, B, Lmax, Hq, Hkv, W, S, scale, part, claim, L.max_chunks, pg, s);
+        if (d == 64) return launch_typed<__nv_bfloat16, 64>(q, kc, vc, seq_lens, gate, o, lse, B, Lmax, Hq, Hkv, W, S, scale, part, claim, L.max_chunks, pg, s);
     } else {
-        if (d == 128) return launch_typed<float, 128>(q, kc, vc, seq_lens, gate, o, lse, B, Lmax, Hq, Hkv, W, S, scale, part, L.max_chunks, pg, s);
-        if (d == 64) return launch_typed<float, 64>(q, kc, vc, seq_lens, gate, o, lse, B, Lmax, Hq, Hkv, W, S, scale, part, L.max_chunks, pg, s);
+        if (d == 128) return launch_typed<float, 128>(q, kc, vc, seq_lens, gate, o, lse, B, Lmax, Hq, Hkv, W, S, scale, part, claim, L.max_chunks, pg, s);
+        if (d == 64) return launch_typed<float, 64>(q, kc, vc, seq_lens, gate, o, lse, B, Lmax, Hq, Hkv, W, S, scale, part, claim, L.max_chunks, pg, s);
     }
     return cudaErrorInvalidValue;
 }
@@ -539,8 +569,9 @@ DecodeWs decode_ws_layout(int B, int Lmax, int Hq, int d, int S) {
     const int64_t longest = (m + kChunk - 1) / kChunk + 1;
     L.max_chunks = longest > kSplit + 1 ? (int)longest : kSplit + 1;
     L.part = 0;
-    L.total = sizeof(float) * (size_t)B * L.max_chunks * Hq * (d + 2);
-    L.total = (L.total + 255) & ~static_cast<size_t>(255);
+    L.claim = sizeof(float) * (size_t)B * L.max_chunks * Hq * (d + 2);
+    L.claim = (L.claim + 255) & ~static_cast<size_t>(255);
+    L.total = L.claim + 256;
     return L;
 }
 

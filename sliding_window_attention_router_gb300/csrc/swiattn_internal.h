@@ -70,6 +70,7 @@ PrefillWs prefill_ws_layout(int B, int N, int Hq, int d);
 
 struct DecodeWs {
     size_t part;   // float [B * max_chunks * Hq * (d+2)]
+    size_t claim;  // int: chunk counter of the split kernel's persistent CTAs (cleared per call)
     size_t total;
     int max_chunks;
     int chunk;

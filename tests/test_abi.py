@@ -227,13 +227,14 @@ def _decode_chunk_len(m):
 def test_decode_workspace_holds_every_chunk_partial(lib):
     """The split kernel writes one partial per (sequence, chunk, query head) and
     the combine reads them back; the workspace must hold the most chunks any
-    visit of up to Lmax entries (plus up to S anchors) can have."""
+    visit of up to Lmax entries (plus up to S anchors) can have.  The partials
+    come first; the last 256 bytes hold the split kernel's chunk counter."""
     import sliding_window_attention_router_gb300 as swa
     Hq, d = 256, 64                  # a chunk's partials: 256 * 66 floats = 67 584 bytes
     per_chunk = Hq * (d + 2) * 4
     for Lmax in (1, 7, 63, 64, 65, 200, 511, 512, 513, 1024, 1025, 2047, 2048, 2049, 4096, 5000):
         for S in (0, 1, 63, 64, 300, 4096):
-            size = swa.decode_anchored_workspace(1, Lmax, Hq, Hq, d, 16, S, swa.BF16)
+            size = swa.decode_anchored_workspace(1, Lmax, Hq, Hq, d, 16, S, swa.BF16) - 256
             assert size % per_chunk == 0
             max_chunks = size // per_chunk
             for lo_span in range(1, Lmax + 1):

@@ -126,8 +126,8 @@ def test_noalloc_decode_reports_out_of_range_lengths(swa):
 
 def test_noalloc_decode_scratch_boundary(swa):
     """The header's example bound: B=16, Hq=16, d=128 fits Lmax = 32000 and
-    not 32001 (max(9, ceil(Lmax/256) + 1) chunks of (d+2) floats per
-    sequence and head).  The rejected call launches nothing, so its caches,
+    not 32001 (max(17, ceil(Lmax/256) + 1) chunks of (d+2) floats per
+    sequence and head, and 256 bytes for the chunk counter).  The rejected call launches nothing, so its caches,
     smaller than Lmax, are never read."""
     lib = swa._load()
     B, Hq, Hkv, d, W = 16, 16, 16, 128, 1024
