@@ -316,7 +316,36 @@ def prefill_section(swa, timer, dev, frac, steps, warmup, seed, with_e2e, N=3276
         e2e_ms, _ = timer.run(e2e_step, max(3, steps // 2), 2)
         h2d = sum(host[n].numel() * host[n].element_size() for n in host)
         d2h = o_host.numel() * o_host.element_size()
-        res.update(e2e_ms=e2e_ms, h2d=h2d, d2h=d2h)
+        # The same calls issued as a stream of requests: consecutive calls
+        # alternate between two streams (each with its own workspace and host
+        # output), so one call's upload can overlap the previous call's
+        # attention and download; timed from the first upload to the last
+        # download.  Every call still copies its inputs in and its output out.
+        pipe = [(torch.cuda.Stream(dev), ws_host, o_host),
+                (torch.cuda.Stream(dev),
+                 torch.empty_like(ws_host), torch.empty(o.shape, dtype=o.dtype, pin_memory=True))]
+
+        def e2e_pipelined(n):
+            main_s = torch.cuda.current_stream(dev)
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record(main_s)
+            for st, _, _ in pipe:
+                st.wait_stream(main_s)
+            for i in range(n):
+                st, ws_i, o_i = pipe[i % 2]
+                with torch.cuda.stream(st):
+                    swa.prefill_host(host["q"], host["k"], host["v"], host["gate"], W, scale,
+                                     out=o_i, workspace=ws_i, device=dev)
+            for st, _, _ in pipe:
+                main_s.wait_stream(st)
+            t1.record(main_s)
+            torch.cuda.synchronize()
+            return t0.elapsed_time(t1)
+
+        n_pipe = max(4, steps)
+        e2e_pipelined(2)
+        pipe_ms = e2e_pipelined(n_pipe)
+        res.update(e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, e2e_pipe_ms=pipe_ms, e2e_pipe_n=n_pipe)
     return res
 
 
@@ -675,9 +704,14 @@ def run_ours(args, dist: Dist):
     e2e = None
     if "e2e_ms" in main:
         e2e_s = sum(main["e2e_ms"]) / 1e3
-        e2e_value, _ = aggregate(main["flops"] * len(main["e2e_ms"]), e2e_s, dist)
+        serial_value, _ = aggregate(main["flops"] * len(main["e2e_ms"]), e2e_s, dist)
+        e2e_value, _ = aggregate(main["flops"] * main["e2e_pipe_n"], main["e2e_pipe_ms"] / 1e3, dist)
         e2e = {"value": e2e_value / 1e12, "unit": "TFLOP/s",
-               "h2d_bytes_per_step": main["h2d"], "d2h_bytes_per_step": main["d2h"]}
+               "h2d_bytes_per_step": main["h2d"], "d2h_bytes_per_step": main["d2h"],
+               "steps": main["e2e_pipe_n"],
+               "issue": "swiattn_prefill_host calls back to back, alternating two streams",
+               "serial": {"value": serial_value / 1e12,
+                          "issue": "one call per timed step, the stream idle between steps"}}
     kern_s = statistics.mean(main["kern_ms"]) / 1e3
     achieved = main["flops"] / kern_s / 1e12
     peak = float(peaks["bf16_tflops"])
