@@ -316,6 +316,36 @@ def test_decode_edges(swa):
             assert np.abs(f64(o) - ref).max() <= BF16_MAX
 
 
+def test_decode_batches_above_32_and_batch_invariance(swa):
+    """Batches of up to 32 sequences run on persistent CTAs that claim chunks
+    longest first; larger ones get one CTA per (chunk, sequence) slot.  Both
+    match the oracle, and every sequence's output is bit for bit the same in a
+    batch of 40, in a batch of 32 and alone (its chunks, and each chunk's
+    arithmetic, depend on the sequence alone)."""
+    g = inp._gen(79)
+    B, Lmax, Hq, Hkv, d, W = 40, 600, 8, 2, 128, 100
+    kc = inp.randn((B, Lmax, Hkv, d), torch.bfloat16, g)
+    vc = inp.randn((B, Lmax, Hkv, d), torch.bfloat16, g)
+    q = inp.randn((B, Hq, d), torch.bfloat16, g)
+    sl = torch.randint(1, Lmax + 1, (B,), generator=g, dtype=torch.int32)
+    sl[:4] = torch.tensor([1, Lmax, W, W + 1], dtype=torch.int32)
+    gate = inp.bernoulli_gates((B,), 0.3, g)
+    scale = 1 / math.sqrt(d)
+    qd, kd, vd, sld, gd = cuda(q, kc, vc, sl, gate)
+    o40, lse40 = swa.decode(qd, kd, vd, sld, gd, W, scale, want_lse=True)
+    o32, lse32 = swa.decode(qd[:32], kd[:32], vd[:32], sld[:32], gd[:32], W, scale, want_lse=True)
+    torch.cuda.synchronize()
+    assert swa.get_device_error() == 0
+    ref = oracle.decode(f64(q), f64(kc), f64(vc), sl.numpy(), gate.numpy(), W, scale)
+    assert_bf16_close(o40, ref, "B=40")
+    assert torch.equal(o40[:32], o32) and torch.equal(lse40[:32], lse32)
+    for b in (0, 1, 3, 17, 31, 32, 39):
+        o1, lse1 = swa.decode(qd[b:b + 1], kd[b:b + 1], vd[b:b + 1], sld[b:b + 1], gd[b:b + 1], W,
+                              scale, want_lse=True)
+        torch.cuda.synchronize()
+        assert torch.equal(o1[0], o40[b]) and torch.equal(lse1[0], lse40[b]), b
+
+
 def test_decode_wide_token_rows(swa):
     """One block reads a token row of every KV head (one thread per 16 bytes).
     Rows within the split kernel's block limit are computed; a wider valid row
