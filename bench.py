@@ -54,6 +54,8 @@ MEASURED_TRAFFIC = {
     # dkdv_kernel + dq_kernel, backward on the dual workload: (314 131 968 + 22 016 768)
     # + (258 405 376 + 47 600 640)
     ("backward", "061e05be4060ff07"): 314131968 + 22016768 + 258405376 + 47600640,
+    # route_kernel, 32768 tokens x 2048: 134 248 192 read + 2 795 520 written
+    ("route", "4a5c0b7bf6e2d8ed"): 134248192 + 2795520,
 }
 # Source text each stored count depends on: whole files, or a file up to a
 # marker (the device code of a kernel file, before its host launcher; the
@@ -63,7 +65,9 @@ KERNEL_SOURCES = {"prefill": (("attn_prefill.cu", "cudaError_t launch_prefill_tc
                               "schedule.cu"),
                   "decode": (("decode.cu", "// Log-sum-exp merge of the chunk partials"),),
                   "dual": (("attn_dual.cu", "cudaError_t launch_dual_tc("), "ptx.cuh"),
-                  "backward": (("attn_bwd.cu", "cudaError_t launch_bwd_dkdv("), "ptx.cuh")}
+                  "backward": (("attn_bwd.cu", "cudaError_t launch_bwd_dkdv("), "ptx.cuh"),
+                  "route": ("route.cu", "route_gemv.cuh"),
+                  "route_backward": ("bwd_simt.cu",)}
 
 
 def kernel_source_hash(kernel: str) -> str:
@@ -782,7 +786,8 @@ def run_ours(args, dist: Dist):
                           "roofline": {"bound": "hbm", "achieved": rt["bytes"] / rk / 1e9,
                                        "peak": hbm, "unit": "GB/s",
                                        "frac": rt["bytes"] / rk / 1e9 / hbm,
-                                       "traffic": None, "kernel": "route_kernel"},
+                                       "traffic": measured_traffic("route"),
+                                       "kernel": "route_kernel"},
                           "workload": "router GEMV, 32768 tokens x d_model 2048, bf16"}
         l4 = layer_4k_section(swa, timer, dev, ks, kw, seed=dist.rank)
         l4s = statistics.mean(l4["step_ms"]) / 1e3
@@ -823,7 +828,8 @@ def run_ours(args, dist: Dist):
         extra["route_backward"] = {
             "gbs": rb["bytes"] / rbs / 1e9, "ms_per_step": rbs * 1e3,
             "roofline": {"bound": "hbm", "achieved": rb["bytes"] / rbk / 1e9, "peak": hbm,
-                         "unit": "GB/s", "frac": rb["bytes"] / rbk / 1e9 / hbm, "traffic": None,
+                         "unit": "GB/s", "frac": rb["bytes"] / rbk / 1e9 / hbm,
+                         "traffic": measured_traffic("route_backward"),
                          "kernel": "route_bwd_logit_kernel + route_bwd_dh_kernel + "
                                    "route_bwd_reduce_kernel"},
             "workload": "router backward bf16: 16384 tokens, 2048 outputs per token, d_model 2048"}
@@ -886,8 +892,8 @@ def run_backward_only(args):
 
 
 def run_section_only(args):
-    """The decode (16 x 32K) or dual-branch (8K) section alone (a profiling
-    aid, not the bench line)."""
+    """The decode (16 x 32K), dual-branch (8K), router or router-backward
+    section alone (a profiling aid, not the bench line)."""
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     import sliding_window_attention_router_gb300 as swa
@@ -898,6 +904,12 @@ def run_section_only(args):
         k = statistics.mean(r["kern_ms"]) / 1e3
         print(json.dumps({"section": "decode", "kernel_gbs": r["bytes"] / k / 1e9,
                           "bytes_per_step": r["bytes"], "n_routed": r["n_routed"]}), flush=True)
+    elif args.only in ("route", "route_backward"):
+        fn = route_section if args.only == "route" else route_backward_section
+        r = fn(swa, timer, dev, args.steps, args.warmup, 0)
+        k = statistics.mean(r["kern_ms"]) / 1e3
+        print(json.dumps({"section": args.only, "kernel_gbs": r["bytes"] / k / 1e9,
+                          "bytes_per_step": r["bytes"]}), flush=True)
     else:
         r = dual_section(swa, timer, dev, args.steps, args.warmup, 0)
         k = statistics.mean(r["kern_ms"]) / 1e3
@@ -920,8 +932,9 @@ def main():
                     help="seconds of oracle work per step of the reference arm")
     ap.add_argument("--only-backward", choices=["dual_8k", "prefill_32k"], default=None,
                     help="profiling runs only: time just the training backward on one workload")
-    ap.add_argument("--only", choices=["decode", "dual"], default=None,
-                    help="profiling runs only: time just the decode or the dual-branch section")
+    ap.add_argument("--only", choices=["decode", "dual", "route", "route_backward"], default=None,
+                    help="profiling runs only: time just one section (decode, dual branch, "
+                         "router, router backward)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

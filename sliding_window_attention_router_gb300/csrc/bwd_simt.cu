@@ -252,11 +252,11 @@ __global__ void __launch_bounds__(256) route_bwd_dh_kernel(
 }
 
 // dw[c] = sum over chunks of the partials: a block takes 32 columns and warp
-// w sums chunks w, w+16, w+32, ... for its lane's column, then the sixteen
-// warp sums are added in warp order (a fixed order, so dw is bitwise
-// repeatable).  db = sum d_logits (the last block, fixed-order tree).
+// w sums chunks w, w+32, w+64, ... for its lane's column, then the 32 warp
+// sums are added in warp order (a fixed order, so dw is bitwise repeatable).
+// db = sum d_logits (the last block, fixed-order tree).
 constexpr int kReduceCols = 32;
-constexpr int kReduceWarps = 16;
+constexpr int kReduceWarps = 32;
 
 __global__ void __launch_bounds__(kReduceWarps * 32) route_bwd_reduce_kernel(
     const float* __restrict__ part, int64_t chunks, int d_model, const float* __restrict__ d_logits,
@@ -284,6 +284,7 @@ __global__ void __launch_bounds__(kReduceWarps * 32) route_bwd_reduce_kernel(
     if (db && last) {
         __shared__ float red[kReduceWarps * 32];
         float acc = 0.f;
+#pragma unroll 8
         for (int64_t t = threadIdx.x; t < tokens; t += blockDim.x) acc += d_logits[t];
         red[threadIdx.x] = acc;
         __syncthreads();
