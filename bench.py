@@ -56,6 +56,9 @@ MEASURED_TRAFFIC = {
     ("backward", "061e05be4060ff07"): 314131968 + 22016768 + 258405376 + 47600640,
     # route_kernel, 32768 tokens x 2048: 134 248 192 read + 2 795 520 written
     ("route", "4a5c0b7bf6e2d8ed"): 134248192 + 2795520,
+    # route_bwd_logit + dh + reduce kernels, 16384 tokens: (201 534 208 + 3 031 552)
+    # + (67 196 672 + 17 656 064) + (2 171 904 + 0); most dh rows are still in L2 at the end
+    ("route_backward", "8a50a8de2fb87f90"): 201534208 + 3031552 + 67196672 + 17656064 + 2171904,
 }
 # Source text each stored count depends on: whole files, or a file up to a
 # marker (the device code of a kernel file, before its host launcher; the
