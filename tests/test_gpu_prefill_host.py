@@ -49,3 +49,40 @@ def test_host_equals_device_fp32(swa):
     torch.cuda.synchronize()
     o_d = swa.prefill(q.cuda(), k.cuda(), v.cuda(), gate.cuda(), 32)
     assert torch.equal(o_h, o_d.cpu())
+
+
+def test_calls_alternating_two_streams(swa):
+    """The bench's end-to-end figure issues host-buffer calls back to back on
+    two streams, each with its own workspace and output, so two calls (their
+    copies and their kernels) can run at once.  Each result must equal the
+    same call made alone, bit for bit."""
+    dev = torch.device("cuda", 0)
+    B, N, H, W = 1, 4096, 8, 512
+    cases = []
+    for seed in (11, 12, 13, 14):
+        g = inp._gen(seed)
+        q, k, v = inp.attention_qkv(B, N, H, H, 128, torch.bfloat16, g)
+        gate = inp.run_gates(N, 0.13, g).reshape(B, N)
+        cases.append(tuple(t.pin_memory() for t in (q, k, v, gate)))
+    alone = []
+    for q, k, v, gate in cases:
+        alone.append(swa.prefill_host(q, k, v, gate, W).clone())
+        torch.cuda.synchronize()
+    ws_bytes = swa.prefill_host_workspace(B, N, H, H, 128, W, torch.bfloat16)
+    lanes = [(torch.cuda.Stream(dev), torch.empty(ws_bytes, dtype=torch.uint8, device=dev))
+             for _ in range(2)]
+    outs = [torch.empty(cases[0][0].shape, dtype=torch.bfloat16, pin_memory=True) for _ in cases]
+    main = torch.cuda.current_stream(dev)
+    for st, _ in lanes:
+        st.wait_stream(main)
+    for rep in range(3):
+        for i, (q, k, v, gate) in enumerate(cases):
+            st, ws = lanes[i % 2]
+            with torch.cuda.stream(st):
+                swa.prefill_host(q, k, v, gate, W, out=outs[i], workspace=ws, device=dev)
+        for st, _ in lanes:
+            main.wait_stream(st)
+        torch.cuda.synchronize()
+        assert swa.get_device_error() == 0
+        for i in range(len(cases)):
+            assert torch.equal(outs[i].view(torch.int16), alone[i].view(torch.int16)), (rep, i)
