@@ -66,8 +66,9 @@ def test_calls_alternating_two_streams(swa):
         cases.append(tuple(t.pin_memory() for t in (q, k, v, gate)))
     alone = []
     for q, k, v, gate in cases:
-        alone.append(swa.prefill_host(q, k, v, gate, W).clone())
-        torch.cuda.synchronize()
+        o = swa.prefill_host(q, k, v, gate, W)
+        torch.cuda.synchronize()   # the host output is valid once the stream has passed the call
+        alone.append(o.clone())
     ws_bytes = swa.prefill_host_workspace(B, N, H, H, 128, W, torch.bfloat16)
     lanes = [(torch.cuda.Stream(dev), torch.empty(ws_bytes, dtype=torch.uint8, device=dev))
              for _ in range(2)]
