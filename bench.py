@@ -45,8 +45,8 @@ L2_FLUSH_BYTES = 256 << 20
 # has changed since reports null.
 MEASURED_TRAFFIC = {
     # prefill_kernel, long-context prefill N=32768 f=0.13 (far items head by head):
-    # 686 008 064 read + 120 857 088 written
-    ("prefill", "055e5142999f96a7"): 686008064 + 120857088,
+    # 684 139 520 read + 117 672 960 written
+    ("prefill", "6d4e9a86574d6344"): 684139520 + 117672960,
     # decode_split2_kernel (persistent CTAs), 16 x 32768 decode: 654 431 488 read + 4 102 656 written
     ("decode", "c0c2b929dbce784b"): 654431488 + 4102656,
     # dual_kernel, dual-branch workload B=2 N=8192 GQA 16/4: 148 151 040 read + 271 419 648 written

@@ -688,6 +688,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // Launched as a programmatic dependent of the schedule: everything above
+    // overlaps it; its work list, far-row list and tile prefixes are read
+    // only after this wait.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     if (warp < 8) {
         warpgroup_reg_inc<kRegsSoftmax>();
@@ -762,10 +766,22 @@ cudaError_t launch_prefill_tc(const TcAttnArgs& a, const int* tile_prefix, unsig
     cudaError_t e = p.S > 0 ? allow_dynamic_smem(prefill_kernel<true>, kSmemBytes, smem_anchored)
                             : allow_dynamic_smem(prefill_kernel<false>, kSmemBytes, smem_plain);
     if (e != cudaSuccess) return e;
-    if (p.S > 0)
-        prefill_kernel<true><<<num_sms, kThreads, kSmemBytes, s>>>(p);
-    else
-        prefill_kernel<false><<<num_sms, kThreads, kSmemBytes, s>>>(p);
+    // A programmatic dependent launch of the schedule kernel before it on the
+    // stream: the CTAs start (TMEM, barriers) while the schedule runs and wait
+    // for its grid before reading the work list.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_sms);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = p.S > 0 ? cudaLaunchKernelEx(&cfg, prefill_kernel<true>, p)
+                : cudaLaunchKernelEx(&cfg, prefill_kernel<false>, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

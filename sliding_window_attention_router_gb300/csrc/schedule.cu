@@ -103,28 +103,24 @@ __device__ __forceinline__ int anchor_blocks(int r0, int N, int W, int S) {
     return (S > 0 && last >= r0 && hi >= 0) ? hi / kBN + 1 : 0;
 }
 
-// Cost (key blocks over both tiles) of pair u of the enumeration
-// [far pairs | band pairs] per batch; 0 when the pair has nothing to do.
-__device__ __forceinline__ int pair_cost(int u, const int* routed_list, const int* routed_count,
-                                         const int* tile_prefix, int N, int W, int S, int NT,
-                                         int NP, int& b, int& kind, int& pair) {
-    b = u / (2 * NP);
-    const int rem = u % (2 * NP);
-    if (rem < NP) {
-        kind = kItemFar;
-        pair = rem;
-        const int R = routed_count[b];
-        int cost = 0;
-        for (int x = 0; x < 2; ++x) {
-            const int r0 = pair * 2 * kBM + x * kBM;
-            if (r0 >= R) break;
-            const int last = min(R, r0 + kBM) - 1;
-            cost += routed_list[(size_t)b * N + last] / kBN + 1;
-        }
-        return cost;
+// Key blocks of far pair `pair` of batch b (both tiles): a far tile walks
+// keys [0, last row]; far_last holds each far tile's last row (-1 past the
+// last far tile).
+__device__ __forceinline__ int far_pair_cost(int b, int pair, const int* far_last, int NT) {
+    int cost = 0;
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+        const int k = 2 * pair + x;
+        const int r = k < NT ? far_last[(size_t)b * NT + k] : -1;
+        if (r >= 0) cost += r / kBN + 1;
     }
-    kind = kItemBand;
-    pair = rem - NP;
+    return cost;
+}
+
+// Key blocks of band pair `pair` of batch b (both tiles, anchor runs
+// included), or 0 when neither tile has a row to write.
+__device__ __forceinline__ int band_pair_cost(int b, int pair, const int* tile_prefix, int N,
+                                              int W, int S, int NT) {
     const int q0 = pair * 2 * kBM;
     const int kv0 = max(0, q0 - W + 1);
     const int na = max(anchor_blocks(q0, N, W, S), anchor_blocks(q0 + kBM, N, W, S));
@@ -152,27 +148,77 @@ __device__ __forceinline__ bool gate_byte(const uint4& v, int u) {
     return ((w >> (8 * (u & 3))) & 0xFFu) != 0;
 }
 
-// The whole prefill schedule in one CTA.  Per batch: each thread counts the far
-// rows of a contiguous chunk of rows (a multiple of 16, so 16-byte gate groups
-// never straddle two threads), one block scan, then each thread writes its far
-// rows (ascending i) and the prefix counts of the 128-row tiles that start in
-// its chunk.  Then the work list, Hq items per 256-row pair (one per query
-// head): far pairs sorted by descending cost, then band pairs in order; and
-// the reset of the attention kernel's work counter.  Far queries are not copied here: the attention kernel gathers
-// them by row index when it loads a far tile.
+// The whole prefill schedule in one CTA, in two passes with one global round
+// trip each.  Pass 1, per batch: each thread counts the far rows of a
+// contiguous chunk of rows (a multiple of 16, so 16-byte gate groups never
+// straddle two threads), one block scan, then each thread writes its far rows
+// (ascending i), the prefix counts of the 128-row tiles that start in its
+// chunk, and the last row of each far tile that ends in its chunk.  Pass 2:
+// the cost of every pair from those per-tile values, a histogram of the far
+// costs and the number of busy band pairs of each thread's run, one scan of
+// both, then the work list, Hq items per 256-row pair (one per query head):
+// far pairs sorted by descending cost, then band pairs in order; and the
+// reset of the attention kernel's work counter.  Far queries are not copied
+// here: the attention kernel gathers them by row index when it loads a far
+// tile.
 constexpr int kPlanThreads = 1024;
 constexpr int kBucketsPerThread = kCostBuckets / kPlanThreads;
+// Per-tile values (far tiles' last rows, tile prefixes) of batches with up to
+// this many tiles in all are also kept in shared memory for pass 2.
+constexpr int kTileCache = 3072;
+
+// Block-wide exclusive scan of two values per thread at once; every thread
+// of the block must call it.
+__device__ __forceinline__ int2 block_exclusive_scan2(int2 v, int2* warp_tot, int2* total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    int2 x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int yx = __shfl_up_sync(0xffffffffu, x.x, o);
+        const int yy = __shfl_up_sync(0xffffffffu, x.y, o);
+        if (lane >= o) {
+            x.x += yx;
+            x.y += yy;
+        }
+    }
+    if (lane == 31) warp_tot[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        int2 t = lane < nwarps ? warp_tot[lane] : make_int2(0, 0);
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int yx = __shfl_up_sync(0xffffffffu, t.x, o);
+            const int yy = __shfl_up_sync(0xffffffffu, t.y, o);
+            if (lane >= o) {
+                t.x += yx;
+                t.y += yy;
+            }
+        }
+        warp_tot[lane] = t;   // inclusive totals per warp
+    }
+    __syncthreads();
+    const int2 before = w > 0 ? warp_tot[w - 1] : make_int2(0, 0);
+    *total = warp_tot[nwarps - 1];
+    __syncthreads();
+    return make_int2(before.x + x.x - v.x, before.y + x.y - v.y);
+}
 
 // Every thread of a kPlanThreads-thread block calls it.
 __device__ void plan_block(const uint8_t* __restrict__ gate, int B, int N, int Hq, int W, int S,
                            int* __restrict__ routed_list, int* __restrict__ routed_count,
-                           int* __restrict__ tile_prefix, WorkItem* __restrict__ items,
-                           int* __restrict__ n_items) {
+                           int* __restrict__ tile_prefix, int* __restrict__ far_last,
+                           WorkItem* __restrict__ items, int* __restrict__ n_items) {
     __shared__ int hist[kCostBuckets];
     __shared__ int warp_tot[32];
+    __shared__ int2 warp_tot2[32];
+    __shared__ int s_last[kTileCache];
+    __shared__ int s_pre[kTileCache];
     const int NT = cdiv(N, kBM);
     const int NP = cdiv(N, 2 * kBM);
+    const bool cached = (int64_t)B * (NT + 1) <= kTileCache;
     const int C = cdiv(cdiv(N, kPlanThreads), 16) * 16;
+    for (int c = threadIdx.x; c < kCostBuckets; c += blockDim.x) hist[c] = 0;
     for (int b = 0; b < B; ++b) {
         const uint8_t* g = gate + (size_t)b * N;
         const bool vec = (reinterpret_cast<uintptr_t>(g) & 15u) == 0;
@@ -187,19 +233,31 @@ __device__ void plan_block(const uint8_t* __restrict__ gate, int B, int N, int H
         int run = block_exclusive_scan(cnt, warp_tot, &total);
         int* list = routed_list + (size_t)b * N;
         int* pre = tile_prefix + (size_t)b * (NT + 1);
+        int* last = (cached ? s_last : far_last) + (size_t)b * NT;
         for (int i = i0; i < i1; i += 16) {
             const uint4 v = load_gates16(g, i, N, vec);
-            if ((i % kBM) == 0) pre[i / kBM] = run;   // 16 divides 128: tile starts begin groups
+            if ((i % kBM) == 0) {   // 16 divides 128: tile starts begin groups
+                pre[i / kBM] = run;
+                if (cached) s_pre[b * (NT + 1) + i / kBM] = run;
+            }
 #pragma unroll
             for (int u = 0; u < 16; ++u)
-                if (i + u >= W && i + u < i1 && gate_byte(v, u)) list[run++] = i + u;
+                if (i + u >= W && i + u < i1 && gate_byte(v, u)) {
+                    if (run % kBM == kBM - 1 || run == total - 1) last[run / kBM] = i + u;
+                    list[run++] = i + u;
+                }
         }
+        // Far tiles past the last one hold no rows.
+        for (int k = cdiv(total, kBM) + threadIdx.x; k < NT; k += blockDim.x) last[k] = -1;
         if (threadIdx.x == 0) {
             routed_count[b] = total;
             pre[NT] = total;
+            if (cached) s_pre[b * (NT + 1) + NT] = total;
         }
     }
-    __syncthreads();   // the lists, counts and prefixes above are read below
+    __syncthreads();   // the per-tile values above are read below
+    const int* fl = cached ? s_last : far_last;
+    const int* tp = cached ? s_pre : tile_prefix;
 
     // Far pairs: counting sort by descending cost (they cost up to N / 128
     // key blocks per tile, so longest first matters for the balance of the
@@ -207,23 +265,31 @@ __device__ void plan_block(const uint8_t* __restrict__ gate, int B, int N, int H
     // same time then walk the K/V prefix of few heads, from key 0 up, and
     // share it in L2 (with the heads interleaved, the 32K workload read
     // 2.2x its algorithmic bytes from HBM; head by head, 1.45x).
-    const int U = B * 2 * NP;
-    for (int c = threadIdx.x; c < kCostBuckets; c += blockDim.x) hist[c] = 0;
-    __syncthreads();
+    const int U = B * NP;
     for (int u = threadIdx.x; u < U; u += blockDim.x) {
-        int b, kind, pair;
-        const int cost = pair_cost(u, routed_list, routed_count, tile_prefix, N, W, S, NT, NP, b, kind, pair);
-        if (kind == kItemFar && cost > 0) atomicAdd(&hist[min(cost, kCostBuckets - 1)], 1);
+        const int cost = far_pair_cost(u / NP, u % NP, fl, NT);
+        if (cost > 0) atomicAdd(&hist[min(cost, kCostBuckets - 1)], 1);
     }
-    __syncthreads();
+    // Band pairs follow, in (batch, pair) order with the heads of a pair
+    // adjacent: their costs are nearly equal (the window and one tile), and
+    // the CTAs that run them at the same time then walk overlapping windows
+    // of the same heads, which L2 serves.  Each thread takes a contiguous run
+    // of pairs; the scan below places the runs.
+    const int CB = cdiv(U, kPlanThreads);
+    const int v0 = min(U, static_cast<int>(threadIdx.x) * CB), v1 = min(U, v0 + CB);
+    int nb = 0;
+    for (int v = v0; v < v1; ++v) nb += band_pair_cost(v / NP, v % NP, tp, N, W, S, NT) > 0;
+    __syncthreads();   // the histogram is complete
     // Exclusive offsets in descending cost order: thread t owns buckets
     // 4095-4t ... 4095-4t-3.
     int own = 0;
 #pragma unroll
     for (int k = 0; k < kBucketsPerThread; ++k)
         own += hist[kCostBuckets - 1 - (threadIdx.x * kBucketsPerThread + k)];
-    int far_total;
-    int run = block_exclusive_scan(own, warp_tot, &far_total);
+    int2 totals;
+    const int2 start = block_exclusive_scan2(make_int2(own, nb), warp_tot2, &totals);
+    const int far_total = totals.x, band_total = totals.y;
+    int run = start.x;
 #pragma unroll
     for (int k = 0; k < kBucketsPerThread; ++k) {
         const int c = kCostBuckets - 1 - (threadIdx.x * kBucketsPerThread + k);
@@ -233,34 +299,17 @@ __device__ void plan_block(const uint8_t* __restrict__ gate, int B, int N, int H
     }
     __syncthreads();
     for (int u = threadIdx.x; u < U; u += blockDim.x) {
-        int b, kind, pair;
-        const int cost = pair_cost(u, routed_list, routed_count, tile_prefix, N, W, S, NT, NP, b, kind, pair);
-        if (kind != kItemFar || cost <= 0) continue;
+        const int b = u / NP, pair = u % NP;
+        const int cost = far_pair_cost(b, pair, fl, NT);
+        if (cost <= 0) continue;
         const int pos = atomicAdd(&hist[min(cost, kCostBuckets - 1)], 1);
-        for (int h = 0; h < Hq; ++h) items[(size_t)h * far_total + pos] = WorkItem{kind, b, h, pair};
+        for (int h = 0; h < Hq; ++h) items[(size_t)h * far_total + pos] = WorkItem{kItemFar, b, h, pair};
     }
-    // Band pairs follow, in (batch, pair) order with the heads of a pair
-    // adjacent: their costs are nearly equal (the window and one tile), and
-    // the CTAs that run them at the same time then walk overlapping windows
-    // of the same heads, which L2 serves.  Each thread takes a contiguous run
-    // of pairs; one scan places the runs.
-    const int V = B * NP;
-    const int CB = cdiv(V, kPlanThreads);
-    const int v0 = min(V, static_cast<int>(threadIdx.x) * CB), v1 = min(V, v0 + CB);
-    int nb = 0;
+    int pos = far_total + start.y;
     for (int v = v0; v < v1; ++v) {
-        int b, kind, pair;
-        const int u = (v / NP) * 2 * NP + NP + v % NP;
-        nb += pair_cost(u, routed_list, routed_count, tile_prefix, N, W, S, NT, NP, b, kind, pair) > 0;
-    }
-    int band_total;
-    int pos = far_total + block_exclusive_scan(nb, warp_tot, &band_total);
-    for (int v = v0; v < v1; ++v) {
-        int b, kind, pair;
-        const int u = (v / NP) * 2 * NP + NP + v % NP;
-        if (pair_cost(u, routed_list, routed_count, tile_prefix, N, W, S, NT, NP, b, kind, pair) <= 0)
-            continue;
-        for (int h = 0; h < Hq; ++h) items[(size_t)pos * Hq + h] = WorkItem{kind, b, h, pair};
+        const int b = v / NP, pair = v % NP;
+        if (band_pair_cost(b, pair, tp, N, W, S, NT) <= 0) continue;
+        for (int h = 0; h < Hq; ++h) items[(size_t)pos * Hq + h] = WorkItem{kItemBand, b, h, pair};
         ++pos;
     }
     if (threadIdx.x == 0) {
@@ -272,8 +321,12 @@ __device__ void plan_block(const uint8_t* __restrict__ gate, int B, int N, int H
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(
     const uint8_t* __restrict__ gate, int B, int N, int Hq, int W, int S,
     int* __restrict__ routed_list, int* __restrict__ routed_count, int* __restrict__ tile_prefix,
-    WorkItem* __restrict__ items, int* __restrict__ n_items) {
-    plan_block(gate, B, N, Hq, W, S, routed_list, routed_count, tile_prefix, items, n_items);
+    int* __restrict__ far_last, WorkItem* __restrict__ items, int* __restrict__ n_items) {
+    // The attention kernel after it is a programmatic dependent launch: let
+    // its CTAs start now (they wait for this grid before reading the list).
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    plan_block(gate, B, N, Hq, W, S, routed_list, routed_count, tile_prefix, far_last, items,
+               n_items);
 }
 
 // Router GEMV fused with the schedule: every CTA computes logits and gates of
@@ -286,9 +339,13 @@ __global__ void __launch_bounds__(kPlanThreads) route_plan_kernel(
     const uint4* __restrict__ h, const uint4* __restrict__ w, float bias, int nvec,
     float* __restrict__ logits, uint8_t* __restrict__ gate, int B, int N, int Hq, int W, int S,
     unsigned int* __restrict__ ticket, int* __restrict__ routed_list,
-    int* __restrict__ routed_count, int* __restrict__ tile_prefix, WorkItem* __restrict__ items,
-    int* __restrict__ n_items) {
+    int* __restrict__ routed_count, int* __restrict__ tile_prefix, int* __restrict__ far_last,
+    WorkItem* __restrict__ items, int* __restrict__ n_items) {
     __shared__ int last;
+    // The attention kernel after it is a programmatic dependent launch: its
+    // CTAs may take the SMs this grid leaves (they wait for the whole grid,
+    // the plan included, before reading the list).
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t tokens = (int64_t)B * N;
     const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -303,7 +360,8 @@ __global__ void __launch_bounds__(kPlanThreads) route_plan_kernel(
     }
     __syncthreads();
     if (!last) return;
-    plan_block(gate, B, N, Hq, W, S, routed_list, routed_count, tile_prefix, items, n_items);
+    plan_block(gate, B, N, Hq, W, S, routed_list, routed_count, tile_prefix, far_last, items,
+               n_items);
 }
 
 }  // namespace
@@ -319,6 +377,8 @@ PrefillWs prefill_ws_layout(int B, int N, int Hq, int d) {
     off = up(off + sizeof(int) * (size_t)B);
     L.tile_prefix = off;
     off = up(off + sizeof(int) * (size_t)B * (NT + 1));
+    L.far_last = off;
+    off = up(off + sizeof(int) * (size_t)B * NT);
     L.n_items = off;
     off = up(off + sizeof(int) * 4);
     L.max_items = static_cast<int>((size_t)B * 2 * ((N + 2 * kBM - 1) / (2 * kBM)) * Hq);
@@ -333,7 +393,8 @@ cudaError_t launch_schedule(const uint8_t* gate, int B, int N, int Hq, int W, in
     plan_kernel<<<1, kPlanThreads, 0, s>>>(
         gate, B, N, Hq, W, S, reinterpret_cast<int*>(ws + L.routed_list),
         reinterpret_cast<int*>(ws + L.routed_count), reinterpret_cast<int*>(ws + L.tile_prefix),
-        reinterpret_cast<WorkItem*>(ws + L.items), reinterpret_cast<int*>(ws + L.n_items));
+        reinterpret_cast<int*>(ws + L.far_last), reinterpret_cast<WorkItem*>(ws + L.items),
+        reinterpret_cast<int*>(ws + L.n_items));
     return cudaGetLastError();
 }
 
@@ -349,16 +410,17 @@ cudaError_t launch_route_plan(const void* h, const void* w, float bias, int d_mo
     int* list = reinterpret_cast<int*>(ws + L.routed_list);
     int* count = reinterpret_cast<int*>(ws + L.routed_count);
     int* prefix = reinterpret_cast<int*>(ws + L.tile_prefix);
+    int* far_last = reinterpret_cast<int*>(ws + L.far_last);
     WorkItem* items = reinterpret_cast<WorkItem*>(ws + L.items);
     int* n_items = reinterpret_cast<int*>(ws + L.n_items);
     if (dtype == 1) {
         route_plan_kernel<__nv_bfloat16><<<blocks, kPlanThreads, 0, s>>>(
             static_cast<const uint4*>(h), static_cast<const uint4*>(w), bias, d_model / 8, logits,
-            gate, B, N, Hq, W, S, ticket, list, count, prefix, items, n_items);
+            gate, B, N, Hq, W, S, ticket, list, count, prefix, far_last, items, n_items);
     } else {
         route_plan_kernel<float><<<blocks, kPlanThreads, 0, s>>>(
             static_cast<const uint4*>(h), static_cast<const uint4*>(w), bias, d_model / 4, logits,
-            gate, B, N, Hq, W, S, ticket, list, count, prefix, items, n_items);
+            gate, B, N, Hq, W, S, ticket, list, count, prefix, far_last, items, n_items);
     }
     return cudaGetLastError();
 }

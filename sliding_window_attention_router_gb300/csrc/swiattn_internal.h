@@ -61,6 +61,7 @@ struct PrefillWs {
     size_t routed_list;   // int32 [B*N]   far rows of each batch, ascending
     size_t routed_count;  // int32 [B]
     size_t tile_prefix;   // int32 [B*(NT+1)] far rows before each 128-row tile
+    size_t far_last;      // int32 [B*NT]     last row of each far tile (-1 past the last)
     size_t n_items;       // int32 [4]
     size_t items;         // WorkItem [max_items]
     size_t total;
