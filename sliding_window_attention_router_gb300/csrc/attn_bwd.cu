@@ -554,6 +554,9 @@ __device__ bool softmax_role(const BwdParams& p, uint8_t* smem, uint64_t* bar, v
 }
 
 __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant__ BwdParams p) {
+    // The dQ kernel after it is a programmatic dependent launch that reads
+    // nothing this kernel writes: its CTAs may take each SM this grid leaves.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     if (smem_u32(smem_raw) & 1023u) {   // operand tiles need 1024-byte alignment
         if (threadIdx.x == 0) atomicOr(p.err, kDevErrLayout);
@@ -1034,9 +1037,25 @@ cudaError_t launch_bwd_dq(const TcBwdArgs& a, unsigned int* err, int num_sms, cu
     p.n_items = counters + 2;
     p.next_item = counters + 3;
     static std::atomic<uint64_t> smem_allowed{0};
-    const cudaError_t e = allow_dynamic_smem(dqk::dq_kernel, dqk::kSmemBytes, smem_allowed);
+    cudaError_t e = allow_dynamic_smem(dqk::dq_kernel, dqk::kSmemBytes, smem_allowed);
     if (e != cudaSuccess) return e;
-    dqk::dq_kernel<<<num_sms, kThreads, dqk::kSmemBytes, s>>>(p);
+    // Launched as a programmatic dependent of the dK/dV kernel before it on
+    // the stream: the two read the same inputs and write disjoint outputs, so
+    // dQ CTAs start on the SMs the dK/dV kernel's last items leave idle.  Its
+    // own inputs (work list, compacted rows) were complete before the dK/dV
+    // kernel started.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_sms);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = dqk::kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, dqk::dq_kernel, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

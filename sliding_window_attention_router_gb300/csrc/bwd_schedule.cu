@@ -215,13 +215,14 @@ __device__ void sort_items(int U, int fan, MakeItem make, BwdItem* items, int* n
 }
 
 // Block 0: dK/dV list.  Block 1: dQ list.  Other blocks: compaction of far
-// rows (q, dO, D, lse, row index), zero-padded to whole 128-row tiles.
+// rows (q, dO, D, lse, row index), zero-padded to whole 128-row tiles; D and
+// lse come from the band statistics (computed before, by row).
 __global__ void __launch_bounds__(kBuildThreads) bwd_build_gather_kernel(
     const int* __restrict__ routed_list, const int* __restrict__ routed_count,
     const int* __restrict__ tile_prefix, int B, int N, int Npad, int Hq, int Hkv, int W,
     BwdItem* __restrict__ items_kv, BwdItem* __restrict__ items_q, int* __restrict__ counters,
-    const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ o,
-    const float* __restrict__ lse, const __nv_bfloat16* __restrict__ d_o,
+    const __nv_bfloat16* __restrict__ q, const float* __restrict__ d_band,
+    const float* __restrict__ l_band, const __nv_bfloat16* __restrict__ d_o,
     __nv_bfloat16* __restrict__ qc, __nv_bfloat16* __restrict__ doc, float* __restrict__ d_far,
     float* __restrict__ l_far, int* __restrict__ rowidx) {
     const int NT = cdiv(N, kBM);
@@ -239,9 +240,7 @@ __global__ void __launch_bounds__(kBuildThreads) bwd_build_gather_kernel(
             items_q, &counters[2], &counters[3]);
         return;
     }
-    // Far rows: half a warp per (compacted row, head), 16 bytes per lane.  The
-    // loop runs per warp (both halves the same trip count), so the half-warp
-    // reductions below are reached by every lane.
+    // Far rows: half a warp per (compacted row, head), 16 bytes per lane.
     const int lane = threadIdx.x & 31, half = lane >> 4, sub = lane & 15;
     const size_t warps = (size_t)(gridDim.x - 2) * (blockDim.x >> 5);
     const size_t w0 = (size_t)(blockIdx.x - 2) * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -252,26 +251,27 @@ __global__ void __launch_bounds__(kBuildThreads) bwd_build_gather_kernel(
             const size_t w = 2 * ww + half;
             const bool live = w < total;
             const int r = (int)(w / Hq), h = (int)(w % Hq);
-            uint4 vq = make_uint4(0u, 0u, 0u, 0u), vd = vq, vo = vq;
+            uint4 vq = make_uint4(0u, 0u, 0u, 0u), vd = vq;
             int i = kNoRow;
-            size_t src = 0;
+            float dv = 0.f, lv = 0.f;
             if (live && r < R) {
                 i = routed_list[(size_t)b * N + r];
-                src = ((size_t)b * N + i) * Hq + h;
+                const size_t src = ((size_t)b * N + i) * Hq + h;
                 vq = reinterpret_cast<const uint4*>(q + src * kHD)[sub];
                 vd = reinterpret_cast<const uint4*>(d_o + src * kHD)[sub];
-                vo = reinterpret_cast<const uint4*>(o + src * kHD)[sub];
+                if (sub == 0) {
+                    const size_t stat = ((size_t)b * Hq + h) * Npad + i;
+                    dv = d_band[stat];
+                    lv = l_band[stat];
+                }
             }
-            float acc = dot8_bf16(vd, vo);
-#pragma unroll
-            for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
             if (live) {
                 const size_t dst = ((size_t)b * Npad + r) * Hq + h;
                 reinterpret_cast<uint4*>(qc + dst * kHD)[sub] = vq;
                 reinterpret_cast<uint4*>(doc + dst * kHD)[sub] = vd;
                 if (sub == 0) {
-                    d_far[((size_t)b * Hq + h) * Npad + r] = acc;
-                    l_far[((size_t)b * Hq + h) * Npad + r] = r < R ? lse[src] * kLog2e : 0.f;
+                    d_far[((size_t)b * Hq + h) * Npad + r] = dv;
+                    l_far[((size_t)b * Hq + h) * Npad + r] = lv;
                     if (h == 0) rowidx[(size_t)b * Npad + r] = i;
                 }
             }
@@ -339,7 +339,8 @@ cudaError_t launch_bwd_schedule(const uint8_t* gate, const void* q, const void* 
     bwd_build_gather_kernel<<<2 + num_sms * 2, kBuildThreads, 0, s>>>(
         list, count, prefix, B, N, L.Npad, Hq, Hkv, W,
         reinterpret_cast<BwdItem*>(ws + L.items_kv), reinterpret_cast<BwdItem*>(ws + L.items_q),
-        reinterpret_cast<int*>(ws + L.counters), static_cast<const __nv_bfloat16*>(q), ob, lse,
+        reinterpret_cast<int*>(ws + L.counters), static_cast<const __nv_bfloat16*>(q),
+        reinterpret_cast<const float*>(ws + L.d_band), reinterpret_cast<const float*>(ws + L.l_band),
         dob, reinterpret_cast<__nv_bfloat16*>(ws + L.qc),
         reinterpret_cast<__nv_bfloat16*>(ws + L.doc), reinterpret_cast<float*>(ws + L.d_far),
         reinterpret_cast<float*>(ws + L.l_far), reinterpret_cast<int*>(ws + L.rowidx));
