@@ -554,12 +554,11 @@ __device__ bool softmax_role(const BwdParams& p, uint8_t* smem, uint64_t* bar, v
 }
 
 __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant__ BwdParams p) {
-    // The dQ kernel after it is a programmatic dependent launch that reads
-    // nothing this kernel writes: its CTAs may take each SM this grid leaves.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     if (smem_u32(smem_raw) & 1023u) {   // operand tiles need 1024-byte alignment
         if (threadIdx.x == 0) atomicOr(p.err, kDevErrLayout);
+        // Exiting lets the dQ kernel launch: not before the schedule it reads.
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         return;
     }
     uint8_t* smem = smem_raw;
@@ -604,6 +603,13 @@ __global__ void __launch_bounds__(kThreads, 1) dkdv_kernel(const __grid_constant
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // Launched as a programmatic dependent of the backward schedule: the
+    // prologue above overlaps it, and its work lists and compacted rows are
+    // read only after this wait.  The dQ kernel after this one may launch
+    // from here on: it reads nothing this kernel writes, and what it reads
+    // is complete now.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp < 8) {
         warpgroup_reg_inc<kRegsSoftmax>();
@@ -1023,9 +1029,22 @@ cudaError_t launch_bwd_dkdv(const TcBwdArgs& a, unsigned int* err, int num_sms, 
     p.n_items = counters;
     p.next_item = counters + 1;
     static std::atomic<uint64_t> smem_allowed{0};
-    const cudaError_t e = allow_dynamic_smem(kv::dkdv_kernel, kv::kSmemBytes, smem_allowed);
+    cudaError_t e = allow_dynamic_smem(kv::dkdv_kernel, kv::kSmemBytes, smem_allowed);
     if (e != cudaSuccess) return e;
-    kv::dkdv_kernel<<<num_sms, kThreads, kv::kSmemBytes, s>>>(p);
+    // A programmatic dependent launch of the backward schedule before it on
+    // the stream (the kernel waits for that grid before reading its lists).
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_sms);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kv::kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kv::dkdv_kernel, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -1042,8 +1061,8 @@ cudaError_t launch_bwd_dq(const TcBwdArgs& a, unsigned int* err, int num_sms, cu
     // Launched as a programmatic dependent of the dK/dV kernel before it on
     // the stream: the two read the same inputs and write disjoint outputs, so
     // dQ CTAs start on the SMs the dK/dV kernel's last items leave idle.  Its
-    // own inputs (work list, compacted rows) were complete before the dK/dV
-    // kernel started.
+    // own inputs (work list, compacted rows) are complete before any dK/dV
+    // CTA lets it launch.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(num_sms);
     cfg.blockDim = dim3(kThreads);

@@ -558,6 +558,9 @@ __device__ bool softmax_role(const DuParams& p, uint8_t* smem, uint64_t* bar, vo
 }
 
 __global__ void __launch_bounds__(kThreads, 1) dual_kernel(const __grid_constant__ DuParams p) {
+    // The epilogue kernel after it is a programmatic dependent launch: it may
+    // be scheduled now and waits for this grid before reading the partials.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));

@@ -109,6 +109,9 @@ __global__ void dual_epilogue_parts_kernel(const float* __restrict__ part,
                                            const float* __restrict__ nll, float* __restrict__ mse,
                                            float* __restrict__ gamma, float* __restrict__ reg,
                                            int BN, int Hq, float gb, float eps, float alpha) {
+    // A programmatic dependent launch of the dual-branch kernel: the partial
+    // sums are read after its grid completes.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= BN) return;
     float acc = 0.f;
@@ -161,9 +164,18 @@ cudaError_t launch_dual_epilogue_parts(const float* mse_part, const float* logit
                                        int B, int N, int Hq, float gamma_base, float eps,
                                        float alpha, cudaStream_t s) {
     const int BN = B * N;
-    dual_epilogue_parts_kernel<<<(BN + 255) / 256, 256, 0, s>>>(mse_part, logits, nll, mse, gamma,
-                                                                reg, BN, Hq, gamma_base, eps,
-                                                                alpha);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((BN + 255) / 256);
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, dual_epilogue_parts_kernel, mse_part, logits,
+                                             nll, mse, gamma, reg, BN, Hq, gamma_base, eps, alpha);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

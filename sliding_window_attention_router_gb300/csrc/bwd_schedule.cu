@@ -225,6 +225,9 @@ __global__ void __launch_bounds__(kBuildThreads) bwd_build_gather_kernel(
     const float* __restrict__ l_band, const __nv_bfloat16* __restrict__ d_o,
     __nv_bfloat16* __restrict__ qc, __nv_bfloat16* __restrict__ doc, float* __restrict__ d_far,
     float* __restrict__ l_far, int* __restrict__ rowidx) {
+    // The dK/dV kernel after it is a programmatic dependent launch: its CTAs
+    // may start on SMs this grid leaves (they wait for it before reading).
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int NT = cdiv(N, kBM);
     if (blockIdx.x == 0) {
         sort_items(
