@@ -273,12 +273,30 @@ __device__ void plan_block(const uint8_t* __restrict__ gate, int B, int N, int H
     // Band pairs follow, in (batch, pair) order with the heads of a pair
     // adjacent: their costs are nearly equal (the window and one tile), and
     // the CTAs that run them at the same time then walk overlapping windows
-    // of the same heads, which L2 serves.  Each thread takes a contiguous run
-    // of pairs; the scan below places the runs.
+    // of the same heads, which L2 serves.  The pairs whose window reaches
+    // back past row 0 (the first E of each batch) cost fewer key blocks the
+    // earlier they start; they close the list, latest first, so the last
+    // items claimed are the shortest.  Each thread takes a contiguous run of
+    // the order; the scan below places the runs.
+    const int E = min(NP, cdiv(W - 1, 2 * kBM));
+    const int UF = B * (NP - E);
+    auto band_at = [&](int v, int& b, int& pair) {
+        if (v < UF) {
+            b = v / (NP - E);
+            pair = E + v % (NP - E);
+        } else {
+            b = (v - UF) / E;
+            pair = E - 1 - (v - UF) % E;
+        }
+    };
     const int CB = cdiv(U, kPlanThreads);
     const int v0 = min(U, static_cast<int>(threadIdx.x) * CB), v1 = min(U, v0 + CB);
     int nb = 0;
-    for (int v = v0; v < v1; ++v) nb += band_pair_cost(v / NP, v % NP, tp, N, W, S, NT) > 0;
+    for (int v = v0; v < v1; ++v) {
+        int b, pair;
+        band_at(v, b, pair);
+        nb += band_pair_cost(b, pair, tp, N, W, S, NT) > 0;
+    }
     __syncthreads();   // the histogram is complete
     // Exclusive offsets in descending cost order: thread t owns buckets
     // 4095-4t ... 4095-4t-3.
@@ -307,7 +325,8 @@ __device__ void plan_block(const uint8_t* __restrict__ gate, int B, int N, int H
     }
     int pos = far_total + start.y;
     for (int v = v0; v < v1; ++v) {
-        const int b = v / NP, pair = v % NP;
+        int b, pair;
+        band_at(v, b, pair);
         if (band_pair_cost(b, pair, tp, N, W, S, NT) <= 0) continue;
         for (int h = 0; h < Hq; ++h) items[(size_t)pos * Hq + h] = WorkItem{kItemBand, b, h, pair};
         ++pos;
