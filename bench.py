@@ -45,15 +45,15 @@ L2_FLUSH_BYTES = 256 << 20
 # has changed since reports null.
 MEASURED_TRAFFIC = {
     # prefill_kernel, long-context prefill N=32768 f=0.13 (far items head by head):
-    # 684 139 520 read + 117 672 960 written
-    ("prefill", "6d4e9a86574d6344"): 684139520 + 117672960,
+    # 697 447 168 read + 120 408 832 written
+    ("prefill", "6508cfe31234c067"): 697447168 + 120408832,
     # decode_split2_kernel (persistent CTAs), 16 x 32768 decode: 654 431 488 read + 4 102 656 written
     ("decode", "c0c2b929dbce784b"): 654431488 + 4102656,
-    # dual_kernel, dual-branch workload B=2 N=8192 GQA 16/4: 148 151 040 read + 271 419 648 written
-    ("dual", "8d3e62db38f8aca6"): 148151040 + 271419648,
-    # dkdv_kernel + dq_kernel, backward on the dual workload: (314 131 968 + 22 016 768)
-    # + (258 405 376 + 47 600 640)
-    ("backward", "061e05be4060ff07"): 314131968 + 22016768 + 258405376 + 47600640,
+    # dual_kernel, dual-branch workload B=2 N=8192 GQA 16/4: 147 451 904 read + 272 084 992 written
+    ("dual", "41d5cbe8b0cb869f"): 147451904 + 272084992,
+    # dkdv_kernel + dq_kernel, backward on the dual workload: (316 144 384 + 22 467 584)
+    # + (255 239 936 + 48 151 552)
+    ("backward", "f439b89d19b1e966"): 316144384 + 22467584 + 255239936 + 48151552,
     # route_kernel, 32768 tokens x 2048: 134 248 192 read + 2 795 520 written
     ("route", "4a5c0b7bf6e2d8ed"): 134248192 + 2795520,
     # route_bwd_logit + dh + reduce kernels, 16384 tokens: (201 534 208 + 3 031 552)
@@ -63,9 +63,9 @@ MEASURED_TRAFFIC = {
 # Source text each stored count depends on: whole files, or a file up to a
 # marker (the device code of a kernel file, before its host launcher; the
 # decode split kernel, before the combine).  The prefill's count also depends
-# on the order of its work list (schedule.cu).
+# on the order of its work list (schedule.cu, up to the fused router kernel).
 KERNEL_SOURCES = {"prefill": (("attn_prefill.cu", "cudaError_t launch_prefill_tc("), "ptx.cuh",
-                              "schedule.cu"),
+                              ("schedule.cu", "// Router GEMV fused with the schedule")),
                   "decode": (("decode.cu", "// Log-sum-exp merge of the chunk partials"),),
                   "dual": (("attn_dual.cu", "cudaError_t launch_dual_tc("), "ptx.cuh"),
                   "backward": (("attn_bwd.cu", "cudaError_t launch_bwd_dkdv("), "ptx.cuh"),
