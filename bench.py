@@ -48,7 +48,7 @@ MEASURED_TRAFFIC = {
     # 697 447 168 read + 120 408 832 written
     ("prefill", "6508cfe31234c067"): 697447168 + 120408832,
     # decode_split2_kernel (persistent CTAs), 16 x 32768 decode: 654 431 488 read + 4 102 656 written
-    ("decode", "c0c2b929dbce784b"): 654431488 + 4102656,
+    ("decode", "97db57687c228419"): 654431488 + 4102656,
     # dual_kernel, dual-branch workload B=2 N=8192 GQA 16/4: 147 451 904 read + 272 084 992 written
     ("dual", "41d5cbe8b0cb869f"): 147451904 + 272084992,
     # dkdv_kernel + dq_kernel, backward on the dual workload: (316 144 384 + 22 467 584)

@@ -3,10 +3,12 @@
 // window or the whole history).  A window token reads the last W cache
 // entries, a routed one all L: the bytes moved are the whole cost.
 //
-// Split-KV: CTA (chunk c, sequence b) streams `chunk` consecutive tokens of the
-// visited range.  A token's K (or V) row for every KV head is one contiguous
-// Hkv*d run, so each thread issues one 16-byte load per token and tensor, and
-// the whole CTA reads it fully coalesced.  Threads of one KV head (d/VEC
+// Split-KV: each chunk of `chunk` consecutive tokens of a visited range is
+// streamed by one CTA (persistent CTAs claim chunks for batches of up to 32
+// sequences; larger batches launch one CTA per chunk slot).  A token's K (or
+// V) row for every KV head is one contiguous Hkv*d run, so each thread issues
+// one 16-byte load per token and tensor, and the whole CTA reads it fully
+// coalesced.  Threads of one KV head (d/VEC
 // consecutive lanes) reduce q.k with xor-shuffles; each holds VEC output
 // columns of the G = Hq/Hkv query heads of its group.  Partial (m, l, o) per
 // chunk go to the workspace; a second kernel merges them by log-sum-exp.
