@@ -1,6 +1,6 @@
 """GPU parity over seeded random shapes: many small configurations of the
-routed prefill (with and without global anchors), the decode and the dual
-branch, drawn from one fixed generator, each compared element by element with
+routed prefill (with and without global anchors), the decode, the dual
+branch and the training backward, drawn from one fixed generator, each compared element by element with
 the fp64 oracle.  The fixed cases of the other test files pick the edges by
 hand; these cover the space between them (batch counts, GQA ratios, window
 sizes, sequence lengths that are not multiples of the tile sizes, gate run
@@ -166,3 +166,43 @@ def test_dual_random_shapes(swa, case):
     for name in ("o_full", "o_swa"):
         err = np.abs(f64(out[name]) - ref[name])
         assert err.max() <= BF16_MAX and err.mean() <= BF16_MEAN, (case, name, err.max(), err.mean())
+
+
+def backward_cases():
+    rng = np.random.default_rng(20261206)
+    cases = []
+    for c in range(6):
+        B = draw(rng, [1, 2])
+        Hkv = draw(rng, [1, 2, 4])
+        G = draw(rng, [1, 2, 4])
+        N = int(rng.integers(2, 900))
+        W = int(rng.integers(1, 500))
+        frac = float(draw(rng, [0.0, 0.13, 0.5, 1.0]))
+        cases.append((c, B, N, Hkv * G, Hkv, W, frac))
+    return cases
+
+
+@pytest.mark.parametrize("case", backward_cases(), ids=lambda c: f"b{c[0]}")
+def test_backward_random_shapes(swa, case):
+    """dQ, dK, dV of the routed prefill (bf16 tensor-core kernels) against the
+    oracle's gradient.  Tolerance as in the backward tests: the gradients are
+    stored as bf16 and P, dS are rounded to bf16 before the contractions, so
+    max|err| <= 1e-2 max|ref| and mean|err| <= 4e-3 mean|ref|."""
+    c, B, N, Hq, Hkv, W, frac = case
+    g = inp._gen(8000 + c)
+    q, k, v = inp.attention_qkv(B, N, Hq, Hkv, 128, torch.bfloat16, g)
+    gate = torch.stack([inp.run_gates(N, frac, g) if 0 < frac < 1 else
+                        torch.full((N,), int(frac), dtype=torch.uint8) for _ in range(B)])
+    do = inp.output_grad((B, N, Hq, 128), torch.bfloat16, 9000 + c)
+    qd, kd, vd, gd, dod = (t.cuda() for t in (q, k, v, gate, do))
+    o, lse = swa.prefill(qd, kd, vd, gd, W, want_lse=True)
+    grads = swa.prefill_backward(qd, kd, vd, gd, o, lse, dod, W)
+    torch.cuda.synchronize()
+    assert swa.get_device_error() == 0
+    refs = oracle.prefill_backward(f64(q), f64(k), f64(v), gate.numpy(), f64(do), W,
+                                   1.0 / math.sqrt(128))
+    for name, got, ref in zip(("dq", "dk", "dv"), grads, refs):
+        r = np.asarray(ref)
+        err = np.abs(f64(got).reshape(r.shape) - r)
+        assert err.max() <= 1e-2 * np.abs(r).max(), (case, name, err.max(), np.abs(r).max())
+        assert err.mean() <= 4e-3 * np.abs(r).mean(), (case, name, err.mean(), np.abs(r).mean())
