@@ -165,7 +165,11 @@ constexpr int kPlanThreads = 1024;
 constexpr int kBucketsPerThread = kCostBuckets / kPlanThreads;
 // Per-tile values (far tiles' last rows, tile prefixes) of batches with up to
 // this many tiles in all are also kept in shared memory for pass 2.
-constexpr int kTileCache = 3072;
+constexpr int kTileCache = 2048;
+// With up to this many pairs, each item's pair is first noted in shared
+// memory by list position, and the items are then written by consecutive
+// threads in list order (coalesced) instead of by the thread of their pair.
+constexpr int kPairCache = 1024;
 
 // Block-wide exclusive scan of two values per thread at once; every thread
 // of the block must call it.
@@ -214,6 +218,7 @@ __device__ void plan_block(const uint8_t* __restrict__ gate, int B, int N, int H
     __shared__ int2 warp_tot2[32];
     __shared__ int s_last[kTileCache];
     __shared__ int s_pre[kTileCache];
+    __shared__ int s_at[2 * kPairCache];   // far position -> pair; band position -> order index
     const int NT = cdiv(N, kBM);
     const int NP = cdiv(N, 2 * kBM);
     const bool cached = (int64_t)B * (NT + 1) <= kTileCache;
@@ -316,20 +321,39 @@ __device__ void plan_block(const uint8_t* __restrict__ gate, int B, int N, int H
         run += h;
     }
     __syncthreads();
+    const bool coalesce = U <= kPairCache;
     for (int u = threadIdx.x; u < U; u += blockDim.x) {
         const int b = u / NP, pair = u % NP;
         const int cost = far_pair_cost(b, pair, fl, NT);
         if (cost <= 0) continue;
         const int pos = atomicAdd(&hist[min(cost, kCostBuckets - 1)], 1);
-        for (int h = 0; h < Hq; ++h) items[(size_t)h * far_total + pos] = WorkItem{kItemFar, b, h, pair};
+        if (coalesce) s_at[pos] = u;
+        else
+            for (int h = 0; h < Hq; ++h) items[(size_t)h * far_total + pos] = WorkItem{kItemFar, b, h, pair};
     }
     int pos = far_total + start.y;
     for (int v = v0; v < v1; ++v) {
         int b, pair;
         band_at(v, b, pair);
         if (band_pair_cost(b, pair, tp, N, W, S, NT) <= 0) continue;
-        for (int h = 0; h < Hq; ++h) items[(size_t)pos * Hq + h] = WorkItem{kItemBand, b, h, pair};
+        if (coalesce) s_at[kPairCache + pos - far_total] = v;
+        else
+            for (int h = 0; h < Hq; ++h) items[(size_t)pos * Hq + h] = WorkItem{kItemBand, b, h, pair};
         ++pos;
+    }
+    if (coalesce) {
+        __syncthreads();
+        const int nfar = far_total * Hq, nall = (far_total + band_total) * Hq;
+        for (int idx = threadIdx.x; idx < nall; idx += blockDim.x) {
+            if (idx < nfar) {   // items[h * far_total + pos]
+                const int u = s_at[idx % far_total];
+                items[idx] = WorkItem{kItemFar, u / NP, idx / far_total, u % NP};
+            } else {            // items[pos * Hq + h], pos >= far_total
+                int b, pair;
+                band_at(s_at[kPairCache + (idx - nfar) / Hq], b, pair);
+                items[idx] = WorkItem{kItemBand, b, (idx - nfar) % Hq, pair};
+            }
+        }
     }
     if (threadIdx.x == 0) {
         n_items[0] = (far_total + band_total) * Hq;
