@@ -45,8 +45,8 @@ L2_FLUSH_BYTES = 256 << 20
 # has changed since reports null.
 MEASURED_TRAFFIC = {
     # prefill_kernel, long-context prefill N=32768 f=0.13 (far items head by head):
-    # 697 447 168 read + 120 408 832 written
-    ("prefill", "d5ac89cba8ec4c0f"): 697447168 + 120408832,
+    # 695 015 168 read + 120 571 648 written
+    ("prefill", "67f32e67fb407016"): 695015168 + 120571648,
     # decode_split2_kernel (persistent CTAs), 16 x 32768 decode: 654 431 488 read + 4 102 656 written
     ("decode", "97db57687c228419"): 654431488 + 4102656,
     # dual_kernel, dual-branch workload B=2 N=8192 GQA 16/4: 147 451 904 read + 272 084 992 written

@@ -240,9 +240,13 @@ __device__ bool consume_item(const PfParams& p, uint64_t* bar, volatile int* sch
 // then one K/V slot per step g: step j of an item carries K_j (j < nblk) and
 // V_{j-1} (j >= 1), so a slot is freed by one commit after S(j) and PV(j-1).
 //
-// Each Q slot's barriers see one load per active tile per item, band (TMA,
-// here) or far (the gatherer warp).  Both warps wait for every load's slot in
-// order, so neither waits on a phase more than one ahead of the barrier.
+// Each Q slot sees one load per active tile per item, band (TMA, here) or far
+// (the gatherer warp).  This warp waits for the slot of every load, in order;
+// it finishes an item's waits before it publishes the next item, and the slot
+// is freed again only after the tile's last S, which needs this warp's K/V
+// loads, issued after its wait: so each wait finds the barrier at the phase
+// it names or the one before.  The gatherer's waits (far loads only) are
+// argued at q_gatherer.
 template <bool ANCH>
 __device__ bool producer(const PfParams& p, uint8_t* smem, uint64_t* bar, volatile int* sched,
                          volatile int* abort_flag, uint32_t& g, uint32_t* q_issued, bool* q_tma_last) {
@@ -343,12 +347,22 @@ __device__ bool q_gatherer(const PfParams& p, uint8_t* smem, uint64_t* bar, vola
         if (!consume_item(p, bar, sched, k, abort_flag, idx)) return false;
         if (idx < 0) break;
         const Plan pl = make_plan<ANCH>(p, idx);
+        // Every load of a slot counts (cnt: its phase), but the gatherer
+        // waits only before its own (far) loads.  Such a wait names the
+        // previous load's release and finds the barrier at that phase or
+        // just past it: not further past (the next release needs this load's
+        // rows), nor further back (the producer waited for the release before
+        // that one before it issued the previous load, in an earlier item,
+        // and published this item only after).  Waiting before band loads as
+        // well, which need nothing from this warp, could find the slot freed
+        // once more already and then wait for a phase that never comes.
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
             if (!tile_active(pl, x)) continue;
-            if (!mbar_wait_w(&bar[BAR_Q_EMPTY + x], (cnt[x] & 1u) ^ 1u, abort_flag, p.err)) return false;
-            ++cnt[x];
-            if (pl.kind == kItemFar) gather_far_q(p, smem, bar, pl, x, lane);
+            const uint32_t use = cnt[x]++;
+            if (pl.kind != kItemFar) continue;
+            if (!mbar_wait_w(&bar[BAR_Q_EMPTY + x], (use & 1u) ^ 1u, abort_flag, p.err)) return false;
+            gather_far_q(p, smem, bar, pl, x, lane);
         }
     }
     return true;
