@@ -6,6 +6,9 @@ hand; these cover the space between them (batch counts, GQA ratios, window
 sizes, sequence lengths that are not multiples of the tile sizes, gate run
 lengths and fractions).
 
+A last test repeats a call made of tiny band and far items many times, each
+call checked for an expired device-side wait.
+
 Tolerances as elsewhere: bf16 attention outputs max-abs 2e-2 and mean-abs
 2e-3; fp32 outputs 1e-4; the visited-key count of every (row, head) exact.
 """
@@ -206,3 +209,22 @@ def test_backward_random_shapes(swa, case):
         err = np.abs(f64(got).reshape(r.shape) - r)
         assert err.max() <= 1e-2 * np.abs(r).max(), (case, name, err.max(), np.abs(r).max())
         assert err.mean() <= 4e-3 * np.abs(r).mean(), (case, name, err.mean(), np.abs(r).mean())
+
+
+def test_prefill_tiny_items_repeated(swa):
+    """Many calls whose work items are one or two key blocks long, band and far
+    items mixed on every CTA (routed rows past the window in short runs, N a few
+    hundred rows per head).  Every call must finish without a device-side wait
+    expiring; the last call's outputs match the oracle."""
+    B, N, Hq, Hkv, W = 4, 700, 8, 2, 100
+    g = inp._gen(7777)
+    q, k, v = inp.attention_qkv(B, N, Hq, Hkv, 128, torch.bfloat16, g)
+    gate = torch.stack([inp.run_gates(N, 0.3, g, mean_run=4.0) for _ in range(B)])
+    scale = 1 / math.sqrt(128)
+    qd, kd, vd, gd = q.cuda(), k.cuda(), v.cuda(), gate.cuda()
+    for _ in range(60):
+        o = swa.prefill(qd, kd, vd, gd, W, scale)
+        assert swa.get_device_error() == 0
+    ref = oracle.prefill(f64(q), f64(k), f64(v), gate.numpy(), W, scale)
+    err = np.abs(f64(o) - ref)
+    assert err.max() <= BF16_MAX and err.mean() <= BF16_MEAN, (err.max(), err.mean())
