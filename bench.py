@@ -45,15 +45,15 @@ L2_FLUSH_BYTES = 256 << 20
 # has changed since reports null.
 MEASURED_TRAFFIC = {
     # prefill_kernel, long-context prefill N=32768 f=0.13 (far items head by head):
-    # 695 015 168 read + 120 571 648 written
-    ("prefill", "67f32e67fb407016"): 695015168 + 120571648,
+    # 696 263 424 read + 121 013 504 written
+    ("prefill", "bee408ca069b0175"): 696263424 + 121013504,
     # decode_split2_kernel (persistent CTAs), 16 x 32768 decode: 654 431 488 read + 4 102 656 written
     ("decode", "97db57687c228419"): 654431488 + 4102656,
-    # dual_kernel, dual-branch workload B=2 N=8192 GQA 16/4: 147 451 904 read + 272 084 992 written
-    ("dual", "41d5cbe8b0cb869f"): 147451904 + 272084992,
-    # dkdv_kernel + dq_kernel, backward on the dual workload: (316 144 384 + 22 467 584)
-    # + (255 239 936 + 48 151 552)
-    ("backward", "f439b89d19b1e966"): 316144384 + 22467584 + 255239936 + 48151552,
+    # dual_kernel, dual-branch workload B=2 N=8192 GQA 16/4: 145 500 672 read + 272 472 576 written
+    ("dual", "c6fed2b434be7565"): 145500672 + 272472576,
+    # dkdv_kernel + dq_kernel, backward on the dual workload: (316 509 440 + 22 529 536)
+    # + (254 476 544 + 47 893 248)
+    ("backward", "6fec5fd8d32061d4"): 316509440 + 22529536 + 254476544 + 47893248,
     # route_kernel, 32768 tokens x 2048: 134 248 192 read + 2 795 520 written
     ("route", "4a5c0b7bf6e2d8ed"): 134248192 + 2795520,
     # route_bwd_logit + dh + reduce kernels, 16384 tokens: (201 534 208 + 3 031 552)

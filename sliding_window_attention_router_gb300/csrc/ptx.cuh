@@ -86,8 +86,10 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 
 // Limit of the bounded waits below, one copy per translation unit that
 // includes this header (kWaitLimitNs unless lowered on purpose, see
-// set_wait_limit_of_unit).
-static __device__ unsigned long long g_wait_limit_ns = kWaitLimitNs;
+// set_wait_limit_of_unit).  In constant memory: read on every wait that is
+// not complete at once, a global-memory copy cost the dual-branch kernel
+// 1.5 % (1110 against 1126 TFLOP/s).
+static __constant__ unsigned long long g_wait_limit_ns = kWaitLimitNs;
 
 // Sets this translation unit's copy of the wait limit on the current device
 // (synchronous; 0 restores kWaitLimitNs).
