@@ -45,15 +45,15 @@ L2_FLUSH_BYTES = 256 << 20
 # has changed since reports null.
 MEASURED_TRAFFIC = {
     # prefill_kernel, long-context prefill N=32768 f=0.13 (far items head by head):
-    # 696 263 424 read + 121 013 504 written
-    ("prefill", "bee408ca069b0175"): 696263424 + 121013504,
+    # 690 492 672 read + 120 766 464 written
+    ("prefill", "5ce455260f44dab2"): 690492672 + 120766464,
     # decode_split2_kernel (persistent CTAs), 16 x 32768 decode: 654 431 488 read + 4 102 656 written
     ("decode", "97db57687c228419"): 654431488 + 4102656,
-    # dual_kernel, dual-branch workload B=2 N=8192 GQA 16/4: 145 500 672 read + 272 472 576 written
-    ("dual", "c6fed2b434be7565"): 145500672 + 272472576,
-    # dkdv_kernel + dq_kernel, backward on the dual workload: (316 509 440 + 22 529 536)
-    # + (254 476 544 + 47 893 248)
-    ("backward", "6fec5fd8d32061d4"): 316509440 + 22529536 + 254476544 + 47893248,
+    # dual_kernel, dual-branch workload B=2 N=8192 GQA 16/4: 144 400 384 read + 270 856 192 written
+    ("dual", "0d140f1582e3c2ea"): 144400384 + 270856192,
+    # dkdv_kernel + dq_kernel, backward on the dual workload: (317 678 848 + 22 807 808)
+    # + (256 428 032 + 48 124 672)
+    ("backward", "c5d579004d6b73b0"): 317678848 + 22807808 + 256428032 + 48124672,
     # route_kernel, 32768 tokens x 2048: 134 248 192 read + 2 795 520 written
     ("route", "4a5c0b7bf6e2d8ed"): 134248192 + 2795520,
     # route_bwd_logit + dh + reduce kernels, 16384 tokens: (201 534 208 + 3 031 552)

@@ -388,14 +388,16 @@ __device__ __forceinline__ bool softmax_block(const DuParams& p, uint64_t* bar, 
     const bool need = resc && l > 0.f;
     if (__any_sync(0xffffffffu, need)) {
         const float f = need ? alpha : 1.f;
+        // Sixteen columns at a time: this runs while the block's 128 scores
+        // are live, so the narrower load keeps the peak register count down.
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-            uint32_t orr[32];
-            tmem_ld32(tO + q4 * 32, orr);
+        for (int q8 = 0; q8 < 8; ++q8) {
+            uint32_t orr[16];
+            tmem_ld16(tO + q8 * 16, orr);
             tmem_ld_wait();
 #pragma unroll
-            for (int t = 0; t < 32; ++t) orr[t] = __float_as_uint(__uint_as_float(orr[t]) * f);
-            tmem_st32(tO + q4 * 32, orr);
+            for (int t = 0; t < 16; ++t) orr[t] = __float_as_uint(__uint_as_float(orr[t]) * f);
+            tmem_st16(tO + q8 * 16, orr);
         }
     }
     const float mb = (m2 == -INFINITY) ? 0.f : m2;
