@@ -134,7 +134,7 @@ __device__ __forceinline__ Plan make_plan(const PfParams& p, int idx) {
     pl.row0 = it.tile * 2 * kBM;
     pl.na = 0;
     pl.ja1[0] = pl.ja1[1] = -1;
-    if (it.kind == kItemFar) {
+    if (it.kind != kItemBand) {   // a far pair, or one of its tiles alone
         const int cnt = p.routed_count[it.b];
         const int* list = p.routed_list + (size_t)it.b * p.N;
         pl.kv0 = 0;
@@ -142,7 +142,8 @@ __device__ __forceinline__ Plan make_plan(const PfParams& p, int idx) {
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
             const int r0 = pl.row0 + x * kBM;
-            pl.nrows[x] = max(0, min(kBM, cnt - r0));
+            const bool off = it.kind == (x == 0 ? kItemFarB : kItemFarA);
+            pl.nrows[x] = off ? 0 : max(0, min(kBM, cnt - r0));
             pl.j0[x] = 0;
             pl.j1[x] = pl.nrows[x] > 0 ? list[r0 + pl.nrows[x] - 1] / kKB : -1;
             maxb = max(maxb, pl.j1[x] + 1);
@@ -256,7 +257,7 @@ __device__ bool producer(const PfParams& p, uint8_t* smem, uint64_t* bar, volati
         if (!publish_item(p, bar, sched, k, n, abort_flag, idx)) return false;
         if (idx < 0) break;
         const Plan pl = make_plan<ANCH>(p, idx);
-        const bool far = pl.kind == kItemFar;
+        const bool far = pl.kind != kItemBand;
         auto load_q = [&](int x) -> bool {
             if (!mbar_wait_w(&bar[BAR_Q_EMPTY + x], (q_issued[x] & 1u) ^ 1u, abort_flag, p.err)) return false;
             ++q_issued[x];
@@ -360,7 +361,7 @@ __device__ bool q_gatherer(const PfParams& p, uint8_t* smem, uint64_t* bar, vola
         for (int x = 0; x < 2; ++x) {
             if (!tile_active(pl, x)) continue;
             const uint32_t use = cnt[x]++;
-            if (pl.kind != kItemFar) continue;
+            if (pl.kind == kItemBand) continue;
             if (!mbar_wait_w(&bar[BAR_Q_EMPTY + x], (use & 1u) ^ 1u, abort_flag, p.err)) return false;
             gather_far_q(p, smem, bar, pl, x, lane);
         }
@@ -479,7 +480,7 @@ __device__ bool softmax_role(const PfParams& p, uint8_t* smem, uint64_t* bar, vo
         if (idx < 0) break;
         const Plan pl = make_plan<ANCH>(p, idx);
         if (!tile_active(pl, x)) continue;
-        const bool far = pl.kind == kItemFar;
+        const bool far = pl.kind != kItemBand;
         int i = -1;
         if (r < pl.nrows[x]) {
             const int rr = pl.row0 + x * kBM + r;

@@ -8,12 +8,14 @@
 // such tiles (256 rows, one head).  For the persistent attention kernel the
 // list holds the far pairs head by head, longest first within a head (cost
 // in key blocks), then the band pairs in row order, the heads of a pair
-// adjacent.
+// adjacent.  A far pair too long for the balance of the launch is listed as
+// its two tiles instead (see plan_block).
 
 #include "route_gemv.cuh"
 #include "swiattn_internal.h"
 
 #include <cuda_bf16.h>
+#include <climits>
 
 namespace swi {
 namespace {
@@ -106,6 +108,11 @@ __device__ __forceinline__ int anchor_blocks(int r0, int N, int W, int S) {
 // Key blocks of far pair `pair` of batch b (both tiles): a far tile walks
 // keys [0, last row]; far_last holds each far tile's last row (-1 past the
 // last far tile).
+__device__ __forceinline__ int far_tile_cost(int b, int k, const int* far_last, int NT) {
+    const int r = k < NT ? far_last[(size_t)b * NT + k] : -1;
+    return r >= 0 ? r / kBN + 1 : 0;
+}
+
 __device__ __forceinline__ int far_pair_cost(int b, int pair, const int* far_last, int NT) {
     int cost = 0;
 #pragma unroll
@@ -210,7 +217,7 @@ __device__ __forceinline__ int2 block_exclusive_scan2(int2 v, int2* warp_tot, in
 
 // Every thread of a kPlanThreads-thread block calls it.
 __device__ void plan_block(const uint8_t* __restrict__ gate, int B, int N, int Hq, int W, int S,
-                           int* __restrict__ routed_list, int* __restrict__ routed_count,
+                           int grid, int* __restrict__ routed_list, int* __restrict__ routed_count,
                            int* __restrict__ tile_prefix, int* __restrict__ far_last,
                            WorkItem* __restrict__ items, int* __restrict__ n_items) {
     __shared__ int hist[kCostBuckets];
@@ -218,12 +225,14 @@ __device__ void plan_block(const uint8_t* __restrict__ gate, int B, int N, int H
     __shared__ int2 warp_tot2[32];
     __shared__ int s_last[kTileCache];
     __shared__ int s_pre[kTileCache];
-    __shared__ int s_at[2 * kPairCache];   // far position -> pair; band position -> order index
+    __shared__ int s_at[2 * kPairCache];   // far position -> pair | kind << 24; band position -> order index
+    __shared__ int s_cost[3];              // far pair costs, band pair costs (sums), largest far pair cost
     const int NT = cdiv(N, kBM);
     const int NP = cdiv(N, 2 * kBM);
     const bool cached = (int64_t)B * (NT + 1) <= kTileCache;
     const int C = cdiv(cdiv(N, kPlanThreads), 16) * 16;
     for (int c = threadIdx.x; c < kCostBuckets; c += blockDim.x) hist[c] = 0;
+    if (threadIdx.x < 3) s_cost[threadIdx.x] = 0;
     for (int b = 0; b < B; ++b) {
         const uint8_t* g = gate + (size_t)b * N;
         const bool vec = (reinterpret_cast<uintptr_t>(g) & 15u) == 0;
@@ -271,9 +280,16 @@ __device__ void plan_block(const uint8_t* __restrict__ gate, int B, int N, int H
     // share it in L2 (with the heads interleaved, the 32K workload read
     // 2.2x its algorithmic bytes from HBM; head by head, 1.45x).
     const int U = B * NP;
+    int far_sum = 0, far_max = 0;
     for (int u = threadIdx.x; u < U; u += blockDim.x) {
         const int cost = far_pair_cost(u / NP, u % NP, fl, NT);
         if (cost > 0) atomicAdd(&hist[min(cost, kCostBuckets - 1)], 1);
+        far_sum += cost;
+        far_max = max(far_max, cost);
+    }
+    if (far_sum > 0) {
+        atomicAdd(&s_cost[0], far_sum);
+        atomicMax(&s_cost[2], far_max);
     }
     // Band pairs follow, in (batch, pair) order with the heads of a pair
     // adjacent: their costs are nearly equal (the window and one tile), and
@@ -296,13 +312,44 @@ __device__ void plan_block(const uint8_t* __restrict__ gate, int B, int N, int H
     };
     const int CB = cdiv(U, kPlanThreads);
     const int v0 = min(U, static_cast<int>(threadIdx.x) * CB), v1 = min(U, v0 + CB);
-    int nb = 0;
+    int nb = 0, band_sum = 0;
     for (int v = v0; v < v1; ++v) {
         int b, pair;
         band_at(v, b, pair);
-        nb += band_pair_cost(b, pair, tp, N, W, S, NT) > 0;
+        const int cost = band_pair_cost(b, pair, tp, N, W, S, NT);
+        nb += cost > 0;
+        band_sum += cost;
     }
-    __syncthreads();   // the histogram is complete
+    if (band_sum > 0) atomicAdd(&s_cost[1], band_sum);
+    __syncthreads();   // the histogram and the cost sums are complete
+    // A far pair costing more than 1.25 x a CTA's mean share of the whole
+    // list (all heads, `grid` CTAs) would end the launch alone: it is listed
+    // as its two tiles, each an item of its own, when both hold rows.  At
+    // N = 32K no pair comes near that; at N = 4K the last pair of each head
+    // does (its 64 key blocks are most of the launch).
+    const int64_t all_cost = (int64_t)Hq * (s_cost[0] + s_cost[1]);
+    const int split_above = (int)min((int64_t)INT_MAX, all_cost * 5 / (4 * (int64_t)max(grid, 1)));
+    auto split_costs = [&](int b, int pair, int cost, int& ca, int& cb) {
+        ca = cost;
+        cb = 0;
+        if (cost <= split_above) return false;
+        const int a = far_tile_cost(b, 2 * pair, fl, NT), c = far_tile_cost(b, 2 * pair + 1, fl, NT);
+        if (a == 0 || c == 0) return false;
+        ca = a;
+        cb = c;
+        return true;
+    };
+    if (s_cost[2] > split_above) {
+        for (int u = threadIdx.x; u < U; u += blockDim.x) {
+            const int cost = far_pair_cost(u / NP, u % NP, fl, NT);
+            int ca, cb;
+            if (!split_costs(u / NP, u % NP, cost, ca, cb)) continue;
+            atomicSub(&hist[min(cost, kCostBuckets - 1)], 1);
+            atomicAdd(&hist[min(ca, kCostBuckets - 1)], 1);
+            atomicAdd(&hist[min(cb, kCostBuckets - 1)], 1);
+        }
+        __syncthreads();
+    }
     // Exclusive offsets in descending cost order: thread t owns buckets
     // 4095-4t ... 4095-4t-3.
     int own = 0;
@@ -321,15 +368,25 @@ __device__ void plan_block(const uint8_t* __restrict__ gate, int B, int N, int H
         run += h;
     }
     __syncthreads();
-    const bool coalesce = U <= kPairCache;
+    const bool coalesce = U <= kPairCache && far_total <= kPairCache;
+    auto place_far = [&](int u, int kind, int cost) {
+        const int pos = atomicAdd(&hist[min(cost, kCostBuckets - 1)], 1);
+        if (coalesce) s_at[pos] = u | (kind << 24);
+        else
+            for (int h = 0; h < Hq; ++h)
+                items[(size_t)h * far_total + pos] = WorkItem{kind, u / NP, h, u % NP};
+    };
     for (int u = threadIdx.x; u < U; u += blockDim.x) {
         const int b = u / NP, pair = u % NP;
         const int cost = far_pair_cost(b, pair, fl, NT);
         if (cost <= 0) continue;
-        const int pos = atomicAdd(&hist[min(cost, kCostBuckets - 1)], 1);
-        if (coalesce) s_at[pos] = u;
-        else
-            for (int h = 0; h < Hq; ++h) items[(size_t)h * far_total + pos] = WorkItem{kItemFar, b, h, pair};
+        int ca, cb;
+        if (split_costs(b, pair, cost, ca, cb)) {
+            place_far(u, kItemFarA, ca);
+            place_far(u, kItemFarB, cb);
+        } else {
+            place_far(u, kItemFar, cost);
+        }
     }
     int pos = far_total + start.y;
     for (int v = v0; v < v1; ++v) {
@@ -346,8 +403,8 @@ __device__ void plan_block(const uint8_t* __restrict__ gate, int B, int N, int H
         const int nfar = far_total * Hq, nall = (far_total + band_total) * Hq;
         for (int idx = threadIdx.x; idx < nall; idx += blockDim.x) {
             if (idx < nfar) {   // items[h * far_total + pos]
-                const int u = s_at[idx % far_total];
-                items[idx] = WorkItem{kItemFar, u / NP, idx / far_total, u % NP};
+                const int e = s_at[idx % far_total], u = e & 0xFFFFFF;
+                items[idx] = WorkItem{e >> 24, u / NP, idx / far_total, u % NP};
             } else {            // items[pos * Hq + h], pos >= far_total
                 int b, pair;
                 band_at(s_at[kPairCache + (idx - nfar) / Hq], b, pair);
@@ -362,13 +419,13 @@ __device__ void plan_block(const uint8_t* __restrict__ gate, int B, int N, int H
 }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(
-    const uint8_t* __restrict__ gate, int B, int N, int Hq, int W, int S,
+    const uint8_t* __restrict__ gate, int B, int N, int Hq, int W, int S, int grid,
     int* __restrict__ routed_list, int* __restrict__ routed_count, int* __restrict__ tile_prefix,
     int* __restrict__ far_last, WorkItem* __restrict__ items, int* __restrict__ n_items) {
     // The attention kernel after it is a programmatic dependent launch: let
     // its CTAs start now (they wait for this grid before reading the list).
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    plan_block(gate, B, N, Hq, W, S, routed_list, routed_count, tile_prefix, far_last, items,
+    plan_block(gate, B, N, Hq, W, S, grid, routed_list, routed_count, tile_prefix, far_last, items,
                n_items);
 }
 
@@ -381,7 +438,7 @@ template <typename T>
 __global__ void __launch_bounds__(kPlanThreads) route_plan_kernel(
     const uint4* __restrict__ h, const uint4* __restrict__ w, float bias, int nvec,
     float* __restrict__ logits, uint8_t* __restrict__ gate, int B, int N, int Hq, int W, int S,
-    unsigned int* __restrict__ ticket, int* __restrict__ routed_list,
+    int grid, unsigned int* __restrict__ ticket, int* __restrict__ routed_list,
     int* __restrict__ routed_count, int* __restrict__ tile_prefix, int* __restrict__ far_last,
     WorkItem* __restrict__ items, int* __restrict__ n_items) {
     __shared__ int last;
@@ -402,7 +459,7 @@ __global__ void __launch_bounds__(kPlanThreads) route_plan_kernel(
     }
     __syncthreads();
     if (!last) return;
-    plan_block(gate, B, N, Hq, W, S, routed_list, routed_count, tile_prefix, far_last, items,
+    plan_block(gate, B, N, Hq, W, S, grid, routed_list, routed_count, tile_prefix, far_last, items,
                n_items);
 }
 
@@ -430,10 +487,10 @@ PrefillWs prefill_ws_layout(int B, int N, int Hq, int d) {
     return L;
 }
 
-cudaError_t launch_schedule(const uint8_t* gate, int B, int N, int Hq, int W, int S,
+cudaError_t launch_schedule(const uint8_t* gate, int B, int N, int Hq, int W, int S, int grid,
                             const PrefillWs& L, char* ws, cudaStream_t s) {
     plan_kernel<<<1, kPlanThreads, 0, s>>>(
-        gate, B, N, Hq, W, S, reinterpret_cast<int*>(ws + L.routed_list),
+        gate, B, N, Hq, W, S, grid, reinterpret_cast<int*>(ws + L.routed_list),
         reinterpret_cast<int*>(ws + L.routed_count), reinterpret_cast<int*>(ws + L.tile_prefix),
         reinterpret_cast<int*>(ws + L.far_last), reinterpret_cast<WorkItem*>(ws + L.items),
         reinterpret_cast<int*>(ws + L.n_items));
@@ -458,11 +515,11 @@ cudaError_t launch_route_plan(const void* h, const void* w, float bias, int d_mo
     if (dtype == 1) {
         route_plan_kernel<__nv_bfloat16><<<blocks, kPlanThreads, 0, s>>>(
             static_cast<const uint4*>(h), static_cast<const uint4*>(w), bias, d_model / 8, logits,
-            gate, B, N, Hq, W, S, ticket, list, count, prefix, far_last, items, n_items);
+            gate, B, N, Hq, W, S, num_sms, ticket, list, count, prefix, far_last, items, n_items);
     } else {
         route_plan_kernel<float><<<blocks, kPlanThreads, 0, s>>>(
             static_cast<const uint4*>(h), static_cast<const uint4*>(w), bias, d_model / 4, logits,
-            gate, B, N, Hq, W, S, ticket, list, count, prefix, far_last, items, n_items);
+            gate, B, N, Hq, W, S, num_sms, ticket, list, count, prefix, far_last, items, n_items);
     }
     return cudaGetLastError();
 }

@@ -261,7 +261,8 @@ int swiattn_prefill_anchored(const void* q, const void* k, const void* v, const 
     DeviceInfo di;
     if (!device_info(di)) return SWIATTN_ECUDA;
     char* ws = static_cast<char*>(workspace);
-    if (launch_schedule(gate, B, N, Hq, W, n_anchor, L, ws, s) != cudaSuccess) return SWIATTN_ECUDA;
+    if (launch_schedule(gate, B, N, Hq, W, n_anchor, di.sms, L, ws, s) != cudaSuccess)
+        return SWIATTN_ECUDA;
     return launch_prefill_after_plan(q, k, v, gate, o, lse, B, N, Hq, Hkv, W, n_anchor, scale, L,
                                      ws, di, s);
 }

@@ -51,6 +51,8 @@ constexpr int kHD = 128;   // head dim of the tensor-core path
 // Work item kinds of the routed-prefill schedule.
 constexpr int kItemBand = 0;   // 256 consecutive rows, window keys, writes non-far rows
 constexpr int kItemFar = 1;    // 256 compacted routed rows, causal keys [0, i]
+constexpr int kItemFarA = 2;   // the same pair's first 128 far rows alone
+constexpr int kItemFarB = 3;   // the same pair's last 128 far rows alone
 
 struct WorkItem {
     int kind, b, h, tile;
@@ -96,8 +98,10 @@ cudaError_t launch_route(const void* h, const void* w, float bias, int64_t token
 
 // Far-row lists, tile prefix counts and the cost-sorted work list of the
 // routed prefill, in one single-CTA launch.  S: global anchors of window rows
-// (adds their key blocks to band items' cost).
-cudaError_t launch_schedule(const uint8_t* gate, int B, int N, int Hq, int W, int S,
+// (adds their key blocks to band items' cost).  grid: CTAs of the attention
+// launch (a far pair costing more than 1.25 x a CTA's mean share is listed as
+// two one-tile items).
+cudaError_t launch_schedule(const uint8_t* gate, int B, int N, int Hq, int W, int S, int grid,
                             const PrefillWs& L, char* ws, cudaStream_t s);
 
 // Router GEMV over the B*N tokens (logits, gates) fused with the schedule
