@@ -480,7 +480,9 @@ PrefillWs prefill_ws_layout(int B, int N, int Hq, int d) {
     off = up(off + sizeof(int) * (size_t)B * NT);
     L.n_items = off;
     off = up(off + sizeof(int) * 4);
-    L.max_items = static_cast<int>((size_t)B * 2 * ((N + 2 * kBM - 1) / (2 * kBM)) * Hq);
+    // Per batch and head at most one far pair per 256 rows, each listed whole
+    // or as its two tiles, and one band pair per 256 rows.
+    L.max_items = static_cast<int>((size_t)B * 3 * ((N + 2 * kBM - 1) / (2 * kBM)) * Hq);
     L.items = off;
     off = up(off + sizeof(WorkItem) * (size_t)L.max_items);
     L.total = off;

@@ -53,8 +53,9 @@ def test_workspace_sizes(lib):
     bf16, f32 = swa.BF16, swa.F32
     n = swa.prefill_workspace(1, 32768, 16, 16, 128, 1024, bf16)
     # the far-row list (int32 per row) and the work list (16 bytes per item,
-    # 16 heads x 2 kinds x 64 pairs); far queries are gathered in place, not copied
-    assert n >= 32768 * 4 + 16 * 2 * 64 * 16 and n % 256 == 0
+    # 16 heads x up to 3 items per 256 rows x 128); far queries are gathered
+    # in place, not copied
+    assert n >= 32768 * 4 + 16 * 3 * 128 * 16 and n % 256 == 0
     assert n < 32768 * 16 * 128 * 2 // 8
     assert swa.prefill_workspace(1, 0, 16, 16, 128, 1024, bf16) == 0
     assert swa.prefill_workspace(1, 64, 6, 4, 128, 8, bf16) == 0   # Hq % Hkv != 0

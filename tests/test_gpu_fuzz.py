@@ -228,3 +228,26 @@ def test_prefill_tiny_items_repeated(swa):
     ref = oracle.prefill(f64(q), f64(k), f64(v), gate.numpy(), W, scale)
     err = np.abs(f64(o) - ref)
     assert err.max() <= BF16_MAX and err.mean() <= BF16_MEAN, (err.max(), err.mean())
+
+
+@pytest.mark.parametrize("N,W", [(4096, 256), (8192, 1024)])
+def test_prefill_most_far_pairs_split(swa, N, W):
+    """One query head, every row routed except the first row of each 128-row
+    tile: every 256-row pair is both a far pair and a band pair, and the far
+    pairs past about a quarter of the sequence each cost more than 1.25 x a
+    CTA's share, so they are listed as two one-tile items.  The work list then
+    holds about 2.8 items per 256 rows (46 for N = 4096, W = 256), more than
+    one far and one band item per pair; the output must still match the
+    oracle."""
+    B, Hq, Hkv = 1, 1, 1
+    g = inp._gen(31337)
+    q, k, v = inp.attention_qkv(B, N, Hq, Hkv, 128, torch.bfloat16, g)
+    gate = torch.ones(B, N, dtype=torch.uint8)
+    gate[:, ::128] = 0
+    scale = 1 / math.sqrt(128)
+    o = swa.prefill(q.cuda(), k.cuda(), v.cuda(), gate.cuda(), W, scale)
+    torch.cuda.synchronize()
+    assert swa.get_device_error() == 0
+    ref = oracle.prefill(f64(q), f64(k), f64(v), gate.numpy(), W, scale)
+    err = np.abs(f64(o) - ref)
+    assert err.max() <= BF16_MAX and err.mean() <= BF16_MEAN, (err.max(), err.mean())
