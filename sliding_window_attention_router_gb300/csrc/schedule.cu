@@ -226,13 +226,13 @@ __device__ void plan_block(const uint8_t* __restrict__ gate, int B, int N, int H
     __shared__ int s_last[kTileCache];
     __shared__ int s_pre[kTileCache];
     __shared__ int s_at[2 * kPairCache];   // far position -> pair | kind << 24; band position -> order index
-    __shared__ int s_cost[3];              // far pair costs, band pair costs (sums), largest far pair cost
+    __shared__ unsigned long long s_cost[3];   // far, band pair cost sums; largest far pair cost
     const int NT = cdiv(N, kBM);
     const int NP = cdiv(N, 2 * kBM);
     const bool cached = (int64_t)B * (NT + 1) <= kTileCache;
     const int C = cdiv(cdiv(N, kPlanThreads), 16) * 16;
     for (int c = threadIdx.x; c < kCostBuckets; c += blockDim.x) hist[c] = 0;
-    if (threadIdx.x < 3) s_cost[threadIdx.x] = 0;
+    if (threadIdx.x < 3) s_cost[threadIdx.x] = 0ull;
     for (int b = 0; b < B; ++b) {
         const uint8_t* g = gate + (size_t)b * N;
         const bool vec = (reinterpret_cast<uintptr_t>(g) & 15u) == 0;
@@ -280,12 +280,12 @@ __device__ void plan_block(const uint8_t* __restrict__ gate, int B, int N, int H
     // share it in L2 (with the heads interleaved, the 32K workload read
     // 2.2x its algorithmic bytes from HBM; head by head, 1.45x).
     const int U = B * NP;
-    int far_sum = 0, far_max = 0;
+    unsigned long long far_sum = 0, far_max = 0;
     for (int u = threadIdx.x; u < U; u += blockDim.x) {
         const int cost = far_pair_cost(u / NP, u % NP, fl, NT);
         if (cost > 0) atomicAdd(&hist[min(cost, kCostBuckets - 1)], 1);
         far_sum += cost;
-        far_max = max(far_max, cost);
+        far_max = max(far_max, static_cast<unsigned long long>(cost));
     }
     if (far_sum > 0) {
         atomicAdd(&s_cost[0], far_sum);
@@ -312,7 +312,8 @@ __device__ void plan_block(const uint8_t* __restrict__ gate, int B, int N, int H
     };
     const int CB = cdiv(U, kPlanThreads);
     const int v0 = min(U, static_cast<int>(threadIdx.x) * CB), v1 = min(U, v0 + CB);
-    int nb = 0, band_sum = 0;
+    int nb = 0;
+    unsigned long long band_sum = 0;
     for (int v = v0; v < v1; ++v) {
         int b, pair;
         band_at(v, b, pair);
@@ -327,8 +328,9 @@ __device__ void plan_block(const uint8_t* __restrict__ gate, int B, int N, int H
     // as its two tiles, each an item of its own, when both hold rows.  At
     // N = 32K no pair comes near that; at N = 4K the last pair of each head
     // does (its 64 key blocks are most of the launch).
-    const int64_t all_cost = (int64_t)Hq * (s_cost[0] + s_cost[1]);
-    const int split_above = (int)min((int64_t)INT_MAX, all_cost * 5 / (4 * (int64_t)max(grid, 1)));
+    const unsigned long long all_cost = (unsigned long long)Hq * (s_cost[0] + s_cost[1]);
+    const int split_above =
+        (int)min((unsigned long long)INT_MAX, all_cost * 5ull / (4ull * max(grid, 1)));
     auto split_costs = [&](int b, int pair, int cost, int& ca, int& cb) {
         ca = cost;
         cb = 0;
@@ -339,7 +341,7 @@ __device__ void plan_block(const uint8_t* __restrict__ gate, int B, int N, int H
         cb = c;
         return true;
     };
-    if (s_cost[2] > split_above) {
+    if (s_cost[2] > (unsigned long long)split_above) {
         for (int u = threadIdx.x; u < U; u += blockDim.x) {
             const int cost = far_pair_cost(u / NP, u % NP, fl, NT);
             int ca, cb;
