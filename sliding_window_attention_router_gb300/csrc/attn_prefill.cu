@@ -3,7 +3,8 @@
 //
 // A work item holds 256 query rows of one (batch, head): two 128-row tiles A
 // and B.  Band items take 256 consecutive rows and walk their window keys; far
-// items take 256 compacted routed rows and walk keys [0, max i].  The CTA
+// items take 256 compacted routed rows and walk keys [0, max i] (a far item
+// may hold one of its two tiles alone, the other then inactive).  The CTA
 // streams one sequence of 64-key blocks; each tile uses the contiguous run of
 // blocks its rows can see, so every K/V block is loaded once for both tiles.
 //
