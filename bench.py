@@ -45,8 +45,8 @@ L2_FLUSH_BYTES = 256 << 20
 # has changed since reports null.
 MEASURED_TRAFFIC = {
     # prefill_kernel, long-context prefill N=32768 f=0.13 (far items head by head):
-    # 693 671 168 read + 120 828 672 written
-    ("prefill", "dfc2f219bcf86163"): 693671168 + 120828672,
+    # 727 854 336 read + 121 214 976 written
+    ("prefill", "fa6972f10e0d546f"): 727854336 + 121214976,
     # decode_split2_kernel (persistent CTAs), 16 x 32768 decode: 654 431 488 read + 4 102 656 written
     ("decode", "97db57687c228419"): 654431488 + 4102656,
     # dual_kernel, dual-branch workload B=2 N=8192 GQA 16/4: 144 400 384 read + 270 856 192 written

@@ -121,7 +121,7 @@ struct Plan {
     int na;            // anchor blocks at the head of the sequence (keys from 0)
     int ja1[2];        // anchor run per tile: blocks 0 .. ja1 (-1: none)
     int j0[2], j1[2];  // window (or far) run per tile (j0 > j1: tile empty)
-    int nrows[2];      // valid rows per tile
+    int rlo[2], nrows[2];   // valid local rows of each tile: [rlo, nrows)
 };
 
 template <bool ANCH>
@@ -133,20 +133,27 @@ __device__ __forceinline__ Plan make_plan(const PfParams& p, int idx) {
     pl.kvh = it.h / (p.Hq / p.Hkv);
     pl.kind = it.kind;
     pl.row0 = it.tile * 2 * kBM;
+    pl.rlo[0] = pl.rlo[1] = 0;
     pl.na = 0;
     pl.ja1[0] = pl.ja1[1] = -1;
     if (it.kind != kItemBand) {   // a far pair, or one of its tiles alone
         const int cnt = p.routed_count[it.b];
         const int* list = p.routed_list + (size_t)it.b * p.N;
+        // The first far tile holds the count's remainder (its first `front`
+        // slots are empty), so the part-filled tile walks the shortest key
+        // range, not the longest.  Local row r of tile x is compacted row
+        // row0 + 128 x + r.
+        pl.row0 -= (kBM - cnt % kBM) % kBM;
         pl.kv0 = 0;
         int maxb = 0;
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
             const int r0 = pl.row0 + x * kBM;
             const bool off = it.kind == (x == 0 ? kItemFarB : kItemFarA);
+            pl.rlo[x] = max(0, -r0);
             pl.nrows[x] = off ? 0 : max(0, min(kBM, cnt - r0));
             pl.j0[x] = 0;
-            pl.j1[x] = pl.nrows[x] > 0 ? list[r0 + pl.nrows[x] - 1] / kKB : -1;
+            pl.j1[x] = pl.nrows[x] > pl.rlo[x] ? list[r0 + pl.nrows[x] - 1] / kKB : -1;
             maxb = max(maxb, pl.j1[x] + 1);
         }
         pl.nblk = maxb;
@@ -300,8 +307,9 @@ __device__ bool producer(const PfParams& p, uint8_t* smem, uint64_t* bar, volati
 // c = row0 + 128x + r, i.e. query row routed_list[c]; its 256 bytes (head h)
 // are copied in 16-byte chunks with cp.async into the same 128-byte-swizzled
 // K-major layout the TMA writes for band tiles: chunk u of the row (half u/8)
-// lands at 16-byte slot (u%8) ^ (r%8) of the row's 128 bytes.  Rows past the
-// routed count are zero-filled.  Half-warps take one row each, so every load
+// lands at 16-byte slot (u%8) ^ (r%8) of the row's 128 bytes.  Rows outside
+// [0, routed count) (the first far tile's empty front slots, rows past the
+// count) are zero-filled.  Half-warps take one row each, so every load
 // instruction reads two whole rows.  The copies complete, each lane fences its
 // writes for the tensor core's async proxy, then one arrival fills the slot.
 __device__ void gather_far_q(const PfParams& p, uint8_t* smem, uint64_t* bar, const Plan& pl, int x,
@@ -313,7 +321,7 @@ __device__ void gather_far_q(const PfParams& p, uint8_t* smem, uint64_t* bar, co
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
         const int c = c0 + u * 32 + lane;
-        src[u] = c < R ? list[c] : -1;
+        src[u] = (c >= 0 && c < R) ? list[c] : -1;
     }
     const uint32_t tile = smem_u32(smem + kOffQ + x * kTileBytes);
     const int sub = lane & 15;
@@ -483,7 +491,7 @@ __device__ bool softmax_role(const PfParams& p, uint8_t* smem, uint64_t* bar, vo
         if (!tile_active(pl, x)) continue;
         const bool far = pl.kind != kItemBand;
         int i = -1;
-        if (r < pl.nrows[x]) {
+        if (r >= pl.rlo[x] && r < pl.nrows[x]) {
             const int rr = pl.row0 + x * kBM + r;
             i = far ? p.routed_list[(size_t)pl.b * p.N + rr] : rr;
         }

@@ -248,6 +248,10 @@ __device__ void plan_block(const uint8_t* __restrict__ gate, int B, int N, int H
         int* list = routed_list + (size_t)b * N;
         int* pre = tile_prefix + (size_t)b * (NT + 1);
         int* last = (cached ? s_last : far_last) + (size_t)b * NT;
+        // Far tile t holds compacted rows [128 t - front, 128 t - front + 128):
+        // the first one takes the remainder (the attention kernel derives the
+        // same offset from the count).
+        const int front = (kBM - total % kBM) % kBM;
         for (int i = i0; i < i1; i += 16) {
             const uint4 v = load_gates16(g, i, N, vec);
             if ((i % kBM) == 0) {   // 16 divides 128: tile starts begin groups
@@ -257,12 +261,12 @@ __device__ void plan_block(const uint8_t* __restrict__ gate, int B, int N, int H
 #pragma unroll
             for (int u = 0; u < 16; ++u)
                 if (i + u >= W && i + u < i1 && gate_byte(v, u)) {
-                    if (run % kBM == kBM - 1 || run == total - 1) last[run / kBM] = i + u;
+                    if ((run + front) % kBM == kBM - 1 || run == total - 1) last[(run + front) / kBM] = i + u;
                     list[run++] = i + u;
                 }
         }
         // Far tiles past the last one hold no rows.
-        for (int k = cdiv(total, kBM) + threadIdx.x; k < NT; k += blockDim.x) last[k] = -1;
+        for (int k = cdiv(total + front, kBM) + threadIdx.x; k < NT; k += blockDim.x) last[k] = -1;
         if (threadIdx.x == 0) {
             routed_count[b] = total;
             pre[NT] = total;
