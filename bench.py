@@ -46,14 +46,14 @@ L2_FLUSH_BYTES = 256 << 20
 MEASURED_TRAFFIC = {
     # prefill_kernel, long-context prefill N=32768 f=0.13 (far items head by head):
     # 727 854 336 read + 121 214 976 written
-    ("prefill", "fa6972f10e0d546f"): 727854336 + 121214976,
+    ("prefill", "cf365a2309de5abb"): 727854336 + 121214976,
     # decode_split2_kernel (persistent CTAs), 16 x 32768 decode: 654 431 488 read + 4 102 656 written
     ("decode", "97db57687c228419"): 654431488 + 4102656,
     # dual_kernel, dual-branch workload B=2 N=8192 GQA 16/4: 144 400 384 read + 270 856 192 written
     ("dual", "0d140f1582e3c2ea"): 144400384 + 270856192,
-    # dkdv_kernel + dq_kernel, backward on the dual workload: (317 678 848 + 22 807 808)
-    # + (256 428 032 + 48 124 672)
-    ("backward", "c5d579004d6b73b0"): 317678848 + 22807808 + 256428032 + 48124672,
+    # dkdv_kernel + dq_kernel, backward on the dual workload: (315 288 064 + 22 582 016)
+    # + (254 839 296 + 48 433 152)
+    ("backward", "789f57cbf56f040a"): 315288064 + 22582016 + 254839296 + 48433152,
     # route_kernel, 32768 tokens x 2048: 134 248 192 read + 2 795 520 written
     ("route", "4a5c0b7bf6e2d8ed"): 134248192 + 2795520,
     # route_bwd_logit + dh + reduce kernels, 16384 tokens: (201 534 208 + 3 031 552)

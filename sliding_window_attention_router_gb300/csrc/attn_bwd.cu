@@ -451,7 +451,7 @@ __device__ bool softmax_role(const BwdParams& p, uint8_t* smem, uint64_t* bar, v
                 // visible; otherwise every thread counts the rows below its
                 // target, the tile's 128 row indices spread 4 per lane.
                 const int* gR = p.rowidx + (size_t)pl.b * p.Npad + t.row0;
-                const int nvalid = min(kBM, R - t.row0);
+                const int nvalid = min(kBM, R + far_front(R) - t.row0);
                 e = nvalid - 1;
                 if (nvalid == kBM && gR[0] >= pl.k0 + kBN - 1 + p.W) {
                     a = 0;

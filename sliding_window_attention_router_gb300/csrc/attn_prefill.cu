@@ -143,7 +143,7 @@ __device__ __forceinline__ Plan make_plan(const PfParams& p, int idx) {
         // slots are empty), so the part-filled tile walks the shortest key
         // range, not the longest.  Local row r of tile x is compacted row
         // row0 + 128 x + r.
-        pl.row0 -= (kBM - cnt % kBM) % kBM;
+        pl.row0 -= far_front(cnt);
         pl.kv0 = 0;
         int maxb = 0;
 #pragma unroll

@@ -107,9 +107,10 @@ __device__ __forceinline__ BwdItem kv_item(int u, const int* routed_list, const 
     const int k0 = it.t * kBN;
     it.a0 = cdiv(min(N, k0 + kBN - 1 + W) - k0, kBM);   // band query tiles
     const int R = routed_count[it.b];
+    const int front = far_front(R);
     const int first = lower_bound_dev(routed_list + (size_t)it.b * N, R, k0 + W);
-    it.a1 = first < R ? first / kBM : 0;                // far tiles [a1, a2)
-    it.a2 = first < R ? cdiv(R, kBM) : 0;
+    it.a1 = first < R ? (first + front) / kBM : 0;      // far tiles [a1, a2)
+    it.a2 = first < R ? (R + front) / kBM : 0;
     it.cost = (Hq / Hkv) * (it.a0 + it.a2 - it.a1);
     return it;
 }
@@ -137,10 +138,11 @@ __device__ __forceinline__ BwdItem q_item(int u, const int* routed_list, const i
         it.kind = kBwdQFar;
         it.t = rem - NT;
         const int R = routed_count[it.b];
+        const int front = far_front(R);
         it.a0 = 0;
         it.a1 = 0;
-        if (it.t * kBM < R) {
-            const int last = routed_list[(size_t)it.b * N + min(R, (it.t + 1) * kBM) - 1];
+        if (it.t * kBM < R + front) {
+            const int last = routed_list[(size_t)it.b * N + min(R, (it.t + 1) * kBM - front) - 1];
             it.a1 = last / kBN + 1;
             it.cost = it.a1;
         }
@@ -249,15 +251,17 @@ __global__ void __launch_bounds__(kBuildThreads) bwd_build_gather_kernel(
     const size_t w0 = (size_t)(blockIdx.x - 2) * (blockDim.x >> 5) + (threadIdx.x >> 5);
     for (int b = 0; b < B; ++b) {
         const int R = routed_count[b];
-        const size_t total = (size_t)cdiv(R, kBM) * kBM * Hq;   // (row, head) pairs to write
+        const int front = far_front(R);
+        const size_t total = (size_t)(R + front) * Hq;   // (position, head) pairs to write
         for (size_t ww = w0; 2 * ww < total; ww += warps) {
             const size_t w = 2 * ww + half;
             const bool live = w < total;
-            const int r = (int)(w / Hq), h = (int)(w % Hq);
+            const int pos = (int)(w / Hq), h = (int)(w % Hq);
+            const int r = pos - front;   // compacted far row at this position
             uint4 vq = make_uint4(0u, 0u, 0u, 0u), vd = vq;
             int i = kNoRow;
             float dv = 0.f, lv = 0.f;
-            if (live && r < R) {
+            if (live && r >= 0 && r < R) {
                 i = routed_list[(size_t)b * N + r];
                 const size_t src = ((size_t)b * N + i) * Hq + h;
                 vq = reinterpret_cast<const uint4*>(q + src * kHD)[sub];
@@ -269,13 +273,13 @@ __global__ void __launch_bounds__(kBuildThreads) bwd_build_gather_kernel(
                 }
             }
             if (live) {
-                const size_t dst = ((size_t)b * Npad + r) * Hq + h;
+                const size_t dst = ((size_t)b * Npad + pos) * Hq + h;
                 reinterpret_cast<uint4*>(qc + dst * kHD)[sub] = vq;
                 reinterpret_cast<uint4*>(doc + dst * kHD)[sub] = vd;
                 if (sub == 0) {
-                    d_far[((size_t)b * Hq + h) * Npad + r] = dv;
-                    l_far[((size_t)b * Hq + h) * Npad + r] = lv;
-                    if (h == 0) rowidx[(size_t)b * Npad + r] = i;
+                    d_far[((size_t)b * Hq + h) * Npad + pos] = dv;
+                    l_far[((size_t)b * Hq + h) * Npad + pos] = lv;
+                    if (h == 0) rowidx[(size_t)b * Npad + pos] = i;
                 }
             }
         }

@@ -251,7 +251,7 @@ __device__ void plan_block(const uint8_t* __restrict__ gate, int B, int N, int H
         // Far tile t holds compacted rows [128 t - front, 128 t - front + 128):
         // the first one takes the remainder (the attention kernel derives the
         // same offset from the count).
-        const int front = (kBM - total % kBM) % kBM;
+        const int front = far_front(total);
         for (int i = i0; i < i1; i += 16) {
             const uint4 v = load_gates16(g, i, N, vec);
             if ((i % kBM) == 0) {   // 16 divides 128: tile starts begin groups

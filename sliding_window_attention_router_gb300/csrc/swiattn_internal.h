@@ -58,6 +58,11 @@ struct WorkItem {
     int kind, b, h, tile;
 };
 
+// Far rows fill 128-row tiles in ascending row order; the first tile holds
+// the remainder of the count R, its first far_front(R) slots empty, so the
+// part-filled tile holds the earliest rows (the shortest key prefix).
+__host__ __device__ inline int far_front(int R) { return (kBM - R % kBM) % kBM; }
+
 // Workspace layout of swiattn_prefill (byte offsets from a 256-aligned base).
 struct PrefillWs {
     size_t routed_list;   // int32 [B*N]   far rows of each batch, ascending
