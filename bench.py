@@ -46,7 +46,7 @@ L2_FLUSH_BYTES = 256 << 20
 MEASURED_TRAFFIC = {
     # prefill_kernel, long-context prefill N=32768 f=0.13 (far items head by head):
     # 727 854 336 read + 121 214 976 written
-    ("prefill", "cf365a2309de5abb"): 727854336 + 121214976,
+    ("prefill", "532909cf403d4c6c"): 727854336 + 121214976,
     # decode_split2_kernel (persistent CTAs), 16 x 32768 decode: 654 431 488 read + 4 102 656 written
     ("decode", "97db57687c228419"): 654431488 + 4102656,
     # dual_kernel, dual-branch workload B=2 N=8192 GQA 16/4: 144 400 384 read + 270 856 192 written

@@ -226,13 +226,12 @@ __device__ void plan_block(const uint8_t* __restrict__ gate, int B, int N, int H
     __shared__ int s_last[kTileCache];
     __shared__ int s_pre[kTileCache];
     __shared__ int s_at[2 * kPairCache];   // far position -> pair | kind << 24; band position -> order index
-    __shared__ unsigned long long s_cost[3];   // far, band pair cost sums; largest far pair cost
+    __shared__ float3 s_cost[32];   // per warp: far, band pair cost sums, largest far pair cost
     const int NT = cdiv(N, kBM);
     const int NP = cdiv(N, 2 * kBM);
     const bool cached = (int64_t)B * (NT + 1) <= kTileCache;
     const int C = cdiv(cdiv(N, kPlanThreads), 16) * 16;
     for (int c = threadIdx.x; c < kCostBuckets; c += blockDim.x) hist[c] = 0;
-    if (threadIdx.x < 3) s_cost[threadIdx.x] = 0ull;
     for (int b = 0; b < B; ++b) {
         const uint8_t* g = gate + (size_t)b * N;
         const bool vec = (reinterpret_cast<uintptr_t>(g) & 15u) == 0;
@@ -284,17 +283,14 @@ __device__ void plan_block(const uint8_t* __restrict__ gate, int B, int N, int H
     // share it in L2 (with the heads interleaved, the 32K workload read
     // 2.2x its algorithmic bytes from HBM; head by head, 1.45x).
     const int U = B * NP;
-    unsigned long long far_sum = 0, far_max = 0;
+    int far_sum = 0, far_max = 0;
     for (int u = threadIdx.x; u < U; u += blockDim.x) {
         const int cost = far_pair_cost(u / NP, u % NP, fl, NT);
         if (cost > 0) atomicAdd(&hist[min(cost, kCostBuckets - 1)], 1);
         far_sum += cost;
-        far_max = max(far_max, static_cast<unsigned long long>(cost));
+        far_max = max(far_max, cost);
     }
-    if (far_sum > 0) {
-        atomicAdd(&s_cost[0], far_sum);
-        atomicMax(&s_cost[2], far_max);
-    }
+
     // Band pairs follow, in (batch, pair) order with the heads of a pair
     // adjacent: their costs are nearly equal (the window and one tile), and
     // the CTAs that run them at the same time then walk overlapping windows
@@ -316,8 +312,7 @@ __device__ void plan_block(const uint8_t* __restrict__ gate, int B, int N, int H
     };
     const int CB = cdiv(U, kPlanThreads);
     const int v0 = min(U, static_cast<int>(threadIdx.x) * CB), v1 = min(U, v0 + CB);
-    int nb = 0;
-    unsigned long long band_sum = 0;
+    int nb = 0, band_sum = 0;
     for (int v = v0; v < v1; ++v) {
         int b, pair;
         band_at(v, b, pair);
@@ -325,16 +320,34 @@ __device__ void plan_block(const uint8_t* __restrict__ gate, int B, int N, int H
         nb += cost > 0;
         band_sum += cost;
     }
-    if (band_sum > 0) atomicAdd(&s_cost[1], band_sum);
-    __syncthreads();   // the histogram and the cost sums are complete
+    // Cost sums and the largest far pair cost: warp shuffles, then one slot
+    // per warp (one shared address taking an atomic from every thread cost
+    // ~6000 cycles here), read by every thread after the barrier.
+    {
+        float fs = static_cast<float>(far_sum), bs = static_cast<float>(band_sum);
+        int fm = far_max;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            fs += __shfl_xor_sync(0xffffffffu, fs, o);
+            bs += __shfl_xor_sync(0xffffffffu, bs, o);
+            fm = max(fm, __shfl_xor_sync(0xffffffffu, fm, o));
+        }
+        if ((threadIdx.x & 31) == 0) s_cost[threadIdx.x >> 5] = make_float3(fs, bs, static_cast<float>(fm));
+    }
+    __syncthreads();   // the histogram and the per-warp cost sums are complete
+    float far_total_cost = 0.f, band_total_cost = 0.f, far_max_cost = 0.f;
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) {
+        far_total_cost += s_cost[w].x;
+        band_total_cost += s_cost[w].y;
+        far_max_cost = fmaxf(far_max_cost, s_cost[w].z);
+    }
     // A far pair costing more than 1.25 x a CTA's mean share of the whole
     // list (all heads, `grid` CTAs) would end the launch alone: it is listed
     // as its two tiles, each an item of its own, when both hold rows.  At
     // N = 32K no pair comes near that; at N = 4K the last pair of each head
     // does (its 64 key blocks are most of the launch).
-    const unsigned long long all_cost = (unsigned long long)Hq * (s_cost[0] + s_cost[1]);
-    const int split_above =
-        (int)min((unsigned long long)INT_MAX, all_cost * 5ull / (4ull * max(grid, 1)));
+    const float all_cost = static_cast<float>(Hq) * (far_total_cost + band_total_cost);
+    const int split_above = static_cast<int>(fminf(2.0e9f, all_cost * 1.25f / static_cast<float>(max(grid, 1))));
     auto split_costs = [&](int b, int pair, int cost, int& ca, int& cb) {
         ca = cost;
         cb = 0;
@@ -345,7 +358,7 @@ __device__ void plan_block(const uint8_t* __restrict__ gate, int B, int N, int H
         cb = c;
         return true;
     };
-    if (s_cost[2] > (unsigned long long)split_above) {
+    if (far_max_cost > static_cast<float>(split_above)) {
         for (int u = threadIdx.x; u < U; u += blockDim.x) {
             const int cost = far_pair_cost(u / NP, u % NP, fl, NT);
             int ca, cb;
