@@ -6,8 +6,10 @@ hand; these cover the space between them (batch counts, GQA ratios, window
 sizes, sequence lengths that are not multiples of the tile sizes, gate run
 lengths and fractions).
 
-A last test repeats a call made of tiny band and far items many times, each
-call checked for an expired device-side wait.
+A test repeats a call made of tiny band and far items many times, each call
+checked for an expired device-side wait; others cover a work list where most
+far pairs are split into one-tile items, and far-row counts at the edges of
+the far tiling (prefill and backward).
 
 Tolerances as elsewhere: bf16 attention outputs max-abs 2e-2 and mean-abs
 2e-3; fp32 outputs 1e-4; the visited-key count of every (row, head) exact.
@@ -251,3 +253,35 @@ def test_prefill_most_far_pairs_split(swa, N, W):
     ref = oracle.prefill(f64(q), f64(k), f64(v), gate.numpy(), W, scale)
     err = np.abs(f64(o) - ref)
     assert err.max() <= BF16_MAX and err.mean() <= BF16_MEAN, (err.max(), err.mean())
+
+
+@pytest.mark.parametrize("R", [1, 128, 129, 200])
+def test_far_row_counts_at_tile_edges(swa, R):
+    """Far-row counts at the edges of the far tiling (the first far tile holds
+    the remainder of the count: 127 empty slots for R = 1 and 129, none for
+    R = 128): prefill outputs and the backward's dQ, dK, dV against the
+    oracle, with the routed rows spread over [W, N)."""
+    B, N, Hq, Hkv, W = 1, 1024, 2, 1, 64
+    g = inp._gen(4242 + R)
+    q, k, v = inp.attention_qkv(B, N, Hq, Hkv, 128, torch.bfloat16, g)
+    rows = torch.randperm(N - W, generator=g)[:R] + W
+    gate = torch.zeros(B, N, dtype=torch.uint8)
+    gate[0, rows] = 1
+    scale = 1 / math.sqrt(128)
+    qd, kd, vd, gd = q.cuda(), k.cuda(), v.cuda(), gate.cuda()
+    o, lse = swa.prefill(qd, kd, vd, gd, W, scale, want_lse=True)
+    torch.cuda.synchronize()
+    assert swa.get_device_error() == 0
+    ref = oracle.prefill(f64(q), f64(k), f64(v), gate.numpy(), W, scale)
+    err = np.abs(f64(o) - ref)
+    assert err.max() <= BF16_MAX and err.mean() <= BF16_MEAN, (err.max(), err.mean())
+    do = inp.output_grad((B, N, Hq, 128), torch.bfloat16, 77 + R)
+    grads = swa.prefill_backward(qd, kd, vd, gd, o, lse, do.cuda(), W)
+    torch.cuda.synchronize()
+    assert swa.get_device_error() == 0
+    refs = oracle.prefill_backward(f64(q), f64(k), f64(v), gate.numpy(), f64(do), W, scale)
+    for name, got, r in zip(("dq", "dk", "dv"), grads, refs):
+        r = np.asarray(r)
+        e = np.abs(f64(got).reshape(r.shape) - r)
+        assert e.max() <= 1e-2 * np.abs(r).max(), (name, e.max(), np.abs(r).max())
+        assert e.mean() <= 4e-3 * np.abs(r).mean(), (name, e.mean(), np.abs(r).mean())
