@@ -20,8 +20,6 @@ import torch
 
 import swiattn_inputs as inp
 
-pytestmark = pytest.mark.gpu
-
 BAND, FAR, FAR_A, FAR_B = 0, 1, 2, 3
 
 
@@ -110,6 +108,7 @@ def cases():
     return out
 
 
+@pytest.mark.gpu
 @pytest.mark.parametrize("case", cases(), ids=lambda c: f"{c[5]}{c[0]}")
 def test_work_list_covers_every_tile_once(swa, case):
     c, B, N, Hq, W, kind = case
@@ -130,3 +129,30 @@ def test_work_list_covers_every_tile_once(swa, case):
     nfar, nsplit = check(items, gate.numpy(), W, Hq)
     if kind == "split":
         assert nsplit > 0
+
+
+def test_checker_accepts_valid_lists_and_catches_planted_mistakes():
+    rng = np.random.default_rng(0)
+    for _ in range(200):
+        B, Hq = int(rng.integers(1, 3)), int(rng.integers(1, 3))
+        N, W = int(rng.integers(1, 1200)), int(rng.integers(1, 400))
+        gate = (rng.random((B, N)) < rng.random()).astype(np.uint8)
+        far, band = expected(gate, W, Hq)
+        items = []
+        for b, h, p in sorted({(b, h, t // 2) for b, h, t in far}):
+            if rng.random() < 0.5 and (b, h, 2 * p + 1) in far:
+                items += [[FAR_A, b, h, p], [FAR_B, b, h, p]]
+            else:
+                items.append([FAR, b, h, p])
+        items += [[BAND, b, h, p] for b, h, p in sorted(band)]
+        items = np.array(items, dtype=np.int64).reshape(-1, 4)
+        check(items, gate, W, Hq)
+        if len(items) > 1:
+            with pytest.raises(AssertionError):
+                check(np.concatenate([items, items[-1:]]), gate, W, Hq)   # duplicated
+            with pytest.raises(AssertionError):
+                check(items[:-1], gate, W, Hq)                            # dropped
+        nfar = int((items[:, 0] != BAND).sum())
+        if 0 < nfar < len(items):
+            with pytest.raises(AssertionError):
+                check(items[::-1].copy(), gate, W, Hq)                    # band before far
