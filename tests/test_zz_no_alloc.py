@@ -75,12 +75,23 @@ def test_noalloc_decode_rejects_partials_beyond_scratch(swa):
     rc = _call_noalloc(lib, q, small, small, sl, gate, o, lse, W, 0.1, swa.BF16)
     assert rc == 0
     vp = ctypes.c_void_p
-    rc = lib.swiattn_decode_noalloc(vp(q.data_ptr()), vp(small.data_ptr()), vp(small.data_ptr()),
-                                    vp(sl.data_ptr()), vp(gate.data_ptr()), vp(o.data_ptr()),
-                                    vp(lse.data_ptr()), B, 32512, Hq, Hkv, d, W, 0.1, swa.BF16,
-                                    vp(torch.cuda.current_stream().cuda_stream))
-    assert rc == 1   # SWIATTN_EINVAL, nothing launched
+    # At B = Hq = 16, d = 128 the partials fit 16 MiB up to Lmax = 32 000
+    # (126 chunks: 16 773 376 bytes with the counter) and not from 32 001
+    # (127 chunks: 16 906 496 bytes).
+    for Lmax in (32001, 32512):
+        rc = lib.swiattn_decode_noalloc(vp(q.data_ptr()), vp(small.data_ptr()),
+                                        vp(small.data_ptr()), vp(sl.data_ptr()),
+                                        vp(gate.data_ptr()), vp(o.data_ptr()), vp(lse.data_ptr()),
+                                        B, Lmax, Hq, Hkv, d, W, 0.1, swa.BF16,
+                                        vp(torch.cuda.current_stream().cuda_stream))
+        assert rc == 1, Lmax   # SWIATTN_EINVAL, nothing launched
     torch.cuda.synchronize()
+    # The largest accepted Lmax runs (full-size caches; 8 tokens of each read).
+    big = torch.zeros(B, 32000, Hkv, d, dtype=torch.bfloat16, device="cuda")
+    assert _call_noalloc(lib, q, big, big, sl, gate, o, lse, W, 0.1, swa.BF16) == 0
+    torch.cuda.synchronize()
+    assert swa.get_device_error() == 0
+    assert torch.equal(o, torch.zeros_like(o))   # zero values: a zero output
 
 
 def test_noalloc_decode_without_lse(swa):
